@@ -1,0 +1,258 @@
+"""CPU oracle for NVFP4 paged KV -- test infrastructure only.
+
+Thin ctypes wrapper over ``nvfp4_oracle.c`` (plain C99, fp64). Only the tests, the smoke
+check and the benchmark's CPU-baseline leg may import this package; the GPU library never
+does, and the two share no code. See ``nvfp4_oracle.c`` for the arithmetic convention and
+the readings taken where the source pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nvfp4_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+
+BF16, FP16, FP8_E4M3 = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fused multiply-add, OpenMP over pages / heads)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-Wall", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            d, i, p, sz = ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            sig = {
+                "orc_max_threads": (i, []),
+                "orc_set_threads": (None, [i]),
+                "orc_round_to_format": (d, [d, i, i]),
+                "orc_fp32": (d, [d]),
+                "orc_bf16_round": (d, [d]),
+                "orc_fp16_round": (d, [d]),
+                "orc_e2m1_value": (d, [i]),
+                "orc_e2m1_encode": (i, [d]),
+                "orc_e4m3_value": (d, [i]),
+                "orc_e4m3_encode": (i, [d]),
+                "orc_bf16_value": (d, [i]),
+                "orc_bf16_bits": (i, [d]),
+                "orc_fp16_value": (d, [i]),
+                "orc_fp16_bits": (i, [d]),
+                "orc_e2m1_encode_f32": (None, [p, sz, p]),
+                "orc_e4m3_encode_f32": (None, [p, sz, p]),
+                "orc_tensor_amax": (d, [i, i, i, i, p, p, i, d]),
+                "orc_global_scale_from_amax": (d, [d]),
+                "orc_quantize_pages": (None, [i, i, i, i, p, p, d, d, p, p, p, i]),
+                "orc_dequantize_pages": (None, [i, i, i, p, p, p, d, i, p, p, d, i]),
+                "orc_paged_decode_attention": (None, [i, i, i, i, i, p, p, p, d, p, p, d, p,
+                                                      i, p, d, p, p, p]),
+                "orc_paged_decode_attention_bf16": (None, [i, i, i, i, i, p, p, p, p, i, p,
+                                                           d, p]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _ids(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+# ---------------------------------------------------------------- scalar conversions
+
+def max_threads() -> int:
+    return _load().orc_max_threads()
+
+
+def set_threads(n: int) -> None:
+    _load().orc_set_threads(int(n))
+
+
+def round_to_format(y: float, p: int, emin: int) -> float:
+    return _load().orc_round_to_format(float(y), int(p), int(emin))
+
+
+def fp32(y: float) -> float:
+    return _load().orc_fp32(float(y))
+
+
+def bf16_round(y: float) -> float:
+    return _load().orc_bf16_round(float(y))
+
+
+def fp16_round(y: float) -> float:
+    return _load().orc_fp16_round(float(y))
+
+
+def e2m1_value(code: int) -> float:
+    return _load().orc_e2m1_value(int(code))
+
+
+def e2m1_encode(y: float) -> int:
+    return _load().orc_e2m1_encode(float(y))
+
+
+def e4m3_value(b: int) -> float:
+    return _load().orc_e4m3_value(int(b))
+
+
+def e4m3_encode(y: float) -> int:
+    return _load().orc_e4m3_encode(float(y))
+
+
+def bf16_value(h: int) -> float:
+    return _load().orc_bf16_value(int(h))
+
+
+def bf16_bits(v: float) -> int:
+    return _load().orc_bf16_bits(float(v))
+
+
+def fp16_value(h: int) -> float:
+    return _load().orc_fp16_value(int(h))
+
+
+def fp16_bits(v: float) -> int:
+    return _load().orc_fp16_bits(float(v))
+
+
+def e2m1_encode_f32(x: np.ndarray) -> np.ndarray:
+    """E2M1 codes (RNE, satfinite, sign kept) of finite fp32 values, one per byte."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_e2m1_encode_f32(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def e4m3_encode_f32(x: np.ndarray) -> np.ndarray:
+    """E4M3 bytes (RNE, satfinite at 448, sign kept) of finite fp32 values."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_e4m3_encode_f32(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- page codec
+
+def _src_dtype(src: np.ndarray, dtype: int) -> np.ndarray:
+    want = np.uint8 if dtype == FP8_E4M3 else np.uint16
+    src = np.ascontiguousarray(src)
+    if src.dtype != want:
+        raise TypeError(f"source bit patterns must be {want}, got {src.dtype}")
+    return src
+
+
+def tensor_amax(src, dtype, H, D, T, src_page_ids=None, num_pages=None, src_scale=1.0):
+    src = _src_dtype(src, dtype)
+    ids = _ids(src_page_ids)
+    n = len(ids) if ids is not None else (num_pages if num_pages is not None
+                                         else src.size // (H * T * D))
+    return _load().orc_tensor_amax(H, D, T, dtype, _ptr(src), _ptr(ids), n, float(src_scale))
+
+
+def global_scale(src, dtype, H, D, T, src_page_ids=None, num_pages=None, src_scale=1.0):
+    """g = fp32(amax / 2688), or 1.0 when that is zero."""
+    amax = tensor_amax(src, dtype, H, D, T, src_page_ids, num_pages, src_scale)
+    return _load().orc_global_scale_from_amax(amax)
+
+
+def quantize_pages(src, dtype, H, D, T, g, num_dst_pages=None, src_page_ids=None,
+                   dst_page_ids=None, num_pages=None, src_scale=1.0):
+    """Encode pages to NVFP4. Returns (data [P][H][T][D/2] u8, scales [P][H][T][D/16] u8)."""
+    src = _src_dtype(src, dtype)
+    sids, dids = _ids(src_page_ids), _ids(dst_page_ids)
+    if num_pages is None:
+        num_pages = len(sids) if sids is not None else src.size // (H * T * D)
+    if num_dst_pages is None:
+        num_dst_pages = int(dids.max()) + 1 if dids is not None and len(dids) else num_pages
+    data = np.zeros((num_dst_pages, H, T, D // 2), dtype=np.uint8)
+    scales = np.zeros((num_dst_pages, H, T, D // 16), dtype=np.uint8)
+    _load().orc_quantize_pages(H, D, T, dtype, _ptr(src), _ptr(sids), float(src_scale),
+                               float(g), _ptr(data), _ptr(scales), _ptr(dids), int(num_pages))
+    return data, scales
+
+
+def dequantize_pages(data, scales, H, D, T, g, out_dtype=BF16, num_dst_pages=None,
+                     src_page_ids=None, dst_page_ids=None, num_pages=None, out_scale=1.0):
+    """Decode NVFP4 pages to BF16/FP16 bit patterns (uint16) or FP8 E4M3 bytes."""
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    sids, dids = _ids(src_page_ids), _ids(dst_page_ids)
+    if num_pages is None:
+        num_pages = len(sids) if sids is not None else data.size // (H * T * D // 2)
+    if num_dst_pages is None:
+        num_dst_pages = int(dids.max()) + 1 if dids is not None and len(dids) else num_pages
+    odt = np.uint8 if out_dtype == FP8_E4M3 else np.uint16
+    out = np.zeros((num_dst_pages, H, T, D), dtype=odt)
+    _load().orc_dequantize_pages(H, D, T, _ptr(data), _ptr(scales), _ptr(sids), float(g),
+                                 int(out_dtype), _ptr(out), _ptr(dids), float(out_scale),
+                                 int(num_pages))
+    return out
+
+
+# ---------------------------------------------------------------- attention
+
+def paged_decode_attention(q_bf16, k_data, k_scales, g_k, v_data, v_scales, g_v, page_table,
+                           seq_lens, sm_scale, H, T, want_lse=True, want=None):
+    """Exact (fp64) GQA decode attention over NVFP4 pages.
+
+    q_bf16: uint16 [B, Hq, D]; page_table: int32 [B, max_pages]; seq_lens: int32 [B].
+    want: optional bool [B, Hq] selecting the (sequence, head) pairs to compute (others stay 0).
+    Returns (out fp64 [B, Hq, D], lse fp64 [B, Hq]).
+    """
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    B, Hq, D = q.shape
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    kd, ks = np.ascontiguousarray(k_data, np.uint8), np.ascontiguousarray(k_scales, np.uint8)
+    vd, vs = np.ascontiguousarray(v_data, np.uint8), np.ascontiguousarray(v_scales, np.uint8)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64) if want_lse else None
+    wm = None if want is None else np.ascontiguousarray(want, dtype=np.uint8).reshape(B, Hq)
+    _load().orc_paged_decode_attention(B, Hq, H, D, T, _ptr(q), _ptr(kd), _ptr(ks), float(g_k),
+                                       _ptr(vd), _ptr(vs), float(g_v), _ptr(pt), pt.shape[1],
+                                       _ptr(sl), float(sm_scale), _ptr(wm), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def paged_decode_attention_bf16(q_bf16, k_bf16, v_bf16, page_table, seq_lens, sm_scale, H, T):
+    """The same attention over unquantized BF16 pages (uint16 [P][H][T][D]); fp64 output."""
+    q = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    B, Hq, D = q.shape
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    k = np.ascontiguousarray(k_bf16, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bf16, dtype=np.uint16)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    _load().orc_paged_decode_attention_bf16(B, Hq, H, D, T, _ptr(q), _ptr(k), _ptr(v), _ptr(pt),
+                                            pt.shape[1], _ptr(sl), float(sm_scale), _ptr(out))
+    return out

@@ -1,0 +1,358 @@
+"""Pins of the CPU oracle's page codec (encode, decode, global scale).
+
+Format sources: "Accelerating Long-Context and Agentic Inference with NVFP4 KV Cache" (LMSYS
+blog; introduction + Figure 1, "NVFP4 KV Implementation in SGLang", "NVFP4 KV Decode Attention
+Kernel Implementation") and "KV Cache Compression in TensorRT LLM" (NVIDIA; "NVFP4 Cold-Page
+Compression", Figure 6, Figure 10, "Evaluation" > Accuracy + Figure 15)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import read_golden
+from test_oracle_format import brute_e2m1
+
+E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def bf16_bits_of(values):
+    return torch.tensor(values, dtype=torch.float32).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def bf16_from_bits(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16) \
+        .float().numpy()
+
+
+def unpack_codes(data):
+    lo, hi = data & 15, data >> 4
+    return np.stack([lo, hi], axis=-1).reshape(*data.shape[:-1], data.shape[-1] * 2)
+
+
+# ------------------------------------------------------------------------------------ golden
+
+def test_worked_block_golden():
+    rows = {r[0]: r[1:] for r in read_golden("block_g1.txt")}
+    g = float(rows["g"][0])
+    x = [float(v) for v in rows["x"]]
+    src = bf16_bits_of(x).reshape(1, 1, 1, 16)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H=1, D=16, T=1, g=g)
+    assert scales.ravel()[0] == int(rows["scale"][0], 16)
+    assert [int(b) for b in data.ravel()] == [int(b, 16) for b in rows["packed"]]
+    assert [int(c) for c in unpack_codes(data).ravel()] == [int(c) for c in rows["codes"]]
+
+
+def test_storage_ratio_golden():
+    facts = {k: float(v) for k, v in read_golden("storage.txt")}
+    H, D, T, P = 8, 128, 64, 3
+    src = np.zeros((P, H, T, D), np.uint16)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H, D, T, g=1.0)
+    n = P * H * T * D
+    nvfp4 = data.nbytes + scales.nbytes
+    assert nvfp4 * 16 == facts["bytes_per_16_values"] * n
+    assert nvfp4 / n == facts["bytes_per_value"]
+    assert nvfp4 / (n * 1) == facts["fraction_of_fp8"]
+    assert 100 * (1 - nvfp4 / (n * 1)) == facts["fp8_shrink_percent"]
+    assert 100 * (1 - nvfp4 / (n * 2)) == facts["bf16_shrink_percent"]
+    assert abs((n * 1) / nvfp4 - facts["capacity_vs_fp8"]) < 1e-12
+
+
+# ------------------------------------------------------------------------------------ encode
+
+@pytest.mark.parametrize("g", [1.0, 2.0 ** -7, 2.0 ** 5])
+def test_grid_exactness_every_scale(g):
+    """A block holding e * s * g for every code e, with 6 as its maximum, is representable in
+    NVFP4 exactly: encode picks s, the codes come back and decode returns the block unchanged."""
+    blocks, want_scale, want_codes = [], [], []
+    order = [7, 0, 1, 2, 3, 4, 5, 6, 15, 8, 9, 10, 11, 12, 13, 14]
+    for sb in range(1, 0x7F):
+        s = oracle.e4m3_value(sb)
+        rot = order[:1] + order[1 + sb % 15:] + order[1:1 + sb % 15]  # move positions around
+        blocks.append([math.copysign(E2M1[c & 7], -1.0 if c & 8 else 1.0) * s * g for c in rot])
+        want_scale.append(sb)
+        want_codes.append(rot)
+    src = bf16_bits_of(blocks).reshape(len(blocks), 1, 1, 16)
+    assert np.array_equal(bf16_from_bits(src).reshape(-1, 16), np.array(blocks, np.float32))
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H=1, D=16, T=1, g=g)
+    assert scales.ravel().tolist() == want_scale
+    assert unpack_codes(data).reshape(-1, 16).tolist() == want_codes
+    back = oracle.dequantize_pages(data, scales, H=1, D=16, T=1, g=g)
+    assert np.array_equal(back, src)
+
+
+def test_tie_table_inside_blocks():
+    ties = [(float(x), int(c)) for x, c in read_golden("e2m1_ties.txt")]
+    xs = [6.0] + [x for x, _ in ties] + [0.0]
+    src = bf16_bits_of(xs).reshape(1, 1, 1, 16)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H=1, D=16, T=1, g=1.0)
+    assert scales.ravel()[0] == 0x38
+    assert unpack_codes(data).ravel().tolist() == [7] + [c for _, c in ties] + [0]
+
+
+def test_scale_saturation_and_underflow():
+    g = 1.0
+    big = [2688.0 * 4, -2688.0 * 2, 2688.0, 100.0] + [0.0] * 12       # a/(6g) > 448
+    tiny = [2.0 ** -12, -2.0 ** -13] + [0.0] * 14                      # a/(6g) < 2^-10
+    src = bf16_bits_of([big, tiny]).reshape(2, 1, 1, 16)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H=1, D=16, T=1, g=g)
+    assert scales.ravel().tolist() == [0x7E, 0x00]
+    c = unpack_codes(data).reshape(2, 16)
+    assert c[0, :3].tolist() == [7, 15, 7]          # saturated at +-6 * 448
+    assert c[1, :2].tolist() == [0, 8]              # zero scale: signed zeros only
+
+
+def test_encode_steps_against_ieee_fp32_arithmetic():
+    """The oracle's fp64-then-round steps equal the same steps run in IEEE fp32 (numpy float32
+    arithmetic, torch's E4M3 cast, brute-force E2M1 search) on random blocks and random g."""
+    rng = np.random.default_rng(5)
+    nblk = 400
+    x = (rng.normal(0, 1, (nblk, 16)) * np.exp(rng.uniform(-8, 8, (nblk, 1)))).astype(np.float32)
+    src = bf16_bits_of(x).reshape(nblk, 1, 1, 16)
+    xb = bf16_from_bits(src).reshape(nblk, 16)
+    for g in (np.float32(1.0), np.float32(0.0123), np.float32(3.7)):
+        data, scales = oracle.quantize_pages(src, oracle.BF16, H=1, D=16, T=1, g=float(g))
+        codes = unpack_codes(data).reshape(nblk, 16)
+        d = np.float32(6.0) * g
+        for i in range(nblk):
+            a = np.max(np.abs(xb[i]))
+            q = np.float32(a) / d
+            sb = int(torch.tensor([q]).to(torch.float8_e4m3fn).view(torch.uint8)[0]) \
+                if q < 464 else 0x7E
+            assert scales.ravel()[i] == sb
+            s = np.float32(oracle.e4m3_value(sb))
+            sg = s * g
+            r = np.float32(0.0) if sg == 0 else np.float32(1.0) / sg
+            for k in range(16):
+                y = np.float32(xb[i, k]) * r
+                assert codes[i, k] == brute_e2m1(float(y)), (i, k)
+
+
+def test_closed_form_error_bound():
+    """|x/(s g) - e(c)| is at most half the local grid gap when the block scale is normal, and
+    the saturation overshoot of the block maximum is at most 6/0.9375 - 6 = 0.4. The encoder
+    rounds s*g, 1/(s*g) and x*r to fp32, so the exact quotient may sit up to three fp32
+    roundings (relative 2^-22 covers them) past a midpoint."""
+    rng = np.random.default_rng(6)
+    P, H, T, D = 8, 2, 16, 64
+    x = rng.normal(0, 1, (P, H, T, D)).astype(np.float32)
+    src = bf16_bits_of(x).reshape(P, H, T, D)
+    xb = bf16_from_bits(src).reshape(-1, 16).astype(np.float64)
+    g = oracle.global_scale(src, oracle.BF16, H, D, T)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H, D, T, g)
+    codes = unpack_codes(data).reshape(-1, 16)
+    s = np.array([oracle.e4m3_value(b) for b in scales.ravel()])
+    for i in range(xb.shape[0]):
+        if s[i] < 2.0 ** -6:
+            continue
+        y = xb[i] / (s[i] * g)
+        e = np.array([oracle.e2m1_value(c) for c in codes[i]])
+        a = np.abs(y)
+        gap = np.where(a < 2, 0.25, np.where(a < 4, 0.5, 1.0))
+        over = a > 6
+        slack = a * 2.0 ** -22
+        assert np.all(np.abs(y - e)[~over] <= (gap + slack)[~over])
+        assert np.all(a[over] - 6 <= 0.4 + slack[over])
+
+
+def test_layout_positions_and_page_ids():
+    """Block (page, head, token, block) of the source lands at the same position of the
+    destination page given by the page-id lists (layout [page][head][token][D/2], scales
+    [page][head][token][D/16]; element 2j in the low nibble)."""
+    H, T, D, P = 3, 4, 32, 5
+    NB = D // 16
+    src_ids = np.array([3, 0, 4, 1, 2], np.int32)
+    dst_ids = np.array([6, 2, 0, 5, 1], np.int32)
+    x = np.zeros((P, H, T, D), np.float32)
+    want_scale = np.zeros((7, H, T, NB), np.uint8)
+    want_pos = {}
+    for i in range(P):
+        for h in range(H):
+            for t in range(T):
+                for b in range(NB):
+                    sb = 1 + ((i * 37 + h * 11 + t * 5 + b * 3) % 125)
+                    k = (i + 2 * h + 3 * t + b) % 16
+                    x[src_ids[i], h, t, b * 16 + k] = 6.0 * oracle.e4m3_value(sb)
+                    want_scale[dst_ids[i], h, t, b] = sb
+                    want_pos[(int(dst_ids[i]), h, t, b)] = k
+    src = bf16_bits_of(x).reshape(P, H, T, D)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H, D, T, g=1.0, num_dst_pages=7,
+                                         src_page_ids=src_ids, dst_page_ids=dst_ids)
+    assert np.array_equal(scales, want_scale)
+    codes = unpack_codes(data)
+    for (p, h, t, b), k in want_pos.items():
+        blk = codes[p, h, t, b * 16:(b + 1) * 16]
+        assert blk[k] == 7 and np.all(np.delete(blk, k) == 0)
+    for p in (3, 4):  # pages nobody wrote stay zero
+        assert not data[p].any() and not scales[p].any()
+    # decode with the inverse gather restores the source page order
+    back = oracle.dequantize_pages(data, scales, H, D, T, g=1.0, src_page_ids=dst_ids,
+                                   dst_page_ids=src_ids, num_dst_pages=P)
+    assert np.array_equal(back, src)
+
+
+# ------------------------------------------------------------------------------------ decode
+
+def test_decode_against_ieee_fp32_arithmetic():
+    """BF16 output = bf16(fp32(e*s) * g), FP16 = fp16(...), FP8 = e4m3(fp32(v * fp32(g/o))):
+    checked against numpy float32 products and torch / numpy casts for random codes, scales,
+    g and output scale."""
+    rng = np.random.default_rng(7)
+    n = 4096
+    data = rng.integers(0, 256, (n // 16, 1, 1, 8), dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, (n // 16, 1, 1, 1), dtype=np.uint8)
+    codes = unpack_codes(data).reshape(-1)
+    sv = np.repeat(np.array([oracle.e4m3_value(b) for b in scales.ravel()]), 16)
+    v = np.array([oracle.e2m1_value(c) for c in codes]) * sv           # exact
+    for g in (np.float32(1.0), np.float32(0.3331), np.float32(1.7e-3)):
+        prod = v.astype(np.float32) * g                                # IEEE fp32 product
+        bf = oracle.dequantize_pages(data, scales, 1, 16, 1, float(g), oracle.BF16)
+        want = torch.from_numpy(prod).to(torch.bfloat16).view(torch.int16).numpy() \
+            .view(np.uint16)
+        assert np.array_equal(bf.reshape(-1), want)
+        h = oracle.dequantize_pages(data, scales, 1, 16, 1, float(g), oracle.FP16)
+        assert np.array_equal(h.reshape(-1), prod.astype(np.float16).view(np.uint16))
+        for o in (np.float32(1.0), np.float32(0.05)):
+            m = g / o
+            y = v.astype(np.float32) * m
+            f8 = oracle.dequantize_pages(data, scales, 1, 16, 1, float(g), oracle.FP8_E4M3,
+                                         out_scale=float(o))
+            ok = np.abs(y) < 464
+            want8 = torch.from_numpy(y[ok]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(f8.reshape(-1)[ok], want8)
+            sat = f8.reshape(-1)[~ok]
+            assert np.all((sat & 0x7F) == 0x7E)
+
+
+# ------------------------------------------------------------------------------ global scale
+
+def test_global_scale_rule():
+    H, D, T = 1, 16, 1
+    for amax, want in ((2688.0, 1.0), (5376.0, 2.0), (1.0, float(np.float32(1.0) /
+                                                                  np.float32(2688.0)))):
+        src = bf16_bits_of([[0.5, -amax] + [0.0] * 14]).reshape(1, 1, 1, 16)
+        assert oracle.global_scale(src, oracle.BF16, H, D, T) == want
+    zero = np.zeros((2, 1, 1, 16), np.uint16)
+    assert oracle.global_scale(zero, oracle.BF16, H, D, T) == 1.0
+    # FP8 source: x = e4m3 * src_scale
+    f8 = np.zeros((1, 1, 1, 16), np.uint8)
+    f8[0, 0, 0, 3] = 0xFE  # -448
+    assert oracle.global_scale(f8, oracle.FP8_E4M3, H, D, T, src_scale=6.0) == 1.0
+    # only listed pages count
+    src = bf16_bits_of([[1.0] * 16, [2688.0] * 16]).reshape(2, 1, 1, 16)
+    assert oracle.global_scale(src, oracle.BF16, H, D, T, src_page_ids=[0]) == \
+        float(np.float32(1.0) / np.float32(2688.0))
+
+
+def test_global_scale_maps_tensor_max_to_top_of_both_grids():
+    rng = np.random.default_rng(8)
+    x = rng.normal(0, 3, (4, 2, 8, 32)).astype(np.float32)
+    src = bf16_bits_of(x).reshape(x.shape)
+    g = oracle.global_scale(src, oracle.BF16, 2, 32, 8)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, 2, 32, 8, g)
+    flat = bf16_from_bits(src).reshape(-1, 16)
+    i = int(np.argmax(np.abs(flat).max(axis=1)))
+    assert scales.reshape(-1)[i] == 0x7E                               # 448
+    assert (unpack_codes(data).reshape(-1, 16)[i] & 7).max() == 7      # 6
+
+
+# ------------------------------------------------------------------------------ round trips
+
+def _trips(src, dtype, H, D, T, g, trips=4, src_scale=1.0):
+    """Values after 1..trips quantize/dequantize round trips in the source dtype."""
+    outs, cur, cur_scale = [], src, src_scale
+    for _ in range(trips):
+        data, scales = oracle.quantize_pages(cur, dtype, H, D, T, g, src_scale=cur_scale)
+        if dtype == oracle.FP8_E4M3:
+            cur = oracle.dequantize_pages(data, scales, H, D, T, g, oracle.FP8_E4M3,
+                                          out_scale=src_scale)
+        else:
+            cur = oracle.dequantize_pages(data, scales, H, D, T, g, dtype)
+        outs.append(cur)
+    return outs
+
+
+def _values(bits, dtype, scale=1.0):
+    if dtype == oracle.FP8_E4M3:
+        return np.array([oracle.e4m3_value(b) * scale for b in bits.ravel()])
+    if dtype == oracle.BF16:
+        return bf16_from_bits(bits).ravel().astype(np.float64)
+    return bits.ravel().view(np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", [oracle.BF16, oracle.FP16, oracle.FP8_E4M3])
+@pytest.mark.parametrize("g_mode", ["unit", "amax"])
+def test_round_trips_do_not_accumulate_error(dtype, g_mode):
+    """Every finite value of the source dtype, (i) alone in a block and (ii) among random
+    values, through 4 round trips ("KV Cache Compression in TensorRT LLM", Evaluation >
+    Accuracy, Figure 15: the distance to the original stays the one-trip quantization error and
+    the distance to the previous trip is zero from the second trip on).
+
+    Under the round-to-nearest scale pick this holds exactly for every block whose E4M3 block
+    scale is zero or a normal number. A block whose scale is subnormal (amax < 6 g 2^-6) may
+    move once more on trip 2 -- its maximum can encode to 4 instead of 6 on the coarse
+    subnormal scale grid, so trip 2 picks a finer scale -- and never after. The test asserts the
+    property on the first kind, and on the second that only subnormal-scale blocks move and
+    that nothing moves from trip 3 on."""
+    if dtype == oracle.FP8_E4M3:
+        pats = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)
+    else:
+        allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+        with np.errstate(invalid="ignore"):
+            vals = _values(allp, dtype)
+        pats = allp[np.isfinite(vals)]
+    n = len(pats)
+    nblk = -(-n // 16) * 16
+    alone = np.zeros((nblk, 16), pats.dtype)
+    alone[:n, 5] = pats                                            # one value per block
+    rng = np.random.default_rng(9)
+    mixed = np.zeros(nblk * 16, pats.dtype)
+    mixed[:n] = pats
+    mixed[n:] = pats[rng.integers(0, n, nblk * 16 - n)]
+    mixed = mixed[rng.permutation(nblk * 16)].reshape(nblk, 16)
+    for blocks in (alone, mixed):
+        src = blocks.reshape(nblk // 16, 1, 16, 16)
+        if g_mode == "unit":
+            g = 1.0
+        else:
+            g = oracle.global_scale(src, dtype, 1, 16, 16)
+        outs = _trips(src, dtype, 1, 16, 16, g)
+        _, sc1 = oracle.quantize_pages(src, dtype, 1, 16, 16, g)
+        s1 = np.array([oracle.e4m3_value(b) for b in range(256)])[sc1.reshape(-1)]
+        settled = (s1 == 0) | (s1 >= 2.0 ** -6)                    # zero or normal scale
+        x = _values(src, dtype).reshape(nblk, 16)
+        err = [np.abs(_values(o, dtype).reshape(nblk, 16) - x) for o in outs]
+        moved2 = (outs[1] != outs[0]).reshape(nblk, 16).any(axis=1)
+        assert not np.any(moved2 & settled), "a normal-scale block moved on trip 2"
+        assert np.all(s1[moved2] < 2.0 ** -6)
+        for k in range(1, 4):
+            assert np.array_equal(err[k][settled], err[0][settled])
+        for k in range(2, 4):
+            assert np.array_equal(outs[k], outs[k - 1]), f"trip {k + 1} moved"
+
+
+def test_fp8_and_fp16_sources_reduce_to_bf16_source():
+    """The encoder starts from the exact fp32 value of each element, so a FP8 source with a
+    power-of-two src_scale and a FP16 source holding the same values as a BF16 source must give
+    identical codes and scales (values chosen representable in all three)."""
+    rng = np.random.default_rng(13)
+    H, T, D, P = 2, 8, 32, 6
+    f8 = rng.integers(0, 0x7F, (P, H, T, D), dtype=np.uint8)
+    f8 |= (rng.integers(0, 2, f8.shape, dtype=np.uint8) << 7)
+    for src_scale in (1.0, 2.0 ** -5, 2.0 ** 3):
+        vals = np.array([oracle.e4m3_value(b) for b in range(256)])[f8] * src_scale
+        bf = bf16_bits_of(vals.tolist()).reshape(f8.shape)
+        assert np.array_equal(bf16_from_bits(bf), vals.astype(np.float32))
+        h16 = vals.astype(np.float16)
+        assert np.array_equal(h16.astype(np.float64), vals)
+        g = oracle.global_scale(bf, oracle.BF16, H, D, T)
+        assert oracle.global_scale(f8, oracle.FP8_E4M3, H, D, T, src_scale=src_scale) == g
+        want = oracle.quantize_pages(bf, oracle.BF16, H, D, T, g)
+        got8 = oracle.quantize_pages(f8, oracle.FP8_E4M3, H, D, T, g, src_scale=src_scale)
+        got16 = oracle.quantize_pages(h16.view(np.uint16), oracle.FP16, H, D, T, g)
+        for a, b in zip(want, got8):
+            assert np.array_equal(a, b)
+        for a, b in zip(want, got16):
+            assert np.array_equal(a, b)

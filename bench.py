@@ -1,0 +1,621 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 paged-KV hot path on GB300; prints one JSON line.
+
+A step is one pass of the whole path over one batch of synthetic input:
+  * page round-trip workload (4096 pages x 32 tokens x 8 KV heads x 128, K and V BF16 ~ N(0,1)
+    with 1% of blocks x1e3 and 1% x1e-3): tensor amax -> global scale, encode to NVFP4,
+    decode to BF16, decode to FP8 E4M3 (output scale amax/448), for K and for V;
+  * long-context decode workload (8 sequences of 32K-128K tokens, 64 query / 8 KV heads,
+    head_dim 128, 64-token pages, split-KV): paged GQA decode attention over the NVFP4 cache.
+`value` is the algorithmic HBM bytes of the step (what each kernel must read and write at
+minimum) divided by the step time, in GB/s, summed over ranks. Inputs are larger than the
+129 MB L2 and are not reused between kernels of a step except where the path itself reuses
+them; per-kernel numbers are taken separately with an L2 flush before each launch.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own batch (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GB = 1e9
+METRIC = "NVFP4 paged decode-attn KV GB/s + quant/dequant GB/s, % of GB300 HBM peak"
+WORKLOAD = ("page round-trip 4096x32x8x128 K+V (amax, encode, decode->BF16, decode->FP8) + "
+            "long-context decode 8 seqs U[32K,128K] 64q/8kv d128 page64 split-KV")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernels", action="store_true", help="skip per-kernel timings")
+    ap.add_argument("--ref-pages", type=int, default=256,
+                    help="reference arm: page round-trip pages per step")
+    ap.add_argument("--ref-max-tokens", type=int, default=0,
+                    help="reference arm: cap on the sampled sequence length (0 = none)")
+    ap.add_argument("--profile-case", default="",
+                    help="run only one kernel family a few times (for ncu): decode_batch | "
+                         "long_context | quantize | dequantize | dequantize_fp8 | amax")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() \
+        else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (SM clock, throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        smax = [num(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        loaded = [s for s in sm if math.isfinite(s)]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(x for x in smax if math.isfinite(x)) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- the path
+
+class Path:
+    """Device buffers of both workloads and the launches of one step."""
+
+    def __init__(self, kv, dev, seed):
+        import torch
+        import synthetic
+        self.kv, self.dev = kv, dev
+        # page round-trip workload
+        rt = synthetic.RoundTripWorkload(seed=seed)
+        self.rt = rt
+        self.k, self.v = rt.make(device=dev)
+        P, H, T, D = rt.P, rt.H, rt.T, rt.D
+        self.lay_rt = kv.Layout(H, D, T)
+        u8 = torch.uint8
+        self.rt_out = []
+        for _ in range(2):
+            self.rt_out.append(dict(
+                g=torch.empty(1, dtype=torch.float32, device=dev),
+                data=torch.empty((P, H, T, D // 2), dtype=u8, device=dev),
+                scales=torch.empty((P, H, T, D // 16), dtype=u8, device=dev),
+                bf16=torch.empty((P, H, T, D), dtype=torch.bfloat16, device=dev),
+                fp8=torch.empty((P, H, T, D), dtype=u8, device=dev),
+                fp8_scale=torch.empty(1, dtype=torch.float32, device=dev)))
+        self.gs_ws = torch.empty(kv.nvfp4_kv_global_scale_workspace_size(), dtype=u8,
+                                 device=dev)
+        for src, o in zip((self.k, self.v), self.rt_out):
+            # FP8 workspace scale amax / 448 (= 6 g), fixed per tensor at set-up
+            o["fp8_scale"].copy_(src.float().abs().max() / 448.0)
+        n_rt = P * H * T * D
+        self.bytes_rt = {
+            "amax": 2 * n_rt * 2,
+            "quantize": 2 * n_rt * (2 + 0.5625),
+            "dequantize_bf16": 2 * n_rt * (0.5625 + 2),
+            "dequantize_fp8": 2 * n_rt * (0.5625 + 1),
+        }
+        # long-context decode workload: NVFP4 cache built once by the encoder
+        wl = synthetic.long_context(seed=seed)
+        self.wl = wl
+        q, k, v, pt, sl = wl.make(device=dev)
+        self.lay_lc = kv.Layout(wl.H, wl.D, wl.T)
+        self.q, self.pt, self.sl = q, pt, sl
+        Pl = wl.pool_pages
+        mk = lambda w: torch.empty((Pl, wl.H, wl.T, w), dtype=u8, device=dev)  # noqa: E731
+        self.c_kd, self.c_ks, self.c_vd, self.c_vs = mk(wl.D // 2), mk(wl.D // 16), \
+            mk(wl.D // 2), mk(wl.D // 16)
+        self.c_gk = torch.empty(1, dtype=torch.float32, device=dev)
+        self.c_gv = torch.empty(1, dtype=torch.float32, device=dev)
+        kv.nvfp4_kv_compute_global_scale(self.lay_lc, k, self.c_gk, workspace=self.gs_ws)
+        kv.nvfp4_kv_compute_global_scale(self.lay_lc, v, self.c_gv, workspace=self.gs_ws)
+        kv.nvfp4_kv_quantize_pages(self.lay_lc, k, self.c_gk, self.c_kd, self.c_ks)
+        kv.nvfp4_kv_quantize_pages(self.lay_lc, v, self.c_gv, self.c_vd, self.c_vs)
+        del k, v
+        self.out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=dev)
+        wsb = kv.nvfp4_paged_decode_workspace_size(self.lay_lc, wl.B, wl.Hq, pt.shape[1], 0)
+        self.dec_ws = torch.empty(wsb, dtype=u8, device=dev)
+        kv_tokens = wl.kv_tokens
+        self.bytes_decode = (kv_tokens * wl.H * (wl.D + wl.D // 8) * 2      # K+V data+scales
+                             + wl.B * wl.Hq * wl.D * 2 * 2                   # q in, out
+                             + pt.numel() * 4 + wl.B * 4 + wl.B * wl.Hq * 4)  # table, lens, lse
+        self.decode_tokens = wl.B
+        self.launches_per_step = 2 * 2 + 2 + 2 + 2 + 2   # amax(2 kernels) x2, q x2, dq x4, dec 2
+        torch.cuda.synchronize()
+
+    # individual launches --------------------------------------------------------------
+    def amax(self, i):
+        src = (self.k, self.v)[i]
+        self.kv.nvfp4_kv_compute_global_scale(self.lay_rt, src, self.rt_out[i]["g"],
+                                              workspace=self.gs_ws)
+
+    def quantize(self, i):
+        o = self.rt_out[i]
+        self.kv.nvfp4_kv_quantize_pages(self.lay_rt, (self.k, self.v)[i], o["g"], o["data"],
+                                        o["scales"])
+
+    def dequantize_bf16(self, i):
+        o = self.rt_out[i]
+        self.kv.nvfp4_kv_dequantize_pages(self.lay_rt, o["data"], o["scales"], o["g"],
+                                          o["bf16"])
+
+    def dequantize_fp8(self, i):
+        o = self.rt_out[i]
+        self.kv.nvfp4_kv_dequantize_pages(self.lay_rt, o["data"], o["scales"], o["g"],
+                                          o["fp8"], dst_dtype=self.kv.FP8_E4M3,
+                                          dst_scale=o["fp8_scale"])
+
+    def decode(self):
+        wl = self.wl
+        self.kv.nvfp4_paged_decode_attention(
+            self.lay_lc, self.q, self.c_kd, self.c_ks, self.c_gk, self.c_vd, self.c_vs,
+            self.c_gv, self.pt, self.sl, wl.sm_scale, self.out, lse=self.lse,
+            workspace=self.dec_ws)
+
+    def step(self, dec_events=None):
+        for i in range(2):
+            self.amax(i)
+            self.quantize(i)
+            self.dequantize_bf16(i)
+            self.dequantize_fp8(i)
+        if dec_events is not None:
+            dec_events[0].record()
+        self.decode()
+        if dec_events is not None:
+            dec_events[1].record()
+
+    @property
+    def step_bytes(self):
+        return sum(self.bytes_rt.values()) + self.bytes_decode
+
+
+def time_kernel(fn, flush, reps=15):
+    """Median CUDA-event time (ms) of fn() with an L2 flush before each launch."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def kernel_table(path, peak):
+    """Per-kernel achieved GB/s (L2 flushed before every launch), plus the decode-batch
+    workload and the extend workload as extra single-kernel cases."""
+    import torch
+    import synthetic
+    kv, dev = path.kv, path.dev
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+
+    def add(name, fn, nbytes, launches, extra=None):
+        ms = time_kernel(fn, flush)
+        gbs = nbytes / (ms * 1e-3) / GB
+        d = {"ms": round(ms, 4), "bytes": int(nbytes), "GB_s": round(gbs, 1),
+             "frac_of_peak": round(gbs / peak, 4), "launches": launches}
+        if extra:
+            d.update(extra)
+        res[name] = d
+
+    n = path.rt.P * path.rt.H * path.rt.T * path.rt.D
+    add("amax_K (page round-trip)", lambda: path.amax(0), n * 2, 2)
+    add("quantize_K (page round-trip)", lambda: path.quantize(0), n * 2.5625, 1)
+    add("dequantize_K_bf16 (page round-trip)", lambda: path.dequantize_bf16(0), n * 2.5625, 1)
+    add("dequantize_K_fp8 (page round-trip)", lambda: path.dequantize_fp8(0), n * 1.5625, 1)
+    wl = path.wl
+    add("decode (long context)", path.decode, path.bytes_decode, 2,
+        {"kv_tokens": wl.kv_tokens})
+    res["decode (long context)"]["kv_tokens_per_s"] = round(
+        wl.kv_tokens / (res["decode (long context)"]["ms"] * 1e-3), 1)
+    # decode batch workload (32 x 8192 tokens, GQA 4)
+    db = synthetic.decode_batch(seed=1)
+    q, k, v, pt, sl = db.make(device=dev)
+    lay = kv.Layout(db.H, db.D, db.T)
+    u8 = torch.uint8
+    P = db.pool_pages
+    kd = torch.empty((P, db.H, db.T, db.D // 2), dtype=u8, device=dev)
+    ks = torch.empty((P, db.H, db.T, db.D // 16), dtype=u8, device=dev)
+    vd, vs = torch.empty_like(kd), torch.empty_like(ks)
+    gk = torch.empty(1, dtype=torch.float32, device=dev)
+    gv = torch.empty(1, dtype=torch.float32, device=dev)
+    kv.nvfp4_kv_compute_global_scale(lay, k, gk)
+    kv.nvfp4_kv_compute_global_scale(lay, v, gv)
+    kv.nvfp4_kv_quantize_pages(lay, k, gk, kd, ks)
+    kv.nvfp4_kv_quantize_pages(lay, v, gv, vd, vs)
+    del k, v
+    out = torch.empty((db.B, db.Hq, db.D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(kv.nvfp4_paged_decode_workspace_size(lay, db.B, db.Hq, pt.shape[1], 0),
+                     dtype=u8, device=dev)
+    nbytes = db.kv_tokens * db.H * (db.D + db.D // 8) * 2 + db.B * db.Hq * db.D * 4 + \
+        pt.numel() * 4 + db.B * 4
+    add("decode (decode batch 32x8192, GQA 4)",
+        lambda: kv.nvfp4_paged_decode_attention(lay, q, kd, ks, gk, vd, vs, gv, pt, sl,
+                                                db.sm_scale, out, workspace=ws),
+        nbytes, 2)
+    r = res["decode (decode batch 32x8192, GQA 4)"]
+    r["decode_tokens_per_s"] = round(db.B / (r["ms"] * 1e-3), 1)
+    r["kv_tokens_per_s"] = round(db.kv_tokens / (r["ms"] * 1e-3), 1)
+    del kd, ks, vd, vs, q, out, ws
+    # extend workload: gather + dequantize a 1024-page prefix into FP8, encode a 128-page chunk
+    ex = synthetic.ExtendWorkload(seed=2)
+    prefix, ept, chunk, chunk_dst = ex.make(device=dev)
+    lay = kv.Layout(ex.H, ex.D, ex.T)
+    pool = prefix.shape[0]
+    pd = torch.empty((pool, ex.H, ex.T, ex.D // 2), dtype=u8, device=dev)
+    ps = torch.empty((pool, ex.H, ex.T, ex.D // 16), dtype=u8, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    kv.nvfp4_kv_compute_global_scale(lay, prefix, g)
+    kv.nvfp4_kv_quantize_pages(lay, prefix, g, pd, ps)
+    ids = ept.reshape(-1).contiguous()
+    wsp = torch.empty((ids.numel(), ex.H, ex.T, ex.D), dtype=u8, device=dev)
+    per = ex.H * ex.T * ex.D
+    add("extend prefix gather->FP8 (1024 pages)",
+        lambda: kv.nvfp4_kv_dequantize_pages(lay, pd, ps, g, wsp, dst_dtype=kv.FP8_E4M3,
+                                             src_page_ids=ids),
+        ids.numel() * per * 1.5625 + ids.numel() * 4, 1)
+    add("extend chunk encode (128 pages)",
+        lambda: kv.nvfp4_kv_quantize_pages(lay, chunk, g, pd, ps, dst_page_ids=chunk_dst),
+        chunk.shape[0] * per * 2.5625 + chunk.shape[0] * 4, 1)
+    del flush
+    return res
+
+
+# ---------------------------------------------------------------------------- CPU baseline
+
+def oracle_sample(seed=0, pages=1024, decode_seqs=1, max_tokens=None):
+    """Run the oracle on a bounded sample of the same workload; returns (bytes, seconds,
+    threads, description)."""
+    import numpy as np
+    import torch
+    import oracle
+    import synthetic
+    rt = synthetic.RoundTripWorkload(P=pages, seed=seed)
+    k, _ = rt.make()
+    kb = synthetic.bf16_bits(k)
+    H, D, T = rt.H, rt.D, rt.T
+    n = kb.size
+    t0 = time.perf_counter()
+    g = oracle.global_scale(kb, oracle.BF16, H, D, T)
+    d, s = oracle.quantize_pages(kb, oracle.BF16, H, D, T, g)
+    oracle.dequantize_pages(d, s, H, D, T, g, oracle.BF16)
+    oracle.dequantize_pages(d, s, H, D, T, g, oracle.FP8_E4M3, out_scale=6 * g)
+    t_codec = time.perf_counter() - t0
+    codec_bytes = n * (2 + 2.5625 + 2.5625 + 1.5625)
+    # decode: the first `decode_seqs` sequences of the long-context workload, all 64 heads
+    wl = synthetic.long_context(seed=seed)
+    lens = wl.seq_lens[:decode_seqs]
+    if max_tokens:
+        lens = [min(L, max_tokens) for L in lens]
+    T2 = wl.T
+    dpages = sum(-(-L // T2) for L in lens)
+    g2 = synthetic.gen(seed + 7)
+    q = synthetic.randn_bf16((decode_seqs, wl.Hq, wl.D), g2)
+    kd = np.random.default_rng(seed).integers(0, 256, (dpages, wl.H, T2, wl.D // 2), np.uint8)
+    ks = np.random.default_rng(seed + 1).integers(0x20, 0x48, (dpages, wl.H, T2, wl.D // 16),
+                                                  np.uint8)
+    vd = np.random.default_rng(seed + 2).integers(0, 256, kd.shape, np.uint8)
+    vs = np.random.default_rng(seed + 3).integers(0x20, 0x48, ks.shape, np.uint8)
+    maxp = max(-(-L // T2) for L in lens)
+    pt = np.zeros((decode_seqs, maxp), np.int32)
+    off = 0
+    for b, L in enumerate(lens):
+        npg = -(-L // T2)
+        pt[b, :npg] = np.arange(off, off + npg)
+        off += npg
+    t0 = time.perf_counter()
+    oracle.paged_decode_attention(synthetic.bf16_bits(q), kd, ks, 0.01, vd, vs, 0.01, pt,
+                                  np.array(lens, np.int32), wl.sm_scale, wl.H, T2)
+    t_dec = time.perf_counter() - t0
+    dec_bytes = sum(lens) * wl.H * (wl.D + wl.D // 8) * 2
+    desc = (f"oracle on {rt.P} page round-trip pages of K (amax, encode, decode BF16 + FP8) and "
+            f"{decode_seqs} long-context sequence(s) ({sum(lens)} tokens, {wl.Hq} query heads)")
+    return codec_bytes + dec_bytes, t_codec + t_dec, oracle.max_threads(), desc
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    kw = dict(pages=args.ref_pages, decode_seqs=1, max_tokens=args.ref_max_tokens or None)
+    for _ in range(args.warmup):
+        oracle_sample(args.seed, **kw)
+    tot_b, tot_t = 0.0, 0.0
+    desc, thr = "", 1
+    for _ in range(args.steps):
+        b, t, thr, desc = oracle_sample(args.seed, **kw)
+        tot_b += b
+        tot_t += t
+    v = tot_b / tot_t / GB
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": desc},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": thr,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+# ---------------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the NVFP4 KV path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import nvfp4_paged_kv_gb300 as kv
+    from nvfp4_paged_kv_gb300 import build
+    build.build()
+    kv.load()
+    peak, peak_kind = peaks()
+
+    if args.profile_case:
+        profile_case(kv, dev, args.profile_case)
+        return
+
+    path = Path(kv, dev, args.seed + 1000 * rank)
+    for _ in range(args.warmup):
+        path.step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(args.steps):
+            path.step(ev[i])
+        end.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = dist_max(start.elapsed_time(end), world)
+    ms_step = ms_total / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    step_bytes = path.step_bytes
+    value = step_bytes * world / (ms_step * 1e-3) / GB
+    clocks = clk.summary()
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (129 MB)",
+                   "bytes_per_step_per_gpu": int(step_bytes),
+                   "frac_of_peak": round(value / world / peak, 4),
+                   "peak_GB_s": peak, "peak_kind": peak_kind,
+                   "long_context_seq_lens": path.wl.seq_lens},
+        "roofline": {"bound": "hbm", "kernel": "nvfp4_paged_decode_attention (split + combine)",
+                     "achieved": round(path.bytes_decode / (dec_ms * 1e-3) / GB, 1),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(path.bytes_decode / (dec_ms * 1e-3) / GB / peak, 4),
+                     "traffic": None, "peak_kind": peak_kind,
+                     "launch_ms": round(dec_ms, 4), "algorithmic_bytes": int(path.bytes_decode)},
+        "clocks": clocks,
+        "gpu_launches": path.launches_per_step * args.steps,
+    }
+    if not args.no_kernels and rank == 0:
+        result["kernels"] = kernel_table(path, peak)
+    if not args.no_e2e:
+        result["e2e"] = e2e(path, args, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, t, thr, desc = oracle_sample(args.seed, pages=1024, decode_seqs=1)
+        result["cpu_baseline"] = {"value": round(b / t / GB, 4), "unit": "GB/s", "cores": thr,
+                                  "kind": "oracle", "sample": desc,
+                                  "seconds": round(t, 2)}
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def e2e(path, args, world):
+    """Same metric through the public API with host buffers: every step copies its inputs from
+    pinned host memory and reads every result back."""
+    import torch
+    dev = path.dev
+    ins = [path.k, path.v, path.q, path.pt, path.sl, path.c_kd, path.c_ks, path.c_vd,
+           path.c_vs]
+    outs = [path.rt_out[i][key] for i in range(2)
+            for key in ("g", "data", "scales", "bf16", "fp8")] + [path.out, path.lse]
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def one():
+        for h, d in zip(h_in, ins):
+            d.copy_(h, non_blocking=True)
+        path.step()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    n = max(2, args.steps // 2)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = dist_max(a.elapsed_time(b), world) / n
+    return {"value": round(path.step_bytes * world / (ms * 1e-3) / GB, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 3)}
+
+
+def profile_case(kv, dev, case):
+    """A few launches of one kernel family on one workload, for ncu captures."""
+    import torch
+    import synthetic
+    u8 = torch.uint8
+    if case in ("decode_batch", "long_context"):
+        wl = synthetic.decode_batch() if case == "decode_batch" else synthetic.long_context()
+        q, k, v, pt, sl = wl.make(device=dev)
+        lay = kv.Layout(wl.H, wl.D, wl.T)
+        P = wl.pool_pages
+        kd = torch.empty((P, wl.H, wl.T, wl.D // 2), dtype=u8, device=dev)
+        ks = torch.empty((P, wl.H, wl.T, wl.D // 16), dtype=u8, device=dev)
+        vd, vs = torch.empty_like(kd), torch.empty_like(ks)
+        gk = torch.empty(1, dtype=torch.float32, device=dev)
+        gv = torch.empty(1, dtype=torch.float32, device=dev)
+        kv.nvfp4_kv_compute_global_scale(lay, k, gk)
+        kv.nvfp4_kv_compute_global_scale(lay, v, gv)
+        kv.nvfp4_kv_quantize_pages(lay, k, gk, kd, ks)
+        kv.nvfp4_kv_quantize_pages(lay, v, gv, vd, vs)
+        del k, v
+        out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
+        for _ in range(4):
+            kv.nvfp4_paged_decode_attention(lay, q, kd, ks, gk, vd, vs, gv, pt, sl,
+                                            wl.sm_scale, out)
+    else:
+        rt = synthetic.RoundTripWorkload()
+        k, _ = rt.make(device=dev)
+        lay = kv.Layout(rt.H, rt.D, rt.T)
+        g = torch.empty(1, dtype=torch.float32, device=dev)
+        d = torch.empty((rt.P, rt.H, rt.T, rt.D // 2), dtype=u8, device=dev)
+        s = torch.empty((rt.P, rt.H, rt.T, rt.D // 16), dtype=u8, device=dev)
+        kv.nvfp4_kv_compute_global_scale(lay, k, g)
+        kv.nvfp4_kv_quantize_pages(lay, k, g, d, s)
+        for _ in range(4):
+            if case == "quantize":
+                kv.nvfp4_kv_quantize_pages(lay, k, g, d, s)
+            elif case == "dequantize":
+                kv.nvfp4_kv_dequantize_pages(lay, d, s, g, k)
+            elif case == "dequantize_fp8":
+                o = torch.empty(k.shape, dtype=u8, device=dev)
+                kv.nvfp4_kv_dequantize_pages(lay, d, s, g, o, dst_dtype=kv.FP8_E4M3)
+            else:
+                kv.nvfp4_kv_compute_global_scale(lay, k, g)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": case, "ok": True}))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * nvfp4_kv.h -- C ABI of libnvfp4kv.so: NVFP4 paged KV cache codec and paged decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * NVFP4 stores each K/V value as a 4-bit E2M1 code, with one E4M3 scale per block of 16 values
+ * and one FP32 scale per tensor ("Accelerating Long-Context and Agentic Inference with NVFP4 KV
+ * Cache", LMSYS blog: introduction and Figure 1; "KV Cache Compression in TensorRT LLM", NVIDIA:
+ * "NVFP4 Cold-Page Compression", Figure 6). A block of 16 values takes 8 bytes of packed codes
+ * plus 1 byte of scale (LMSYS, "NVFP4 KV Decode Attention Kernel Implementation").
+ *
+ * ------------------------------------------------------------------------------------------
+ * Page layout (one K or V tensor of one layer; all buffers caller-owned device memory)
+ *   H = layout.num_kv_heads, T = layout.page_size (tokens), D = layout.head_dim (D % 16 == 0)
+ *   packed data  : uint8 [pool_pages][H][T][D/2]   element 2j in the low nibble of byte j,
+ *                                                  element 2j+1 in the high nibble
+ *   block scales : uint8 [pool_pages][H][T][D/16]  E4M3 bit patterns; block b of a token covers
+ *                                                  elements 16b .. 16b+15 of its head_dim
+ *   16/8-bit pages (BF16 / FP16 / FP8 E4M3 sources and outputs): [pool_pages][H][T][D]
+ *   The two NVFP4 pools are read together by attention (TensorRT LLM page, Figure 6: "two pools").
+ *
+ * Numerics (all bit-exact and reproducible; g is the FP32 tensor scale):
+ *   encode  a = max |x| over the block; s = E4M3_rne_satfinite(fp32(a / fp32(6 g)));
+ *           r = fp32(1 / fp32(s g)) (0 if s g == 0); code_i = E2M1_rne_satfinite(fp32(x_i r)),
+ *           sign kept (a negative value rounding to zero is code 0x8). FP8 sources are first
+ *           widened to x = fp32(e4m3 * src_scale).
+ *   decode  v = e2m1(code) * e4m3(s) (exact); BF16/FP16 out = round_rne(fp32(v g));
+ *           FP8 out = E4M3_rne_satfinite(fp32(v fp32(g / dst_scale))).
+ *   global scale  g = fp32(amax / 2688) (2688 = 448 * 6 maps the tensor maximum to the top of
+ *           both grids); g = 1 when that is zero. A caller may pass any positive g (the LMSYS
+ *           page's experiments use 1.0, "Limitations and Ongoing Items").
+ *
+ * Conventions shared by every call:
+ *   - Every pointer except `layout` is device memory owned by the caller; the library never
+ *     allocates, frees or synchronises. Work is enqueued on `stream` (may be 0) and returns
+ *     without waiting; scalars that come from earlier GPU work (global scales) are passed by
+ *     device pointer so a sequence of calls needs no host round trip.
+ *   - The return value reports host-side validation (NVFP4KV_ERR_INVALID_ARG /
+ *     NVFP4KV_ERR_UNSUPPORTED / NVFP4KV_ERR_WORKSPACE) and launch failures (NVFP4KV_ERR_CUDA).
+ *     On an error nothing is enqueued.
+ *   - Data-dependent faults found on the device (a page id outside [0, pool_pages), a sequence
+ *     length outside [0, max_pages_per_seq * T], a pipeline wait that ran out) are OR-ed into the
+ *     caller's `status` word (optional, int32 device memory, NVFP4KV_STATUS_* bits); the
+ *     offending page / sequence is skipped and nothing traps. The caller clears the word.
+ *   - Buffers must be 16-byte aligned; sources and destinations must not overlap.
+ *   - Inputs must be finite. Unused slots of a page (past the end of a sequence) are never read
+ *     by attention; the codec encodes every slot of every listed page.
+ */
+#ifndef NVFP4_KV_H_
+#define NVFP4_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* nvfp4kv_stream_t;
+
+typedef enum nvfp4kv_status {
+    NVFP4KV_OK = 0,
+    NVFP4KV_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size or enum value        */
+    NVFP4KV_ERR_UNSUPPORTED = 2,  /* valid but not implemented shape (e.g. head_dim 96 decode) */
+    NVFP4KV_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than required          */
+    NVFP4KV_ERR_CUDA = 4          /* a CUDA launch or runtime call failed                     */
+} nvfp4kv_status;
+
+/* Bits OR-ed into the optional device status word. */
+#define NVFP4KV_STATUS_PAGE_OOB 0x1      /* a page id was outside [0, pool_pages): skipped        */
+#define NVFP4KV_STATUS_BAD_SEQ_LEN 0x2   /* seq_len < 0 or > max_pages_per_seq * T: seq skipped   */
+#define NVFP4KV_STATUS_TIMEOUT 0x4       /* a copy-completion wait exceeded its limit: unit skipped */
+
+typedef enum nvfp4kv_dtype {
+    NVFP4KV_BF16 = 0,
+    NVFP4KV_FP16 = 1,
+    NVFP4KV_FP8_E4M3 = 2
+} nvfp4kv_dtype;
+
+/* Geometry of one paged K or V tensor. head_dim % 16 == 0; all fields > 0. */
+typedef struct nvfp4kv_layout {
+    int32_t num_kv_heads; /* H */
+    int32_t head_dim;     /* D */
+    int32_t page_size;    /* T, tokens per page */
+} nvfp4kv_layout;
+
+/* Human-readable name of a status value (static storage). */
+const char* nvfp4kv_status_string(nvfp4kv_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t nvfp4kv_version(void);
+
+/* ------------------------------------------------------------------------------------------
+ * Tensor scale. g = fp32(amax / 2688) over every slot of the listed pages, 1.0 when that is 0.
+ * The calibrated per-tensor FP32 scale of NVFP4's two-level scaling (LMSYS page, introduction;
+ * "Limitations and Ongoing Items": calibration of the FP32 global scale may reduce overflow and
+ * underflow).
+ *   src            pages of src_dtype, [src_pool_pages][H][T][D]
+ *   src_page_ids   [num_pages] page ids into src (NULL = 0 .. num_pages-1)
+ *   src_scale      FP8 sources only: device scalar, x = fp32(e4m3 * src_scale) (NULL = 1)
+ *   global_scale_out  device float written with g
+ *   workspace      device scratch of nvfp4_kv_global_scale_workspace_size() bytes
+ * num_pages == 0 writes g = 1.
+ * ------------------------------------------------------------------------------------------ */
+size_t nvfp4_kv_global_scale_workspace_size(void);
+
+nvfp4kv_status nvfp4_kv_compute_global_scale(const nvfp4kv_layout* layout,
+                                             nvfp4kv_dtype src_dtype, const void* src,
+                                             int32_t src_pool_pages,
+                                             const int32_t* src_page_ids, int32_t num_pages,
+                                             const float* src_scale, float* global_scale_out,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Encode pages to NVFP4 (block amax -> E4M3 scale pick -> E2M1 round-to-nearest-even -> pack).
+ * LMSYS page, "Path 1: Initial prefill" and "Path 2: Chunked prefill / Extend" (the current
+ * K/V is quantized and written into the NVFP4 cache); TensorRT LLM page, "How It Works"
+ * ("Encode and decode, fused with the copy": a batch of pages per call, on the caller's stream).
+ *   src / src_page_ids / src_pool_pages   as above (BF16, FP16 or FP8 E4M3 pages)
+ *   src_scale      FP8 sources: device scalar (NULL = 1); ignored for 16-bit sources
+ *   global_scale   device scalar g (> 0)
+ *   dst_data, dst_scales  NVFP4 pools [dst_pool_pages][H][T][D/2] and [..][D/16]
+ *   dst_page_ids   [num_pages] destination page ids (NULL = 0 .. num_pages-1)
+ * Listed page i goes from src page src_page_ids[i] to dst page dst_page_ids[i]. Two entries
+ * naming the same destination page race.
+ * ------------------------------------------------------------------------------------------ */
+nvfp4kv_status nvfp4_kv_quantize_pages(const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype,
+                                       const void* src, int32_t src_pool_pages,
+                                       const int32_t* src_page_ids, const float* src_scale,
+                                       const float* global_scale, uint8_t* dst_data,
+                                       uint8_t* dst_scales, int32_t dst_pool_pages,
+                                       const int32_t* dst_page_ids, int32_t num_pages,
+                                       int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Decode NVFP4 pages to BF16 / FP16 pages, or to FP8 E4M3 pages (the FP8 workspace the
+ * extend path gathers the cached prefix into: LMSYS page, "Path 2: Chunked prefill / Extend";
+ * the onboard decode of the TensorRT LLM page, "How It Works").
+ *   src_data, src_scales, src_pool_pages, src_page_ids   NVFP4 pools and the pages to read
+ *   global_scale   device scalar g of the tensor
+ *   dst_dtype      NVFP4KV_BF16, NVFP4KV_FP16 or NVFP4KV_FP8_E4M3
+ *   dst            [dst_pool_pages][H][T][D] of dst_dtype
+ *   dst_page_ids   destination pages (NULL = 0 .. num_pages-1: a gather into consecutive slots)
+ *   dst_scale      FP8 output only: device scalar, y = value / dst_scale (NULL = 1)
+ * ------------------------------------------------------------------------------------------ */
+nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uint8_t* src_data,
+                                         const uint8_t* src_scales, int32_t src_pool_pages,
+                                         const int32_t* src_page_ids, const float* global_scale,
+                                         nvfp4kv_dtype dst_dtype, void* dst,
+                                         int32_t dst_pool_pages, const int32_t* dst_page_ids,
+                                         const float* dst_scale, int32_t num_pages,
+                                         int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Paged GQA decode attention reading NVFP4 K/V directly from the cache (LMSYS page, "Path 3:
+ * Decode" and "NVFP4 KV Decode Attention Kernel Implementation", Figure 3: BF16 queries, packed
+ * K/V tiles and their E4M3 block scales staged in shared memory, e2m1x2 conversion in
+ * registers, scales applied with packed multiplies, tensor-core matmuls, the global K/V scales
+ * folded into the attention scaling).
+ *
+ * For query head qh of sequence b, with KV head h = qh / (num_q_heads / num_kv_heads), token t
+ * at page page_table[b][t / T], slot t % T, and k_t, v_t the decoded values times g_K, g_V:
+ *   out[b][qh] = sum_t softmax_t(sm_scale * q . k_t) v_t        (BF16, round to nearest even)
+ *   lse[b][qh] = log(sum_t exp(sm_scale * q . k_t))              (natural log; optional)
+ * A sequence of length 0 gives out = 0 and lse = -inf.
+ *
+ * Long sequences are cut into at most max_num_splits chunks (split-KV); each chunk produces a
+ * partial (max, sum, unnormalised output) in the workspace and a second kernel merges them.
+ *   q              BF16 [batch][num_q_heads][D]
+ *   k_data, k_scales, v_data, v_scales   NVFP4 pools [pool_pages][H][T][..]
+ *   k_global_scale, v_global_scale       device scalars g_K, g_V
+ *   page_table     int32 [batch][max_pages_per_seq] device
+ *   seq_lens       int32 [batch] device; 0 <= seq_len <= max_pages_per_seq * T
+ *   sm_scale       softmax scale (e.g. 1/sqrt(D))
+ *   max_num_splits 0 = automatic, else 1..64
+ *   workspace      device scratch of nvfp4_paged_decode_workspace_size(...) bytes
+ *   out            BF16 [batch][num_q_heads][D]
+ *   lse            float [batch][num_q_heads] or NULL
+ * Supported: head_dim 64, 128 or 256; 1 <= num_q_heads / num_kv_heads <= 8 (and
+ * num_q_heads % num_kv_heads == 0); page_size % 16 == 0.
+ * ------------------------------------------------------------------------------------------ */
+size_t nvfp4_paged_decode_workspace_size(const nvfp4kv_layout* layout, int32_t batch,
+                                         int32_t num_q_heads, int32_t max_pages_per_seq,
+                                         int32_t max_num_splits);
+
+nvfp4kv_status nvfp4_paged_decode_attention(
+    const nvfp4kv_layout* layout, int32_t batch, int32_t num_q_heads, const void* q,
+    const uint8_t* k_data, const uint8_t* k_scales, const float* k_global_scale,
+    const uint8_t* v_data, const uint8_t* v_scales, const float* v_global_scale,
+    int32_t pool_pages, const int32_t* page_table, int32_t max_pages_per_seq,
+    const int32_t* seq_lens, float sm_scale, int32_t max_num_splits, void* workspace,
+    size_t workspace_bytes, void* out, float* lse, int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * The two roundings of the encoder on their own, for exhaustive verification over fp32 inputs:
+ * target 0 writes E2M1 codes (RNE, satfinite at 6, sign kept, one code per byte), target 1
+ * writes E4M3 bytes (RNE, satfinite at 448, sign kept). x: n finite floats; out: n bytes.
+ * ------------------------------------------------------------------------------------------ */
+nvfp4kv_status nvfp4_kv_round_f32(const float* x, size_t n, int32_t target, uint8_t* out,
+                                  nvfp4kv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_KV_H_ */

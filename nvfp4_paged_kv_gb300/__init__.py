@@ -1,0 +1,238 @@
+"""NVFP4 paged KV cache for GB300: Python binding of ``libnvfp4kv.so``.
+
+Every call here is argument marshalling around the C ABI declared in ``include/nvfp4_kv.h``:
+tensors become device pointers, the current torch stream becomes the stream argument, and a
+non-OK status becomes an exception. All arithmetic runs in the library's CUDA kernels; there is
+no CPU path, and importing a function whose library is not built raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "Layout", "BF16", "FP16", "FP8_E4M3", "STATUS_PAGE_OOB", "STATUS_BAD_SEQ_LEN",
+    "STATUS_TIMEOUT", "NVFP4KVError", "load", "lib_path", "version",
+    "nvfp4_kv_global_scale_workspace_size", "nvfp4_kv_compute_global_scale",
+    "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages",
+    "nvfp4_paged_decode_workspace_size", "nvfp4_paged_decode_attention", "nvfp4_kv_round_f32",
+]
+
+BF16, FP16, FP8_E4M3 = 0, 1, 2
+STATUS_PAGE_OOB, STATUS_BAD_SEQ_LEN, STATUS_TIMEOUT = 0x1, 0x2, 0x4
+_STATUS_NAMES = {1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA"}
+
+
+class Layout(ctypes.Structure):
+    """Geometry of one paged K or V tensor (``nvfp4kv_layout``)."""
+    _fields_ = [("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32)]
+
+    def __init__(self, num_kv_heads: int, head_dim: int, page_size: int):
+        super().__init__(int(num_kv_heads), int(head_dim), int(page_size))
+
+    def __repr__(self):
+        return (f"Layout(num_kv_heads={self.num_kv_heads}, head_dim={self.head_dim}, "
+                f"page_size={self.page_size})")
+
+
+class NVFP4KVError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {code})")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libnvfp4kv.so; raise if it has not been built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                f"{_build.LIB} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_build.LIB)
+        P, I32, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        LP = ctypes.POINTER(Layout)
+        sigs = {
+            "nvfp4kv_status_string": (ctypes.c_char_p, [I32]),
+            "nvfp4kv_version": (I32, []),
+            "nvfp4_kv_global_scale_workspace_size": (SZ, []),
+            "nvfp4_kv_compute_global_scale": (I32, [LP, I32, P, I32, P, I32, P, P, P, SZ, P, P]),
+            "nvfp4_kv_quantize_pages": (I32, [LP, I32, P, I32, P, P, P, P, P, I32, P, I32, P, P]),
+            "nvfp4_kv_dequantize_pages": (I32, [LP, P, P, I32, P, P, I32, P, I32, P, P, I32, P,
+                                                P]),
+            "nvfp4_paged_decode_workspace_size": (SZ, [LP, I32, I32, I32, I32]),
+            "nvfp4_paged_decode_attention": (I32, [LP, I32, I32, P, P, P, P, P, P, P, I32, P,
+                                                   I32, P, F, I32, P, SZ, P, P, P, P]),
+            "nvfp4_kv_round_f32": (I32, [P, SZ, I32, P, P]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def version() -> int:
+    return load().nvfp4kv_version()
+
+
+# ------------------------------------------------------------------------------ marshalling
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor, got {type(t)}")
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the NVFP4 KV library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the NVFP4 KV library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        msg = load().nvfp4kv_status_string(code).decode()
+        raise NVFP4KVError(fn, code, msg)
+
+
+def _dtype_code(t: torch.Tensor, explicit: Optional[int]) -> int:
+    if explicit is not None:
+        return int(explicit)
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return FP16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return FP8_E4M3
+    raise TypeError(f"unsupported page dtype {t.dtype}")
+
+
+def _ids(t: Optional[torch.Tensor]):
+    if t is not None and t.dtype != torch.int32:
+        raise TypeError("page id lists must be int32")
+    return _ptr(t)
+
+
+# ------------------------------------------------------------------------------ entry points
+
+def nvfp4_kv_global_scale_workspace_size() -> int:
+    return int(load().nvfp4_kv_global_scale_workspace_size())
+
+
+def nvfp4_kv_compute_global_scale(layout: Layout, src: torch.Tensor, out: torch.Tensor, *,
+                                  src_dtype=None, src_page_ids=None, num_pages=None,
+                                  src_scale=None, workspace=None, status=None, stream=None):
+    """out[0] = fp32(amax / 2688) over the listed pages of `src` ([pool, H, T, D])."""
+    lib = load()
+    if num_pages is None:
+        num_pages = src_page_ids.numel() if src_page_ids is not None else src.shape[0]
+    if workspace is None:
+        workspace = torch.empty(nvfp4_kv_global_scale_workspace_size(), dtype=torch.uint8,
+                                device=src.device)
+    code = lib.nvfp4_kv_compute_global_scale(
+        ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
+        _ids(src_page_ids), int(num_pages), _ptr(src_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    _check("nvfp4_kv_compute_global_scale", code)
+    return out
+
+
+def nvfp4_kv_quantize_pages(layout: Layout, src: torch.Tensor, global_scale: torch.Tensor,
+                            dst_data: torch.Tensor, dst_scales: torch.Tensor, *,
+                            src_dtype=None, src_page_ids=None, dst_page_ids=None,
+                            num_pages=None, src_scale=None, status=None, stream=None):
+    """Encode pages of `src` into the NVFP4 pools (dst_data [pool,H,T,D/2] u8,
+    dst_scales [pool,H,T,D/16] u8)."""
+    lib = load()
+    if num_pages is None:
+        num_pages = src_page_ids.numel() if src_page_ids is not None else src.shape[0]
+    code = lib.nvfp4_kv_quantize_pages(
+        ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
+        _ids(src_page_ids), _ptr(src_scale), _ptr(global_scale), _ptr(dst_data),
+        _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), int(num_pages), _ptr(status),
+        _stream(stream))
+    _check("nvfp4_kv_quantize_pages", code)
+
+
+def nvfp4_kv_dequantize_pages(layout: Layout, src_data: torch.Tensor, src_scales: torch.Tensor,
+                              global_scale: torch.Tensor, dst: torch.Tensor, *, dst_dtype=None,
+                              src_page_ids=None, dst_page_ids=None, num_pages=None,
+                              dst_scale=None, status=None, stream=None):
+    """Decode NVFP4 pages into `dst` ([pool, H, T, D] of BF16 / FP16 / FP8 E4M3)."""
+    lib = load()
+    if num_pages is None:
+        num_pages = src_page_ids.numel() if src_page_ids is not None else src_data.shape[0]
+    code = lib.nvfp4_kv_dequantize_pages(
+        ctypes.byref(layout), _ptr(src_data), _ptr(src_scales), src_data.shape[0],
+        _ids(src_page_ids), _ptr(global_scale), _dtype_code(dst, dst_dtype), _ptr(dst),
+        dst.shape[0], _ids(dst_page_ids), _ptr(dst_scale), int(num_pages), _ptr(status),
+        _stream(stream))
+    _check("nvfp4_kv_dequantize_pages", code)
+
+
+def nvfp4_paged_decode_workspace_size(layout: Layout, batch: int, num_q_heads: int,
+                                      max_pages_per_seq: int, max_num_splits: int = 0) -> int:
+    return int(load().nvfp4_paged_decode_workspace_size(
+        ctypes.byref(layout), int(batch), int(num_q_heads), int(max_pages_per_seq),
+        int(max_num_splits)))
+
+
+def nvfp4_paged_decode_attention(layout: Layout, q: torch.Tensor, k_data, k_scales,
+                                 k_global_scale, v_data, v_scales, v_global_scale,
+                                 page_table: torch.Tensor, seq_lens: torch.Tensor,
+                                 sm_scale: float, out: torch.Tensor, *, lse=None,
+                                 max_num_splits: int = 0, workspace=None, status=None,
+                                 stream=None):
+    """out[b, qh] = softmax(sm_scale q.K^T) V over the sequence's NVFP4 pages (BF16)."""
+    lib = load()
+    B, Hq, _ = q.shape
+    maxp = page_table.shape[1]
+    if workspace is None:
+        need = nvfp4_paged_decode_workspace_size(layout, B, Hq, maxp, max_num_splits)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("page_table and seq_lens must be int32")
+    code = lib.nvfp4_paged_decode_attention(
+        ctypes.byref(layout), B, Hq, _ptr(q), _ptr(k_data), _ptr(k_scales),
+        _ptr(k_global_scale), _ptr(v_data), _ptr(v_scales), _ptr(v_global_scale),
+        k_data.shape[0], _ptr(page_table), maxp, _ptr(seq_lens), float(sm_scale),
+        int(max_num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    _check("nvfp4_paged_decode_attention", code)
+    return out
+
+
+def nvfp4_kv_round_f32(x: torch.Tensor, target: int, out: torch.Tensor, stream=None):
+    """target 0: E2M1 codes, target 1: E4M3 bytes, of fp32 inputs (one byte each)."""
+    code = load().nvfp4_kv_round_f32(_ptr(x), x.numel(), int(target), _ptr(out),
+                                     _stream(stream))
+    _check("nvfp4_kv_round_f32", code)

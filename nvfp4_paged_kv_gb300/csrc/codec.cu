@@ -1,0 +1,572 @@
+// NVFP4 page codec for sm_103a: encode (quantize), decode (dequantize to BF16 / FP16 / FP8) and
+// the tensor amax -> global scale reduction.
+//
+// Format: 4-bit E2M1 values, one E4M3 scale per 16-value block, one FP32 scale per tensor
+// ("Accelerating Long-Context and Agentic Inference with NVFP4 KV Cache", LMSYS: introduction,
+// Figure 1; "KV Cache Compression in TensorRT LLM", NVIDIA: "NVFP4 Cold-Page Compression",
+// Figure 6). Encode and decode run on a batch of pages per call on the caller's stream, as the
+// TensorRT LLM codec does ("How It Works": the cache manager calls the codec with batches of
+// pages on its own stream); the extend path's FP8 workspace fill is the FP8-output decode
+// (LMSYS, "Path 2: Chunked prefill / Extend").
+//
+// All three kernels stream HBM once: every byte of input is loaded with one coalesced vector
+// load (256-bit for 16-bit pages), every byte of output is written once, nothing is staged
+// through shared memory because no value is reused. Work is cut into (page, chunk-of-blocks)
+// items so that small batches still fill all SMs; the page id is read once per item.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "host_util.h"
+
+namespace nvfp4kv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBlocksPerThread = 4;                      // 16-value blocks per thread per item
+constexpr int kItemBlocks = kThreads * kBlocksPerThread; // blocks per work item
+
+// ------------------------------------------------------------------------------------------
+// Streaming loads / stores
+// ------------------------------------------------------------------------------------------
+struct U8x32 {
+    uint32_t w[8];
+};
+
+__device__ __forceinline__ U8x32 ld_stream_32B(const void* p) {
+    U8x32 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                   "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_stream_16B(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_4B(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_1B(const void* p) {
+    uint16_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// ------------------------------------------------------------------------------------------
+// Encode one block of 16 exact fp32 values.
+//   a  = max |x_i|                                  (exact)
+//   s  = E4M3_rne_satfinite(fp32(a / d)), d = fp32(6 g)   -- one IEEE division
+//   r  = fp32(1 / fp32(s g)), or 0 when s g == 0            -- one IEEE reciprocal
+//   c_i = E2M1_rne_satfinite(fp32(x_i * r)), sign kept
+// Packed codes: element 2j in the low nibble of byte j.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void encode_block16(const float (&x)[16], float g, float d,
+                                               uint32_t& w0, uint32_t& w1, uint32_t& sbyte) {
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(x[k]));
+    const float q = __fdiv_rn(a, d);
+    sbyte = f32x2_to_e4m3x2(q, 0.0f) & 0xFFu;
+    const float s = e4m3_to_f32(sbyte);
+    const float sg = __fmul_rn(s, g);
+    const float r = (sg == 0.0f) ? 0.0f : __frcp_rn(sg);
+    w0 = 0u;
+    w1 = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w0 |= f32x2_to_e2m1x2(__fmul_rn(x[2 * j], r), __fmul_rn(x[2 * j + 1], r)) << (8 * j);
+        w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r))
+              << (8 * j);
+    }
+}
+
+struct QuantParams {
+    const void* src;
+    const int32_t* src_ids;
+    const float* src_scale;
+    const float* g;
+    uint8_t* dst_data;
+    uint8_t* dst_scales;
+    const int32_t* dst_ids;
+    int32_t src_pool;
+    int32_t dst_pool;
+    int32_t num_pages;
+    int32_t bpp;            // 16-value blocks per page = H * T * D / 16
+    int32_t items_per_page; // ceil(bpp / kItemBlocks)
+    int32_t* status;
+};
+
+// SRC: NVFP4KV_BF16, NVFP4KV_FP16 or NVFP4KV_FP8_E4M3. A32: the 16-bit source is 32-byte
+// aligned, so each block is one 256-bit load (else two 128-bit loads).
+template <int SRC, bool A32>
+__global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantParams p) {
+    const float g = __ldg(p.g);
+    const float d = __fmul_rn(6.0f, g);
+    const float sscale = (SRC == NVFP4KV_FP8_E4M3 && p.src_scale) ? __ldg(p.src_scale) : 1.0f;
+    const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
+    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int32_t i = static_cast<int32_t>(item / p.items_per_page);
+        const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
+        const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
+        const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
+        if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool) {
+            if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+            continue;
+        }
+        const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
+        const int64_t dst_blk0 = static_cast<int64_t>(dp) * p.bpp;
+        const int32_t blk_begin = k * kItemBlocks + threadIdx.x;
+
+        if constexpr (SRC == NVFP4KV_FP8_E4M3) {
+            uint4 raw[kBlocksPerThread];
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t blk = blk_begin + u * kThreads;
+                if (blk < p.bpp)
+                    raw[u] = ld_stream_16B(static_cast<const uint8_t*>(p.src) +
+                                           (src_blk0 + blk) * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t blk = blk_begin + u * kThreads;
+                if (blk >= p.bpp) continue;
+                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+                float x[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t lo = e4m3x2_to_f16x2(wv[j] & 0xFFFFu);
+                    const uint32_t hi = e4m3x2_to_f16x2(wv[j] >> 16);
+                    x[4 * j + 0] = __fmul_rn(f16_lo(lo), sscale);
+                    x[4 * j + 1] = __fmul_rn(f16_hi(lo), sscale);
+                    x[4 * j + 2] = __fmul_rn(f16_lo(hi), sscale);
+                    x[4 * j + 3] = __fmul_rn(f16_hi(hi), sscale);
+                }
+                uint32_t w0, w1, sb;
+                encode_block16(x, g, d, w0, w1, sb);
+                *reinterpret_cast<uint2*>(p.dst_data + (dst_blk0 + blk) * 8) = make_uint2(w0, w1);
+                p.dst_scales[dst_blk0 + blk] = static_cast<uint8_t>(sb);
+            }
+        } else {
+            U8x32 raw[kBlocksPerThread];
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t blk = blk_begin + u * kThreads;
+                if (blk < p.bpp) {
+                    const uint8_t* a = static_cast<const uint8_t*>(p.src) + (src_blk0 + blk) * 32;
+                    if constexpr (A32) {
+                        raw[u] = ld_stream_32B(a);
+                    } else {
+                        const uint4 lo = ld_stream_16B(a), hi = ld_stream_16B(a + 16);
+                        raw[u] = U8x32{{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w}};
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t blk = blk_begin + u * kThreads;
+                if (blk >= p.bpp) continue;
+                float x[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if constexpr (SRC == NVFP4KV_BF16) {
+                        x[2 * j] = bf16_lo(raw[u].w[j]);
+                        x[2 * j + 1] = bf16_hi(raw[u].w[j]);
+                    } else {
+                        x[2 * j] = f16_lo(raw[u].w[j]);
+                        x[2 * j + 1] = f16_hi(raw[u].w[j]);
+                    }
+                }
+                uint32_t w0, w1, sb;
+                encode_block16(x, g, d, w0, w1, sb);
+                *reinterpret_cast<uint2*>(p.dst_data + (dst_blk0 + blk) * 8) = make_uint2(w0, w1);
+                p.dst_scales[dst_blk0 + blk] = static_cast<uint8_t>(sb);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Decode. One thread turns half a block (8 codes = 4 bytes, plus the block's scale byte) into
+// 8 outputs. v = e2m1(c) * e4m3(s) is formed exactly in FP16 (cvt.rn.f16x2.e2m1x2 and
+// cvt.rn.f16x2.e4m3x2 are exact, and the product has at most 6 significant bits), widened to
+// fp32 exactly, multiplied by g (BF16 / FP16 out) or m = fp32(g / dst_scale) (FP8 out) with
+// one IEEE fp32 multiply, and rounded to the output type to nearest even (FP8 saturating).
+// ------------------------------------------------------------------------------------------
+struct DequantParams {
+    const uint8_t* src_data;
+    const uint8_t* src_scales;
+    const int32_t* src_ids;
+    const float* g;
+    const float* dst_scale;
+    void* dst;
+    const int32_t* dst_ids;
+    int32_t src_pool;
+    int32_t dst_pool;
+    int32_t num_pages;
+    int32_t bpp;            // blocks per page
+    int32_t items_per_page; // ceil(2 * bpp / kItemBlocks)
+    int32_t* status;
+};
+
+template <int DST>
+__global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const DequantParams p) {
+    const float g = __ldg(p.g);
+    const float mult = (DST == NVFP4KV_FP8_E4M3)
+                           ? (p.dst_scale ? __fdiv_rn(g, __ldg(p.dst_scale)) : g)
+                           : g;
+    const int32_t units = 2 * p.bpp; // half blocks per page
+    const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
+    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int32_t i = static_cast<int32_t>(item / p.items_per_page);
+        const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
+        const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
+        const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
+        if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool) {
+            if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+            continue;
+        }
+        const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
+        const int64_t dst_unit0 = static_cast<int64_t>(dp) * units;
+        const int32_t u_begin = k * kItemBlocks + threadIdx.x;
+        uint32_t code[kBlocksPerThread], sbyte[kBlocksPerThread];
+#pragma unroll
+        for (int u = 0; u < kBlocksPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit < units) {
+                code[u] = ld_stream_4B(p.src_data + (src_blk0 * 2 + unit) * 4);
+                sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + (unit >> 1));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBlocksPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit >= units) continue;
+            const uint32_t s2 = e4m3x2_to_f16x2(sbyte[u] * 0x0101u); // (s, s)
+            float y[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t v2 = hmul2_u32(e2m1x2_to_f16x2(code[u] >> (8 * j)), s2);
+                y[2 * j] = __fmul_rn(f16_lo(v2), mult);
+                y[2 * j + 1] = __fmul_rn(f16_hi(v2), mult);
+            }
+            if constexpr (DST == NVFP4KV_FP8_E4M3) {
+                uint2 o;
+                o.x = f32x2_to_e4m3x2(y[0], y[1]) | (f32x2_to_e4m3x2(y[2], y[3]) << 16);
+                o.y = f32x2_to_e4m3x2(y[4], y[5]) | (f32x2_to_e4m3x2(y[6], y[7]) << 16);
+                *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.dst) + (dst_unit0 + unit) * 8) =
+                    o;
+            } else {
+                uint4 o;
+                if constexpr (DST == NVFP4KV_BF16) {
+                    o.x = pack_bf16x2(y[0], y[1]);
+                    o.y = pack_bf16x2(y[2], y[3]);
+                    o.z = pack_bf16x2(y[4], y[5]);
+                    o.w = pack_bf16x2(y[6], y[7]);
+                } else {
+                    o.x = pack_f16x2(y[0], y[1]);
+                    o.y = pack_f16x2(y[2], y[3]);
+                    o.z = pack_f16x2(y[4], y[5]);
+                    o.w = pack_f16x2(y[6], y[7]);
+                }
+                *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) +
+                                          (dst_unit0 + unit) * 16) = o;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Tensor amax and global scale. Non-negative IEEE values order like their bit patterns, so the
+// maximum of |x| is taken on the sign-cleared 16-bit (BF16 / FP16) or 8-bit (FP8) patterns with
+// SIMD unsigned maxima; one partial per CTA goes to the workspace and a one-CTA kernel
+// finishes: g = fp32(amax / 2688), or 1 when that is 0. For FP8 sources the maximum of
+// fp32(e4m3 * src_scale) is fp32(max|e4m3| * |src_scale|) because rounding is monotone.
+// ------------------------------------------------------------------------------------------
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxMaxCtas = 1024;
+constexpr int kAmaxLoads = 4;   // 16-byte loads per thread per item
+
+struct AmaxParams {
+    const void* src;
+    const int32_t* src_ids;
+    int32_t src_pool;
+    int32_t num_pages;
+    int64_t page_bytes;   // bytes of one page (a multiple of 16)
+    int32_t items_per_page;
+    int32_t item_bytes;   // kAmaxThreads * 16 * kAmaxLoads
+    uint32_t* partial;    // [gridDim.x] max pattern per CTA
+    int32_t* status;
+};
+
+template <int SRC>
+__global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) {
+    const uint32_t mask = (SRC == NVFP4KV_FP8_E4M3) ? 0x7F7F7F7Fu : 0x7FFF7FFFu;
+    uint32_t m = 0u;
+    const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
+    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int32_t i = static_cast<int32_t>(item / p.items_per_page);
+        const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
+        const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
+        if (sp < 0 || sp >= p.src_pool) {
+            if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+            continue;
+        }
+        const uint8_t* base = static_cast<const uint8_t*>(p.src) + sp * p.page_bytes;
+        const int64_t off0 = static_cast<int64_t>(k) * p.item_bytes + threadIdx.x * 16;
+        uint4 raw[kAmaxLoads];
+        bool ok[kAmaxLoads];
+#pragma unroll
+        for (int u = 0; u < kAmaxLoads; ++u) {
+            const int64_t off = off0 + static_cast<int64_t>(u) * kAmaxThreads * 16;
+            ok[u] = off < p.page_bytes;
+            if (ok[u]) raw[u] = ld_stream_16B(base + off);
+        }
+#pragma unroll
+        for (int u = 0; u < kAmaxLoads; ++u) {
+            if (!ok[u]) continue;
+            const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if constexpr (SRC == NVFP4KV_FP8_E4M3)
+                    m = __vmaxu4(m, wv[j] & mask);
+                else
+                    m = __vmaxu2(m, wv[j] & mask);
+            }
+        }
+    }
+    // combine the lanes of the packed maximum, then reduce over the CTA
+    if constexpr (SRC == NVFP4KV_FP8_E4M3) {
+        m = max(max(m & 0xFFu, (m >> 8) & 0xFFu), max((m >> 16) & 0xFFu, m >> 24));
+    } else {
+        m = max(m & 0xFFFFu, m >> 16);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __shared__ uint32_t red[kAmaxThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = 0u;
+        for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
+        p.partial[blockIdx.x] = r;
+    }
+}
+
+template <int SRC>
+__global__ void global_scale_finish_kernel(const uint32_t* partial, int32_t n,
+                                           const float* src_scale, float* out) {
+    uint32_t m = 0u;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, partial[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __shared__ uint32_t red[32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = 0u;
+        for (int w = 0; w < (blockDim.x + 31) / 32; ++w) r = max(r, red[w]);
+        float amax;
+        if constexpr (SRC == NVFP4KV_FP8_E4M3) {
+            const float e = e4m3_to_f32(r);
+            amax = __fmul_rn(e, fabsf(src_scale ? *src_scale : 1.0f));
+        } else if constexpr (SRC == NVFP4KV_BF16) {
+            amax = __uint_as_float(r << 16);
+        } else {
+            amax = __half2float(__ushort_as_half(static_cast<uint16_t>(r)));
+        }
+        const float g = __fdiv_rn(amax, 2688.0f);
+        *out = (g == 0.0f) ? 1.0f : g;
+    }
+}
+
+__global__ void write_one_kernel(float* out) { *out = 1.0f; }
+
+// ------------------------------------------------------------------------------------------
+// The encoder's two roundings on their own (exhaustive verification over fp32 inputs).
+// ------------------------------------------------------------------------------------------
+__global__ void round_f32_kernel(const float* x, size_t n, int32_t target, uint8_t* out) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const float v = x[i];
+        out[i] = static_cast<uint8_t>(target == 0 ? (f32x2_to_e2m1x2(v, 0.0f) & 0xFu)
+                                                  : (f32x2_to_e4m3x2(v, 0.0f) & 0xFFu));
+    }
+}
+
+int grid_for(int64_t items, int ctas_per_sm) {
+    const int64_t cap = static_cast<int64_t>(num_sms()) * ctas_per_sm;
+    return static_cast<int>(items < cap ? (items < 1 ? 1 : items) : cap);
+}
+
+}  // namespace
+}  // namespace nvfp4kv
+
+using namespace nvfp4kv;
+
+extern "C" size_t nvfp4_kv_global_scale_workspace_size(void) {
+    return static_cast<size_t>(kAmaxMaxCtas) * sizeof(uint32_t);
+}
+
+extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
+    const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype, const void* src,
+    int32_t src_pool_pages, const int32_t* src_page_ids, int32_t num_pages,
+    const float* src_scale, float* global_scale_out, void* workspace, size_t workspace_bytes,
+    int32_t* status, nvfp4kv_stream_t stream) {
+    if (!layout_ok(layout) || !dtype_ok(src_dtype) || !global_scale_out || num_pages < 0 ||
+        src_pool_pages < 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (num_pages == 0) {
+        write_one_kernel<<<1, 1, 0, s>>>(global_scale_out);
+        return launch_status();
+    }
+    if (!src || !aligned16(src)) return NVFP4KV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < nvfp4_kv_global_scale_workspace_size() ||
+        !aligned16(workspace))
+        return NVFP4KV_ERR_WORKSPACE;
+    const int64_t elems = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
+                          layout->head_dim;
+    AmaxParams p{};
+    p.src = src;
+    p.src_ids = src_page_ids;
+    if (!src_page_ids && src_pool_pages < num_pages) return NVFP4KV_ERR_INVALID_ARG;
+    p.src_pool = src_pool_pages;
+    p.num_pages = num_pages;
+    p.page_bytes = elems * static_cast<int64_t>(dtype_bytes(src_dtype));
+    p.item_bytes = kAmaxThreads * 16 * kAmaxLoads;
+    p.items_per_page = static_cast<int32_t>((p.page_bytes + p.item_bytes - 1) / p.item_bytes);
+    p.partial = static_cast<uint32_t*>(workspace);
+    p.status = status;
+    int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 4);
+    if (grid > kAmaxMaxCtas) grid = kAmaxMaxCtas;
+    switch (src_dtype) {
+    case NVFP4KV_BF16:
+        amax_kernel<NVFP4KV_BF16><<<grid, kAmaxThreads, 0, s>>>(p);
+        global_scale_finish_kernel<NVFP4KV_BF16><<<1, 1024, 0, s>>>(p.partial, grid, src_scale,
+                                                                    global_scale_out);
+        break;
+    case NVFP4KV_FP16:
+        amax_kernel<NVFP4KV_FP16><<<grid, kAmaxThreads, 0, s>>>(p);
+        global_scale_finish_kernel<NVFP4KV_FP16><<<1, 1024, 0, s>>>(p.partial, grid, src_scale,
+                                                                    global_scale_out);
+        break;
+    default:
+        amax_kernel<NVFP4KV_FP8_E4M3><<<grid, kAmaxThreads, 0, s>>>(p);
+        global_scale_finish_kernel<NVFP4KV_FP8_E4M3><<<1, 1024, 0, s>>>(
+            p.partial, grid, src_scale, global_scale_out);
+        break;
+    }
+    return launch_status();
+}
+
+extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
+    const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype, const void* src,
+    int32_t src_pool_pages, const int32_t* src_page_ids, const float* src_scale,
+    const float* global_scale, uint8_t* dst_data, uint8_t* dst_scales, int32_t dst_pool_pages,
+    const int32_t* dst_page_ids, int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream) {
+    if (!layout_ok(layout) || !dtype_ok(src_dtype) || num_pages < 0 || src_pool_pages < 0 ||
+        dst_pool_pages < 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (num_pages == 0) return NVFP4KV_OK;
+    if (!src || !global_scale || !dst_data || !dst_scales || !aligned16(src) ||
+        !aligned16(dst_data) || !aligned16(dst_scales))
+        return NVFP4KV_ERR_INVALID_ARG;
+    // without id lists the pages are 0..num_pages-1 and the pools must hold them
+    if ((!src_page_ids && src_pool_pages < num_pages) ||
+        (!dst_page_ids && dst_pool_pages < num_pages))
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
+                          (layout->head_dim / 16);
+    if (bpp64 > (int64_t{1} << 30)) return NVFP4KV_ERR_UNSUPPORTED;
+    QuantParams p{};
+    p.src = src;
+    p.src_ids = src_page_ids;
+    p.src_scale = src_scale;
+    p.g = global_scale;
+    p.dst_data = dst_data;
+    p.dst_scales = dst_scales;
+    p.dst_ids = dst_page_ids;
+    p.src_pool = src_pool_pages;
+    p.dst_pool = dst_pool_pages;
+    p.num_pages = num_pages;
+    p.bpp = static_cast<int32_t>(bpp64);
+    p.items_per_page = (p.bpp + kItemBlocks - 1) / kItemBlocks;
+    p.status = status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
+    const bool a32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
+    switch (src_dtype) {
+    case NVFP4KV_BF16:
+        if (a32) quantize_pages_kernel<NVFP4KV_BF16, true><<<grid, kThreads, 0, s>>>(p);
+        else quantize_pages_kernel<NVFP4KV_BF16, false><<<grid, kThreads, 0, s>>>(p);
+        break;
+    case NVFP4KV_FP16:
+        if (a32) quantize_pages_kernel<NVFP4KV_FP16, true><<<grid, kThreads, 0, s>>>(p);
+        else quantize_pages_kernel<NVFP4KV_FP16, false><<<grid, kThreads, 0, s>>>(p);
+        break;
+    default: quantize_pages_kernel<NVFP4KV_FP8_E4M3, false><<<grid, kThreads, 0, s>>>(p); break;
+    }
+    return launch_status();
+}
+
+extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
+    const nvfp4kv_layout* layout, const uint8_t* src_data, const uint8_t* src_scales,
+    int32_t src_pool_pages, const int32_t* src_page_ids, const float* global_scale,
+    nvfp4kv_dtype dst_dtype, void* dst, int32_t dst_pool_pages, const int32_t* dst_page_ids,
+    const float* dst_scale, int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream) {
+    if (!layout_ok(layout) || !dtype_ok(dst_dtype) || num_pages < 0 || src_pool_pages < 0 ||
+        dst_pool_pages < 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (num_pages == 0) return NVFP4KV_OK;
+    if (!src_data || !src_scales || !global_scale || !dst || !aligned16(src_data) ||
+        !aligned16(src_scales) || !aligned16(dst))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if ((!src_page_ids && src_pool_pages < num_pages) ||
+        (!dst_page_ids && dst_pool_pages < num_pages))
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
+                          (layout->head_dim / 16);
+    if (bpp64 > (int64_t{1} << 29)) return NVFP4KV_ERR_UNSUPPORTED;
+    DequantParams p{};
+    p.src_data = src_data;
+    p.src_scales = src_scales;
+    p.src_ids = src_page_ids;
+    p.g = global_scale;
+    p.dst_scale = dst_scale;
+    p.dst = dst;
+    p.dst_ids = dst_page_ids;
+    p.src_pool = src_pool_pages;
+    p.dst_pool = dst_pool_pages;
+    p.num_pages = num_pages;
+    p.bpp = static_cast<int32_t>(bpp64);
+    p.items_per_page = (2 * p.bpp + kItemBlocks - 1) / kItemBlocks;
+    p.status = status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
+    switch (dst_dtype) {
+    case NVFP4KV_BF16: dequantize_pages_kernel<NVFP4KV_BF16><<<grid, kThreads, 0, s>>>(p); break;
+    case NVFP4KV_FP16: dequantize_pages_kernel<NVFP4KV_FP16><<<grid, kThreads, 0, s>>>(p); break;
+    default: dequantize_pages_kernel<NVFP4KV_FP8_E4M3><<<grid, kThreads, 0, s>>>(p); break;
+    }
+    return launch_status();
+}
+
+extern "C" nvfp4kv_status nvfp4_kv_round_f32(const float* x, size_t n, int32_t target,
+                                             uint8_t* out, nvfp4kv_stream_t stream) {
+    if ((target != 0 && target != 1) || (n > 0 && (!x || !out))) return NVFP4KV_ERR_INVALID_ARG;
+    if (n == 0) return NVFP4KV_OK;
+    const int64_t blocks = static_cast<int64_t>((n + 255) / 256);
+    round_f32_kernel<<<grid_for(blocks, 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        x, n, target, out);
+    return launch_status();
+}

@@ -1,0 +1,48 @@
+// Host-side helpers shared by the C-ABI entry points: validation, device properties, launch
+// error mapping. No device code here.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4_kv.h"
+
+namespace nvfp4kv {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool layout_ok(const nvfp4kv_layout* l) {
+    return l && l->num_kv_heads > 0 && l->head_dim > 0 && l->page_size > 0 &&
+           (l->head_dim % 16) == 0;
+}
+
+inline bool dtype_ok(int32_t d) {
+    return d == NVFP4KV_BF16 || d == NVFP4KV_FP16 || d == NVFP4KV_FP8_E4M3;
+}
+
+inline size_t dtype_bytes(int32_t d) { return d == NVFP4KV_FP8_E4M3 ? 1 : 2; }
+
+// Streaming multiprocessor count of the current device (cached per device id).
+inline int num_sms() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+inline nvfp4kv_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? NVFP4KV_OK : NVFP4KV_ERR_CUDA;
+}
+
+}  // namespace nvfp4kv

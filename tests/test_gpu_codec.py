@@ -1,0 +1,257 @@
+"""GPU parity of the NVFP4 codec against the CPU oracle: bit-exact codes, scales, decoded
+values and global scales, through the C ABI.
+
+Cases span several CUDA work items and ragged tails (page counts and block counts that are not
+multiples of the kernels' item sizes), every source / output dtype, page-id gathers and
+scatters, the full page round-trip workload (4096 pages x 32 tokens x 8 heads x 128) and the
+extend workload (a 1024-page prefix gathered into an FP8 workspace plus a 512-token chunk per
+sequence quantized into new pages)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kv(cuda):
+    from nvfp4_paged_kv_gb300 import build
+    build.build()
+    import nvfp4_paged_kv_gb300 as m
+    m.load()
+    return m
+
+
+def _src_bits(t: torch.Tensor):
+    if t.dtype == torch.bfloat16 or t.dtype == torch.float16:
+        return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().contiguous().view(torch.uint8).numpy()
+
+
+def _odt(t: torch.Tensor):
+    return {torch.bfloat16: oracle.BF16, torch.float16: oracle.FP16}.get(t.dtype,
+                                                                        oracle.FP8_E4M3)
+
+
+def _make_src(kind, P, H, T, D, seed):
+    g = synthetic.gen(seed)
+    if kind == "bf16":
+        return synthetic.outlier_blocks_bf16(P, H, T, D, g)
+    if kind == "fp16":
+        return synthetic.outlier_blocks_bf16(P, H, T, D, g, big=30.0, small=1e-2).to(
+            torch.float16)
+    return synthetic.random_fp8_bytes((P, H, T, D), g)
+
+
+def _scalar(x, dev):
+    return torch.tensor([x], dtype=torch.float32, device=dev)
+
+
+# ------------------------------------------------------------------------------ roundings
+
+@pytest.mark.slow
+@pytest.mark.parametrize("target", [0, 1])
+def test_rounding_exhaustive_fp32(kv, cuda, target):
+    """Every finite fp32 bit pattern through the encoder's E2M1 (target 0) and E4M3 (target 1)
+    rounding, GPU against the oracle, bit for bit."""
+    chunk = 1 << 28
+    x_dev = torch.empty(chunk, dtype=torch.int32, device=cuda)
+    out_dev = torch.empty(chunk, dtype=torch.uint8, device=cuda)
+    base = np.arange(chunk, dtype=np.uint32)
+    for k in range(1 << 4):
+        start = k * chunk
+        torch.arange(start, start + chunk, dtype=torch.int64, device=cuda).to(torch.int32,
+                                                                               out=x_dev)
+        kv.nvfp4_kv_round_f32(x_dev.view(torch.float32), target, out_dev)
+        got = out_dev.cpu().numpy()
+        xs = (base + np.uint32(start)).view(np.float32)
+        fin = np.isfinite(xs)
+        want = (oracle.e2m1_encode_f32 if target == 0 else oracle.e4m3_encode_f32)(
+            np.where(fin, xs, np.float32(0)))
+        bad = np.nonzero((got != want) & fin)[0]
+        assert bad.size == 0, [(hex(int(base[i]) + start), got[i], want[i]) for i in bad[:8]]
+
+
+# ------------------------------------------------------------------------------ encode
+
+@pytest.mark.parametrize("kind", ["bf16", "fp16", "fp8"])
+@pytest.mark.parametrize("shape", [(7, 3, 5, 48), (33, 8, 32, 128), (5, 2, 64, 256),
+                                   (1, 1, 1, 16), (300, 2, 16, 64)])
+@pytest.mark.parametrize("ids", [False, True])
+def test_quantize_parity(kv, cuda, kind, shape, ids):
+    P, H, T, D = shape
+    src = _make_src(kind, P, H, T, D, seed=P + D)
+    lay = kv.Layout(H, D, T)
+    rng = np.random.default_rng(P * 7 + D)
+    src_scale = 0.37 if kind == "fp8" else 1.0
+    sbits = _src_bits(src)
+    if ids:
+        n = max(1, P - 2)
+        sid = rng.permutation(P)[:n].astype(np.int32)
+        did = rng.permutation(P + 3)[:n].astype(np.int32)
+        npool = P + 3
+    else:
+        n, sid, did, npool = P, None, None, P
+    g = oracle.global_scale(sbits, _odt(src), H, D, T, src_page_ids=sid, src_scale=src_scale)
+    want_d, want_s = oracle.quantize_pages(sbits, _odt(src), H, D, T, g, num_dst_pages=npool,
+                                           src_page_ids=sid, dst_page_ids=did,
+                                           src_scale=src_scale)
+    src_dev = src.to(cuda)
+    gs = torch.empty(1, dtype=torch.float32, device=cuda)
+    ss = _scalar(src_scale, cuda) if kind == "fp8" else None
+    sid_t = None if sid is None else torch.from_numpy(sid).to(cuda)
+    did_t = None if did is None else torch.from_numpy(did).to(cuda)
+    kv.nvfp4_kv_compute_global_scale(lay, src_dev, gs, src_page_ids=sid_t, src_scale=ss,
+                                     src_dtype=kv.FP8_E4M3 if kind == "fp8" else None)
+    assert gs.item() == np.float32(g)
+    data = torch.zeros((npool, H, T, D // 2), dtype=torch.uint8, device=cuda)
+    scales = torch.zeros((npool, H, T, D // 16), dtype=torch.uint8, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kv.nvfp4_kv_quantize_pages(lay, src_dev, gs, data, scales, src_page_ids=sid_t,
+                               dst_page_ids=did_t, src_scale=ss, status=status,
+                               src_dtype=kv.FP8_E4M3 if kind == "fp8" else None)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert np.array_equal(scales.cpu().numpy(), want_s)
+    assert np.array_equal(data.cpu().numpy(), want_d)
+
+
+# ------------------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("out_kind", ["bf16", "fp16", "fp8"])
+@pytest.mark.parametrize("shape", [(9, 3, 16, 48), (40, 8, 32, 128), (1, 1, 1, 16)])
+def test_dequantize_parity(kv, cuda, out_kind, shape):
+    P, H, T, D = shape
+    rng = np.random.default_rng(P + H + D)
+    data = rng.integers(0, 256, (P, H, T, D // 2), dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, (P, H, T, D // 16), dtype=np.uint8)  # every finite scale
+    g = float(np.float32(0.0731))
+    out_scale = float(np.float32(0.25)) if out_kind == "fp8" else 1.0
+    odt = {"bf16": oracle.BF16, "fp16": oracle.FP16, "fp8": oracle.FP8_E4M3}[out_kind]
+    sid = rng.permutation(P).astype(np.int32)
+    did = rng.permutation(P + 2)[:P].astype(np.int32)
+    want = oracle.dequantize_pages(data, scales, H, D, T, g, odt, num_dst_pages=P + 2,
+                                   src_page_ids=sid, dst_page_ids=did, out_scale=out_scale)
+    lay = kv.Layout(H, D, T)
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8": torch.uint8}[out_kind]
+    dst = torch.zeros((P + 2, H, T, D), dtype=tdt, device=cuda)
+    kv.nvfp4_kv_dequantize_pages(
+        lay, torch.from_numpy(data).to(cuda), torch.from_numpy(scales).to(cuda),
+        _scalar(g, cuda), dst, src_page_ids=torch.from_numpy(sid).to(cuda),
+        dst_page_ids=torch.from_numpy(did).to(cuda),
+        dst_scale=_scalar(out_scale, cuda) if out_kind == "fp8" else None,
+        dst_dtype=odt)
+    got = dst.cpu().contiguous()
+    got = got.view(torch.int16).numpy().view(np.uint16) if out_kind != "fp8" else got.numpy()
+    assert np.array_equal(got, want)
+
+
+def test_page_roundtrip_workload_full_size(kv, cuda):
+    """4096 pages x 32 tokens x 8 KV heads x 128, K and V ~ N(0,1) BF16 with 1% of blocks x1e3
+    and 1% x1e-3; g = amax/(448*6) per tensor; encode, decode to BF16 and to FP8 E4M3 (output
+    scale amax/448). Every byte against the oracle."""
+    wl = synthetic.RoundTripWorkload()
+    k, v = wl.make(device=cuda)
+    lay = kv.Layout(wl.H, wl.D, wl.T)
+    for t in (k, v):
+        bits = _src_bits(t)
+        g = oracle.global_scale(bits, oracle.BF16, wl.H, wl.D, wl.T)
+        amax = oracle.tensor_amax(bits, oracle.BF16, wl.H, wl.D, wl.T)
+        out_scale = float(np.float32(amax) / np.float32(448.0))
+        wd, wsc = oracle.quantize_pages(bits, oracle.BF16, wl.H, wl.D, wl.T, g)
+        gs = torch.empty(1, dtype=torch.float32, device=cuda)
+        kv.nvfp4_kv_compute_global_scale(lay, t, gs)
+        assert gs.item() == np.float32(g)
+        data = torch.empty((wl.P, wl.H, wl.T, wl.D // 2), dtype=torch.uint8, device=cuda)
+        scales = torch.empty((wl.P, wl.H, wl.T, wl.D // 16), dtype=torch.uint8, device=cuda)
+        kv.nvfp4_kv_quantize_pages(lay, t, gs, data, scales)
+        assert np.array_equal(scales.cpu().numpy(), wsc)
+        assert np.array_equal(data.cpu().numpy(), wd)
+        back = torch.empty_like(t)
+        kv.nvfp4_kv_dequantize_pages(lay, data, scales, gs, back)
+        want_b = oracle.dequantize_pages(wd, wsc, wl.H, wl.D, wl.T, g, oracle.BF16)
+        assert np.array_equal(_src_bits(back), want_b)
+        f8 = torch.empty(t.shape, dtype=torch.uint8, device=cuda)
+        kv.nvfp4_kv_dequantize_pages(lay, data, scales, gs, f8, dst_dtype=kv.FP8_E4M3,
+                                     dst_scale=_scalar(out_scale, cuda))
+        want_f = oracle.dequantize_pages(wd, wsc, wl.H, wl.D, wl.T, g, oracle.FP8_E4M3,
+                                         out_scale=out_scale)
+        assert np.array_equal(f8.cpu().numpy(), want_f)
+        del data, scales, back, f8
+
+
+def test_extend_workload(kv, cuda):
+    """16 sequences: a 4096-token NVFP4 prefix each, gathered by page table and dequantized into
+    a contiguous FP8 E4M3 workspace, and a 512-token BF16 chunk each quantized into new pages of
+    the same pool."""
+    wl = synthetic.ExtendWorkload()
+    prefix, pt, chunk, chunk_dst = wl.make(device=cuda)
+    lay = kv.Layout(wl.H, wl.D, wl.T)
+    pool = prefix.shape[0]
+    pbits = _src_bits(prefix)
+    g = oracle.global_scale(pbits, oracle.BF16, wl.H, wl.D, wl.T)
+    pool_d, pool_s = oracle.quantize_pages(pbits, oracle.BF16, wl.H, wl.D, wl.T, g)
+    gs = _scalar(g, cuda)
+    data = torch.from_numpy(pool_d).to(cuda)
+    scales = torch.from_numpy(pool_s).to(cuda)
+    ids = pt.reshape(-1).contiguous()
+    ws = torch.empty((ids.numel(), wl.H, wl.T, wl.D), dtype=torch.uint8, device=cuda)
+    kv.nvfp4_kv_dequantize_pages(lay, data, scales, gs, ws, dst_dtype=kv.FP8_E4M3,
+                                 src_page_ids=ids)
+    want = oracle.dequantize_pages(pool_d, pool_s, wl.H, wl.D, wl.T, g, oracle.FP8_E4M3,
+                                   src_page_ids=ids.cpu().numpy())
+    assert np.array_equal(ws.cpu().numpy(), want)
+    # the current chunk goes into the free pages of the pool (same tensor scale)
+    kv.nvfp4_kv_quantize_pages(lay, chunk, gs, data, scales, dst_page_ids=chunk_dst)
+    cd = chunk_dst.cpu().numpy()
+    wd, wsc = oracle.quantize_pages(_src_bits(chunk), oracle.BF16, wl.H, wl.D, wl.T, g,
+                                    num_dst_pages=pool, dst_page_ids=cd)
+    got_d, got_s = data.cpu().numpy(), scales.cpu().numpy()
+    assert np.array_equal(got_d[cd], wd[cd]) and np.array_equal(got_s[cd], wsc[cd])
+    untouched = np.setdiff1d(np.arange(pool), cd)
+    assert np.array_equal(got_d[untouched], pool_d[untouched])
+
+
+# ------------------------------------------------------------------------------ faults
+
+def test_out_of_range_page_ids_are_flagged_and_skipped(kv, cuda):
+    P, H, T, D = 6, 2, 16, 64
+    src = _make_src("bf16", P, H, T, D, seed=3).to(cuda)
+    lay = kv.Layout(H, D, T)
+    gs = _scalar(0.5, cuda)
+    sid = torch.tensor([0, 1, 99, 3, -1, 5], dtype=torch.int32, device=cuda)
+    data = torch.zeros((P, H, T, D // 2), dtype=torch.uint8, device=cuda)
+    scales = torch.zeros((P, H, T, D // 16), dtype=torch.uint8, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kv.nvfp4_kv_quantize_pages(lay, src, gs, data, scales, src_page_ids=sid, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & kv.STATUS_PAGE_OOB
+    wd, wsc = oracle.quantize_pages(_src_bits(src), oracle.BF16, H, D, T, 0.5)
+    got = data.cpu().numpy()
+    for i in (0, 1, 3, 5):
+        assert np.array_equal(got[i], wd[i])
+    assert not got[2].any() and not got[4].any()
+    status.zero_()
+    dst = torch.zeros_like(src)
+    kv.nvfp4_kv_dequantize_pages(lay, data, scales, gs, dst, dst_page_ids=sid, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & kv.STATUS_PAGE_OOB
+    status.zero_()
+    kv.nvfp4_kv_compute_global_scale(lay, src, gs, src_page_ids=sid, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & kv.STATUS_PAGE_OOB
+
+
+def test_zero_pages_and_zero_tensor(kv, cuda):
+    lay = kv.Layout(2, 32, 16)
+    gs = torch.zeros(1, dtype=torch.float32, device=cuda)
+    empty = torch.zeros((0, 2, 16, 32), dtype=torch.bfloat16, device=cuda)
+    kv.nvfp4_kv_compute_global_scale(lay, empty, gs)
+    assert gs.item() == 1.0
+    z = torch.zeros((3, 2, 16, 32), dtype=torch.bfloat16, device=cuda)
+    gs.zero_()
+    kv.nvfp4_kv_compute_global_scale(lay, z, gs)
+    assert gs.item() == 1.0

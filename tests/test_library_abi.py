@@ -1,0 +1,111 @@
+"""The C ABI library on the host: it builds, loads, exports every function the header declares,
+and rejects invalid arguments before touching the GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nvfp4_kv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_paged_kv_gb300 import build
+    build.build()
+    import nvfp4_paged_kv_gb300 as kv
+    return kv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(nvfp4\w*)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages",
+                 "nvfp4_paged_decode_attention", "nvfp4_paged_decode_workspace_size",
+                 "nvfp4_kv_compute_global_scale", "nvfp4_kv_global_scale_workspace_size",
+                 "nvfp4_kv_round_f32", "nvfp4kv_status_string", "nvfp4kv_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_function(lib):
+    import subprocess
+    from nvfp4_paged_kv_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings_and_version(lib):
+    for code in range(5):
+        assert lib.nvfp4kv_status_string(code).decode().startswith("NVFP4KV_")
+    assert lib.nvfp4kv_version() >= 100
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    import nvfp4_paged_kv_gb300 as kv
+    good = kv.Layout(8, 128, 64)
+    bad_d = kv.Layout(8, 120, 64)
+    fake = ctypes.c_void_p(4096)       # never dereferenced: validation fails first
+    mis = ctypes.c_void_p(4096 + 8)    # misaligned
+    q = lib.nvfp4_kv_quantize_pages
+    # head_dim not a multiple of 16
+    assert q(ctypes.byref(bad_d), 0, fake, 1, None, None, fake, fake, fake, 1, None, 1, None,
+             None) == 1
+    # null destination
+    assert q(ctypes.byref(good), 0, fake, 1, None, None, fake, None, fake, 1, None, 1, None,
+             None) == 1
+    # misaligned source
+    assert q(ctypes.byref(good), 0, mis, 1, None, None, fake, fake, fake, 1, None, 1, None,
+             None) == 1
+    # pool smaller than the page count without id lists
+    assert q(ctypes.byref(good), 0, fake, 1, None, None, fake, fake, fake, 1, None, 2, None,
+             None) == 1
+    # bad dtype
+    assert q(ctypes.byref(good), 7, fake, 1, None, None, fake, fake, fake, 1, None, 1, None,
+             None) == 1
+    # zero pages is a no-op
+    assert q(ctypes.byref(good), 0, None, 0, None, None, None, None, None, 0, None, 0, None,
+             None) == 0
+    dq = lib.nvfp4_kv_dequantize_pages
+    assert dq(ctypes.byref(good), fake, fake, 1, None, fake, 9, fake, 1, None, None, 1, None,
+              None) == 1
+    att = lib.nvfp4_paged_decode_attention
+    args = [ctypes.byref(good), 2, 32, fake, fake, fake, fake, fake, fake, fake, 10, fake, 4,
+            fake, 0.1, 0, fake, 1 << 20, fake, None, None, None]
+    # unsupported head_dim for decode (96), GQA group > 8, split count > 64
+    a = list(args)
+    a[0] = ctypes.byref(kv.Layout(8, 96, 64))
+    assert att(*a) == 2
+    a = list(args)
+    a[2] = 8 * 16
+    assert att(*a) == 2
+    a = list(args)
+    a[15] = 65
+    assert att(*a) == 1
+    # workspace too small
+    a = list(args)
+    a[17] = 16
+    assert att(*a) == 3
+
+
+def test_workspace_sizes(lib):
+    import nvfp4_paged_kv_gb300 as kv
+    lay = kv.Layout(8, 128, 64)
+    assert kv.nvfp4_kv_global_scale_workspace_size() >= 4
+    # one split: B * Hq * (D + 2) floats, each region 256-byte aligned
+    n1 = kv.nvfp4_paged_decode_workspace_size(lay, 4, 32, 1, 1)
+    assert n1 >= 4 * 32 * (128 + 2) * 4
+    n64 = kv.nvfp4_paged_decode_workspace_size(lay, 4, 32, 4096, 64)
+    assert n64 >= 64 * 4 * 32 * (128 + 2) * 4
+    assert kv.nvfp4_paged_decode_workspace_size(lay, 4, 32, 4096, 65) == 0

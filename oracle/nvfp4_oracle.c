@@ -287,6 +287,7 @@ double orc_tensor_amax(int H, int D, int T, int src_dtype, const void* src,
 {
     size_t page_elems = (size_t)H * T * D;
     double amax = 0.0;
+    src_scale = fp32(src_scale); /* the source scale is an FP32 scalar */
 #pragma omp parallel for reduction(max : amax) schedule(static)
     for (int i = 0; i < num_pages; ++i) {
         size_t sp = (size_t)(src_page_ids ? src_page_ids[i] : i);
@@ -341,6 +342,8 @@ void orc_quantize_pages(int H, int D, int T, int src_dtype, const void* src,
 {
     int NB = D / 16;
     size_t page_elems = (size_t)H * T * D;
+    src_scale = fp32(src_scale); /* FP32 scalars (tensor scale, source scale) */
+    g = fp32(g);
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < num_pages; ++i) {
         size_t sp = (size_t)(src_page_ids ? src_page_ids[i] : i);
@@ -372,6 +375,8 @@ void orc_dequantize_pages(int H, int D, int T, const uint8_t* src_data, const ui
 {
     int NB = D / 16;
     size_t page_elems = (size_t)H * T * D;
+    g = fp32(g); /* FP32 scalars (tensor scale, FP8 output scale) */
+    out_scale = fp32(out_scale);
     double m = fp32(g / out_scale); /* FP8 output multiplier (R8) */
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < num_pages; ++i) {

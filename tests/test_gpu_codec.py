@@ -63,8 +63,8 @@ def test_rounding_exhaustive_fp32(kv, cuda, target):
     base = np.arange(chunk, dtype=np.uint32)
     for k in range(1 << 4):
         start = k * chunk
-        torch.arange(start, start + chunk, dtype=torch.int64, device=cuda).to(torch.int32,
-                                                                               out=x_dev)
+        pat = torch.arange(start, start + chunk, dtype=torch.int64, device=cuda)
+        x_dev.copy_(torch.where(pat >= 2 ** 31, pat - 2 ** 32, pat))
         kv.nvfp4_kv_round_f32(x_dev.view(torch.float32), target, out_dev)
         got = out_dev.cpu().numpy()
         xs = (base + np.uint32(start)).view(np.float32)
@@ -86,7 +86,7 @@ def test_quantize_parity(kv, cuda, kind, shape, ids):
     src = _make_src(kind, P, H, T, D, seed=P + D)
     lay = kv.Layout(H, D, T)
     rng = np.random.default_rng(P * 7 + D)
-    src_scale = 0.37 if kind == "fp8" else 1.0
+    src_scale = float(np.float32(0.37)) if kind == "fp8" else 1.0
     sbits = _src_bits(src)
     if ids:
         n = max(1, P - 2)

@@ -429,6 +429,9 @@ void orc_paged_decode_attention(int B, int Hq, int H, int D, int T, const uint16
                                 double* out, double* lse)
 {
     int G = Hq / H;
+    g_k = fp32(g_k); /* FP32 scalars of the call: tensor scales and softmax scale */
+    g_v = fp32(g_v);
+    sm_scale = fp32(sm_scale);
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b)
         for (int qh = 0; qh < Hq; ++qh) {
@@ -487,6 +490,7 @@ void orc_paged_decode_attention_bf16(int B, int Hq, int H, int D, int T, const u
                                      const int32_t* seq_lens, double sm_scale, double* out)
 {
     int G = Hq / H;
+    sm_scale = fp32(sm_scale);
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b)
         for (int qh = 0; qh < Hq; ++qh) {

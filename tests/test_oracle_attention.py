@@ -98,7 +98,7 @@ def test_brute_force_tiny(shape):
     pt = rng.permutation(P)[:B * maxp].reshape(B, maxp).astype(np.int32)
     sl = np.array(lens, np.int32)
     q = bf16_bits_of(rng.normal(0, 1, (B, Hq, D)).tolist()).reshape(B, Hq, D)
-    sm = 1.0 / math.sqrt(D)
+    sm = float(np.float32(1.0 / math.sqrt(D)))   # the call takes an FP32 softmax scale
     out, lse = oracle.paged_decode_attention(q, kd, ks, g_k, vd, vs, g_v, pt, sl, sm, H, T)
     kv, vv = dense_values(kd, ks, g_k), dense_values(vd, vs, g_v)
     ref, ref_lse = brute_attention(bf16_val(q), kv, vv, pt, sl, sm, H, T)
@@ -120,13 +120,14 @@ def _setup(B=1, Hq=4, H=2, D=32, T=4, L=10, seed=12):
 
 def test_single_token_returns_its_value():
     _, kd, ks, vd, vs, pt, sl, q = _setup(L=1, T=4)
-    out, lse = oracle.paged_decode_attention(q, kd, ks, 1.5, vd, vs, 0.5, pt, sl, 0.3, 2, 4)
+    sm = float(np.float32(0.3))
+    out, lse = oracle.paged_decode_attention(q, kd, ks, 1.5, vd, vs, 0.5, pt, sl, sm, 2, 4)
     vv = dense_values(vd, vs, 0.5)
     kv = dense_values(kd, ks, 1.5)
     qv = bf16_val(q)
     for qh in range(4):
         assert np.array_equal(out[0, qh], vv[pt[0, 0], qh // 2, 0])
-        assert lse[0, qh] == pytest.approx(0.3 * float(qv[0, qh] @ kv[pt[0, 0], qh // 2, 0]),
+        assert lse[0, qh] == pytest.approx(sm * float(qv[0, qh] @ kv[pt[0, 0], qh // 2, 0]),
                                            rel=1e-14, abs=1e-14)
 
 

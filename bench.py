@@ -223,7 +223,8 @@ class Path:
         wsb = kv.nvfp4_paged_decode_workspace_size(self.lay_lc, wl.B, wl.Hq, pt.shape[1], 0)
         self.dec_ws = torch.empty(wsb, dtype=u8, device=dev)
         kv_tokens = wl.kv_tokens
-        self.bytes_decode = (kv_tokens * wl.H * (wl.D + wl.D // 8) * 2      # K+V data+scales
+        # per (token, KV head): K and V packed data D/2 each + K and V scales D/16 each
+        self.bytes_decode = (kv_tokens * wl.H * (wl.D + wl.D // 8)          # K+V data+scales
                              + wl.B * wl.Hq * wl.D * 2 * 2                   # q in, out
                              + pt.numel() * 4 + wl.B * 4 + wl.B * wl.Hq * 4)  # table, lens, lse
         self.decode_tokens = wl.B
@@ -338,7 +339,7 @@ def kernel_table(path, peak):
     out = torch.empty((db.B, db.Hq, db.D), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(kv.nvfp4_paged_decode_workspace_size(lay, db.B, db.Hq, pt.shape[1], 0),
                      dtype=u8, device=dev)
-    nbytes = db.kv_tokens * db.H * (db.D + db.D // 8) * 2 + db.B * db.Hq * db.D * 4 + \
+    nbytes = db.kv_tokens * db.H * (db.D + db.D // 8) + db.B * db.Hq * db.D * 4 + \
         pt.numel() * 4 + db.B * 4
     add("decode (decode batch 32x8192, GQA 4)",
         lambda: kv.nvfp4_paged_decode_attention(lay, q, kd, ks, gk, vd, vs, gv, pt, sl,
@@ -418,7 +419,7 @@ def oracle_sample(seed=0, pages=1024, decode_seqs=1, max_tokens=None):
     oracle.paged_decode_attention(synthetic.bf16_bits(q), kd, ks, 0.01, vd, vs, 0.01, pt,
                                   np.array(lens, np.int32), wl.sm_scale, wl.H, T2)
     t_dec = time.perf_counter() - t0
-    dec_bytes = sum(lens) * wl.H * (wl.D + wl.D // 8) * 2
+    dec_bytes = sum(lens) * wl.H * (wl.D + wl.D // 8)
     desc = (f"oracle on {rt.P} page round-trip pages of K (amax, encode, decode BF16 + FP8) and "
             f"{decode_seqs} long-context sequence(s) ({sum(lens)} tokens, {wl.Hq} query heads)")
     return codec_bytes + dec_bytes, t_codec + t_dec, oracle.max_threads(), desc
@@ -523,7 +524,7 @@ def main():
     if not args.no_e2e:
         result["e2e"] = e2e(path, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, t, thr, desc = oracle_sample(args.seed, pages=1024, decode_seqs=1)
+        b, t, thr, desc = oracle_sample(args.seed, pages=4096, decode_seqs=8)
         result["cpu_baseline"] = {"value": round(b / t / GB, 4), "unit": "GB/s", "cores": thr,
                                   "kind": "oracle", "sample": desc,
                                   "seconds": round(t, 2)}

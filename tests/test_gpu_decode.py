@@ -154,13 +154,20 @@ def test_split_count_invariance(kv, cuda):
         out, lse = run_decode(kv, cuda, cache, q, pt, sl, 1 / math.sqrt(D), splits=splits)
         check(out, lse, ref, ref_lse, tag=f"splits={splits}")
         outs.append(out)
+    # Split counts differ in fp32 summation order and in the running maximum each chunk uses,
+    # so P (rounded to FP16, 2^-11 relative) rounds differently: the outputs may differ by one
+    # BF16 ulp (2^-7 relative) plus 2^-10 of the largest |v| (two FP16 roundings of P).
+    vmax = float(v.float().abs().max())
+    bound = np.abs(outs[0]) * 2.0 ** -7 + vmax * 2.0 ** -10
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() <= 4e-3
+        d = np.abs(o - outs[0])
+        assert np.all(d <= bound), (d.max(), float((d - bound).max()))
 
 
 def test_mha_and_dominant_key(kv, cuda):
     """Group size 1 (MHA) with one key aligned to the query far above the rest: the output is
-    that token's value."""
+    that token's decoded value. Outputs here are O(1), where rounding to BF16 alone moves them by
+    up to 2^-9 relative, so the check is: within one BF16 ulp of the oracle."""
     H, D, T, B = 4, 128, 16, 1
     L = 50
     g = synthetic.gen(5)
@@ -173,7 +180,8 @@ def test_mha_and_dominant_key(kv, cuda):
     cache = Cache(kv, cuda, k.to(torch.bfloat16), v, H, D, T)
     out, lse = run_decode(kv, cuda, cache, q, pt, sl, 1.0)
     ref, ref_lse = oracle_decode(cache, q, pt, sl, 1.0)
-    check(out, lse, ref, ref_lse)
+    assert np.all(np.abs(out - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6)
+    assert np.abs(lse - ref_lse).max() <= LSE_ABS
 
 
 def test_decode_batch_workload_sampled(kv, cuda):

@@ -193,6 +193,34 @@ nvfp4kv_status nvfp4_paged_decode_attention(
     size_t workspace_bytes, void* out, float* lse, int32_t* status, nvfp4kv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * nvfp4_paged_decode_attention for callers that cannot allocate device memory. The source
+ * pages have no counterpart to this call; it exists for library users who cannot provide a
+ * workspace: a plugin inside a framework that owns every device allocation, a serving process
+ * that has given all free HBM to its KV-cache pool, or a hot path that must not call cudaMalloc
+ * because that synchronises the device.
+ *
+ * Same arguments, numerics, kernels and split plan as nvfp4_paged_decode_attention, minus the
+ * workspace: the split partials live in a fixed array of NVFP4KV_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the process exits. The call
+ * allocates nothing. The caller still provides inputs and outputs.
+ *   - A call whose workspace need (nvfp4_paged_decode_workspace_size with the same arguments)
+ *     exceeds NVFP4KV_NOALLOC_SCRATCH_BYTES returns NVFP4KV_ERR_WORKSPACE and enqueues nothing.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents behind. Calls that
+ *     can overlap on the GPU (different streams without ordering between them) race on it.
+ * ------------------------------------------------------------------------------------------ */
+#define NVFP4KV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
+
+nvfp4kv_status nvfp4_paged_decode_attention_noalloc(
+    const nvfp4kv_layout* layout, int32_t batch, int32_t num_q_heads, const void* q,
+    const uint8_t* k_data, const uint8_t* k_scales, const float* k_global_scale,
+    const uint8_t* v_data, const uint8_t* v_scales, const float* v_global_scale,
+    int32_t pool_pages, const int32_t* page_table, int32_t max_pages_per_seq,
+    const int32_t* seq_lens, float sm_scale, int32_t max_num_splits, void* out, float* lse,
+    int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * The two roundings of the encoder on their own, for exhaustive verification over fp32 inputs:
  * target 0 writes E2M1 codes (RNE, satfinite at 6, sign kept, one code per byte), target 1
  * writes E4M3 bytes (RNE, satfinite at 448, sign kept). x: n finite floats; out: n bytes.

@@ -24,7 +24,9 @@ __all__ = [
     "nvfp4_kv_global_scale_workspace_size", "nvfp4_kv_compute_global_scale",
     "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages",
     "nvfp4_paged_decode_workspace_size", "nvfp4_paged_decode_attention", "nvfp4_kv_round_f32",
+    "nvfp4_paged_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
+NOALLOC_SCRATCH_BYTES = 32 << 20   # NVFP4KV_NOALLOC_SCRATCH_BYTES
 
 BF16, FP16, FP8_E4M3 = 0, 1, 2
 STATUS_PAGE_OOB, STATUS_BAD_SEQ_LEN, STATUS_TIMEOUT = 0x1, 0x2, 0x4
@@ -83,6 +85,8 @@ def load():
             "nvfp4_paged_decode_attention": (I32, [LP, I32, I32, P, P, P, P, P, P, P, I32, P,
                                                    I32, P, F, I32, P, SZ, P, P, P, P]),
             "nvfp4_kv_round_f32": (I32, [P, SZ, I32, P, P]),
+            "nvfp4_paged_decode_attention_noalloc": (I32, [LP, I32, I32, P, P, P, P, P, P, P,
+                                                           I32, P, I32, P, F, I32, P, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -228,6 +232,28 @@ def nvfp4_paged_decode_attention(layout: Layout, q: torch.Tensor, k_data, k_scal
         int(max_num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
     _check("nvfp4_paged_decode_attention", code)
+    return out
+
+
+def nvfp4_paged_decode_attention_noalloc(layout: Layout, q: torch.Tensor, k_data, k_scales,
+                                         k_global_scale, v_data, v_scales, v_global_scale,
+                                         page_table: torch.Tensor, seq_lens: torch.Tensor,
+                                         sm_scale: float, out: torch.Tensor, *, lse=None,
+                                         max_num_splits: int = 0, status=None, stream=None):
+    """The decode attention for callers that cannot allocate: no workspace argument, the split
+    partials use the library's fixed NOALLOC_SCRATCH_BYTES device array. Calls that overlap on
+    the GPU race on that array; the first call on a device must precede any stream capture."""
+    lib = load()
+    B, Hq, _ = q.shape
+    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("page_table and seq_lens must be int32")
+    code = lib.nvfp4_paged_decode_attention_noalloc(
+        ctypes.byref(layout), B, Hq, _ptr(q), _ptr(k_data), _ptr(k_scales),
+        _ptr(k_global_scale), _ptr(v_data), _ptr(v_scales), _ptr(v_global_scale),
+        k_data.shape[0], _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
+        float(sm_scale), int(max_num_splits), _ptr(out), _ptr(lse), _ptr(status),
+        _stream(stream))
+    _check("nvfp4_paged_decode_attention_noalloc", code)
     return out
 
 

@@ -20,6 +20,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
 BF16, FP16, FP8_E4M3 = 0, 1, 2
+DIM_PAIRS, TOKEN_PAIRS = 0, 1   # byte packing of an NVFP4 pool (see nvfp4_oracle.c, R2)
 
 _lock = threading.Lock()
 _lib = None
@@ -64,10 +65,10 @@ def _load():
                 "orc_e4m3_encode_f32": (None, [p, sz, p]),
                 "orc_tensor_amax": (d, [i, i, i, i, p, p, i, d]),
                 "orc_global_scale_from_amax": (d, [d]),
-                "orc_quantize_pages": (None, [i, i, i, i, p, p, d, d, p, p, p, i]),
-                "orc_dequantize_pages": (None, [i, i, i, p, p, p, d, i, p, p, d, i]),
-                "orc_paged_decode_attention": (None, [i, i, i, i, i, p, p, p, d, p, p, d, p,
-                                                      i, p, d, p, p, p]),
+                "orc_quantize_pages": (None, [i, i, i, i, i, p, p, d, d, p, p, p, i]),
+                "orc_dequantize_pages": (None, [i, i, i, i, p, p, p, d, i, p, p, d, i]),
+                "orc_paged_decode_attention": (None, [i, i, i, i, i, i, i, p, p, p, d, p, p, d,
+                                                      p, i, p, d, p, p, p]),
                 "orc_paged_decode_attention_bf16": (None, [i, i, i, i, i, p, p, p, p, i, p,
                                                            d, p]),
             }
@@ -185,24 +186,34 @@ def global_scale(src, dtype, H, D, T, src_page_ids=None, num_pages=None, src_sca
     return _load().orc_global_scale_from_amax(amax)
 
 
+def pool_shapes(P, H, T, D, packing=DIM_PAIRS):
+    """numpy shapes of the packed-code and scale pools of P pages."""
+    if packing == TOKEN_PAIRS:
+        return (P, H, T // 2, D), (P, H, T // 2, D // 16, 2)
+    return (P, H, T, D // 2), (P, H, T, D // 16)
+
+
 def quantize_pages(src, dtype, H, D, T, g, num_dst_pages=None, src_page_ids=None,
-                   dst_page_ids=None, num_pages=None, src_scale=1.0):
-    """Encode pages to NVFP4. Returns (data [P][H][T][D/2] u8, scales [P][H][T][D/16] u8)."""
+                   dst_page_ids=None, num_pages=None, src_scale=1.0, packing=DIM_PAIRS):
+    """Encode pages to NVFP4. Returns (data, scales) shaped as pool_shapes(...) says."""
     src = _src_dtype(src, dtype)
     sids, dids = _ids(src_page_ids), _ids(dst_page_ids)
     if num_pages is None:
         num_pages = len(sids) if sids is not None else src.size // (H * T * D)
     if num_dst_pages is None:
         num_dst_pages = int(dids.max()) + 1 if dids is not None and len(dids) else num_pages
-    data = np.zeros((num_dst_pages, H, T, D // 2), dtype=np.uint8)
-    scales = np.zeros((num_dst_pages, H, T, D // 16), dtype=np.uint8)
-    _load().orc_quantize_pages(H, D, T, dtype, _ptr(src), _ptr(sids), float(src_scale),
-                               float(g), _ptr(data), _ptr(scales), _ptr(dids), int(num_pages))
+    ds, ss = pool_shapes(num_dst_pages, H, T, D, packing)
+    data = np.zeros(ds, dtype=np.uint8)
+    scales = np.zeros(ss, dtype=np.uint8)
+    _load().orc_quantize_pages(H, D, T, int(packing), dtype, _ptr(src), _ptr(sids),
+                               float(src_scale), float(g), _ptr(data), _ptr(scales), _ptr(dids),
+                               int(num_pages))
     return data, scales
 
 
 def dequantize_pages(data, scales, H, D, T, g, out_dtype=BF16, num_dst_pages=None,
-                     src_page_ids=None, dst_page_ids=None, num_pages=None, out_scale=1.0):
+                     src_page_ids=None, dst_page_ids=None, num_pages=None, out_scale=1.0,
+                     packing=DIM_PAIRS):
     """Decode NVFP4 pages to BF16/FP16 bit patterns (uint16) or FP8 E4M3 bytes."""
     data = np.ascontiguousarray(data, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
@@ -213,16 +224,17 @@ def dequantize_pages(data, scales, H, D, T, g, out_dtype=BF16, num_dst_pages=Non
         num_dst_pages = int(dids.max()) + 1 if dids is not None and len(dids) else num_pages
     odt = np.uint8 if out_dtype == FP8_E4M3 else np.uint16
     out = np.zeros((num_dst_pages, H, T, D), dtype=odt)
-    _load().orc_dequantize_pages(H, D, T, _ptr(data), _ptr(scales), _ptr(sids), float(g),
-                                 int(out_dtype), _ptr(out), _ptr(dids), float(out_scale),
-                                 int(num_pages))
+    _load().orc_dequantize_pages(H, D, T, int(packing), _ptr(data), _ptr(scales), _ptr(sids),
+                                 float(g), int(out_dtype), _ptr(out), _ptr(dids),
+                                 float(out_scale), int(num_pages))
     return out
 
 
 # ---------------------------------------------------------------- attention
 
 def paged_decode_attention(q_bf16, k_data, k_scales, g_k, v_data, v_scales, g_v, page_table,
-                           seq_lens, sm_scale, H, T, want_lse=True, want=None):
+                           seq_lens, sm_scale, H, T, want_lse=True, want=None,
+                           k_packing=DIM_PAIRS, v_packing=DIM_PAIRS):
     """Exact (fp64) GQA decode attention over NVFP4 pages.
 
     q_bf16: uint16 [B, Hq, D]; page_table: int32 [B, max_pages]; seq_lens: int32 [B].
@@ -238,9 +250,10 @@ def paged_decode_attention(q_bf16, k_data, k_scales, g_k, v_data, v_scales, g_v,
     out = np.zeros((B, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Hq), dtype=np.float64) if want_lse else None
     wm = None if want is None else np.ascontiguousarray(want, dtype=np.uint8).reshape(B, Hq)
-    _load().orc_paged_decode_attention(B, Hq, H, D, T, _ptr(q), _ptr(kd), _ptr(ks), float(g_k),
-                                       _ptr(vd), _ptr(vs), float(g_v), _ptr(pt), pt.shape[1],
-                                       _ptr(sl), float(sm_scale), _ptr(wm), _ptr(out), _ptr(lse))
+    _load().orc_paged_decode_attention(B, Hq, H, D, T, int(k_packing), int(v_packing), _ptr(q),
+                                       _ptr(kd), _ptr(ks), float(g_k), _ptr(vd), _ptr(vs),
+                                       float(g_v), _ptr(pt), pt.shape[1], _ptr(sl),
+                                       float(sm_scale), _ptr(wm), _ptr(out), _ptr(lse))
     return out, lse
 
 

@@ -24,8 +24,14 @@
  *
  * Readings of points the pages leave open (each one stated again where it is used):
  *   R1 block axis: a block is 16 consecutive elements along head_dim of one token.
- *   R2 nibble order: element 2j is the low nibble of byte j, element 2j+1 the high nibble.
- *   R3 page layout (HND): data[page][head][token][head_dim/2], scales[page][head][token][head_dim/16].
+ *   R2 byte packing, two forms (a pool uses one):
+ *      dim pairs   (packing 0): data[page][head][token][head_dim/2], byte j holds head dims 2j
+ *                  (low nibble) and 2j+1 (high nibble) of one token; scales[page][head][token][D/16].
+ *      token pairs (packing 1): data[page][head][token/2][head_dim], byte d holds head dim d of
+ *                  tokens 2p (low nibble) and 2p+1 (high nibble); scales[page][head][token/2][D/16][2],
+ *                  the scales of a block for tokens 2p and 2p+1 side by side.
+ *      Both hold the same codes and scales; only the byte order inside a page differs.
+ *   R3 page layout (HND): every (page, head) owns one contiguous run of T tokens.
  *   R4 scale pick: s = E4M3_rne_satfinite(fp32(amax_block / fp32(6 g))).
  *   R5 element code: c = E2M1_rne_satfinite(fp32(x * r)), r = fp32(1 / fp32(s g)) or 0 if s g == 0;
  *      the sign is kept, so a negative value that rounds to zero is code 0x8.
@@ -221,6 +227,37 @@ static double load_src(int dtype, const void* src, size_t idx, double src_scale)
     }
 }
 
+/* Byte index of element (page p, head h, token t, head dim d) in a packed-code pool, and which
+   nibble holds it (R2). */
+static size_t code_index(int packing, size_t p, int h, int t, int d, int H, int T, int D, int* hi)
+{
+    if (packing == 1) {
+        *hi = t & 1;
+        return (((size_t)p * H + h) * (size_t)(T / 2) + (size_t)(t / 2)) * (size_t)D + (size_t)d;
+    }
+    *hi = d & 1;
+    return (((size_t)p * H + h) * (size_t)T + (size_t)t) * (size_t)(D / 2) + (size_t)(d / 2);
+}
+
+/* Byte index of the scale of block b (head dims 16b..16b+15) of token t (R2). */
+static size_t scale_index(int packing, size_t p, int h, int t, int b, int H, int T, int NB)
+{
+    if (packing == 1)
+        return ((((size_t)p * H + h) * (size_t)(T / 2) + (size_t)(t / 2)) * (size_t)NB + (size_t)b) * 2 +
+               (size_t)(t & 1);
+    return (((size_t)p * H + h) * (size_t)T + (size_t)t) * (size_t)NB + (size_t)b;
+}
+
+static int get_code(const uint8_t* data, size_t idx, int hi)
+{
+    return hi ? (data[idx] >> 4) : (data[idx] & 15);
+}
+
+static void put_code(uint8_t* data, size_t idx, int hi, int code)
+{
+    data[idx] = hi ? (uint8_t)((data[idx] & 0x0F) | (code << 4)) : (uint8_t)((data[idx] & 0xF0) | code);
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Exported scalar conversions (used by the tests to pin the roundings and by the exhaustive  */
 /* fp32 sweeps).                                                                               */
@@ -310,7 +347,7 @@ double orc_global_scale_from_amax(double amax)
 /* Encode one block of 16 values (steps A2..A4). R4, R5.                                       */
 /* ------------------------------------------------------------------------------------------ */
 
-static void encode_block(const double* x, double g, uint8_t* codes8, uint8_t* scale_out)
+static void encode_block(const double* x, double g, int* c, uint8_t* scale_out)
 {
     double d = fp32(6.0 * g);                 /* fp32(6 g)                                */
     double a = 0.0;                           /* block amax (exact)                       */
@@ -321,11 +358,8 @@ static void encode_block(const double* x, double g, uint8_t* codes8, uint8_t* sc
     double s = e4m3_value(s_code);
     double sg = fp32(s * g);
     double r = (sg == 0.0) ? 0.0 : fp32(1.0 / sg);
-    int c[16];
     for (int i = 0; i < 16; ++i)
         c[i] = e2m1_encode(fp32(x[i] * r));
-    for (int j = 0; j < 8; ++j) /* R2: low nibble first */
-        codes8[j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
     *scale_out = s_code;
 }
 
@@ -335,7 +369,7 @@ static void encode_block(const double* x, double g, uint8_t* codes8, uint8_t* sc
  * through one encoder; [LMSYS Path 1 / Path 2]: the current K/V is quantized and written into
  * the NVFP4 cache. Layout R3; src pages are [page][H][T][D] in src_dtype.
  */
-void orc_quantize_pages(int H, int D, int T, int src_dtype, const void* src,
+void orc_quantize_pages(int H, int D, int T, int packing, int src_dtype, const void* src,
                         const int32_t* src_page_ids, double src_scale, double g,
                         uint8_t* dst_data, uint8_t* dst_scales, const int32_t* dst_page_ids,
                         int num_pages)
@@ -352,13 +386,19 @@ void orc_quantize_pages(int H, int D, int T, int src_dtype, const void* src,
             for (int t = 0; t < T; ++t)
                 for (int b = 0; b < NB; ++b) {
                     double x[16];
+                    int c[16];
                     size_t row = ((size_t)h * T + t); /* token row within the page */
                     for (int k = 0; k < 16; ++k)
                         x[k] = load_src(src_dtype, src, sp * page_elems + row * D + b * 16 + k,
                                         src_scale);
-                    uint8_t* codes = dst_data + dp * (page_elems / 2) + row * (D / 2) + b * 8;
-                    uint8_t* sc = dst_scales + dp * (page_elems / 16) + row * NB + b;
-                    encode_block(x, g, codes, sc);
+                    uint8_t sc;
+                    encode_block(x, g, c, &sc);
+                    for (int k = 0; k < 16; ++k) {
+                        int hi;
+                        size_t idx = code_index(packing, dp, h, t, b * 16 + k, H, T, D, &hi);
+                        put_code(dst_data, idx, hi, c[k]);
+                    }
+                    dst_scales[scale_index(packing, dp, h, t, b, H, T, NB)] = sc;
                 }
     }
 }
@@ -369,9 +409,10 @@ void orc_quantize_pages(int H, int D, int T, int src_dtype, const void* src,
  * [LMSYS Path 2]: the cached prefix is gathered, dequantized and written into an FP8 workspace.
  * out_dtype: ORC_BF16 / ORC_FP16 (uint16 bit patterns) or ORC_FP8_E4M3 (bytes).
  */
-void orc_dequantize_pages(int H, int D, int T, const uint8_t* src_data, const uint8_t* src_scales,
-                          const int32_t* src_page_ids, double g, int out_dtype, void* dst,
-                          const int32_t* dst_page_ids, double out_scale, int num_pages)
+void orc_dequantize_pages(int H, int D, int T, int packing, const uint8_t* src_data,
+                          const uint8_t* src_scales, const int32_t* src_page_ids, double g,
+                          int out_dtype, void* dst, const int32_t* dst_page_ids, double out_scale,
+                          int num_pages)
 {
     int NB = D / 16;
     size_t page_elems = (size_t)H * T * D;
@@ -382,14 +423,14 @@ void orc_dequantize_pages(int H, int D, int T, const uint8_t* src_data, const ui
     for (int i = 0; i < num_pages; ++i) {
         size_t sp = (size_t)(src_page_ids ? src_page_ids[i] : i);
         size_t dp = (size_t)(dst_page_ids ? dst_page_ids[i] : i);
-        for (size_t row = 0; row < (size_t)H * T; ++row)
-            for (int b = 0; b < NB; ++b) {
-                double s = e4m3_value(src_scales[sp * (page_elems / 16) + row * NB + b]);
-                const uint8_t* codes = src_data + sp * (page_elems / 2) + row * (D / 2) + b * 8;
-                for (int k = 0; k < 16; ++k) {
-                    int c = (k & 1) ? (codes[k >> 1] >> 4) : (codes[k >> 1] & 15);
-                    double v = e2m1_value(c) * s; /* exact */
-                    size_t o = dp * page_elems + row * D + b * 16 + k;
+        for (int h = 0; h < H; ++h)
+            for (int t = 0; t < T; ++t)
+                for (int d = 0; d < D; ++d) {
+                    int hi;
+                    size_t idx = code_index(packing, sp, h, t, d, H, T, D, &hi);
+                    double s = e4m3_value(src_scales[scale_index(packing, sp, h, t, d / 16, H, T, NB)]);
+                    double v = e2m1_value(get_code(src_data, idx, hi)) * s; /* exact */
+                    size_t o = dp * page_elems + ((size_t)h * T + t) * D + d;
                     if (out_dtype == ORC_BF16)
                         ((uint16_t*)dst)[o] = bf16_bits(bf16_round(fp32(v * g)));
                     else if (out_dtype == ORC_FP16)
@@ -397,7 +438,6 @@ void orc_dequantize_pages(int H, int D, int T, const uint8_t* src_data, const ui
                     else
                         ((uint8_t*)dst)[o] = e4m3_encode(fp32(v * m));
                 }
-            }
     }
 }
 
@@ -412,16 +452,17 @@ void orc_dequantize_pages(int H, int D, int T, const uint8_t* src_data, const ui
 /* [B][Hq]) selects the pairs to compute so that large cases can be sampled.                    */
 /* ------------------------------------------------------------------------------------------ */
 
-static double dequant_elem(const uint8_t* data, const uint8_t* scales, size_t page, int h, int t,
-                           int d, int H, int T, int D)
+static double dequant_elem(int packing, const uint8_t* data, const uint8_t* scales, size_t page,
+                           int h, int t, int d, int H, int T, int D)
 {
-    size_t row = ((size_t)page * H + h) * T + t;
-    uint8_t byte = data[row * (D / 2) + d / 2];
-    int c = (d & 1) ? (byte >> 4) : (byte & 15);
-    return e2m1_value(c) * e4m3_value(scales[row * (D / 16) + d / 16]);
+    int hi;
+    size_t idx = code_index(packing, page, h, t, d, H, T, D, &hi);
+    return e2m1_value(get_code(data, idx, hi)) *
+           e4m3_value(scales[scale_index(packing, page, h, t, d / 16, H, T, D / 16)]);
 }
 
-void orc_paged_decode_attention(int B, int Hq, int H, int D, int T, const uint16_t* q_bf16,
+void orc_paged_decode_attention(int B, int Hq, int H, int D, int T, int k_packing,
+                                int v_packing, const uint16_t* q_bf16,
                                 const uint8_t* k_data, const uint8_t* k_scales, double g_k,
                                 const uint8_t* v_data, const uint8_t* v_scales, double g_v,
                                 const int32_t* page_table, int max_pages_per_seq,
@@ -455,7 +496,7 @@ void orc_paged_decode_attention(int B, int Hq, int H, int D, int T, const uint16
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d)
                     dot += bf16_value(qv[d]) *
-                           (dequant_elem(k_data, k_scales, page, h, t % T, d, H, T, D) * g_k);
+                           (dequant_elem(k_packing, k_data, k_scales, page, h, t % T, d, H, T, D) * g_k);
                 double zt = sm_scale * dot;
                 if (zt > zmax)
                     zmax = zt;
@@ -467,11 +508,11 @@ void orc_paged_decode_attention(int B, int Hq, int H, int D, int T, const uint16
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d)
                     dot += bf16_value(qv[d]) *
-                           (dequant_elem(k_data, k_scales, page, h, t % T, d, H, T, D) * g_k);
+                           (dequant_elem(k_packing, k_data, k_scales, page, h, t % T, d, H, T, D) * g_k);
                 double w = exp(sm_scale * dot - zmax);
                 l += w;
                 for (int d = 0; d < D; ++d)
-                    o[d] += w * (dequant_elem(v_data, v_scales, page, h, t % T, d, H, T, D) * g_v);
+                    o[d] += w * (dequant_elem(v_packing, v_data, v_scales, page, h, t % T, d, H, T, D) * g_v);
             }
             for (int d = 0; d < D; ++d)
                 o[d] /= l;

@@ -227,3 +227,29 @@ def test_bf16_attention_equals_nvfp4_attention_on_representable_kv():
     out, _ = oracle.paged_decode_attention(q, kd, ks, g, vd, vs, g, pt, sl, 0.2, 2, 4)
     out_b = oracle.paged_decode_attention_bf16(q, kb, vb, pt, sl, 0.2, 2, 4)
     np.testing.assert_allclose(out, out_b, rtol=1e-13, atol=1e-15)
+
+
+def test_value_packing_does_not_change_attention():
+    """The same V codes and scales stored token-pair packed give the same attention as stored
+    dim-pair packed (and likewise for K)."""
+    rng, kd, ks, vd, vs, pt, sl, q = _setup(B=2, Hq=4, H=2, D=32, T=4, L=7)
+    P, H, T, half = vd.shape
+    D = 2 * half
+
+    def to_token_pairs(data, scales):
+        codes = np.stack([data & 15, data >> 4], axis=-1).reshape(P, H, T, D)
+        tp = (codes[:, :, 0::2, :] | (codes[:, :, 1::2, :] << 4)).astype(np.uint8)
+        sc = np.stack([scales[:, :, 0::2, :], scales[:, :, 1::2, :]], axis=-1)
+        return np.ascontiguousarray(tp), np.ascontiguousarray(sc)
+
+    vtd, vts = to_token_pairs(vd, vs)
+    ktd, kts = to_token_pairs(kd, ks)
+    want, want_lse = oracle.paged_decode_attention(q, kd, ks, 0.7, vd, vs, 1.3, pt, sl, 0.25, H,
+                                                   T)
+    got, got_lse = oracle.paged_decode_attention(q, kd, ks, 0.7, vtd, vts, 1.3, pt, sl, 0.25, H,
+                                                 T, v_packing=oracle.TOKEN_PAIRS)
+    assert np.array_equal(got, want) and np.array_equal(got_lse, want_lse)
+    got2, _ = oracle.paged_decode_attention(q, ktd, kts, 0.7, vtd, vts, 1.3, pt, sl, 0.25, H, T,
+                                            k_packing=oracle.TOKEN_PAIRS,
+                                            v_packing=oracle.TOKEN_PAIRS)
+    assert np.array_equal(got2, want)

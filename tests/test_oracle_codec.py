@@ -356,3 +356,72 @@ def test_fp8_and_fp16_sources_reduce_to_bf16_source():
             assert np.array_equal(a, b)
         for a, b in zip(want, got16):
             assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------------------ packings
+
+def _dense_dim_pairs(data, scales):
+    """[P,H,T,D] codes and [P,H,T,D/16] scales of a dim-pair pool."""
+    return unpack_codes(data), scales
+
+
+def _dense_token_pairs(data, scales):
+    """[P,H,T,D] codes and [P,H,T,D/16] scales of a token-pair pool: byte (pair p, dim d) holds
+    token 2p in its low nibble and token 2p+1 in its high nibble; scales [P,H,T/2,NB,2]."""
+    P, H, T2, D = data.shape
+    codes = np.empty((P, H, 2 * T2, D), np.uint8)
+    codes[:, :, 0::2, :] = data & 15
+    codes[:, :, 1::2, :] = data >> 4
+    sc = np.empty((P, H, 2 * T2, scales.shape[3]), np.uint8)
+    sc[:, :, 0::2, :] = scales[..., 0]
+    sc[:, :, 1::2, :] = scales[..., 1]
+    return codes, sc
+
+
+@pytest.mark.parametrize("D,T", [(16, 2), (64, 16), (128, 6)])
+def test_token_pair_packing_is_a_permutation_of_dim_pairs(D, T):
+    rng = np.random.default_rng(D + T)
+    P, H = 5, 3
+    x = rng.normal(0, 1, (P, H, T, D)).astype(np.float32)
+    src = bf16_bits_of(x).reshape(P, H, T, D)
+    g = oracle.global_scale(src, oracle.BF16, H, D, T)
+    ids = np.array([4, 0, 2], np.int32)
+    a = oracle.quantize_pages(src, oracle.BF16, H, D, T, g, src_page_ids=ids, dst_page_ids=ids,
+                              num_dst_pages=P, packing=oracle.DIM_PAIRS)
+    b = oracle.quantize_pages(src, oracle.BF16, H, D, T, g, src_page_ids=ids, dst_page_ids=ids,
+                              num_dst_pages=P, packing=oracle.TOKEN_PAIRS)
+    assert b[0].shape == (P, H, T // 2, D) and b[1].shape == (P, H, T // 2, D // 16, 2)
+    ca, sa = _dense_dim_pairs(*a)
+    cb, sb = _dense_token_pairs(*b)
+    assert np.array_equal(ca, cb) and np.array_equal(sa, sb)
+    for out in (oracle.BF16, oracle.FP8_E4M3):
+        da = oracle.dequantize_pages(*a, H, D, T, g, out, src_page_ids=ids, dst_page_ids=ids,
+                                     num_dst_pages=P)
+        db = oracle.dequantize_pages(*b, H, D, T, g, out, src_page_ids=ids, dst_page_ids=ids,
+                                     num_dst_pages=P, packing=oracle.TOKEN_PAIRS)
+        assert np.array_equal(da, db)
+
+
+def test_token_pair_positions():
+    """One marked value per (token, block): its code lands in byte (token // 2, dim), nibble
+    token % 2, and its scale in [token // 2][block][token % 2]."""
+    H, T, D, P = 2, 4, 32, 2
+    x = np.zeros((P, H, T, D), np.float32)
+    want = {}
+    for p in range(P):
+        for h in range(H):
+            for t in range(T):
+                for blk in range(2):
+                    sb = 1 + (p * 29 + h * 13 + t * 7 + blk * 3) % 120
+                    k = (p + 3 * h + 5 * t + blk) % 16
+                    x[p, h, t, 16 * blk + k] = -6.0 * oracle.e4m3_value(sb)
+                    want[(p, h, t, blk)] = (k, sb)
+    src = bf16_bits_of(x).reshape(P, H, T, D)
+    data, scales = oracle.quantize_pages(src, oracle.BF16, H, D, T, 1.0,
+                                         packing=oracle.TOKEN_PAIRS)
+    for (p, h, t, blk), (k, sb) in want.items():
+        assert scales[p, h, t // 2, blk, t % 2] == sb
+        for j in range(16):
+            byte = data[p, h, t // 2, 16 * blk + j]
+            code = (byte >> 4) if t % 2 else (byte & 15)
+            assert code == (15 if j == k else 0)

@@ -179,6 +179,8 @@ class Path:
         self.k, self.v = rt.make(device=dev)
         P, H, T, D = rt.P, rt.H, rt.T, rt.D
         self.lay_rt = kv.Layout(H, D, T)
+        # K pages in the dim-pair packing, V pages in the token-pair packing (what decode reads)
+        self.lay_rt_kv = (self.lay_rt, self.lay_rt.with_packing(kv.PACK_TOKEN_PAIRS))
         u8 = torch.uint8
         self.rt_out = []
         for _ in range(2):
@@ -216,7 +218,8 @@ class Path:
         kv.nvfp4_kv_compute_global_scale(self.lay_lc, k, self.c_gk, workspace=self.gs_ws)
         kv.nvfp4_kv_compute_global_scale(self.lay_lc, v, self.c_gv, workspace=self.gs_ws)
         kv.nvfp4_kv_quantize_pages(self.lay_lc, k, self.c_gk, self.c_kd, self.c_ks)
-        kv.nvfp4_kv_quantize_pages(self.lay_lc, v, self.c_gv, self.c_vd, self.c_vs)
+        kv.nvfp4_kv_quantize_pages(self.lay_lc.with_packing(kv.PACK_TOKEN_PAIRS), v, self.c_gv,
+                                   self.c_vd, self.c_vs)
         del k, v
         self.out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=dev)
@@ -239,17 +242,17 @@ class Path:
 
     def quantize(self, i):
         o = self.rt_out[i]
-        self.kv.nvfp4_kv_quantize_pages(self.lay_rt, (self.k, self.v)[i], o["g"], o["data"],
-                                        o["scales"])
+        self.kv.nvfp4_kv_quantize_pages(self.lay_rt_kv[i], (self.k, self.v)[i], o["g"],
+                                        o["data"], o["scales"])
 
     def dequantize_bf16(self, i):
         o = self.rt_out[i]
-        self.kv.nvfp4_kv_dequantize_pages(self.lay_rt, o["data"], o["scales"], o["g"],
+        self.kv.nvfp4_kv_dequantize_pages(self.lay_rt_kv[i], o["data"], o["scales"], o["g"],
                                           o["bf16"])
 
     def dequantize_fp8(self, i):
         o = self.rt_out[i]
-        self.kv.nvfp4_kv_dequantize_pages(self.lay_rt, o["data"], o["scales"], o["g"],
+        self.kv.nvfp4_kv_dequantize_pages(self.lay_rt_kv[i], o["data"], o["scales"], o["g"],
                                           o["fp8"], dst_dtype=self.kv.FP8_E4M3,
                                           dst_scale=o["fp8_scale"])
 
@@ -312,9 +315,14 @@ def kernel_table(path, peak):
 
     n = path.rt.P * path.rt.H * path.rt.T * path.rt.D
     add("amax_K (page round-trip)", lambda: path.amax(0), n * 2, 2)
-    add("quantize_K (page round-trip)", lambda: path.quantize(0), n * 2.5625, 1)
+    add("quantize_K dim pairs (page round-trip)", lambda: path.quantize(0), n * 2.5625, 1)
+    add("quantize_V token pairs (page round-trip)", lambda: path.quantize(1), n * 2.5625, 1)
     add("dequantize_K_bf16 (page round-trip)", lambda: path.dequantize_bf16(0), n * 2.5625, 1)
+    add("dequantize_V_bf16 token pairs (page round-trip)", lambda: path.dequantize_bf16(1),
+        n * 2.5625, 1)
     add("dequantize_K_fp8 (page round-trip)", lambda: path.dequantize_fp8(0), n * 1.5625, 1)
+    add("dequantize_V_fp8 token pairs (page round-trip)", lambda: path.dequantize_fp8(1),
+        n * 1.5625, 1)
     wl = path.wl
     add("decode (long context)", path.decode, path.bytes_decode, 2,
         {"kv_tokens": wl.kv_tokens})
@@ -334,7 +342,7 @@ def kernel_table(path, peak):
     kv.nvfp4_kv_compute_global_scale(lay, k, gk)
     kv.nvfp4_kv_compute_global_scale(lay, v, gv)
     kv.nvfp4_kv_quantize_pages(lay, k, gk, kd, ks)
-    kv.nvfp4_kv_quantize_pages(lay, v, gv, vd, vs)
+    kv.nvfp4_kv_quantize_pages(lay.with_packing(kv.PACK_TOKEN_PAIRS), v, gv, vd, vs)
     del k, v
     out = torch.empty((db.B, db.Hq, db.D), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(kv.nvfp4_paged_decode_workspace_size(lay, db.B, db.Hq, pt.shape[1], 0),
@@ -589,7 +597,7 @@ def profile_case(kv, dev, case):
         kv.nvfp4_kv_compute_global_scale(lay, k, gk)
         kv.nvfp4_kv_compute_global_scale(lay, v, gv)
         kv.nvfp4_kv_quantize_pages(lay, k, gk, kd, ks)
-        kv.nvfp4_kv_quantize_pages(lay, v, gv, vd, vs)
+        kv.nvfp4_kv_quantize_pages(lay.with_packing(kv.PACK_TOKEN_PAIRS), v, gv, vd, vs)
         del k, v
         out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
         for _ in range(4):

@@ -10,11 +10,20 @@
  *
  * ------------------------------------------------------------------------------------------
  * Page layout (one K or V tensor of one layer; all buffers caller-owned device memory)
- *   H = layout.num_kv_heads, T = layout.page_size (tokens), D = layout.head_dim (D % 16 == 0)
- *   packed data  : uint8 [pool_pages][H][T][D/2]   element 2j in the low nibble of byte j,
- *                                                  element 2j+1 in the high nibble
- *   block scales : uint8 [pool_pages][H][T][D/16]  E4M3 bit patterns; block b of a token covers
- *                                                  elements 16b .. 16b+15 of its head_dim
+ *   H = layout.num_kv_heads, T = layout.page_size (tokens), D = layout.head_dim (D % 16 == 0).
+ *   Block b of a token covers head dims 16b .. 16b+15 and has one E4M3 scale byte. Each
+ *   (page, head) owns one contiguous run of T tokens in both pools. Two byte packings:
+ *   NVFP4KV_PACK_DIM_PAIRS (layout.packing = 0; the K cache of the decode call)
+ *     packed data  : uint8 [pool_pages][H][T][D/2]        byte j of a token: head dim 2j in the
+ *                                                         low nibble, 2j+1 in the high nibble
+ *     block scales : uint8 [pool_pages][H][T][D/16]
+ *   NVFP4KV_PACK_TOKEN_PAIRS (layout.packing = 1; the V cache of the decode call; T even)
+ *     packed data  : uint8 [pool_pages][H][T/2][D]        byte d of token pair p: head dim d of
+ *                                                         token 2p (low) and 2p+1 (high nibble)
+ *     block scales : uint8 [pool_pages][H][T/2][D/16][2]  block scales of tokens 2p, 2p+1
+ *   Both packings hold the same codes and scales and have the same size; the decode kernel
+ *   reduces over head dims for Q.K (dim pairs feed its matmul directly) and over tokens for P.V
+ *   (token pairs feed it directly).
  *   16/8-bit pages (BF16 / FP16 / FP8 E4M3 sources and outputs): [pool_pages][H][T][D]
  *   The two NVFP4 pools are read together by attention (TensorRT LLM page, Figure 6: "two pools").
  *
@@ -71,17 +80,23 @@ typedef enum nvfp4kv_status {
 #define NVFP4KV_STATUS_BAD_SEQ_LEN 0x2   /* seq_len < 0 or > max_pages_per_seq * T: seq skipped   */
 #define NVFP4KV_STATUS_TIMEOUT 0x4       /* a copy-completion wait exceeded its limit: unit skipped */
 
+typedef enum nvfp4kv_packing {
+    NVFP4KV_PACK_DIM_PAIRS = 0,   /* a byte holds two head dims of one token (K cache)          */
+    NVFP4KV_PACK_TOKEN_PAIRS = 1  /* a byte holds one head dim of two tokens (V cache)          */
+} nvfp4kv_packing;
+
 typedef enum nvfp4kv_dtype {
     NVFP4KV_BF16 = 0,
     NVFP4KV_FP16 = 1,
     NVFP4KV_FP8_E4M3 = 2
 } nvfp4kv_dtype;
 
-/* Geometry of one paged K or V tensor. head_dim % 16 == 0; all fields > 0. */
+/* Geometry of one paged K or V tensor. head_dim % 16 == 0; the first three fields > 0. */
 typedef struct nvfp4kv_layout {
     int32_t num_kv_heads; /* H */
     int32_t head_dim;     /* D */
-    int32_t page_size;    /* T, tokens per page */
+    int32_t page_size;    /* T, tokens per page (even for NVFP4KV_PACK_TOKEN_PAIRS) */
+    int32_t packing;      /* nvfp4kv_packing of the NVFP4 pool; read by the codec calls */
 } nvfp4kv_layout;
 
 /* Human-readable name of a status value (static storage). */
@@ -168,7 +183,8 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
  * Long sequences are cut into at most max_num_splits chunks (split-KV); each chunk produces a
  * partial (max, sum, unnormalised output) in the workspace and a second kernel merges them.
  *   q              BF16 [batch][num_q_heads][D]
- *   k_data, k_scales, v_data, v_scales   NVFP4 pools [pool_pages][H][T][..]
+ *   k_data, k_scales   NVFP4 K pool in NVFP4KV_PACK_DIM_PAIRS (layout.packing is not read)
+ *   v_data, v_scales   NVFP4 V pool in NVFP4KV_PACK_TOKEN_PAIRS
  *   k_global_scale, v_global_scale       device scalars g_K, g_V
  *   page_table     int32 [batch][max_pages_per_seq] device
  *   seq_lens       int32 [batch] device; 0 <= seq_len <= max_pages_per_seq * T

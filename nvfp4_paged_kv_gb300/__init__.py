@@ -19,7 +19,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "Layout", "BF16", "FP16", "FP8_E4M3", "STATUS_PAGE_OOB", "STATUS_BAD_SEQ_LEN",
+    "Layout", "BF16", "FP16", "FP8_E4M3", "PACK_DIM_PAIRS", "PACK_TOKEN_PAIRS",
+    "STATUS_PAGE_OOB", "STATUS_BAD_SEQ_LEN",
     "STATUS_TIMEOUT", "NVFP4KVError", "load", "lib_path", "version",
     "nvfp4_kv_global_scale_workspace_size", "nvfp4_kv_compute_global_scale",
     "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages",
@@ -29,21 +30,26 @@ __all__ = [
 NOALLOC_SCRATCH_BYTES = 32 << 20   # NVFP4KV_NOALLOC_SCRATCH_BYTES
 
 BF16, FP16, FP8_E4M3 = 0, 1, 2
+PACK_DIM_PAIRS, PACK_TOKEN_PAIRS = 0, 1   # nvfp4kv_packing: K pools, V pools of the decode call
 STATUS_PAGE_OOB, STATUS_BAD_SEQ_LEN, STATUS_TIMEOUT = 0x1, 0x2, 0x4
 _STATUS_NAMES = {1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA"}
 
 
 class Layout(ctypes.Structure):
-    """Geometry of one paged K or V tensor (``nvfp4kv_layout``)."""
+    """Geometry and byte packing of one paged K or V tensor (``nvfp4kv_layout``)."""
     _fields_ = [("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("page_size", ctypes.c_int32)]
+                ("page_size", ctypes.c_int32), ("packing", ctypes.c_int32)]
 
-    def __init__(self, num_kv_heads: int, head_dim: int, page_size: int):
-        super().__init__(int(num_kv_heads), int(head_dim), int(page_size))
+    def __init__(self, num_kv_heads: int, head_dim: int, page_size: int,
+                 packing: int = PACK_DIM_PAIRS):
+        super().__init__(int(num_kv_heads), int(head_dim), int(page_size), int(packing))
+
+    def with_packing(self, packing: int) -> "Layout":
+        return Layout(self.num_kv_heads, self.head_dim, self.page_size, packing)
 
     def __repr__(self):
         return (f"Layout(num_kv_heads={self.num_kv_heads}, head_dim={self.head_dim}, "
-                f"page_size={self.page_size})")
+                f"page_size={self.page_size}, packing={self.packing})")
 
 
 class NVFP4KVError(RuntimeError):

@@ -63,32 +63,17 @@ __device__ __forceinline__ uint32_t ld_stream_1B(const void* p) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Encode one block of 16 exact fp32 values.
-//   a  = max |x_i|                                  (exact)
-//   s  = E4M3_rne_satfinite(fp32(a / d)), d = fp32(6 g)   -- one IEEE division
-//   r  = fp32(1 / fp32(s g)), or 0 when s g == 0            -- one IEEE reciprocal
+// Encode one block of 16 exact fp32 values x:
+//   a  = max |x_i|                                          (exact)
+//   s  = E4M3_rne_satfinite(fp32(a / d)), d = fp32(6 g)      one IEEE division
+//   r  = fp32(1 / fp32(s g)), or 0 when s g == 0             one IEEE reciprocal
 //   c_i = E2M1_rne_satfinite(fp32(x_i * r)), sign kept
-// Packed codes: element 2j in the low nibble of byte j.
 // ------------------------------------------------------------------------------------------
-__device__ __forceinline__ void encode_block16(const float (&x)[16], float g, float d,
-                                               uint32_t& w0, uint32_t& w1, uint32_t& sbyte) {
-    float a = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(x[k]));
-    const float q = __fdiv_rn(a, d);
-    sbyte = f32x2_to_e4m3x2(q, 0.0f) & 0xFFu;
-    const float s = e4m3_to_f32(sbyte);
-    const float sg = __fmul_rn(s, g);
-    const float r = (sg == 0.0f) ? 0.0f : __frcp_rn(sg);
-    w0 = 0u;
-    w1 = 0u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        w0 |= f32x2_to_e2m1x2(__fmul_rn(x[2 * j], r), __fmul_rn(x[2 * j + 1], r)) << (8 * j);
-        w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r))
-              << (8 * j);
-    }
+// n / d for n * d < 2^40 with a 64-bit multiply: magic = ceil(2^40 / d).
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint64_t magic) {
+    return static_cast<uint32_t>((static_cast<uint64_t>(n) * magic) >> 40);
 }
+inline uint64_t div_magic(uint32_t d) { return ((uint64_t{1} << 40) + d - 1) / d; }
 
 struct QuantParams {
     const void* src;
@@ -102,14 +87,83 @@ struct QuantParams {
     int32_t dst_pool;
     int32_t num_pages;
     int32_t bpp;            // 16-value blocks per page = H * T * D / 16
-    int32_t items_per_page; // ceil(bpp / kItemBlocks)
+    int32_t nb;             // blocks per token row = D / 16
+    uint64_t nb_magic;      // div_magic(nb)
+    int32_t units;          // work units per page (blocks, or block pairs for token pairs)
+    int32_t items_per_page; // ceil(units / kItemUnits)
     int32_t* status;
 };
 
-// SRC: NVFP4KV_BF16, NVFP4KV_FP16 or NVFP4KV_FP8_E4M3. A32: the 16-bit source is 32-byte
-// aligned, so each block is one 256-bit load (else two 128-bit loads).
+// One block of 16 source values as loaded: 32 bytes (16-bit sources) or 16 bytes (FP8).
 template <int SRC, bool A32>
+__device__ __forceinline__ U8x32 load_raw(const void* src, int64_t blk) {
+    U8x32 raw;
+    if constexpr (SRC == NVFP4KV_FP8_E4M3) {
+        const uint4 v = ld_stream_16B(static_cast<const uint8_t*>(src) + blk * 16);
+        raw.w[0] = v.x;
+        raw.w[1] = v.y;
+        raw.w[2] = v.z;
+        raw.w[3] = v.w;
+    } else {
+        const uint8_t* a = static_cast<const uint8_t*>(src) + blk * 32;
+        if constexpr (A32) {
+            raw = ld_stream_32B(a);
+        } else {
+            const uint4 lo = ld_stream_16B(a), hi = ld_stream_16B(a + 16);
+            raw = U8x32{{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w}};
+        }
+    }
+    return raw;
+}
+
+// The 16 values as exact fp32 (BF16 / FP16 widening is exact; FP8 sources are
+// x = fp32(e4m3 * src_scale)).
+template <int SRC>
+__device__ __forceinline__ void widen(const U8x32& raw, float sscale, float (&x)[16]) {
+    if constexpr (SRC == NVFP4KV_FP8_E4M3) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t h[2];
+            e4m3x4_to_f16x2x2(raw.w[j], h);
+            x[4 * j + 0] = __fmul_rn(f16_lo(h[0]), sscale);
+            x[4 * j + 1] = __fmul_rn(f16_hi(h[0]), sscale);
+            x[4 * j + 2] = __fmul_rn(f16_lo(h[1]), sscale);
+            x[4 * j + 3] = __fmul_rn(f16_hi(h[1]), sscale);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if constexpr (SRC == NVFP4KV_BF16) {
+                x[2 * j] = bf16_lo(raw.w[j]);
+                x[2 * j + 1] = bf16_hi(raw.w[j]);
+            } else {
+                x[2 * j] = f16_lo(raw.w[j]);
+                x[2 * j + 1] = f16_hi(raw.w[j]);
+            }
+        }
+    }
+}
+
+// Block scale pick of one block: s, and r = fp32(1 / fp32(s g)) (0 when s g == 0).
+__device__ __forceinline__ void pick_scale(const float (&x)[16], float g, float d,
+                                           uint32_t& sbyte, float& r) {
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(x[k]));
+    sbyte = f32x2_to_e4m3x2(__fdiv_rn(a, d), 0.0f) & 0xFFu;
+    const float sg = __fmul_rn(e4m3_to_f32(sbyte), g);
+    r = (sg == 0.0f) ? 0.0f : __frcp_rn(sg);
+}
+
+// SRC: NVFP4KV_BF16, NVFP4KV_FP16 or NVFP4KV_FP8_E4M3. A32: a 16-bit source is 32-byte aligned
+// (one 256-bit load per block). PACK: NVFP4KV_PACK_DIM_PAIRS (a unit is one block of one token)
+// or NVFP4KV_PACK_TOKEN_PAIRS (a unit is the same block of tokens 2p and 2p+1; the E2M1 pair
+// conversion of (token 2p, token 2p+1) at one head dim is directly the interleaved byte).
+template <int SRC, bool A32, int PACK>
 __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantParams p) {
+    constexpr int kUnitsPerThread = (PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? kBlocksPerThread / 2
+                                                                        : kBlocksPerThread;
+    constexpr int kItemUnits = kThreads * kUnitsPerThread;
     const float g = __ldg(p.g);
     const float d = __fmul_rn(6.0f, g);
     const float sscale = (SRC == NVFP4KV_FP8_E4M3 && p.src_scale) ? __ldg(p.src_scale) : 1.0f;
@@ -125,82 +179,81 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
         }
         const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
         const int64_t dst_blk0 = static_cast<int64_t>(dp) * p.bpp;
-        const int32_t blk_begin = k * kItemBlocks + threadIdx.x;
-
-        if constexpr (SRC == NVFP4KV_FP8_E4M3) {
-            uint4 raw[kBlocksPerThread];
+        const int32_t u_begin = k * kItemUnits + threadIdx.x;
+        if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+            U8x32 raw[kUnitsPerThread];
 #pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t blk = blk_begin + u * kThreads;
-                if (blk < p.bpp)
-                    raw[u] = ld_stream_16B(static_cast<const uint8_t*>(p.src) +
-                                           (src_blk0 + blk) * 16);
+            for (int u = 0; u < kUnitsPerThread; ++u) {
+                const int32_t blk = u_begin + u * kThreads;
+                if (blk < p.units) raw[u] = load_raw<SRC, A32>(p.src, src_blk0 + blk);
             }
 #pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t blk = blk_begin + u * kThreads;
-                if (blk >= p.bpp) continue;
-                const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            for (int u = 0; u < kUnitsPerThread; ++u) {
+                const int32_t blk = u_begin + u * kThreads;
+                if (blk >= p.units) continue;
                 float x[16];
+                widen<SRC>(raw[u], sscale, x);
+                uint32_t sb;
+                float r;
+                pick_scale(x, g, d, sb, r);
+                uint32_t w0 = 0u, w1 = 0u;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t lo = e4m3x2_to_f16x2(wv[j] & 0xFFFFu);
-                    const uint32_t hi = e4m3x2_to_f16x2(wv[j] >> 16);
-                    x[4 * j + 0] = __fmul_rn(f16_lo(lo), sscale);
-                    x[4 * j + 1] = __fmul_rn(f16_hi(lo), sscale);
-                    x[4 * j + 2] = __fmul_rn(f16_lo(hi), sscale);
-                    x[4 * j + 3] = __fmul_rn(f16_hi(hi), sscale);
+                    w0 |= f32x2_to_e2m1x2(__fmul_rn(x[2 * j], r), __fmul_rn(x[2 * j + 1], r))
+                          << (8 * j);
+                    w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r))
+                          << (8 * j);
                 }
-                uint32_t w0, w1, sb;
-                encode_block16(x, g, d, w0, w1, sb);
                 *reinterpret_cast<uint2*>(p.dst_data + (dst_blk0 + blk) * 8) = make_uint2(w0, w1);
                 p.dst_scales[dst_blk0 + blk] = static_cast<uint8_t>(sb);
             }
         } else {
-            U8x32 raw[kBlocksPerThread];
+            U8x32 raw0[kUnitsPerThread], raw1[kUnitsPerThread];
 #pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t blk = blk_begin + u * kThreads;
-                if (blk < p.bpp) {
-                    const uint8_t* a = static_cast<const uint8_t*>(p.src) + (src_blk0 + blk) * 32;
-                    if constexpr (A32) {
-                        raw[u] = ld_stream_32B(a);
-                    } else {
-                        const uint4 lo = ld_stream_16B(a), hi = ld_stream_16B(a + 16);
-                        raw[u] = U8x32{{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w}};
-                    }
+            for (int u = 0; u < kUnitsPerThread; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit < p.units) {
+                    const uint32_t row_pair = fast_div(unit, p.nb_magic);
+                    const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
+                    const int64_t blk = src_blk0 + static_cast<int64_t>(2 * row_pair) * p.nb + b;
+                    raw0[u] = load_raw<SRC, A32>(p.src, blk);
+                    raw1[u] = load_raw<SRC, A32>(p.src, blk + p.nb);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t blk = blk_begin + u * kThreads;
-                if (blk >= p.bpp) continue;
-                float x[16];
+            for (int u = 0; u < kUnitsPerThread; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit >= p.units) continue;
+                float x0[16], x1[16];
+                widen<SRC>(raw0[u], sscale, x0);
+                widen<SRC>(raw1[u], sscale, x1);
+                uint32_t s0, s1;
+                float r0, r1;
+                pick_scale(x0, g, d, s0, r0);
+                pick_scale(x1, g, d, s1, r1);
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if constexpr (SRC == NVFP4KV_BF16) {
-                        x[2 * j] = bf16_lo(raw[u].w[j]);
-                        x[2 * j + 1] = bf16_hi(raw[u].w[j]);
-                    } else {
-                        x[2 * j] = f16_lo(raw[u].w[j]);
-                        x[2 * j + 1] = f16_hi(raw[u].w[j]);
-                    }
-                }
-                uint32_t w0, w1, sb;
-                encode_block16(x, g, d, w0, w1, sb);
-                *reinterpret_cast<uint2*>(p.dst_data + (dst_blk0 + blk) * 8) = make_uint2(w0, w1);
-                p.dst_scales[dst_blk0 + blk] = static_cast<uint8_t>(sb);
+                for (int e = 0; e < 16; ++e)
+                    w[e >> 2] |= f32x2_to_e2m1x2(__fmul_rn(x0[e], r0), __fmul_rn(x1[e], r1))
+                                 << (8 * (e & 3));
+                // unit index = (row pair, block): data at unit * 16, scales at unit * 2
+                const int64_t o = dst_blk0 / 2 + unit;
+                *reinterpret_cast<uint4*>(p.dst_data + o * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint16_t*>(p.dst_scales + o * 2) =
+                    static_cast<uint16_t>(s0 | (s1 << 8));
             }
         }
     }
 }
 
 // ------------------------------------------------------------------------------------------
-// Decode. One thread turns half a block (8 codes = 4 bytes, plus the block's scale byte) into
-// 8 outputs. v = e2m1(c) * e4m3(s) is formed exactly in FP16 (cvt.rn.f16x2.e2m1x2 and
+// Decode. v = e2m1(c) * e4m3(s) is formed exactly in FP16 (cvt.rn.f16x2.e2m1x2 and
 // cvt.rn.f16x2.e4m3x2 are exact, and the product has at most 6 significant bits), widened to
 // fp32 exactly, multiplied by g (BF16 / FP16 out) or m = fp32(g / dst_scale) (FP8 out) with
 // one IEEE fp32 multiply, and rounded to the output type to nearest even (FP8 saturating).
+// A unit is 8 codes: half a block of one token (dim pairs: 4 code bytes + the block's scale,
+// 8 outputs of one token) or 8 head dims of a token pair (token pairs: 8 code bytes + the
+// pair's 2 scales, 8 outputs for each of the two tokens).
 // ------------------------------------------------------------------------------------------
 struct DequantParams {
     const uint8_t* src_data;
@@ -214,17 +267,39 @@ struct DequantParams {
     int32_t dst_pool;
     int32_t num_pages;
     int32_t bpp;            // blocks per page
-    int32_t items_per_page; // ceil(2 * bpp / kItemBlocks)
+    int32_t nb;             // blocks per token row
+    uint64_t nb2_magic;     // div_magic(2 * nb)
+    int32_t units;          // units per page
+    int32_t items_per_page; // ceil(units / kItemBlocks)
     int32_t* status;
 };
 
 template <int DST>
+__device__ __forceinline__ void store8(void* dst, int64_t elem, const float (&y)[8]) {
+    if constexpr (DST == NVFP4KV_FP8_E4M3) {
+        uint2 o;
+        o.x = f32x2_to_e4m3x2(y[0], y[1]) | (f32x2_to_e4m3x2(y[2], y[3]) << 16);
+        o.y = f32x2_to_e4m3x2(y[4], y[5]) | (f32x2_to_e4m3x2(y[6], y[7]) << 16);
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + elem) = o;
+    } else {
+        uint4 o;
+        if constexpr (DST == NVFP4KV_BF16) {
+            o = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                           pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+        } else {
+            o = make_uint4(pack_f16x2(y[0], y[1]), pack_f16x2(y[2], y[3]),
+                           pack_f16x2(y[4], y[5]), pack_f16x2(y[6], y[7]));
+        }
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst) + elem * 2) = o;
+    }
+}
+
+template <int DST, int PACK>
 __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const DequantParams p) {
     const float g = __ldg(p.g);
     const float mult = (DST == NVFP4KV_FP8_E4M3)
                            ? (p.dst_scale ? __fdiv_rn(g, __ldg(p.dst_scale)) : g)
                            : g;
-    const int32_t units = 2 * p.bpp; // half blocks per page
     const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
     for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int32_t i = static_cast<int32_t>(item / p.items_per_page);
@@ -236,50 +311,72 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
             continue;
         }
         const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
-        const int64_t dst_unit0 = static_cast<int64_t>(dp) * units;
+        const int64_t dst_elem0 = static_cast<int64_t>(dp) * p.bpp * 16;
         const int32_t u_begin = k * kItemBlocks + threadIdx.x;
-        uint32_t code[kBlocksPerThread], sbyte[kBlocksPerThread];
+        if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+            uint32_t code[kBlocksPerThread], sbyte[kBlocksPerThread];
 #pragma unroll
-        for (int u = 0; u < kBlocksPerThread; ++u) {
-            const int32_t unit = u_begin + u * kThreads;
-            if (unit < units) {
-                code[u] = ld_stream_4B(p.src_data + (src_blk0 * 2 + unit) * 4);
-                sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + (unit >> 1));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kBlocksPerThread; ++u) {
-            const int32_t unit = u_begin + u * kThreads;
-            if (unit >= units) continue;
-            const uint32_t s2 = e4m3x2_to_f16x2(sbyte[u] * 0x0101u); // (s, s)
-            float y[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t v2 = hmul2_u32(e2m1x2_to_f16x2(code[u] >> (8 * j)), s2);
-                y[2 * j] = __fmul_rn(f16_lo(v2), mult);
-                y[2 * j + 1] = __fmul_rn(f16_hi(v2), mult);
-            }
-            if constexpr (DST == NVFP4KV_FP8_E4M3) {
-                uint2 o;
-                o.x = f32x2_to_e4m3x2(y[0], y[1]) | (f32x2_to_e4m3x2(y[2], y[3]) << 16);
-                o.y = f32x2_to_e4m3x2(y[4], y[5]) | (f32x2_to_e4m3x2(y[6], y[7]) << 16);
-                *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.dst) + (dst_unit0 + unit) * 8) =
-                    o;
-            } else {
-                uint4 o;
-                if constexpr (DST == NVFP4KV_BF16) {
-                    o.x = pack_bf16x2(y[0], y[1]);
-                    o.y = pack_bf16x2(y[2], y[3]);
-                    o.z = pack_bf16x2(y[4], y[5]);
-                    o.w = pack_bf16x2(y[6], y[7]);
-                } else {
-                    o.x = pack_f16x2(y[0], y[1]);
-                    o.y = pack_f16x2(y[2], y[3]);
-                    o.z = pack_f16x2(y[4], y[5]);
-                    o.w = pack_f16x2(y[6], y[7]);
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit < p.units) {
+                    code[u] = ld_stream_4B(p.src_data + (src_blk0 * 2 + unit) * 4);
+                    sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + (unit >> 1));
                 }
-                *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) +
-                                          (dst_unit0 + unit) * 16) = o;
+            }
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit >= p.units) continue;
+                const uint32_t s2 = e4m3x2_to_f16x2(sbyte[u] * 0x0101u);  // (s, s)
+                uint32_t v[4];
+                e2m1x8_to_f16x2x4(code[u], v);
+                float y[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t v2 = hmul2_u32(v[j], s2);
+                    y[2 * j] = __fmul_rn(f16_lo(v2), mult);
+                    y[2 * j + 1] = __fmul_rn(f16_hi(v2), mult);
+                }
+                store8<DST>(p.dst, dst_elem0 + static_cast<int64_t>(unit) * 8, y);
+            }
+        } else {
+            uint2 code[kBlocksPerThread];
+            uint32_t spair[kBlocksPerThread];
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit < p.units) {
+                    code[u] = *reinterpret_cast<const uint2*>(p.src_data + src_blk0 * 8 +
+                                                              static_cast<int64_t>(unit) * 8);
+                    // the unit's block: (row pair, block) = unit / 2; its two scales side by side
+                    spair[u] = *reinterpret_cast<const uint16_t*>(p.src_scales + src_blk0 +
+                                                                  (unit >> 1) * 2);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kBlocksPerThread; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit >= p.units) continue;
+                const uint32_t s2 = e4m3x2_to_f16x2(spair[u]);  // (s token 2p, s token 2p+1)
+                const uint32_t row_pair = fast_div(unit, p.nb2_magic);
+                const int32_t rem = unit - static_cast<int32_t>(row_pair) * 2 * p.nb;  // 8-dim slot
+                float y0[8], y1[8];
+                const uint32_t words[2] = {code[u].x, code[u].y};
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t v[4];
+                    e2m1x8_to_f16x2x4(words[q], v);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t v2 = hmul2_u32(v[j], s2);  // (token 2p, token 2p+1)
+                        y0[4 * q + j] = __fmul_rn(f16_lo(v2), mult);
+                        y1[4 * q + j] = __fmul_rn(f16_hi(v2), mult);
+                    }
+                }
+                const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * row_pair) * p.nb * 16 +
+                                   rem * 8;
+                store8<DST>(p.dst, e0, y0);
+                store8<DST>(p.dst, e0 + p.nb * 16, y1);
             }
         }
     }
@@ -485,9 +582,13 @@ extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
     if ((!src_page_ids && src_pool_pages < num_pages) ||
         (!dst_page_ids && dst_pool_pages < num_pages))
         return NVFP4KV_ERR_INVALID_ARG;
+    const int pack = layout->packing;
+    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
     const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
                           (layout->head_dim / 16);
-    if (bpp64 > (int64_t{1} << 30)) return NVFP4KV_ERR_UNSUPPORTED;
+    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
     QuantParams p{};
     p.src = src;
     p.src_ids = src_page_ids;
@@ -500,22 +601,37 @@ extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
     p.dst_pool = dst_pool_pages;
     p.num_pages = num_pages;
     p.bpp = static_cast<int32_t>(bpp64);
-    p.items_per_page = (p.bpp + kItemBlocks - 1) / kItemBlocks;
+    p.nb = layout->head_dim / 16;
+    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
+    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
+    const int item_units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? kItemBlocks / 2 : kItemBlocks;
+    p.items_per_page = (p.units + item_units - 1) / item_units;
     p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
     const bool a32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
+#define NVFP4KV_QLAUNCH(SRC, A32, PK) \
+    quantize_pages_kernel<SRC, A32, PK><<<grid, kThreads, 0, s>>>(p)
+#define NVFP4KV_QPACK(SRC, A32)                                          \
+    do {                                                                  \
+        if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                             \
+            NVFP4KV_QLAUNCH(SRC, A32, NVFP4KV_PACK_TOKEN_PAIRS);          \
+        else                                                              \
+            NVFP4KV_QLAUNCH(SRC, A32, NVFP4KV_PACK_DIM_PAIRS);            \
+    } while (0)
     switch (src_dtype) {
     case NVFP4KV_BF16:
-        if (a32) quantize_pages_kernel<NVFP4KV_BF16, true><<<grid, kThreads, 0, s>>>(p);
-        else quantize_pages_kernel<NVFP4KV_BF16, false><<<grid, kThreads, 0, s>>>(p);
+        if (a32) NVFP4KV_QPACK(NVFP4KV_BF16, true);
+        else NVFP4KV_QPACK(NVFP4KV_BF16, false);
         break;
     case NVFP4KV_FP16:
-        if (a32) quantize_pages_kernel<NVFP4KV_FP16, true><<<grid, kThreads, 0, s>>>(p);
-        else quantize_pages_kernel<NVFP4KV_FP16, false><<<grid, kThreads, 0, s>>>(p);
+        if (a32) NVFP4KV_QPACK(NVFP4KV_FP16, true);
+        else NVFP4KV_QPACK(NVFP4KV_FP16, false);
         break;
-    default: quantize_pages_kernel<NVFP4KV_FP8_E4M3, false><<<grid, kThreads, 0, s>>>(p); break;
+    default: NVFP4KV_QPACK(NVFP4KV_FP8_E4M3, false); break;
     }
+#undef NVFP4KV_QPACK
+#undef NVFP4KV_QLAUNCH
     return launch_status();
 }
 
@@ -534,9 +650,13 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     if ((!src_page_ids && src_pool_pages < num_pages) ||
         (!dst_page_ids && dst_pool_pages < num_pages))
         return NVFP4KV_ERR_INVALID_ARG;
+    const int pack = layout->packing;
+    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
     const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
                           (layout->head_dim / 16);
-    if (bpp64 > (int64_t{1} << 29)) return NVFP4KV_ERR_UNSUPPORTED;
+    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
     DequantParams p{};
     p.src_data = src_data;
     p.src_scales = src_scales;
@@ -549,15 +669,27 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     p.dst_pool = dst_pool_pages;
     p.num_pages = num_pages;
     p.bpp = static_cast<int32_t>(bpp64);
-    p.items_per_page = (2 * p.bpp + kItemBlocks - 1) / kItemBlocks;
+    p.nb = layout->head_dim / 16;
+    p.nb2_magic = div_magic(static_cast<uint32_t>(2 * p.nb));
+    // 8 codes per dim-pair unit (2 per block); 16 codes per token-pair unit (2 per block pair)
+    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp : 2 * p.bpp;
+    p.items_per_page = (p.units + kItemBlocks - 1) / kItemBlocks;
     p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
+#define NVFP4KV_DQLAUNCH(DST)                                                                \
+    do {                                                                                      \
+        if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                                                 \
+            dequantize_pages_kernel<DST, NVFP4KV_PACK_TOKEN_PAIRS><<<grid, kThreads, 0, s>>>(p); \
+        else                                                                                  \
+            dequantize_pages_kernel<DST, NVFP4KV_PACK_DIM_PAIRS><<<grid, kThreads, 0, s>>>(p);   \
+    } while (0)
     switch (dst_dtype) {
-    case NVFP4KV_BF16: dequantize_pages_kernel<NVFP4KV_BF16><<<grid, kThreads, 0, s>>>(p); break;
-    case NVFP4KV_FP16: dequantize_pages_kernel<NVFP4KV_FP16><<<grid, kThreads, 0, s>>>(p); break;
-    default: dequantize_pages_kernel<NVFP4KV_FP8_E4M3><<<grid, kThreads, 0, s>>>(p); break;
+    case NVFP4KV_BF16: NVFP4KV_DQLAUNCH(NVFP4KV_BF16); break;
+    case NVFP4KV_FP16: NVFP4KV_DQLAUNCH(NVFP4KV_FP16); break;
+    default: NVFP4KV_DQLAUNCH(NVFP4KV_FP8_E4M3); break;
     }
+#undef NVFP4KV_DQLAUNCH
     return launch_status();
 }
 

@@ -33,6 +33,24 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
     return out;
 }
 
+// The four bytes of w, each as two E2M1 codes -> FP16 pair (o[k] from byte k). The bytes are
+// split with a vector move into 8-bit registers, which the conversions read directly (no shifts).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// The two 16-bit halves of w, each as two E4M3 bytes -> FP16 pair (o[0] from the low half).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t (&o)[2]) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(o[0]), "=r"(o[1])
+        : "r"(w));
+}
+
 // Two E4M3 bytes (low byte -> low half) to two exact FP16 values: cvt.rn.f16x2.e4m3x2.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes_in_low_bits) {
     uint32_t out;

@@ -8,26 +8,27 @@
 // ("supplied through the attention BMM scaling parameters").
 //
 // Design for GB300 (the SM120 kernel of the LMSYS page is prior art, not the blueprint):
-//  * one CTA per (sequence, KV head, split) of 4 warps; a split is a run of 64-token stages.
-//    Each stage is staged into shared memory by 1-D bulk async copies (TMA engine, one issuing
-//    thread, L2 evict-first) of the packed K/V rows and their E4M3 scales, page by page through
-//    the page table, into a 4-deep ring tracked by mbarriers with transaction counts.
-//  * each warp owns 16 tokens of a stage. S^T = K^ Q^T on the tensor cores with tokens as the
-//    M = 16 dimension and the GQA query group as N = 8 (mma.sync m16n8k16, FP16 in, FP32
-//    accumulate): the decoded K values e2m1 * e4m3 are exact in FP16 (cvt.rn.f16x2.e2m1x2,
-//    cvt.rn.f16x2.e4m3x2, one packed multiply), and Q is brought into FP16 exactly by a
-//    per-head power of two. The head dimension inside a k-step is permuted identically in K and
-//    Q so that every K fragment register is one converted byte.
-//  * online softmax in the log2 domain with warp shuffles for the column maxima; the running
-//    maximum is only moved when it grows by more than 2^8, so rescaling of the accumulators is
-//    rare. P^T goes from the score accumulator layout to the B-operand layout with movmatrix.
-//  * O^T += V^^T P^T with head_dim as M: V tiles are read transposed with ldmatrix.trans, each
-//    register is split into four e2m1x2 conversions and re-paired by token with byte permutes,
-//    and the V block scales are applied per element pair (exact in FP16).
-//  * the 4 warps merge their (max, sum, output) in shared memory and the CTA writes one
-//    partial per (sequence, query head, split); a second kernel merges the splits by their
-//    log-sum-exp and writes BF16 output and the natural-log LSE.
-// Everything is HBM-bound: 144 bytes of K+V per (token, KV head) at head_dim 128.
+//  * one CTA per (sequence, KV head, split) of 4 warps; a split is a run of 64-token stages and
+//    warp w owns the 16-token tiles w, w+4, w+8, ... of it. Each warp streams its own tiles
+//    through a private 4-slot shared-memory ring with asynchronous copies (cp.async, 16 bytes
+//    per lane, completion per warp by wait_group): packed K rows, token-pair packed V rows and
+//    both scale pools of a tile are four contiguous runs of its page. The warps never wait for
+//    one another until the final merge, so each keeps three tiles in flight behind the one it
+//    computes. V rows land XOR-swizzled by 16-byte chunk so the fragment reads hit distinct banks.
+//  * S^T = K^ Q^T runs on the tensor cores with tokens as M = 16 and the GQA query group as
+//    N = 8 (mma.sync m16n8k16, FP16 in, FP32 accumulate). K is stored dim-pair packed, so every
+//    converted byte (cvt.rn.f16x2.e2m1x2) is one A-register: two adjacent head dims of one
+//    token, exact in FP16, times its E4M3 block scale (exact). Q is brought into FP16 exactly by
+//    a per-head power of two; head dims inside a k-step are permuted identically in K and Q.
+//  * online softmax in the log2 domain, column maxima by warp shuffles; the running maximum
+//    moves only when it grows by more than 2^8, so accumulator rescaling is rare. P^T moves from
+//    the score layout to the B-operand layout with movmatrix.
+//  * O^T += V^^T P^T with head dims as M: V is stored token-pair packed, so every converted byte
+//    is one A-register (one head dim of two adjacent tokens) times the pair's two block scales.
+//  * the 4 warps merge (max, sum, output) in shared memory and the CTA writes one partial per
+//    (sequence, query head, split); a second kernel merges the splits by log-sum-exp and writes
+//    the BF16 output and the natural-log LSE.
+// Bytes per (token, KV head) at head_dim 128: 64 + 8 (K) + 64 + 8 (V) = 144.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -39,24 +40,33 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kDecThreads = kWarps * 32;
-constexpr int kStageTokens = 64;
-constexpr int kStages = 4;
+constexpr int kStageTokens = 64;  // split granularity (4 warps x 16-token tiles)
+constexpr int kSlots = 4;         // tiles per warp ring
 constexpr int kMaxGroup = 8;
 constexpr int kMaxSplits = 64;
-constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;  // 0.5 s per copy-completion wait
+constexpr int kPageBuf = 256; // page ids of a split kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct Geo {
-    static constexpr int KD = kStageTokens * D / 2;   // packed bytes of one stage of K (or V)
-    static constexpr int KS = kStageTokens * D / 16;  // scale bytes of one stage of K (or V)
-    static constexpr int STAGE = 2 * (KD + KS);
-    static constexpr int NB = D / 16;                 // blocks (= scales) per token row
-    static constexpr int KSTEPS = D / 16;             // k-steps of S^T = K Q^T
-    static constexpr int SEGS = D / 32;               // 16-byte segments of a packed token row
-    static constexpr int CHUNK = D / 8;               // bytes of a K row owned by one quad lane
-    static constexpr int SMEM = kStages * STAGE;
+    static constexpr int NB = D / 16;            // blocks (= scales) per token row
+    static constexpr int TK = 16 * D / 2;         // packed K rows of a 16-token tile
+    static constexpr int TV = 8 * D;              // token-pair V rows of a tile (8 pairs)
+    static constexpr int TS = 16 * NB;            // one scale pool of a tile
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = TK;
+    static constexpr int KS_OFF = TK + TV;
+    static constexpr int VS_OFF = TK + TV + TS;
+    static constexpr int SLOT = TK + TV + 2 * TS;  // 18 D bytes
+    static constexpr int RING = kSlots * SLOT;     // per warp
+    static constexpr int SMEM = kWarps * RING;
+    static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
+    static constexpr int CHUNK = D / 8;            // bytes of a row one quad lane owns
+    static constexpr int CW = CHUNK / 4;           // ... as 32-bit words
+    static constexpr int VCH = D / 16;             // 16-byte chunks per V pair row
+    static constexpr int SWZ = (VCH < 8 ? VCH : 8) - 1;  // chunk XOR mask
+    static_assert(kWarps * kMaxGroup * D * 4 <= SMEM, "merge buffer must fit in the rings");
 };
 
 struct DecodeParams {
@@ -83,40 +93,61 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// E4M3 byte `k` of word w, as an FP16 pair (s, s).
-__device__ __forceinline__ uint32_t scale_bcast(uint32_t w, int k) {
-    const uint32_t b = (w >> (8 * k)) & 0xFFu;
-    return e4m3x2_to_f16x2(b * 0x0101u);
-}
+// The two halves of an FP16 pair, each broadcast to both halves.
+__device__ __forceinline__ uint32_t h2_lo_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
+__device__ __forceinline__ uint32_t h2_hi_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
 
 template <int N>
-__device__ __forceinline__ void lds_words(uint32_t (&w)[N], const uint8_t* p) {
+__device__ __forceinline__ void lds_words(uint32_t (&w)[N], uint32_t addr) {
     if constexpr (N == 1) {
-        w[0] = *reinterpret_cast<const uint32_t*>(p);
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[0]) : "r"(addr));
     } else if constexpr (N == 2) {
-        const uint2 v = *reinterpret_cast<const uint2*>(p);
-        w[0] = v.x;
-        w[1] = v.y;
+        asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
     } else {
 #pragma unroll
-        for (int i = 0; i < N; i += 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p + 4 * i);
-            w[i] = v.x;
-            w[i + 1] = v.y;
-            w[i + 2] = v.z;
-            w[i + 3] = v.w;
-        }
+        for (int i = 0; i < N; i += 4)
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w[i]), "=r"(w[i + 1]), "=r"(w[i + 2]), "=r"(w[i + 3])
+                         : "r"(addr + 4 * i));
     }
 }
 
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// Shared-memory offset of byte x of token-pair row pr of a tile's V rows: 16-byte chunks are
+// XOR-swizzled by the row so that the 4 lanes of a quad (rows c and c+4) hit distinct banks.
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const DecodeParams p) {
+__device__ __forceinline__ uint32_t v_swz(int pr, int x) {
+    return static_cast<uint32_t>(pr * D + ((((x >> 4) ^ (pr & Geo<D>::SWZ))) << 4) + (x & 15));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
+    decode_split_kernel(const DecodeParams p) {
     using G_ = Geo<D>;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ uint64_t stage_mask[kStages];
     __shared__ float red_m[kWarps][kMaxGroup];
     __shared__ float red_l[kWarps][kMaxGroup];
+    __shared__ int page_ids[kPageBuf];
 
     const int split = blockIdx.x;
     const int h = blockIdx.y;
@@ -136,64 +167,58 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const Deco
     const int st_begin = split * p.stages_per_split;
     const int st_end = min(st_begin + p.stages_per_split, total_stages);
     if (st_begin >= st_end) return;  // beyond this sequence: no partial (combine skips it)
-    const int nst = st_end - st_begin;
+    const int tok_begin = st_begin * kStageTokens;
+    const int tok_end = min(st_end * kStageTokens, L);
     const int G = p.G;
     const int64_t part_row = (static_cast<int64_t>(b) * p.Hq + h * G) * p.num_splits + split;
 
-    // ---------------------------------------------------------------- producer (thread 0)
-    const uint64_t policy = l2_policy_evict_first();
-    auto issue_stage = [&](int gs, int slot) {
-        const int tok0 = gs * kStageTokens;
-        uint8_t* st = smem + slot * G_::STAGE;
-        int piece_tok[kStageTokens / 16], piece_n[kStageTokens / 16], piece_pg[kStageTokens / 16];
-        int np = 0;
-        uint64_t mask = 0;
-        uint32_t bytes = 0;
-        for (int t = tok0; t < tok0 + kStageTokens && t < L;) {
-            const int pidx = t / p.T;
-            const int off = t - pidx * p.T;
-            const int n = min(p.T - off, tok0 + kStageTokens - t);
-            const int page = __ldg(p.page_table + static_cast<int64_t>(b) * p.max_pages + pidx);
-            if (page >= 0 && page < p.pool_pages) {
-                piece_tok[np] = t;
-                piece_n[np] = n;
-                piece_pg[np] = page;
-                ++np;
-                bytes += 2u * n * (D / 2 + G_::NB);
-                const int valid = min(n, L - t);
-                const uint64_t bits = (valid >= 64) ? ~0ull : ((1ull << valid) - 1ull);
-                mask |= bits << (t - tok0);
-            } else {
-                flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
-            }
-            t += n;
-        }
-        stage_mask[slot] = mask;
-        mbar_arrive_expect_tx(&full_bar[slot], bytes);
-        for (int i = 0; i < np; ++i) {
-            const int off = piece_tok[i] - (piece_tok[i] / p.T) * p.T;
-            const int64_t row = (static_cast<int64_t>(piece_pg[i]) * p.H + h) * p.T + off;
-            const int lt = piece_tok[i] - tok0;
-            const uint32_t nd = piece_n[i] * (D / 2), ns = piece_n[i] * G_::NB;
-            bulk_g2s(st + lt * (D / 2), p.kd + row * (D / 2), nd, &full_bar[slot], policy);
-            bulk_g2s(st + G_::KD + lt * (D / 2), p.vd + row * (D / 2), nd, &full_bar[slot],
-                     policy);
-            bulk_g2s(st + 2 * G_::KD + lt * G_::NB, p.ks + row * G_::NB, ns, &full_bar[slot],
-                     policy);
-            bulk_g2s(st + 2 * G_::KD + G_::KS + lt * G_::NB, p.vs + row * G_::NB, ns,
-                     &full_bar[slot], policy);
-        }
+    // The split's page ids, read once here instead of on each tile's critical path.
+    const int first_page = tok_begin / p.T;
+    const int end_page = (tok_end + p.T - 1) / p.T;
+    const int32_t* pt_row = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+    for (int i = tid; i < end_page - first_page && i < kPageBuf; i += kDecThreads)
+        page_ids[i] = __ldg(pt_row + first_page + i);
+    __syncthreads();
+    auto page_of = [&](int pidx) {
+        const int k = pidx - first_page;
+        const int pg = (k < kPageBuf) ? page_ids[k] : __ldg(pt_row + pidx);
+        return (pg >= 0 && pg < p.pool_pages) ? pg : -1;
     };
 
-    if (tid == 0) {
+    // ---------------------------------------------------------------- this warp's tiles
+    // tile k of this warp covers tokens tok_begin + 16 (4k + warp) .. +15 (one page: T % 16 == 0)
+    const int n_tiles = max(0, (tok_end - tok_begin - 16 * warp + 16 * kWarps - 1) / (16 * kWarps));
+    const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + warp * G_::RING;
+    auto issue_tile = [&](int k) {
+        if (k < n_tiles) {
+            const int t0 = tok_begin + 16 * (kWarps * k + warp);
+            const int pidx = t0 / p.T;
+            const int page = page_of(pidx);
+            if (page >= 0) {
+                const int64_t row0 = (static_cast<int64_t>(page) * p.H + h) * p.T + (t0 - pidx * p.T);
+                const uint32_t slot = ring + (k % kSlots) * G_::SLOT;
+                const uint8_t* ksrc = p.kd + row0 * (D / 2);
+                const uint8_t* vsrc = p.vd + (row0 / 2) * D;
 #pragma unroll
-        for (int s = 0; s < kStages; ++s) mbar_init(&full_bar[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < kStages && s < nst; ++s) issue_stage(st_begin + s, s);
-    }
+                for (int i = 0; i < D / 64; ++i) {
+                    const int j = lane + 32 * i;               // 16-byte chunk of the tile
+                    cp_async16(slot + G_::K_OFF + 16 * j, ksrc + 16 * j);
+                    const int pr = j / G_::VCH, cj = j - pr * G_::VCH;
+                    cp_async16(slot + G_::V_OFF + pr * D + 16 * (cj ^ (pr & G_::SWZ)), vsrc + 16 * j);
+                }
+                if (lane < G_::NB)
+                    cp_async16(slot + G_::KS_OFF + 16 * lane, p.ks + row0 * G_::NB + 16 * lane);
+                else if (lane < 2 * G_::NB)
+                    cp_async16(slot + G_::VS_OFF + 16 * (lane - G_::NB),
+                               p.vs + row0 * G_::NB + 16 * (lane - G_::NB));
+            } else if (lane == 0) {
+                flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < kSlots - 1; ++k) issue_tile(k);
 
     // ---------------------------------------------------------------- Q fragments
     // Lane (r, c) holds head r of the group; k-step j covers head dims c*D/4 + 4j + {0..3}
@@ -240,62 +265,76 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const Deco
     const float cs0 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c);
     const float cs1 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c + 4);
 
-    float o[G_::SEGS][2][4];
+    // V rows of this lane: chunk rho of every token pair; M-tile m row r <-> head dim
+    // rho*D/8 + 2m, row r+8 <-> that dim + 1 (rho spreads the quad lanes over the banks).
+    const int rho = (r >> 1) | ((r & 1) << 2);
+    float o[G_::KSTEPS][4];
 #pragma unroll
-    for (int s = 0; s < G_::SEGS; ++s)
+    for (int m = 0; m < G_::KSTEPS; ++m)
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[s][x][k] = 0.0f;
+        for (int k = 0; k < 4; ++k) o[m][k] = 0.0f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    const uint32_t vsel = 0x6240u + (r >> 2) * 0x1111u;  // V scale byte pairing (see below)
 
     // ---------------------------------------------------------------- main loop
-    bool timed_out = false;
-    int failed_at = 0;
-    for (int j = 0; j < nst; ++j) {
-        const int slot = j % kStages;
-        const uint32_t parity = (j / kStages) & 1;
-        const bool ok = mbar_wait_bounded(&full_bar[slot], parity, kWaitLimitNs);
-        const uint32_t tmask =
-            ok ? static_cast<uint32_t>(stage_mask[slot] >> (16 * warp)) & 0xFFFFu : 0u;
+    for (int kt = 0; kt < n_tiles; ++kt) {
+        issue_tile(kt + kSlots - 1);    // into the slot tile kt-1 used (released below)
+        cp_async_wait<kSlots - 1>();    // this lane's copies of tile kt are done ...
+        __syncwarp();                   // ... and so are the other lanes'
+        const int t0 = tok_begin + 16 * (kWarps * kt + warp);
+        uint32_t tmask = 0u;
+        if (page_of(t0 / p.T) >= 0) {
+            const int valid = min(16, L - t0);
+            tmask = (valid >= 16) ? 0xFFFFu : ((1u << valid) - 1u);
+        }
         if (tmask != 0u) {
-            const uint8_t* st = smem + slot * G_::STAGE;
-            const uint8_t* kd_s = st;
-            const uint8_t* vd_s = st + G_::KD;
-            const uint8_t* ks_s = st + 2 * G_::KD;
-            const uint8_t* vs_s = ks_s + G_::KS;
-            const int row0 = 16 * warp + r;
-            const int row1 = row0 + 8;
-
+            const uint32_t st = ring + (kt % kSlots) * G_::SLOT;
+            const int row0 = r;
+            const int row1 = r + 8;
             // ---- S^T = K^ Q^T (tokens x query heads)
-            uint32_t kw0[G_::CHUNK / 4], kw1[G_::CHUNK / 4];
-            lds_words(kw0, kd_s + row0 * (D / 2) + c * G_::CHUNK);
-            lds_words(kw1, kd_s + row1 * (D / 2) + c * G_::CHUNK);
-            uint32_t ksw0, ksw1;  // this lane's D/64 scale bytes of rows row0 / row1
+            uint32_t kw0[G_::CW], kw1[G_::CW];
+            lds_words(kw0, st + G_::K_OFF + row0 * (D / 2) + c * G_::CHUNK);
+            lds_words(kw1, st + G_::K_OFF + row1 * (D / 2) + c * G_::CHUNK);
+            uint32_t ks0[(D / 64 + 1) / 2], ks1[(D / 64 + 1) / 2];  // FP16 scale pairs
             if constexpr (D == 64) {
-                ksw0 = ks_s[row0 * G_::NB + c];
-                ksw1 = ks_s[row1 * G_::NB + c];
+                const uint32_t b0 = lds_u8(st + G_::KS_OFF + row0 * G_::NB + c);
+                const uint32_t b1 = lds_u8(st + G_::KS_OFF + row1 * G_::NB + c);
+                ks0[0] = e4m3x2_to_f16x2(b0 * 0x0101u);
+                ks1[0] = e4m3x2_to_f16x2(b1 * 0x0101u);
             } else if constexpr (D == 128) {
-                ksw0 = *reinterpret_cast<const uint16_t*>(ks_s + row0 * G_::NB + 2 * c);
-                ksw1 = *reinterpret_cast<const uint16_t*>(ks_s + row1 * G_::NB + 2 * c);
+                ks0[0] = e4m3x2_to_f16x2(lds_u16(st + G_::KS_OFF + row0 * G_::NB + 2 * c));
+                ks1[0] = e4m3x2_to_f16x2(lds_u16(st + G_::KS_OFF + row1 * G_::NB + 2 * c));
             } else {
-                ksw0 = *reinterpret_cast<const uint32_t*>(ks_s + row0 * G_::NB + 4 * c);
-                ksw1 = *reinterpret_cast<const uint32_t*>(ks_s + row1 * G_::NB + 4 * c);
+                uint32_t w0[1], w1[1];
+                lds_words(w0, st + G_::KS_OFF + row0 * G_::NB + 4 * c);
+                lds_words(w1, st + G_::KS_OFF + row1 * G_::NB + 4 * c);
+                e4m3x4_to_f16x2x2(w0[0], ks0);
+                e4m3x4_to_f16x2x2(w1[0], ks1);
             }
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int k = 0; k < G_::KSTEPS; ++k) {
-                const uint32_t w0 = kw0[k / 2], w1 = kw1[k / 2];
-                const int sh = (k & 1) * 16;
-                const uint32_t s0 = scale_bcast(ksw0, k / 4);
-                const uint32_t s1 = scale_bcast(ksw1, k / 4);
-                uint32_t a[4];
-                a[0] = h2_mul(e2m1x2_to_f16x2(w0 >> sh), s0);
-                a[1] = h2_mul(e2m1x2_to_f16x2(w1 >> sh), s1);
-                a[2] = h2_mul(e2m1x2_to_f16x2(w0 >> (sh + 8)), s0);
-                a[3] = h2_mul(e2m1x2_to_f16x2(w1 >> (sh + 8)), s1);
-                mma_f16_16816(acc, a, qf[k][0], qf[k][1]);
+            for (int q = 0; q < G_::CW; ++q) {
+                uint32_t c0[4], c1[4];
+                e2m1x8_to_f16x2x4(kw0[q], c0);
+                e2m1x8_to_f16x2x4(kw1[q], c1);
+#pragma unroll
+                for (int hk = 0; hk < 2; ++hk) {
+                    const int k = 2 * q + hk;  // k-step: bytes 2k, 2k+1 of the lane's chunk
+                    const int blk = k / 4;     // block of the lane's chunk
+                    uint32_t s0, s1;
+                    if constexpr (D == 64) {
+                        s0 = ks0[0];
+                        s1 = ks1[0];
+                    } else {
+                        s0 = (blk & 1) ? h2_hi_hi(ks0[blk >> 1]) : h2_lo_lo(ks0[blk >> 1]);
+                        s1 = (blk & 1) ? h2_hi_hi(ks1[blk >> 1]) : h2_lo_lo(ks1[blk >> 1]);
+                    }
+                    uint32_t a[4];
+                    a[0] = h2_mul(c0[2 * hk], s0);
+                    a[1] = h2_mul(c1[2 * hk], s1);
+                    a[2] = h2_mul(c0[2 * hk + 1], s0);
+                    a[3] = h2_mul(c1[2 * hk + 1], s1);
+                    mma_f16_16816(acc, a, qf[k][0], qf[k][1]);
+                }
             }
 
             // ---- online softmax (log2 domain), columns = query heads 2c, 2c+1
@@ -319,14 +358,12 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const Deco
                 l0 *= a0;
                 l1 *= a1;
 #pragma unroll
-                for (int s = 0; s < G_::SEGS; ++s)
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        o[s][x][0] *= a0;
-                        o[s][x][1] *= a1;
-                        o[s][x][2] *= a0;
-                        o[s][x][3] *= a1;
-                    }
+                for (int m = 0; m < G_::KSTEPS; ++m) {
+                    o[m][0] *= a0;
+                    o[m][1] *= a1;
+                    o[m][2] *= a0;
+                    o[m][3] *= a1;
+                }
             }
             const float p0 = ex2_approx(x0 - m0), p1 = ex2_approx(x1 - m1);
             const float p2 = ex2_approx(x2 - m0), p3 = ex2_approx(x3 - m1);
@@ -336,86 +373,60 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const Deco
             const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
             const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
 
-            // ---- V block scales: pair (token a = 2c + 8hf, token b = a + 1) of block
-            // 2*seg + (r >> 2), for every segment seg; zero for tokens outside the sequence.
-            uint32_t vsp[G_::SEGS][2];
+            // ---- O^T += V^^T P^T. Lane pairs: pr0 (tokens 2c, 2c+1), pr1 (tokens 2c+8, 2c+9)
+            const int pr0 = c, pr1 = c + 4;
+            uint32_t keep0 = 0xFFFFFFFFu, keep1 = 0xFFFFFFFFu;
+            if (tmask != 0xFFFFu) {
+                keep0 = (((tmask >> (2 * c)) & 1u) ? 0x0000FFFFu : 0u) |
+                        (((tmask >> (2 * c + 1)) & 1u) ? 0xFFFF0000u : 0u);
+                keep1 = (((tmask >> (2 * c + 8)) & 1u) ? 0x0000FFFFu : 0u) |
+                        (((tmask >> (2 * c + 9)) & 1u) ? 0xFFFF0000u : 0u);
+            }
+            // the lane's chunk covers head dims rho*D/8 .. +D/8-1: blocks (rho*D/8)/16 ...
+            constexpr int kBlkPerChunk = (D / 8 + 15) / 16;
+            uint32_t vsc0[kBlkPerChunk], vsc1[kBlkPerChunk];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int ta = 16 * warp + 2 * c + 8 * hf;
-                uint32_t wa[G_::NB / 4], wb[G_::NB / 4];
-                lds_words(wa, vs_s + ta * G_::NB);
-                lds_words(wb, vs_s + (ta + 1) * G_::NB);
-                uint32_t keep = 0xFFFFFFFFu;
-                if (tmask != 0xFFFFu) {
-                    keep = (((tmask >> (2 * c + 8 * hf)) & 1u) ? 0x0000FFFFu : 0u) |
-                           (((tmask >> (2 * c + 1 + 8 * hf)) & 1u) ? 0xFFFF0000u : 0u);
-                }
+            for (int q = 0; q < kBlkPerChunk; ++q) {
+                const int blk = (rho * (D / 8)) / 16 + q;
+                vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk)) &
+                          keep0;
+                vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk)) &
+                          keep1;
+            }
+            uint32_t vw0[G_::CW], vw1[G_::CW];
 #pragma unroll
-                for (int u = 0; u < G_::NB / 4; ++u) {
-                    const uint32_t pr = prmt(wa[u], wb[u], vsel);
-                    vsp[2 * u][hf] = e4m3x2_to_f16x2(pr & 0xFFFFu) & keep;
-                    vsp[2 * u + 1][hf] = e4m3x2_to_f16x2(pr >> 16) & keep;
+            for (int q = 0; q < G_::CW; q += (G_::CW >= 4 ? 4 : G_::CW)) {
+                const int x = rho * G_::CHUNK + 4 * q;  // logical byte of the chunk piece
+                uint32_t t0[G_::CW >= 4 ? 4 : G_::CW], t1[G_::CW >= 4 ? 4 : G_::CW];
+                lds_words(t0, st + G_::V_OFF + v_swz<D>(pr0, x));
+                lds_words(t1, st + G_::V_OFF + v_swz<D>(pr1, x));
+#pragma unroll
+                for (int i = 0; i < (G_::CW >= 4 ? 4 : G_::CW); ++i) {
+                    vw0[q + i] = t0[i];
+                    vw1[q + i] = t1[i];
                 }
             }
-
-            // ---- O^T += V^^T P^T, head dims as M: M-tile (seg, x) row r <-> dim
-            // 32 seg + 4 r + 2 x, row r + 8 <-> that dim + 1.
 #pragma unroll
-            for (int g4 = 0; g4 < D / 64; ++g4) {
-                const int mi = lane >> 3;  // which of the 4 matrices this lane addresses
-                const int seg_l = 2 * g4 + (mi >> 1);
-                const int tok_l = 16 * warp + 8 * (mi & 1) + (lane & 7);
-                uint32_t R[4];
-                ldmatrix_x4_trans(R, smem_u32(vd_s + tok_l * (D / 2) + seg_l * 16));
+            for (int q = 0; q < G_::CW; ++q) {
+                uint32_t c0[4], c1[4];
+                e2m1x8_to_f16x2x4(vw0[q], c0);
+                e2m1x8_to_f16x2x4(vw1[q], c1);
 #pragma unroll
-                for (int sx = 0; sx < 2; ++sx) {
-                    const int seg = 2 * g4 + sx;
-                    uint32_t va[2][4];
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const uint32_t w = R[2 * sx + hf];
-                        const uint32_t X0 = e2m1x2_to_f16x2(w);
-                        const uint32_t X1 = e2m1x2_to_f16x2(w >> 8);
-                        const uint32_t Y0 = e2m1x2_to_f16x2(w >> 16);
-                        const uint32_t Y1 = e2m1x2_to_f16x2(w >> 24);
-                        const uint32_t sc = vsp[seg][hf];
-                        va[0][2 * hf + 0] = h2_mul(prmt(X0, Y0, 0x5410u), sc);
-                        va[0][2 * hf + 1] = h2_mul(prmt(X0, Y0, 0x7632u), sc);
-                        va[1][2 * hf + 0] = h2_mul(prmt(X1, Y1, 0x5410u), sc);
-                        va[1][2 * hf + 1] = h2_mul(prmt(X1, Y1, 0x7632u), sc);
-                    }
-                    mma_f16_16816(o[seg][0], va[0], pb0, pb1);
-                    mma_f16_16816(o[seg][1], va[1], pb0, pb1);
+                for (int hm = 0; hm < 2; ++hm) {
+                    const int m = 2 * q + hm;            // M-tile: bytes 2m, 2m+1 of the chunk
+                    const int sq = (2 * m) / 16;         // block of that byte within the chunk
+                    uint32_t a[4];
+                    a[0] = h2_mul(c0[2 * hm], vsc0[sq]);
+                    a[1] = h2_mul(c0[2 * hm + 1], vsc0[sq]);
+                    a[2] = h2_mul(c1[2 * hm], vsc1[sq]);
+                    a[3] = h2_mul(c1[2 * hm + 1], vsc1[sq]);
+                    mma_f16_16816(o[m], a, pb0, pb1);
                 }
             }
         }
-        timed_out = !ok;
-        if (__syncthreads_or(timed_out ? 1 : 0)) {
-            timed_out = true;
-            failed_at = j;
-            break;
-        }
-        if (tid == 0 && j + kStages < nst) issue_stage(st_begin + j + kStages, slot);
+        __syncwarp();                   // every lane is done reading the slot before it refills
     }
-
-    if (timed_out) {
-        // Some copy never completed: wait (bounded) for every stage still in flight, then
-        // leave an empty partial so the combine pass ignores this unit.
-        if (tid == 0) {
-            flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
-            // stages failed_at .. failed_at + kStages - 1 may have been issued
-            for (int jj = failed_at; jj < nst && jj < failed_at + kStages; ++jj)
-                (void)mbar_wait_bounded(&full_bar[jj % kStages], (jj / kStages) & 1, kWaitLimitNs);
-        }
-        __syncthreads();
-        for (int i = tid; i < G * D; i += kDecThreads)
-            p.part_o[(part_row + static_cast<int64_t>(i / D) * p.num_splits) * D + i % D] = 0.0f;
-        if (tid < G) {
-            p.part_m[part_row + static_cast<int64_t>(tid) * p.num_splits] = -INFINITY;
-            p.part_l[part_row + static_cast<int64_t>(tid) * p.num_splits] = 0.0f;
-        }
-        return;
-    }
+    cp_async_wait<0>();
 
     // ---------------------------------------------------------------- merge the 4 warps
 #pragma unroll
@@ -429,7 +440,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const Deco
         red_l[warp][2 * c] = l0;
         red_l[warp][2 * c + 1] = l1;
     }
-    __syncthreads();  // all stages consumed: the stage ring is free for the merge buffer
+    __syncthreads();  // every warp is done with its ring: the rings hold the merge buffer
     float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
@@ -438,18 +449,16 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_split_kernel(const Deco
     }
     const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M0);
     const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M1);
-    float* so = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGroup][D]
+    float* so = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGroup][D], over the rings
 #pragma unroll
-    for (int s = 0; s < G_::SEGS; ++s)
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            const int d0 = 32 * s + 4 * r + 2 * x;
-            float* base = so + (warp * kMaxGroup + 2 * c) * D;
-            base[d0] = o[s][x][0] * f0;
-            base[D + d0] = o[s][x][1] * f1;
-            base[d0 + 1] = o[s][x][2] * f0;
-            base[D + d0 + 1] = o[s][x][3] * f1;
-        }
+    for (int m = 0; m < G_::KSTEPS; ++m) {
+        const int d0 = rho * (D / 8) + 2 * m;
+        float* base = so + (warp * kMaxGroup + 2 * c) * D;
+        base[d0] = o[m][0] * f0;
+        base[D + d0] = o[m][1] * f1;
+        base[d0 + 1] = o[m][2] * f0;
+        base[D + d0 + 1] = o[m][3] * f1;
+    }
     __syncthreads();
     for (int i = tid; i < G * D; i += kDecThreads) {
         const int col = i / D, d = i - (i / D) * D;
@@ -498,36 +507,43 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     }
     const int64_t row = (static_cast<int64_t>(b) * p.Hq + qh) * p.num_splits;
     __shared__ float w_s[kMaxSplits];
-    __shared__ float inv_l;
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int s = 0; s < n_act; ++s) M = fmaxf(M, p.part_m[row + s]);
-        float lsum = 0.0f;
-        for (int s = 0; s < n_act; ++s) {
-            const float ms = p.part_m[row + s];
-            const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-            w_s[s] = w;
-            lsum += w * p.part_l[row + s];
-        }
-        inv_l = (lsum > 0.0f) ? __ldg(p.gv) / lsum : 0.0f;
-        if (p.lse)
-            p.lse[static_cast<int64_t>(b) * p.Hq + qh] =
-                (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
-    }
+    __shared__ float red[2][4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // one split per thread (n_act <= 64): maximum, then weights and weighted sum of l
+    const float ms = (tid < n_act) ? p.part_m[row + tid] : -INFINITY;
+    const float ls = (tid < n_act) ? p.part_l[row + tid] : 0.0f;
+    float M = ms;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    if (lane == 0) red[0][warp] = M;
     __syncthreads();
-    for (int d = threadIdx.x; d < p.D; d += blockDim.x) {
+    M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+    const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
+    if (tid < kMaxSplits) w_s[tid] = w;
+    float lsum = w * ls;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    if (lane == 0) red[1][warp] = lsum;
+    __syncthreads();
+    lsum = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+    const float inv_l = (lsum > 0.0f) ? __ldg(p.gv) / lsum : 0.0f;
+    if (tid == 0 && p.lse)
+        p.lse[static_cast<int64_t>(b) * p.Hq + qh] =
+            (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+    for (int d = tid; d < p.D; d += blockDim.x) {
         float acc = 0.0f;
-        for (int s = 0; s < n_act; ++s)
-            if (w_s[s] != 0.0f) acc += w_s[s] * p.part_o[(row + s) * p.D + d];
-        const float y = acc * inv_l;
-        const __nv_bfloat16 yb = __float2bfloat16_rn(y);
+        for (int s = 0; s < n_act; ++s) {
+            const float ws = w_s[s];
+            if (ws != 0.0f) acc += ws * p.part_o[(row + s) * p.D + d];
+        }
+        const __nv_bfloat16 yb = __float2bfloat16_rn(acc * inv_l);
         p.out[(static_cast<int64_t>(b) * p.Hq + qh) * p.D + d] =
             *reinterpret_cast<const uint16_t*>(&yb);
     }
 }
 
 // ------------------------------------------------------------------------------------------
-// Host side: split heuristic and workspace carving
+// Host side: split heuristic, workspace carving, V tensor map
 // ------------------------------------------------------------------------------------------
 struct SplitPlan {
     int num_splits;

@@ -79,10 +79,13 @@ def test_rounding_exhaustive_fp32(kv, cuda, target):
 
 @pytest.mark.parametrize("kind", ["bf16", "fp16", "fp8"])
 @pytest.mark.parametrize("shape", [(7, 3, 5, 48), (33, 8, 32, 128), (5, 2, 64, 256),
-                                   (1, 1, 1, 16), (300, 2, 16, 64)])
+                                   (1, 1, 1, 16), (300, 2, 16, 64), (6, 3, 6, 48)])
 @pytest.mark.parametrize("ids", [False, True])
-def test_quantize_parity(kv, cuda, kind, shape, ids):
+@pytest.mark.parametrize("pack", [0, 1])
+def test_quantize_parity(kv, cuda, kind, shape, ids, pack):
     P, H, T, D = shape
+    if pack == 1 and T % 2:
+        pytest.skip("token-pair packing needs an even page size")
     src = _make_src(kind, P, H, T, D, seed=P + D)
     lay = kv.Layout(H, D, T)
     rng = np.random.default_rng(P * 7 + D)
@@ -98,7 +101,8 @@ def test_quantize_parity(kv, cuda, kind, shape, ids):
     g = oracle.global_scale(sbits, _odt(src), H, D, T, src_page_ids=sid, src_scale=src_scale)
     want_d, want_s = oracle.quantize_pages(sbits, _odt(src), H, D, T, g, num_dst_pages=npool,
                                            src_page_ids=sid, dst_page_ids=did,
-                                           src_scale=src_scale)
+                                           src_scale=src_scale, packing=pack)
+    lay = kv.Layout(H, D, T, pack)
     src_dev = src.to(cuda)
     gs = torch.empty(1, dtype=torch.float32, device=cuda)
     ss = _scalar(src_scale, cuda) if kind == "fp8" else None
@@ -107,8 +111,9 @@ def test_quantize_parity(kv, cuda, kind, shape, ids):
     kv.nvfp4_kv_compute_global_scale(lay, src_dev, gs, src_page_ids=sid_t, src_scale=ss,
                                      src_dtype=kv.FP8_E4M3 if kind == "fp8" else None)
     assert gs.item() == np.float32(g)
-    data = torch.zeros((npool, H, T, D // 2), dtype=torch.uint8, device=cuda)
-    scales = torch.zeros((npool, H, T, D // 16), dtype=torch.uint8, device=cuda)
+    dshape, sshape = oracle.pool_shapes(npool, H, T, D, pack)
+    data = torch.zeros(dshape, dtype=torch.uint8, device=cuda)
+    scales = torch.zeros(sshape, dtype=torch.uint8, device=cuda)
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
     kv.nvfp4_kv_quantize_pages(lay, src_dev, gs, data, scales, src_page_ids=sid_t,
                                dst_page_ids=did_t, src_scale=ss, status=status,
@@ -122,20 +127,26 @@ def test_quantize_parity(kv, cuda, kind, shape, ids):
 # ------------------------------------------------------------------------------ decode
 
 @pytest.mark.parametrize("out_kind", ["bf16", "fp16", "fp8"])
-@pytest.mark.parametrize("shape", [(9, 3, 16, 48), (40, 8, 32, 128), (1, 1, 1, 16)])
-def test_dequantize_parity(kv, cuda, out_kind, shape):
+@pytest.mark.parametrize("shape", [(9, 3, 16, 48), (40, 8, 32, 128), (1, 1, 1, 16),
+                                   (3, 2, 2, 256)])
+@pytest.mark.parametrize("pack", [0, 1])
+def test_dequantize_parity(kv, cuda, out_kind, shape, pack):
     P, H, T, D = shape
+    if pack == 1 and T % 2:
+        pytest.skip("token-pair packing needs an even page size")
     rng = np.random.default_rng(P + H + D)
-    data = rng.integers(0, 256, (P, H, T, D // 2), dtype=np.uint8)
-    scales = rng.integers(0, 0x7F, (P, H, T, D // 16), dtype=np.uint8)  # every finite scale
+    ds, ss = oracle.pool_shapes(P, H, T, D, pack)
+    data = rng.integers(0, 256, ds, dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, ss, dtype=np.uint8)  # every finite scale
     g = float(np.float32(0.0731))
     out_scale = float(np.float32(0.25)) if out_kind == "fp8" else 1.0
     odt = {"bf16": oracle.BF16, "fp16": oracle.FP16, "fp8": oracle.FP8_E4M3}[out_kind]
     sid = rng.permutation(P).astype(np.int32)
     did = rng.permutation(P + 2)[:P].astype(np.int32)
     want = oracle.dequantize_pages(data, scales, H, D, T, g, odt, num_dst_pages=P + 2,
-                                   src_page_ids=sid, dst_page_ids=did, out_scale=out_scale)
-    lay = kv.Layout(H, D, T)
+                                   src_page_ids=sid, dst_page_ids=did, out_scale=out_scale,
+                                   packing=pack)
+    lay = kv.Layout(H, D, T, pack)
     tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp8": torch.uint8}[out_kind]
     dst = torch.zeros((P + 2, H, T, D), dtype=tdt, device=cuda)
     kv.nvfp4_kv_dequantize_pages(
@@ -155,30 +166,32 @@ def test_page_roundtrip_workload_full_size(kv, cuda):
     scale amax/448). Every byte against the oracle."""
     wl = synthetic.RoundTripWorkload()
     k, v = wl.make(device=cuda)
-    lay = kv.Layout(wl.H, wl.D, wl.T)
-    for t in (k, v):
+    for t, pack in ((k, 0), (v, 1)):       # K dim-pair packed, V token-pair packed
+        lay = kv.Layout(wl.H, wl.D, wl.T, pack)
         bits = _src_bits(t)
         g = oracle.global_scale(bits, oracle.BF16, wl.H, wl.D, wl.T)
         amax = oracle.tensor_amax(bits, oracle.BF16, wl.H, wl.D, wl.T)
         out_scale = float(np.float32(amax) / np.float32(448.0))
-        wd, wsc = oracle.quantize_pages(bits, oracle.BF16, wl.H, wl.D, wl.T, g)
+        wd, wsc = oracle.quantize_pages(bits, oracle.BF16, wl.H, wl.D, wl.T, g, packing=pack)
         gs = torch.empty(1, dtype=torch.float32, device=cuda)
         kv.nvfp4_kv_compute_global_scale(lay, t, gs)
         assert gs.item() == np.float32(g)
-        data = torch.empty((wl.P, wl.H, wl.T, wl.D // 2), dtype=torch.uint8, device=cuda)
-        scales = torch.empty((wl.P, wl.H, wl.T, wl.D // 16), dtype=torch.uint8, device=cuda)
+        ds, ss = oracle.pool_shapes(wl.P, wl.H, wl.T, wl.D, pack)
+        data = torch.empty(ds, dtype=torch.uint8, device=cuda)
+        scales = torch.empty(ss, dtype=torch.uint8, device=cuda)
         kv.nvfp4_kv_quantize_pages(lay, t, gs, data, scales)
         assert np.array_equal(scales.cpu().numpy(), wsc)
         assert np.array_equal(data.cpu().numpy(), wd)
         back = torch.empty_like(t)
         kv.nvfp4_kv_dequantize_pages(lay, data, scales, gs, back)
-        want_b = oracle.dequantize_pages(wd, wsc, wl.H, wl.D, wl.T, g, oracle.BF16)
+        want_b = oracle.dequantize_pages(wd, wsc, wl.H, wl.D, wl.T, g, oracle.BF16,
+                                         packing=pack)
         assert np.array_equal(_src_bits(back), want_b)
         f8 = torch.empty(t.shape, dtype=torch.uint8, device=cuda)
         kv.nvfp4_kv_dequantize_pages(lay, data, scales, gs, f8, dst_dtype=kv.FP8_E4M3,
                                      dst_scale=_scalar(out_scale, cuda))
         want_f = oracle.dequantize_pages(wd, wsc, wl.H, wl.D, wl.T, g, oracle.FP8_E4M3,
-                                         out_scale=out_scale)
+                                         out_scale=out_scale, packing=pack)
         assert np.array_equal(f8.cpu().numpy(), want_f)
         del data, scales, back, f8
 

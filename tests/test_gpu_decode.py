@@ -48,8 +48,9 @@ class Cache:
         kv.nvfp4_kv_compute_global_scale(self.lay, vd, self.gv)
         mk = lambda w: torch.empty((P, H, T, w), dtype=torch.uint8, device=dev)  # noqa: E731
         self.kd, self.ks, self.vd, self.vs = mk(D // 2), mk(D // 16), mk(D // 2), mk(D // 16)
-        kv.nvfp4_kv_quantize_pages(self.lay, kd, self.gk, self.kd, self.ks)
-        kv.nvfp4_kv_quantize_pages(self.lay, vd, self.gv, self.vd, self.vs)
+        kv.nvfp4_kv_quantize_pages(self.lay, kd, self.gk, self.kd, self.ks)  # K: dim pairs
+        kv.nvfp4_kv_quantize_pages(self.lay.with_packing(kv.PACK_TOKEN_PAIRS), vd, self.gv,
+                                   self.vd, self.vs)                        # V: token pairs
         torch.cuda.synchronize()
         self.g_k, self.g_v = self.gk.item(), self.gv.item()
         self.host = [t.cpu().numpy() for t in (self.kd, self.ks, self.vd, self.vs)]
@@ -58,9 +59,10 @@ class Cache:
             assert self.g_k == oracle.global_scale(kb, oracle.BF16, H, D, T)
             assert self.g_v == oracle.global_scale(vb, oracle.BF16, H, D, T)
             wkd, wks = oracle.quantize_pages(kb, oracle.BF16, H, D, T, self.g_k)
-            wvd, wvs = oracle.quantize_pages(vb, oracle.BF16, H, D, T, self.g_v)
+            wvd, wvs = oracle.quantize_pages(vb, oracle.BF16, H, D, T, self.g_v,
+                                             packing=oracle.TOKEN_PAIRS)
             for got, want in zip(self.host, (wkd, wks, wvd, wvs)):
-                assert np.array_equal(got, want)
+                assert np.array_equal(got.reshape(want.shape), want)
 
 
 def run_decode(kv, dev, cache, q, pt, sl, sm_scale, splits=0, status=None):
@@ -79,7 +81,7 @@ def oracle_decode(cache, q, pt, sl, sm_scale, want=None):
     kd, ks, vd, vs = cache.host
     return oracle.paged_decode_attention(bits(q), kd, ks, cache.g_k, vd, vs, cache.g_v,
                                          pt.numpy(), sl.numpy(), sm_scale, cache.H, cache.T,
-                                         want=want)
+                                         want=want, v_packing=oracle.TOKEN_PAIRS)
 
 
 def check(out, lse, ref, ref_lse, mask=None, tag=""):

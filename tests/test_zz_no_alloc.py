@@ -45,7 +45,7 @@ def _workload(kv, dev, seed, lens, G=4, H=2, D=128, T=64):
     mk = lambda w: torch.empty((pool, H, T, w), dtype=torch.uint8, device=dev)  # noqa: E731
     kd, ks, vd, vs = mk(D // 2), mk(D // 16), mk(D // 2), mk(D // 16)
     kv.nvfp4_kv_quantize_pages(lay, k, gk, kd, ks)
-    kv.nvfp4_kv_quantize_pages(lay, v, gv, vd, vs)
+    kv.nvfp4_kv_quantize_pages(lay.with_packing(kv.PACK_TOKEN_PAIRS), v, gv, vd, vs)
     return dict(lay=lay, q=q, kd=kd, ks=ks, gk=gk, vd=vd, vs=vs, gv=gv, pt=pt, sl=sl,
                 sm=1.0 / math.sqrt(D))
 

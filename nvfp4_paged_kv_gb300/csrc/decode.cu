@@ -93,10 +93,6 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// The two halves of an FP16 pair, each broadcast to both halves.
-__device__ __forceinline__ uint32_t h2_lo_lo(uint32_t x) { return __byte_perm(x, 0, 0x1010); }
-__device__ __forceinline__ uint32_t h2_hi_hi(uint32_t x) { return __byte_perm(x, 0, 0x3232); }
-
 template <int N>
 __device__ __forceinline__ void lds_words(uint32_t (&w)[N], uint32_t addr) {
     if constexpr (N == 1) {
@@ -189,31 +185,57 @@ __global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
     // tile k of this warp covers tokens tok_begin + 16 (4k + warp) .. +15 (one page: T % 16 == 0)
     const int n_tiles = max(0, (tok_end - tok_begin - 16 * warp + 16 * kWarps - 1) / (16 * kWarps));
     const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + warp * G_::RING;
+    // Loop-invariant per-lane chunk offsets: this lane copies 16-byte chunks j = lane + 32 i of
+    // the tile's K rows and V rows (V chunks land XOR-swizzled) and, for lanes < 2 NB, one chunk
+    // of a scale pool. K rows, V rows and the two scale pools of a tile share one base offset
+    // each: row0 * D/2 bytes for the data, row0 * NB for the scales.
+    uint32_t v_dst[D / 64];
+#pragma unroll
+    for (int i = 0; i < D / 64; ++i) {
+        const int j = lane + 32 * i;
+        const int pr = j / G_::VCH, cj = j - pr * G_::VCH;
+        v_dst[i] = G_::V_OFF + pr * D + 16 * (cj ^ (pr & G_::SWZ));
+    }
+    const bool sc_lane = lane < 2 * G_::NB;
+    const uint8_t* sc_pool = (lane < G_::NB) ? p.ks : p.vs;
+    const uint32_t sc_dst = (lane < G_::NB) ? G_::KS_OFF + 16 * lane : G_::VS_OFF + 16 * (lane - G_::NB);
+    const uint32_t sc_src = 16 * ((lane < G_::NB) ? lane : lane - G_::NB);
+    // Page index / slot of this warp's next tile to issue, advanced by 64 tokens per tile
+    // without divisions (T >= 16, so at most 4 page steps per tile).
+    struct TilePos {
+        int pidx, off;
+        __device__ __forceinline__ void advance(int T) {
+            off += 16 * kWarps;
+            while (off >= T) {
+                off -= T;
+                ++pidx;
+            }
+        }
+    };
+    const int t_first = tok_begin + 16 * warp;
+    TilePos ipos{t_first / p.T, t_first - (t_first / p.T) * p.T};  // next tile to issue
+    TilePos cpos = ipos;                                              // next tile to consume
+    const int64_t head_rows = static_cast<int64_t>(h) * p.T;          // row offset of head h
+    const int64_t page_rows = static_cast<int64_t>(p.H) * p.T;        // rows per page
     auto issue_tile = [&](int k) {
         if (k < n_tiles) {
-            const int t0 = tok_begin + 16 * (kWarps * k + warp);
-            const int pidx = t0 / p.T;
-            const int page = page_of(pidx);
+            const int page = page_of(ipos.pidx);
             if (page >= 0) {
-                const int64_t row0 = (static_cast<int64_t>(page) * p.H + h) * p.T + (t0 - pidx * p.T);
+                const int64_t row0 = page * page_rows + head_rows + ipos.off;
                 const uint32_t slot = ring + (k % kSlots) * G_::SLOT;
-                const uint8_t* ksrc = p.kd + row0 * (D / 2);
-                const uint8_t* vsrc = p.vd + (row0 / 2) * D;
+                const int64_t doff = row0 * (D / 2);
+                const uint8_t* ksrc = p.kd + doff + 16 * lane;
+                const uint8_t* vsrc = p.vd + doff + 16 * lane;
 #pragma unroll
                 for (int i = 0; i < D / 64; ++i) {
-                    const int j = lane + 32 * i;               // 16-byte chunk of the tile
-                    cp_async16(slot + G_::K_OFF + 16 * j, ksrc + 16 * j);
-                    const int pr = j / G_::VCH, cj = j - pr * G_::VCH;
-                    cp_async16(slot + G_::V_OFF + pr * D + 16 * (cj ^ (pr & G_::SWZ)), vsrc + 16 * j);
+                    cp_async16(slot + G_::K_OFF + 16 * lane + 512 * i, ksrc + 512 * i);
+                    cp_async16(slot + v_dst[i], vsrc + 512 * i);
                 }
-                if (lane < G_::NB)
-                    cp_async16(slot + G_::KS_OFF + 16 * lane, p.ks + row0 * G_::NB + 16 * lane);
-                else if (lane < 2 * G_::NB)
-                    cp_async16(slot + G_::VS_OFF + 16 * (lane - G_::NB),
-                               p.vs + row0 * G_::NB + 16 * (lane - G_::NB));
+                if (sc_lane) cp_async16(slot + sc_dst, sc_pool + row0 * G_::NB + sc_src);
             } else if (lane == 0) {
                 flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
             }
+            ipos.advance(p.T);
         }
         cp_async_commit();
     };
@@ -282,10 +304,11 @@ __global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
         __syncwarp();                   // ... and so are the other lanes'
         const int t0 = tok_begin + 16 * (kWarps * kt + warp);
         uint32_t tmask = 0u;
-        if (page_of(t0 / p.T) >= 0) {
+        if (page_of(cpos.pidx) >= 0) {
             const int valid = min(16, L - t0);
             tmask = (valid >= 16) ? 0xFFFFu : ((1u << valid) - 1u);
         }
+        cpos.advance(p.T);
         if (tmask != 0u) {
             const uint32_t st = ring + (kt % kSlots) * G_::SLOT;
             const int row0 = r;
@@ -294,21 +317,15 @@ __global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
             uint32_t kw0[G_::CW], kw1[G_::CW];
             lds_words(kw0, st + G_::K_OFF + row0 * (D / 2) + c * G_::CHUNK);
             lds_words(kw1, st + G_::K_OFF + row1 * (D / 2) + c * G_::CHUNK);
-            uint32_t ks0[(D / 64 + 1) / 2], ks1[(D / 64 + 1) / 2];  // FP16 scale pairs
-            if constexpr (D == 64) {
-                const uint32_t b0 = lds_u8(st + G_::KS_OFF + row0 * G_::NB + c);
-                const uint32_t b1 = lds_u8(st + G_::KS_OFF + row1 * G_::NB + c);
-                ks0[0] = e4m3x2_to_f16x2(b0 * 0x0101u);
-                ks1[0] = e4m3x2_to_f16x2(b1 * 0x0101u);
-            } else if constexpr (D == 128) {
-                ks0[0] = e4m3x2_to_f16x2(lds_u16(st + G_::KS_OFF + row0 * G_::NB + 2 * c));
-                ks1[0] = e4m3x2_to_f16x2(lds_u16(st + G_::KS_OFF + row1 * G_::NB + 2 * c));
-            } else {
-                uint32_t w0[1], w1[1];
-                lds_words(w0, st + G_::KS_OFF + row0 * G_::NB + 4 * c);
-                lds_words(w1, st + G_::KS_OFF + row1 * G_::NB + 4 * c);
-                e4m3x4_to_f16x2x2(w0[0], ks0);
-                e4m3x4_to_f16x2x2(w1[0], ks1);
+            // FP16 (s, s) of the lane's D/64 blocks in rows row0 / row1: the scale byte is
+            // duplicated by an integer multiply, then converted as an E4M3 pair
+            uint32_t ks0[D / 64], ks1[D / 64];
+#pragma unroll
+            for (int q = 0; q < D / 64; ++q) {
+                ks0[q] = e4m3x2_to_f16x2(lds_u8(st + G_::KS_OFF + row0 * G_::NB + c * (D / 64) + q) *
+                                         0x0101u);
+                ks1[q] = e4m3x2_to_f16x2(lds_u8(st + G_::KS_OFF + row1 * G_::NB + c * (D / 64) + q) *
+                                         0x0101u);
             }
             float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -320,19 +337,11 @@ __global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
                 for (int hk = 0; hk < 2; ++hk) {
                     const int k = 2 * q + hk;  // k-step: bytes 2k, 2k+1 of the lane's chunk
                     const int blk = k / 4;     // block of the lane's chunk
-                    uint32_t s0, s1;
-                    if constexpr (D == 64) {
-                        s0 = ks0[0];
-                        s1 = ks1[0];
-                    } else {
-                        s0 = (blk & 1) ? h2_hi_hi(ks0[blk >> 1]) : h2_lo_lo(ks0[blk >> 1]);
-                        s1 = (blk & 1) ? h2_hi_hi(ks1[blk >> 1]) : h2_lo_lo(ks1[blk >> 1]);
-                    }
                     uint32_t a[4];
-                    a[0] = h2_mul(c0[2 * hk], s0);
-                    a[1] = h2_mul(c1[2 * hk], s1);
-                    a[2] = h2_mul(c0[2 * hk + 1], s0);
-                    a[3] = h2_mul(c1[2 * hk + 1], s1);
+                    a[0] = h2_mul(c0[2 * hk], ks0[blk]);
+                    a[1] = h2_mul(c1[2 * hk], ks1[blk]);
+                    a[2] = h2_mul(c0[2 * hk + 1], ks0[blk]);
+                    a[3] = h2_mul(c1[2 * hk + 1], ks1[blk]);
                     mma_f16_16816(acc, a, qf[k][0], qf[k][1]);
                 }
             }
@@ -343,11 +352,25 @@ __global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
                 if (!((tmask >> r) & 1u)) x0 = x1 = -INFINITY;
                 if (!((tmask >> (r + 8)) & 1u)) x2 = x3 = -INFINITY;
             }
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+            // column maxima over the 16 tokens, both columns in one FP16 pair (the running
+            // maximum only has to be close to the true one: p = 2^(x - m) stays below 2^8)
+            __half2 hm = __floats2half2_rn(fmaxf(x0, x2), fmaxf(x1, x3));
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+                const uint32_t u =
+                    __shfl_xor_sync(0xFFFFFFFFu, *reinterpret_cast<const uint32_t*>(&hm), off);
+                hm = __hmax2(hm, *reinterpret_cast<const __half2*>(&u));
+            }
+            float mx0 = __low2float(hm), mx1 = __high2float(hm);
+            if (__any_sync(0xFFFFFFFFu, fmaxf(mx0, mx1) > 65000.0f)) {
+                // scores beyond the FP16 range: reduce in fp32 instead
+                mx0 = fmaxf(x0, x2);
+                mx1 = fmaxf(x1, x3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+                }
             }
             const bool grow = (mx0 > m0 + kRescaleThreshold) || (mx1 > m1 + kRescaleThreshold);
             if (__any_sync(0xFFFFFFFFu, grow)) {
@@ -388,10 +411,12 @@ __global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
 #pragma unroll
             for (int q = 0; q < kBlkPerChunk; ++q) {
                 const int blk = (rho * (D / 8)) / 16 + q;
-                vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk)) &
-                          keep0;
-                vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk)) &
-                          keep1;
+                vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk));
+                vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk));
+                if (tmask != 0xFFFFu) {
+                    vsc0[q] &= keep0;
+                    vsc1[q] &= keep1;
+                }
             }
             uint32_t vw0[G_::CW], vw1[G_::CW];
 #pragma unroll

@@ -78,7 +78,7 @@ typedef enum nvfp4kv_status {
 /* Bits OR-ed into the optional device status word. */
 #define NVFP4KV_STATUS_PAGE_OOB 0x1      /* a page id was outside [0, pool_pages): skipped        */
 #define NVFP4KV_STATUS_BAD_SEQ_LEN 0x2   /* seq_len < 0 or > max_pages_per_seq * T: seq skipped   */
-#define NVFP4KV_STATUS_TIMEOUT 0x4       /* a copy-completion wait exceeded its limit: unit skipped */
+#define NVFP4KV_STATUS_TIMEOUT 0x4       /* reserved for bounded waits; no current kernel sets it  */
 
 typedef enum nvfp4kv_packing {
     NVFP4KV_PACK_DIM_PAIRS = 0,   /* a byte holds two head dims of one token (K cache)          */

@@ -180,8 +180,10 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
  *   lse[b][qh] = log(sum_t exp(sm_scale * q . k_t))              (natural log; optional)
  * A sequence of length 0 gives out = 0 and lse = -inf.
  *
- * Long sequences are cut into at most max_num_splits chunks (split-KV); each chunk produces a
- * partial (max, sum, unnormalised output) in the workspace and a second kernel merges them.
+ * Split-KV: the (sequence, KV head) pairs are cut into 64-token stages (32 at head_dim 256), the
+ * stages of all pairs form one list, and the list is cut into equal runs, one per CTA of the
+ * first kernel. Each (run, pair) piece leaves a partial (max, sum, unnormalised output) in the
+ * workspace and a second kernel merges the partials of each (sequence, query head).
  *   q              BF16 [batch][num_q_heads][D]
  *   k_data, k_scales   NVFP4 K pool in NVFP4KV_PACK_DIM_PAIRS (layout.packing is not read)
  *   v_data, v_scales   NVFP4 V pool in NVFP4KV_PACK_TOKEN_PAIRS
@@ -189,7 +191,9 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
  *   page_table     int32 [batch][max_pages_per_seq] device
  *   seq_lens       int32 [batch] device; 0 <= seq_len <= max_pages_per_seq * T
  *   sm_scale       softmax scale (e.g. 1/sqrt(D))
- *   max_num_splits 0 = automatic, else 1..64
+ *   max_num_splits 0 = automatic: one wave of CTAs on the device (runs of at least 4 stages);
+ *                  n in 1..64: n * batch * num_kv_heads runs (n runs per pair when all
+ *                  sequences have the same length)
  *   workspace      device scratch of nvfp4_paged_decode_workspace_size(...) bytes
  *   out            BF16 [batch][num_q_heads][D]
  *   lse            float [batch][num_q_heads] or NULL

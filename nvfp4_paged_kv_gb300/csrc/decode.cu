@@ -8,28 +8,35 @@
 // ("supplied through the attention BMM scaling parameters").
 //
 // Design for GB300 (the SM120 kernel of the LMSYS page is prior art, not the blueprint):
-//  * one CTA per (sequence, KV head, split) of 4 warps; a split is a run of 64-token stages and
-//    warp w owns the 16-token tiles w, w+4, w+8, ... of it. Each warp streams its own tiles
-//    through a private 4-slot shared-memory ring with asynchronous copies (cp.async, 16 bytes
-//    per lane, completion per warp by wait_group): packed K rows, token-pair packed V rows and
-//    both scale pools of a tile are four contiguous runs of its page. The warps never wait for
-//    one another until the final merge, so each keeps three tiles in flight behind the one it
-//    computes. V rows land XOR-swizzled by 16-byte chunk so the fragment reads hit distinct banks.
+//  * Work is a flat list of stages: stage j of pair (sequence b, KV head h) covers tokens
+//    [TOK j, TOK j + TOK) of b (TOK = 64 tokens, 32 at head_dim 256), pairs in (b, h) order.
+//    One persistent wave of CTAs cuts the list into equal runs, so every SM streams the same
+//    number of bytes whatever the mix of sequence lengths (no tail of idle SMs). A run may
+//    cross pairs; each (CTA, pair) piece leaves one partial record, merged by the combine
+//    kernel. The record of CTA c for pair bh is record c + bh, so records never collide and
+//    their number is bounded by (CTAs + pairs) before any length is known.
+//  * A CTA has 4 warps; warp w takes stages w, w+4, ... of the piece. A stage is SUB MMA tiles
+//    of 16 tokens, streamed through a per-warp 2-slot shared-memory ring by asynchronous copies
+//    (cp.async, 16 bytes per lane, completion per warp by wait_group): the packed K rows,
+//    token-pair packed V rows and both scale pools of a stage are four contiguous runs of its
+//    page. Sub-tiles whose page id is out of range or that lie past the sequence end are
+//    zero-filled, and a small slot header tells the consumer which sub-tiles are real.
 //  * S^T = K^ Q^T runs on the tensor cores with tokens as M = 16 and the GQA query group as
 //    N = 8 (mma.sync m16n8k16, FP16 in, FP32 accumulate). K is stored dim-pair packed, so every
 //    converted byte (cvt.rn.f16x2.e2m1x2) is one A-register: two adjacent head dims of one
 //    token, exact in FP16, times its E4M3 block scale (exact). Q is brought into FP16 exactly by
 //    a per-head power of two; head dims inside a k-step are permuted identically in K and Q.
-//  * online softmax in the log2 domain, column maxima by warp shuffles; the running maximum
-//    moves only when it grows by more than 2^8, so accumulator rescaling is rare. P^T moves from
-//    the score layout to the B-operand layout with movmatrix.
+//  * online softmax per stage in the log2 domain, column maxima by warp shuffles on packed
+//    FP16 pairs; the running maximum moves only when it grows by more than 2^8, so accumulator
+//    rescaling is rare. P^T moves to the B-operand layout with movmatrix.
 //  * O^T += V^^T P^T with head dims as M: V is stored token-pair packed, so every converted byte
 //    is one A-register (one head dim of two adjacent tokens) times the pair's two block scales.
-//  * the 4 warps merge (max, sum, output) in shared memory and the CTA writes one partial per
-//    (sequence, query head, split); a second kernel merges the splits by log-sum-exp and writes
-//    the BF16 output and the natural-log LSE.
+//  * at the end of a piece the 4 warps merge (max, sum, output) in shared memory and the CTA
+//    writes the record; the combine kernel merges the records of each (sequence, query head)
+//    by log-sum-exp and writes the BF16 output and the natural-log LSE.
 // Bytes per (token, KV head) at head_dim 128: 64 + 8 (K) + 64 + 8 (V) = 144.
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -40,32 +47,42 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kDecThreads = kWarps * 32;
-constexpr int kStageTokens = 64;  // split granularity (4 warps x 16-token tiles)
-constexpr int kSlots = 4;         // tiles per warp ring
+constexpr int kSlots = 2;          // stages per warp ring
 constexpr int kMaxGroup = 8;
-constexpr int kMaxSplits = 64;
-constexpr int kPageBuf = 256; // page ids of a split kept in shared memory
+constexpr int kMaxSplits = 64;     // bound of the caller-forced split count
+constexpr int kPageBuf = 256;      // page ids of a piece kept in shared memory
+constexpr int kMaxWeights = 1024;  // combine: merge weights cached in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct Geo {
-    static constexpr int NB = D / 16;            // blocks (= scales) per token row
-    static constexpr int TK = 16 * D / 2;         // packed K rows of a 16-token tile
-    static constexpr int TV = 8 * D;              // token-pair V rows of a tile (8 pairs)
-    static constexpr int TS = 16 * NB;            // one scale pool of a tile
+    static constexpr int TOK = (D == 256) ? 32 : 64;  // tokens of a stage
+    static constexpr int SUB = TOK / 16;              // 16-token MMA tiles of a stage
+    static constexpr int NB = D / 16;                 // blocks (= scales) per token row
+    static constexpr int SK = TOK * D / 2;            // packed K rows of a stage
+    static constexpr int SV = TOK * D / 2;            // token-pair V rows (TOK / 2 rows of D)
+    static constexpr int SS = TOK * NB;               // one scale pool of a stage
     static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = TK;
-    static constexpr int KS_OFF = TK + TV;
-    static constexpr int VS_OFF = TK + TV + TS;
-    static constexpr int SLOT = TK + TV + 2 * TS;  // 18 D bytes
-    static constexpr int RING = kSlots * SLOT;     // per warp
+    static constexpr int V_OFF = SK;
+    static constexpr int KS_OFF = SK + SV;
+    static constexpr int VS_OFF = KS_OFF + SS;
+    static constexpr int HDR_OFF = VS_OFF + SS;  // slot header: real sub-tiles, tokens
+    static constexpr int SLOT = HDR_OFF + 16;
+    static constexpr int RING = kSlots * SLOT;  // per warp
     static constexpr int SMEM = kWarps * RING;
-    static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
-    static constexpr int CHUNK = D / 8;            // bytes of a row one quad lane owns
-    static constexpr int CW = CHUNK / 4;           // ... as 32-bit words
-    static constexpr int VCH = D / 16;             // 16-byte chunks per V pair row
+    static constexpr int KSTEPS = D / 16;       // k-steps of S^T = K Q^T
+    static constexpr int CHUNK = D / 8;         // bytes of a row one quad lane owns
+    static constexpr int CW = CHUNK / 4;        // ... as 32-bit words
+    static constexpr int VCH = D / 16;          // 16-byte chunks per V pair row
     static constexpr int SWZ = (VCH < 8 ? VCH : 8) - 1;  // chunk XOR mask
+    static constexpr int DCH = SK / (16 * 32);  // 16-byte chunks per lane of one data pool
+    static constexpr int SUB_DIV = D / 64;      // data chunk i of a lane lies in sub-tile i / SUB_DIV
+    static constexpr int SCH = SS / 16;         // 16-byte chunks of one scale pool
+    static constexpr int SC_PER_LANE = 2 * SCH / 32;
+    static constexpr int BLOCKS_PER_SM = (D == 64) ? 6 : 3;
+    static_assert(DCH * 32 * 16 == SK && DCH == SUB * SUB_DIV, "copy split");
+    static_assert(SC_PER_LANE * 32 == 2 * SCH, "scale copy split");
     static_assert(kWarps * kMaxGroup * D * 4 <= SMEM, "merge buffer must fit in the rings");
 };
 
@@ -76,14 +93,15 @@ struct DecodeParams {
     const uint8_t* vd;
     const uint8_t* vs;
     const float* gk;
-    const float* gv;
     const int32_t* page_table;
     const int32_t* seq_lens;
-    float* part_o;  // [B][Hq][S][D]
-    float* part_m;  // [B][Hq][S]   running max (log2 domain)
-    float* part_l;  // [B][Hq][S]   sum of exp2(x - m)
+    int32_t* hdr;       // [0] total stages, [1] stages per CTA (written by CTA 0)
+    int32_t* ps;        // [B + 1] first stage of each sequence's pairs (written by CTA 0)
+    float* rec_o;       // [records][G][D] unnormalised output
+    float* rec_ml;      // [records][G][2] running max (log2 domain), sum of exp2(x - max)
     int32_t* status;
-    int32_t B, Hq, H, G, T, pool_pages, max_pages, num_splits, stages_per_split;
+    uint64_t t_magic;   // ceil(2^64 / T)
+    int32_t B, Hq, H, G, T, pool_pages, max_pages, min_w;
     float sm_scale;
 };
 
@@ -120,15 +138,34 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
-// Shared-memory offset of byte x of token-pair row pr of a tile's V rows: 16-byte chunks are
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Shared-memory offset of byte x of token-pair row pr of a stage's V rows: 16-byte chunks are
 // XOR-swizzled by the row so that the 4 lanes of a quad (rows c and c+4) hit distinct banks.
 template <int D>
 __device__ __forceinline__ uint32_t v_swz(int pr, int x) {
     return static_cast<uint32_t>(pr * D + ((((x >> 4) ^ (pr & Geo<D>::SWZ))) << 4) + (x & 15));
 }
 
+// 16-byte asynchronous copy global -> shared, with compile-time offsets on both addresses.
+template <int OFF_S, int OFF_G>
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src),
+                 "n"(OFF_S), "n"(OFF_G)
+                 : "memory");
+}
+// The same with a source size of 16 or 0 bytes (0: the 16 bytes are zero-filled, nothing read).
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -136,416 +173,587 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+template <typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+// f(std::integral_constant<int, i>) for i = 0 .. N-1, each i a compile-time constant.
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
+
+// Stages (of tok tokens) of a sequence of length L; 0 for an invalid length.
+__device__ __forceinline__ int seq_stages(int L, int max_tokens, int tok) {
+    return (L > 0 && L <= max_tokens) ? (L + tok - 1) / tok : 0;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, D == 256 ? 3 : 5)
+__global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
     decode_split_kernel(const DecodeParams p) {
     using G_ = Geo<D>;
+    constexpr int TOK = G_::TOK;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ float red_m[kWarps][kMaxGroup];
     __shared__ float red_l[kWarps][kMaxGroup];
     __shared__ int page_ids[kPageBuf];
+    __shared__ int scan_warp[kWarps];
+    __shared__ int start_bp[2];  // pair walk start: sequence, its first stage
 
-    const int split = blockIdx.x;
-    const int h = blockIdx.y;
-    const int b = blockIdx.z;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int r = lane >> 2;  // row group of the MMA fragments
     const int c = lane & 3;   // column pair of the MMA fragments
+    const int H = p.H, G = p.G, T = p.T;
+    const int max_tokens = p.max_pages * T;
 
-    const int L = __ldg(p.seq_lens + b);
-    if (L < 0 || L > p.max_pages * p.T) {
-        if (tid == 0 && split == 0 && h == 0) flag_status(p.status, NVFP4KV_STATUS_BAD_SEQ_LEN);
-        return;  // the combine pass applies the same rule and writes zeros
+    // ------------------------------------------------ stage prefix over the sequences
+    // Thread t owns sequences [t C, t C + C); PS_b = H * sum_{b' < b} stages(b').
+    const int C = (p.B + kDecThreads - 1) / kDecThreads;
+    const int b_lo = min(p.B, tid * C), b_hi = min(p.B, b_lo + C);
+    int local = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int L = __ldg(p.seq_lens + b);
+        if (blockIdx.x == 0 && (L < 0 || L > max_tokens))
+            flag_status(p.status, NVFP4KV_STATUS_BAD_SEQ_LEN);
+        local += H * seq_stages(L, max_tokens, TOK);
     }
-    const int total_stages = (L + kStageTokens - 1) / kStageTokens;
-    const int st_begin = split * p.stages_per_split;
-    const int st_end = min(st_begin + p.stages_per_split, total_stages);
-    if (st_begin >= st_end) return;  // beyond this sequence: no partial (combine skips it)
-    const int tok_begin = st_begin * kStageTokens;
-    const int tok_end = min(st_end * kStageTokens, L);
-    const int G = p.G;
-    const int64_t part_row = (static_cast<int64_t>(b) * p.Hq + h * G) * p.num_splits + split;
-
-    // The split's page ids, read once here instead of on each tile's critical path.
-    const int first_page = tok_begin / p.T;
-    const int end_page = (tok_end + p.T - 1) / p.T;
-    const int32_t* pt_row = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-    for (int i = tid; i < end_page - first_page && i < kPageBuf; i += kDecThreads)
-        page_ids[i] = __ldg(pt_row + first_page + i);
-    __syncthreads();
-    auto page_of = [&](int pidx) {
-        const int k = pidx - first_page;
-        const int pg = (k < kPageBuf) ? page_ids[k] : __ldg(pt_row + pidx);
-        return (pg >= 0 && pg < p.pool_pages) ? pg : -1;
-    };
-
-    // ---------------------------------------------------------------- this warp's tiles
-    // tile k of this warp covers tokens tok_begin + 16 (4k + warp) .. +15 (one page: T % 16 == 0)
-    const int n_tiles = max(0, (tok_end - tok_begin - 16 * warp + 16 * kWarps - 1) / (16 * kWarps));
-    const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + warp * G_::RING;
-    // Loop-invariant per-lane chunk offsets: this lane copies 16-byte chunks j = lane + 32 i of
-    // the tile's K rows and V rows (V chunks land XOR-swizzled) and, for lanes < 2 NB, one chunk
-    // of a scale pool. K rows, V rows and the two scale pools of a tile share one base offset
-    // each: row0 * D/2 bytes for the data, row0 * NB for the scales.
-    uint32_t v_dst[D / 64];
+    int incl = local;
 #pragma unroll
-    for (int i = 0; i < D / 64; ++i) {
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan_warp[warp] = incl;
+    __syncthreads();
+    int excl = incl - local, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) excl += scan_warp[w];
+        total += scan_warp[w];
+    }
+    const int n_ctas = gridDim.x;
+    const int W = max(p.min_w, max(1, (total + n_ctas - 1) / n_ctas));
+    const int s_begin = blockIdx.x * W;
+    const int s_end = min(total, s_begin + W);
+    if (blockIdx.x == 0) {
+        int acc = excl;
+        for (int b = b_lo; b < b_hi; ++b) {
+            p.ps[b] = acc;
+            acc += H * seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
+        }
+        if (tid == kDecThreads - 1) p.ps[p.B] = total;
+        if (tid == 0) {
+            p.hdr[0] = total;
+            p.hdr[1] = W;
+        }
+    }
+    if (s_begin >= s_end) return;
+    if (s_begin >= excl && s_begin < excl + local) {
+        int acc = excl;
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int n = H * seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
+            if (s_begin < acc + n) {
+                start_bp[0] = b;
+                start_bp[1] = acc;
+                break;
+            }
+            acc += n;
+        }
+    }
+    __syncthreads();
+
+    // ------------------------------------------------ per-lane constants
+    const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + warp * G_::RING;
+    // V chunk j = lane + 32 i of a stage lands XOR-swizzled by its pair row
+    uint32_t v_dst[G_::DCH];
+#pragma unroll
+    for (int i = 0; i < G_::DCH; ++i) {
         const int j = lane + 32 * i;
         const int pr = j / G_::VCH, cj = j - pr * G_::VCH;
         v_dst[i] = G_::V_OFF + pr * D + 16 * (cj ^ (pr & G_::SWZ));
     }
-    const bool sc_lane = lane < 2 * G_::NB;
-    const uint8_t* sc_pool = (lane < G_::NB) ? p.ks : p.vs;
-    const uint32_t sc_dst = (lane < G_::NB) ? G_::KS_OFF + 16 * lane : G_::VS_OFF + 16 * (lane - G_::NB);
-    const uint32_t sc_src = 16 * ((lane < G_::NB) ? lane : lane - G_::NB);
-    // Page index / slot of this warp's next tile to issue, advanced by 64 tokens per tile
-    // without divisions (T >= 16, so at most 4 page steps per tile).
-    struct TilePos {
-        int pidx, off;
-        __device__ __forceinline__ void advance(int T) {
-            off += 16 * kWarps;
-            while (off >= T) {
-                off -= T;
-                ++pidx;
-            }
-        }
-    };
-    const int t_first = tok_begin + 16 * warp;
-    TilePos ipos{t_first / p.T, t_first - (t_first / p.T) * p.T};  // next tile to issue
-    TilePos cpos = ipos;                                              // next tile to consume
-    const int64_t head_rows = static_cast<int64_t>(h) * p.T;          // row offset of head h
-    const int64_t page_rows = static_cast<int64_t>(p.H) * p.T;        // rows per page
-    auto issue_tile = [&](int k) {
-        if (k < n_tiles) {
-            const int page = page_of(ipos.pidx);
-            if (page >= 0) {
-                const int64_t row0 = page * page_rows + head_rows + ipos.off;
-                const uint32_t slot = ring + (k % kSlots) * G_::SLOT;
-                const int64_t doff = row0 * (D / 2);
-                const uint8_t* ksrc = p.kd + doff + 16 * lane;
-                const uint8_t* vsrc = p.vd + doff + 16 * lane;
-#pragma unroll
-                for (int i = 0; i < D / 64; ++i) {
-                    cp_async16(slot + G_::K_OFF + 16 * lane + 512 * i, ksrc + 512 * i);
-                    cp_async16(slot + v_dst[i], vsrc + 512 * i);
-                }
-                if (sc_lane) cp_async16(slot + sc_dst, sc_pool + row0 * G_::NB + sc_src);
-            } else if (lane == 0) {
-                flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
-            }
-            ipos.advance(p.T);
-        }
-        cp_async_commit();
-    };
-#pragma unroll
-    for (int k = 0; k < kSlots - 1; ++k) issue_tile(k);
+    const int rho = (r >> 1) | ((r & 1) << 2);  // V rows of this lane: chunk rho of a pair row
 
-    // ---------------------------------------------------------------- Q fragments
-    // Lane (r, c) holds head r of the group; k-step j covers head dims c*D/4 + 4j + {0..3}
-    // (the same permutation is used for K), as FP16 q * 2^kq.
-    uint32_t qf[G_::KSTEPS][2];
-    float cs_row = 0.0f;
-    {
-        float qv[D / 4];
-        float qmax = 0.0f;
-        if (r < G) {
-            const uint16_t* qp =
-                p.q + (static_cast<int64_t>(b) * p.Hq + h * G + r) * D + c * (D / 4);
+    // ------------------------------------------------ walk the pieces of this CTA's run
+    int b = start_bp[0];
+    int S_b = seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
+    int h = (s_begin - start_bp[1]) / S_b;
+    int j = (s_begin - start_bp[1]) - h * S_b;
+    int s = s_begin;
+    bool first_piece = true;
+    while (s < s_end) {
+        const int j0 = j, j1 = min(S_b, j + (s_end - s));
+        const int L = __ldg(p.seq_lens + b);
+        const int tok_end = min(j1 * TOK, L);
+        const int first_page = (j0 * TOK) / T;
+        const int n_pages = (tok_end + T - 1) / T - first_page;
+        const int32_t* pt_row = p.page_table + static_cast<int64_t>(b) * p.max_pages;
+        if (!first_piece) __syncthreads();  // the previous merge is done with the rings
+        first_piece = false;
+        for (int i = tid; i < n_pages && i < kPageBuf; i += kDecThreads)
+            page_ids[i] = __ldg(pt_row + first_page + i);
+        __syncthreads();
+        auto page_of = [&](int pidx) {
+            const int k = pidx - first_page;
+            const int pg = (k < kPageBuf) ? page_ids[k] : __ldg(pt_row + pidx);
+            return (pg >= 0 && pg < p.pool_pages) ? pg : -1;
+        };
+
+        // ---- issue of one stage (index js within the pair) into a ring slot
+        const int64_t head_rows = static_cast<int64_t>(h) * T;
+        const int64_t page_rows = static_cast<int64_t>(H) * T;
+        const bool page_aligned = (T % TOK) == 0;
+        auto issue_stage = [&](int js, uint32_t slot) {
+            const int t0 = js * TOK;
+            const int nval = min(TOK, L - t0);
+            int64_t row0[G_::SUB];  // token row of each sub-tile in its pool, -1: not real
+            if (page_aligned) {
+                const int pidx = static_cast<int>(__umul64hi(static_cast<uint64_t>(t0), p.t_magic));
+                const int pg = page_of(pidx);
+                const int64_t r0 = pg * page_rows + head_rows + (t0 - pidx * T);
 #pragma unroll
-            for (int i = 0; i < D / 4; i += 8) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(qp + i));
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                for (int u = 0; u < G_::SUB; ++u)
+                    row0[u] = (pg >= 0 && 16 * u < nval) ? r0 + 16 * u : -1;
+            } else {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    qv[i + 2 * k] = bf16_lo(wv[k]);
-                    qv[i + 2 * k + 1] = bf16_hi(wv[k]);
+                for (int u = 0; u < G_::SUB; ++u) {
+                    row0[u] = -1;
+                    if (16 * u < nval) {
+                        const int t = t0 + 16 * u;
+                        const int pidx =
+                            static_cast<int>(__umul64hi(static_cast<uint64_t>(t), p.t_magic));
+                        const int pg = page_of(pidx);
+                        if (pg >= 0) row0[u] = pg * page_rows + head_rows + (t - pidx * T);
+                    }
                 }
             }
+            uint32_t okbits = 0;
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) qmax = fmaxf(qmax, fabsf(qv[i]));
-        } else {
+            for (int u = 0; u < G_::SUB; ++u) okbits |= (row0[u] >= 0 ? 1u : 0u) << u;
+            const uint32_t want = (1u << ((nval + 15) / 16)) - 1u;
+            if (okbits != want && lane == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+            if (page_aligned && okbits == (1u << G_::SUB) - 1) {
+                // the whole stage is one run of each pool: offsets are compile-time constants
+                const int64_t doff = row0[0] * (D / 2) + 16 * lane;
+                const uint8_t* ksrc = p.kd + doff;
+                const uint8_t* vsrc = p.vd + doff;
+                static_for<G_::DCH>([&](auto I) {
+                    constexpr int i = decltype(I)::value;
+                    cp_async16<G_::K_OFF + 512 * i, 512 * i>(slot + 16 * lane, ksrc);
+                    cp_async16<0, 512 * i>(slot + v_dst[i], vsrc);
+                });
+                const int64_t soff = row0[0] * G_::NB;
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) qv[i] = 0.0f;
-        }
-        qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, 1));
-        qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, 2));
-        // qmax * 2^kq in [2^14, 2^15): every BF16 value of the head is exact in FP16 down to
-        // 2^-18 of the head maximum.
-        int kq = (qmax > 0.0f) ? (14 - ilogbf(qmax)) : 0;
-        kq = max(-120, min(kq, 120));
-        const float up = ldexpf(1.0f, kq);
+                for (int k = 0; k < G_::SC_PER_LANE; ++k) {
+                    const int jc = lane + 32 * k;
+                    const bool kpool = jc < G_::SCH;
+                    const int jj = kpool ? jc : jc - G_::SCH;
+                    cp_async16<0, 0>(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
+                                     (kpool ? p.ks : p.vs) + soff + 16 * jj);
+                }
+            } else {
 #pragma unroll
-        for (int j = 0; j < G_::KSTEPS; ++j) {
-            qf[j][0] = pack_f16x2(qv[4 * j] * up, qv[4 * j + 1] * up);
-            qf[j][1] = pack_f16x2(qv[4 * j + 2] * up, qv[4 * j + 3] * up);
-        }
-        if (r < G) cs_row = p.sm_scale * __ldg(p.gk) * kLog2e * ldexpf(1.0f, -kq);
-    }
-    // score scale of this lane's two S^T columns (query heads 2c, 2c+1)
-    const float cs0 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c);
-    const float cs1 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c + 4);
-
-    // V rows of this lane: chunk rho of every token pair; M-tile m row r <-> head dim
-    // rho*D/8 + 2m, row r+8 <-> that dim + 1 (rho spreads the quad lanes over the banks).
-    const int rho = (r >> 1) | ((r & 1) << 2);
-    float o[G_::KSTEPS][4];
+                for (int i = 0; i < G_::DCH; ++i) {
+                    const int u = i / G_::SUB_DIV;
+                    const int jj = lane + 32 * i - u * (D / 2);  // chunk within the sub-tile
+                    const bool ok = row0[u] >= 0;
+                    const int64_t off = ok ? row0[u] * (D / 2) + 16 * jj : 0;
+                    cp_async16_zfill(slot + G_::K_OFF + 16 * (lane + 32 * i), p.kd + off,
+                                     ok ? 16u : 0u);
+                    cp_async16_zfill(slot + v_dst[i], p.vd + off, ok ? 16u : 0u);
+                }
 #pragma unroll
-    for (int m = 0; m < G_::KSTEPS; ++m)
+                for (int k = 0; k < G_::SC_PER_LANE; ++k) {
+                    const int jc = lane + 32 * k;
+                    const bool kpool = jc < G_::SCH;
+                    const int jj = kpool ? jc : jc - G_::SCH;
+                    const int u = jj / (D / 16);
+                    int64_t ru = row0[0];  // row0[u] without a dynamically indexed array
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o[m][k] = 0.0f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-
-    // ---------------------------------------------------------------- main loop
-    for (int kt = 0; kt < n_tiles; ++kt) {
-        issue_tile(kt + kSlots - 1);    // into the slot tile kt-1 used (released below)
-        cp_async_wait<kSlots - 1>();    // this lane's copies of tile kt are done ...
-        __syncwarp();                   // ... and so are the other lanes'
-        const int t0 = tok_begin + 16 * (kWarps * kt + warp);
-        uint32_t tmask = 0u;
-        if (page_of(cpos.pidx) >= 0) {
-            const int valid = min(16, L - t0);
-            tmask = (valid >= 16) ? 0xFFFFu : ((1u << valid) - 1u);
-        }
-        cpos.advance(p.T);
-        if (tmask != 0u) {
-            const uint32_t st = ring + (kt % kSlots) * G_::SLOT;
-            const int row0 = r;
-            const int row1 = r + 8;
-            // ---- S^T = K^ Q^T (tokens x query heads)
-            uint32_t kw0[G_::CW], kw1[G_::CW];
-            lds_words(kw0, st + G_::K_OFF + row0 * (D / 2) + c * G_::CHUNK);
-            lds_words(kw1, st + G_::K_OFF + row1 * (D / 2) + c * G_::CHUNK);
-            // FP16 (s, s) of the lane's D/64 blocks in rows row0 / row1: the scale byte is
-            // duplicated by an integer multiply, then converted as an E4M3 pair
-            uint32_t ks0[D / 64], ks1[D / 64];
-#pragma unroll
-            for (int q = 0; q < D / 64; ++q) {
-                ks0[q] = e4m3x2_to_f16x2(lds_u8(st + G_::KS_OFF + row0 * G_::NB + c * (D / 64) + q) *
-                                         0x0101u);
-                ks1[q] = e4m3x2_to_f16x2(lds_u8(st + G_::KS_OFF + row1 * G_::NB + c * (D / 64) + q) *
-                                         0x0101u);
-            }
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int q = 0; q < G_::CW; ++q) {
-                uint32_t c0[4], c1[4];
-                e2m1x8_to_f16x2x4(kw0[q], c0);
-                e2m1x8_to_f16x2x4(kw1[q], c1);
-#pragma unroll
-                for (int hk = 0; hk < 2; ++hk) {
-                    const int k = 2 * q + hk;  // k-step: bytes 2k, 2k+1 of the lane's chunk
-                    const int blk = k / 4;     // block of the lane's chunk
-                    uint32_t a[4];
-                    a[0] = h2_mul(c0[2 * hk], ks0[blk]);
-                    a[1] = h2_mul(c1[2 * hk], ks1[blk]);
-                    a[2] = h2_mul(c0[2 * hk + 1], ks0[blk]);
-                    a[3] = h2_mul(c1[2 * hk + 1], ks1[blk]);
-                    mma_f16_16816(acc, a, qf[k][0], qf[k][1]);
+                    for (int uu = 1; uu < G_::SUB; ++uu)
+                        if (u == uu) ru = row0[uu];
+                    const bool ok = ru >= 0;
+                    const int64_t off = ok ? ru * G_::NB + 16 * (jj - u * (D / 16)) : 0;
+                    cp_async16_zfill(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
+                                     (kpool ? p.ks : p.vs) + off, ok ? 16u : 0u);
                 }
             }
+            if (lane == 0) sts_u32(slot + G_::HDR_OFF, okbits | (static_cast<uint32_t>(nval) << 8));
+        };
 
-            // ---- online softmax (log2 domain), columns = query heads 2c, 2c+1
-            float x0 = acc[0] * cs0, x1 = acc[1] * cs1, x2 = acc[2] * cs0, x3 = acc[3] * cs1;
-            if (tmask != 0xFFFFu) {
-                if (!((tmask >> r) & 1u)) x0 = x1 = -INFINITY;
-                if (!((tmask >> (r + 8)) & 1u)) x2 = x3 = -INFINITY;
-            }
-            // column maxima over the 16 tokens, both columns in one FP16 pair (the running
-            // maximum only has to be close to the true one: p = 2^(x - m) stays below 2^8)
-            __half2 hm = __floats2half2_rn(fmaxf(x0, x2), fmaxf(x1, x3));
+        // this warp's stages of the piece: j0 + warp, j0 + warp + 4, ...
+        const int n_st = max(0, (j1 - j0 - warp + kWarps - 1) / kWarps);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                const uint32_t u =
-                    __shfl_xor_sync(0xFFFFFFFFu, *reinterpret_cast<const uint32_t*>(&hm), off);
-                hm = __hmax2(hm, *reinterpret_cast<const __half2*>(&u));
+        for (int k = 0; k < kSlots - 1; ++k) {
+            if (k < n_st) issue_stage(j0 + warp + kWarps * k, ring + k * G_::SLOT);
+            cp_async_commit();
+        }
+
+        // ---- Q fragments of (b, h): lane (r, c) holds head r of the group; k-step kk covers
+        // head dims c*D/4 + 4kk + {0..3} (the same permutation is used for K), as FP16 q * 2^kq.
+        uint32_t qf[G_::KSTEPS][2];
+        float cs_row = 0.0f;
+        {
+            float qv[D / 4];
+            float qmax = 0.0f;
+            if (r < G) {
+                const uint16_t* qp =
+                    p.q + (static_cast<int64_t>(b) * p.Hq + h * G + r) * D + c * (D / 4);
+#pragma unroll
+                for (int i = 0; i < D / 4; i += 8) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(qp + i));
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        qv[i + 2 * k] = bf16_lo(wv[k]);
+                        qv[i + 2 * k + 1] = bf16_hi(wv[k]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < D / 4; ++i) qmax = fmaxf(qmax, fabsf(qv[i]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < D / 4; ++i) qv[i] = 0.0f;
             }
-            float mx0 = __low2float(hm), mx1 = __high2float(hm);
-            if (__any_sync(0xFFFFFFFFu, fmaxf(mx0, mx1) > 65000.0f)) {
-                // scores beyond the FP16 range: reduce in fp32 instead
-                mx0 = fmaxf(x0, x2);
-                mx1 = fmaxf(x1, x3);
+            qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, 1));
+            qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, 2));
+            // qmax * 2^kq in [2^14, 2^15): every BF16 value of the head is exact in FP16 down
+            // to 2^-18 of the head maximum.
+            int kq = (qmax > 0.0f) ? (14 - ilogbf(qmax)) : 0;
+            kq = max(-120, min(kq, 120));
+            const float up = ldexpf(1.0f, kq);
+#pragma unroll
+            for (int kk = 0; kk < G_::KSTEPS; ++kk) {
+                qf[kk][0] = pack_f16x2(qv[4 * kk] * up, qv[4 * kk + 1] * up);
+                qf[kk][1] = pack_f16x2(qv[4 * kk + 2] * up, qv[4 * kk + 3] * up);
+            }
+            if (r < G) cs_row = p.sm_scale * __ldg(p.gk) * kLog2e * ldexpf(1.0f, -kq);
+        }
+        // score scale of this lane's two S^T columns (query heads 2c, 2c+1)
+        const float cs0 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c);
+        const float cs1 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c + 4);
+
+        float o[G_::KSTEPS][4];
+#pragma unroll
+        for (int m = 0; m < G_::KSTEPS; ++m)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[m][k] = 0.0f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+        // ---- main loop over this warp's stages
+        for (int i = 0; i < n_st; ++i) {
+            if (i + kSlots - 1 < n_st)
+                issue_stage(j0 + warp + kWarps * (i + kSlots - 1),
+                            ring + ((i + kSlots - 1) % kSlots) * G_::SLOT);
+            cp_async_commit();
+            cp_async_wait<kSlots - 1>();  // this lane's copies of stage i are done ...
+            __syncwarp();                 // ... and so are the other lanes'
+            const uint32_t st = ring + (i % kSlots) * G_::SLOT;
+            const uint32_t hdr = lds_u32(st + G_::HDR_OFF);
+            const uint32_t okbits = hdr & 0xFFu;
+            const int nval = static_cast<int>(hdr >> 8);
+            if (okbits != 0u) {
+                const bool full = (okbits == (1u << G_::SUB) - 1) && nval >= TOK;
+                // valid-token bits of each sub-tile (only read when !full)
+                uint32_t tmask[G_::SUB];
+#pragma unroll
+                for (int u = 0; u < G_::SUB; ++u) {
+                    const int nv = min(16, max(0, nval - 16 * u));
+                    tmask[u] = ((okbits >> u) & 1u) ? ((nv >= 16) ? 0xFFFFu : ((1u << nv) - 1u)) : 0u;
+                }
+
+                // ---- S^T = K^ Q^T for the SUB sub-tiles
+                float x[G_::SUB][4];
+#pragma unroll
+                for (int u = 0; u < G_::SUB; ++u) {
+                    const int row0 = 16 * u + r;
+                    const int row1 = row0 + 8;
+                    uint32_t kw0[G_::CW], kw1[G_::CW];
+                    lds_words(kw0, st + G_::K_OFF + row0 * (D / 2) + c * G_::CHUNK);
+                    lds_words(kw1, st + G_::K_OFF + row1 * (D / 2) + c * G_::CHUNK);
+                    // FP16 (s, s) of the lane's D/64 blocks in rows row0 / row1: the scale byte
+                    // is duplicated by an integer multiply, then converted as an E4M3 pair
+                    uint32_t ks0[D / 64], ks1[D / 64];
+#pragma unroll
+                    for (int q = 0; q < D / 64; ++q) {
+                        ks0[q] = e4m3x2_to_f16x2(
+                            lds_u8(st + G_::KS_OFF + row0 * G_::NB + c * (D / 64) + q) * 0x0101u);
+                        ks1[q] = e4m3x2_to_f16x2(
+                            lds_u8(st + G_::KS_OFF + row1 * G_::NB + c * (D / 64) + q) * 0x0101u);
+                    }
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int q = 0; q < G_::CW; ++q) {
+                        uint32_t c0[4], c1[4];
+                        e2m1x8_to_f16x2x4(kw0[q], c0);
+                        e2m1x8_to_f16x2x4(kw1[q], c1);
+#pragma unroll
+                        for (int hk = 0; hk < 2; ++hk) {
+                            const int kk = 2 * q + hk;  // k-step: bytes 2kk, 2kk+1 of the chunk
+                            const int blk = kk / 4;     // block of the lane's chunk
+                            uint32_t a[4];
+                            a[0] = h2_mul(c0[2 * hk], ks0[blk]);
+                            a[1] = h2_mul(c1[2 * hk], ks1[blk]);
+                            a[2] = h2_mul(c0[2 * hk + 1], ks0[blk]);
+                            a[3] = h2_mul(c1[2 * hk + 1], ks1[blk]);
+                            mma_f16_16816(acc, a, qf[kk][0], qf[kk][1]);
+                        }
+                    }
+                    x[u][0] = acc[0] * cs0;
+                    x[u][1] = acc[1] * cs1;
+                    x[u][2] = acc[2] * cs0;
+                    x[u][3] = acc[3] * cs1;
+                }
+
+                // ---- online softmax over the stage, columns = query heads 2c, 2c+1
+                if (!full) {
+#pragma unroll
+                    for (int u = 0; u < G_::SUB; ++u) {
+                        if (!((tmask[u] >> r) & 1u)) x[u][0] = x[u][1] = -INFINITY;
+                        if (!((tmask[u] >> (r + 8)) & 1u)) x[u][2] = x[u][3] = -INFINITY;
+                    }
+                }
+                float lm0 = fmaxf(x[0][0], x[0][2]), lm1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+                for (int u = 1; u < G_::SUB; ++u) {
+                    lm0 = fmaxf(lm0, fmaxf(x[u][0], x[u][2]));
+                    lm1 = fmaxf(lm1, fmaxf(x[u][1], x[u][3]));
+                }
+                // column maxima over the stage, both columns in one FP16 pair (the running
+                // maximum only has to be close to the true one: p = 2^(x - m) stays below 2^8)
+                __half2 hm = __floats2half2_rn(lm0, lm1);
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+                    const uint32_t uu =
+                        __shfl_xor_sync(0xFFFFFFFFu, *reinterpret_cast<const uint32_t*>(&hm), off);
+                    hm = __hmax2(hm, *reinterpret_cast<const __half2*>(&uu));
                 }
-            }
-            const bool grow = (mx0 > m0 + kRescaleThreshold) || (mx1 > m1 + kRescaleThreshold);
-            if (__any_sync(0xFFFFFFFFu, grow)) {
-                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                const float a0 = ex2_approx(m0 - n0), a1 = ex2_approx(m1 - n1);
-                m0 = n0;
-                m1 = n1;
-                l0 *= a0;
-                l1 *= a1;
+                float mx0 = __low2float(hm), mx1 = __high2float(hm);
+                if (__any_sync(0xFFFFFFFFu, fmaxf(mx0, mx1) > 65000.0f)) {
+                    // scores beyond the FP16 range: reduce in fp32 instead
+                    mx0 = lm0;
+                    mx1 = lm1;
 #pragma unroll
-                for (int m = 0; m < G_::KSTEPS; ++m) {
-                    o[m][0] *= a0;
-                    o[m][1] *= a1;
-                    o[m][2] *= a0;
-                    o[m][3] *= a1;
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+                    }
                 }
-            }
-            const float p0 = ex2_approx(x0 - m0), p1 = ex2_approx(x1 - m1);
-            const float p2 = ex2_approx(x2 - m0), p3 = ex2_approx(x3 - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // P^T (tokens x heads) -> B operand (k = tokens, n = heads)
-            const uint32_t pb0 = movmatrix_trans(pack_f16x2(p0, p1));
-            const uint32_t pb1 = movmatrix_trans(pack_f16x2(p2, p3));
+                const bool grow = (mx0 > m0 + kRescaleThreshold) || (mx1 > m1 + kRescaleThreshold);
+                if (__any_sync(0xFFFFFFFFu, grow)) {
+                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                    const float a0 = ex2_approx(m0 - n0), a1 = ex2_approx(m1 - n1);
+                    m0 = n0;
+                    m1 = n1;
+                    l0 *= a0;
+                    l1 *= a1;
+#pragma unroll
+                    for (int m = 0; m < G_::KSTEPS; ++m) {
+                        o[m][0] *= a0;
+                        o[m][1] *= a1;
+                        o[m][2] *= a0;
+                        o[m][3] *= a1;
+                    }
+                }
+                uint32_t pb[G_::SUB][2];
+#pragma unroll
+                for (int u = 0; u < G_::SUB; ++u) {
+                    const float p0 = ex2_approx(x[u][0] - m0), p1 = ex2_approx(x[u][1] - m1);
+                    const float p2 = ex2_approx(x[u][2] - m0), p3 = ex2_approx(x[u][3] - m1);
+                    l0 += p0 + p2;
+                    l1 += p1 + p3;
+                    // P^T (tokens x heads) -> B operand (k = tokens, n = heads)
+                    pb[u][0] = movmatrix_trans(pack_f16x2(p0, p1));
+                    pb[u][1] = movmatrix_trans(pack_f16x2(p2, p3));
+                }
 
-            // ---- O^T += V^^T P^T. Lane pairs: pr0 (tokens 2c, 2c+1), pr1 (tokens 2c+8, 2c+9)
-            const int pr0 = c, pr1 = c + 4;
-            uint32_t keep0 = 0xFFFFFFFFu, keep1 = 0xFFFFFFFFu;
-            if (tmask != 0xFFFFu) {
-                keep0 = (((tmask >> (2 * c)) & 1u) ? 0x0000FFFFu : 0u) |
-                        (((tmask >> (2 * c + 1)) & 1u) ? 0xFFFF0000u : 0u);
-                keep1 = (((tmask >> (2 * c + 8)) & 1u) ? 0x0000FFFFu : 0u) |
-                        (((tmask >> (2 * c + 9)) & 1u) ? 0xFFFF0000u : 0u);
-            }
-            // the lane's chunk covers head dims rho*D/8 .. +D/8-1: blocks (rho*D/8)/16 ...
-            constexpr int kBlkPerChunk = (D / 8 + 15) / 16;
-            uint32_t vsc0[kBlkPerChunk], vsc1[kBlkPerChunk];
+                // ---- O^T += V^^T P^T. Lane pairs: pr0 (tokens 2c, 2c+1), pr1 (tokens 2c+8, 2c+9)
 #pragma unroll
-            for (int q = 0; q < kBlkPerChunk; ++q) {
-                const int blk = (rho * (D / 8)) / 16 + q;
-                vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk));
-                vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk));
-                if (tmask != 0xFFFFu) {
-                    vsc0[q] &= keep0;
-                    vsc1[q] &= keep1;
+                for (int u = 0; u < G_::SUB; ++u) {
+                    const int pr0 = 8 * u + c, pr1 = pr0 + 4;
+                    // the lane's chunk covers head dims rho*D/8 .. +D/8-1: blocks (rho*D/8)/16 ...
+                    constexpr int kBlkPerChunk = (D / 8 + 15) / 16;
+                    uint32_t vsc0[kBlkPerChunk], vsc1[kBlkPerChunk];
+#pragma unroll
+                    for (int q = 0; q < kBlkPerChunk; ++q) {
+                        const int blk = (rho * (D / 8)) / 16 + q;
+                        vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk));
+                        vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk));
+                    }
+                    if (!full && tmask[u] != 0xFFFFu) {
+                        // tokens past the sequence end in a real page: their V scales may be
+                        // anything, so they are zeroed (P is 0 there already)
+                        const uint32_t tm = tmask[u];
+                        const uint32_t keep0 = (((tm >> (2 * c)) & 1u) ? 0x0000FFFFu : 0u) |
+                                               (((tm >> (2 * c + 1)) & 1u) ? 0xFFFF0000u : 0u);
+                        const uint32_t keep1 = (((tm >> (2 * c + 8)) & 1u) ? 0x0000FFFFu : 0u) |
+                                               (((tm >> (2 * c + 9)) & 1u) ? 0xFFFF0000u : 0u);
+#pragma unroll
+                        for (int q = 0; q < kBlkPerChunk; ++q) {
+                            vsc0[q] &= keep0;
+                            vsc1[q] &= keep1;
+                        }
+                    }
+                    uint32_t vw0[G_::CW], vw1[G_::CW];
+#pragma unroll
+                    for (int q = 0; q < G_::CW; q += (G_::CW >= 4 ? 4 : G_::CW)) {
+                        const int xb = rho * G_::CHUNK + 4 * q;  // logical byte of the chunk piece
+                        uint32_t t0w[G_::CW >= 4 ? 4 : G_::CW], t1w[G_::CW >= 4 ? 4 : G_::CW];
+                        lds_words(t0w, st + G_::V_OFF + v_swz<D>(pr0, xb));
+                        lds_words(t1w, st + G_::V_OFF + v_swz<D>(pr1, xb));
+#pragma unroll
+                        for (int e = 0; e < (G_::CW >= 4 ? 4 : G_::CW); ++e) {
+                            vw0[q + e] = t0w[e];
+                            vw1[q + e] = t1w[e];
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < G_::CW; ++q) {
+                        uint32_t c0[4], c1[4];
+                        e2m1x8_to_f16x2x4(vw0[q], c0);
+                        e2m1x8_to_f16x2x4(vw1[q], c1);
+#pragma unroll
+                        for (int hm2 = 0; hm2 < 2; ++hm2) {
+                            const int m = 2 * q + hm2;   // M-tile: bytes 2m, 2m+1 of the chunk
+                            const int sq = (2 * m) / 16; // block of that byte within the chunk
+                            uint32_t a[4];
+                            a[0] = h2_mul(c0[2 * hm2], vsc0[sq]);
+                            a[1] = h2_mul(c0[2 * hm2 + 1], vsc0[sq]);
+                            a[2] = h2_mul(c1[2 * hm2], vsc1[sq]);
+                            a[3] = h2_mul(c1[2 * hm2 + 1], vsc1[sq]);
+                            mma_f16_16816(o[m], a, pb[u][0], pb[u][1]);
+                        }
+                    }
                 }
             }
-            uint32_t vw0[G_::CW], vw1[G_::CW];
-#pragma unroll
-            for (int q = 0; q < G_::CW; q += (G_::CW >= 4 ? 4 : G_::CW)) {
-                const int x = rho * G_::CHUNK + 4 * q;  // logical byte of the chunk piece
-                uint32_t t0[G_::CW >= 4 ? 4 : G_::CW], t1[G_::CW >= 4 ? 4 : G_::CW];
-                lds_words(t0, st + G_::V_OFF + v_swz<D>(pr0, x));
-                lds_words(t1, st + G_::V_OFF + v_swz<D>(pr1, x));
-#pragma unroll
-                for (int i = 0; i < (G_::CW >= 4 ? 4 : G_::CW); ++i) {
-                    vw0[q + i] = t0[i];
-                    vw1[q + i] = t1[i];
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < G_::CW; ++q) {
-                uint32_t c0[4], c1[4];
-                e2m1x8_to_f16x2x4(vw0[q], c0);
-                e2m1x8_to_f16x2x4(vw1[q], c1);
-#pragma unroll
-                for (int hm = 0; hm < 2; ++hm) {
-                    const int m = 2 * q + hm;            // M-tile: bytes 2m, 2m+1 of the chunk
-                    const int sq = (2 * m) / 16;         // block of that byte within the chunk
-                    uint32_t a[4];
-                    a[0] = h2_mul(c0[2 * hm], vsc0[sq]);
-                    a[1] = h2_mul(c0[2 * hm + 1], vsc0[sq]);
-                    a[2] = h2_mul(c1[2 * hm], vsc1[sq]);
-                    a[3] = h2_mul(c1[2 * hm + 1], vsc1[sq]);
-                    mma_f16_16816(o[m], a, pb0, pb1);
-                }
-            }
+            __syncwarp();  // every lane is done reading the slot before it refills
         }
-        __syncwarp();                   // every lane is done reading the slot before it refills
-    }
-    cp_async_wait<0>();
+        cp_async_wait<0>();
 
-    // ---------------------------------------------------------------- merge the 4 warps
+        // ---- merge the 4 warps and write the piece's record
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
-        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
-    }
-    if (r == 0) {
-        red_m[warp][2 * c] = m0;
-        red_m[warp][2 * c + 1] = m1;
-        red_l[warp][2 * c] = l0;
-        red_l[warp][2 * c + 1] = l1;
-    }
-    __syncthreads();  // every warp is done with its ring: the rings hold the merge buffer
-    float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        M0 = fmaxf(M0, red_m[w][2 * c]);
-        M1 = fmaxf(M1, red_m[w][2 * c + 1]);
-    }
-    const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M0);
-    const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M1);
-    float* so = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGroup][D], over the rings
-#pragma unroll
-    for (int m = 0; m < G_::KSTEPS; ++m) {
-        const int d0 = rho * (D / 8) + 2 * m;
-        float* base = so + (warp * kMaxGroup + 2 * c) * D;
-        base[d0] = o[m][0] * f0;
-        base[D + d0] = o[m][1] * f1;
-        base[d0 + 1] = o[m][2] * f0;
-        base[D + d0 + 1] = o[m][3] * f1;
-    }
-    __syncthreads();
-    for (int i = tid; i < G * D; i += kDecThreads) {
-        const int col = i / D, d = i - (i / D) * D;
-        float acc = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
-        p.part_o[(part_row + static_cast<int64_t>(col) * p.num_splits) * D + d] = acc;
-    }
-    if (tid < G) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
-        float lsum = 0.0f;
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+            l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+        }
+        if (r == 0) {
+            red_m[warp][2 * c] = m0;
+            red_m[warp][2 * c + 1] = m1;
+            red_l[warp][2 * c] = l0;
+            red_l[warp][2 * c + 1] = l1;
+        }
+        __syncthreads();  // every warp is done with its ring: the rings hold the merge buffer
+        float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float mw = red_m[w][tid];
-            if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
+            M0 = fmaxf(M0, red_m[w][2 * c]);
+            M1 = fmaxf(M1, red_m[w][2 * c + 1]);
         }
-        p.part_m[part_row + static_cast<int64_t>(tid) * p.num_splits] = M;
-        p.part_l[part_row + static_cast<int64_t>(tid) * p.num_splits] = lsum;
+        const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M0);
+        const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M1);
+        float* so = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGroup][D], over the rings
+#pragma unroll
+        for (int m = 0; m < G_::KSTEPS; ++m) {
+            const int d0 = rho * (D / 8) + 2 * m;
+            float* base = so + (warp * kMaxGroup + 2 * c) * D;
+            base[d0] = o[m][0] * f0;
+            base[D + d0] = o[m][1] * f1;
+            base[d0 + 1] = o[m][2] * f0;
+            base[D + d0 + 1] = o[m][3] * f1;
+        }
+        __syncthreads();
+        const int64_t rec = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * H + h;
+        float* ro = p.rec_o + rec * G * D;
+        for (int i = tid; i < G * D; i += kDecThreads) {
+            const int col = i / D, d = i - (i / D) * D;
+            float acc = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
+            ro[i] = acc;
+        }
+        if (tid < G) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
+            float lsum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = red_m[w][tid];
+                if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
+            }
+            p.rec_ml[(rec * G + tid) * 2] = M;
+            p.rec_ml[(rec * G + tid) * 2 + 1] = lsum;
+        }
+
+        // ---- next piece: the next pair with at least one stage
+        s += j1 - j0;
+        j = 0;
+        if (s < s_end) {
+            if (++h == H) {
+                h = 0;
+                do {
+                    ++b;
+                    S_b = seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
+                } while (S_b == 0);
+            }
+        }
     }
 }
 
 // ------------------------------------------------------------------------------------------
-// Combine: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s; lse = ln 2 (M + log2 L).
-// The global V scale multiplies the result once here.
+// Combine: for the records R of (sequence b, query head qh),
+//   out = g_V sum_R 2^(m_R - M) o_R / sum_R 2^(m_R - M) l_R;  lse = ln 2 (M + log2 L).
 // ------------------------------------------------------------------------------------------
 struct CombineParams {
-    const float* part_o;
-    const float* part_m;
-    const float* part_l;
+    const float* rec_o;
+    const float* rec_ml;
+    const int32_t* hdr;
+    const int32_t* ps;
     const int32_t* seq_lens;
     const float* gv;
     uint16_t* out;  // BF16 bits [B][Hq][D]
     float* lse;     // [B][Hq] or null
-    int32_t Hq, D, T, max_pages, num_splits, stages_per_split;
+    int32_t Hq, H, G, D, tok, max_tokens;
 };
 
 __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
     const int qh = blockIdx.x, b = blockIdx.y;
-    const int L = __ldg(p.seq_lens + b);
-    int n_act = 0;
-    if (L > 0 && L <= p.max_pages * p.T) {
-        const int total_stages = (L + kStageTokens - 1) / kStageTokens;
-        n_act = (total_stages + p.stages_per_split - 1) / p.stages_per_split;
-    }
-    const int64_t row = (static_cast<int64_t>(b) * p.Hq + qh) * p.num_splits;
-    __shared__ float w_s[kMaxSplits];
-    __shared__ float red[2][4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // one split per thread (n_act <= 64): maximum, then weights and weighted sum of l
-    const float ms = (tid < n_act) ? p.part_m[row + tid] : -INFINITY;
-    const float ls = (tid < n_act) ? p.part_l[row + tid] : 0.0f;
-    float M = ms;
+    const int h = qh / p.G, g = qh - h * p.G;
+    const int L = __ldg(p.seq_lens + b);
+    const int S_b = seq_stages(L, p.max_tokens, p.tok);
+    uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + qh) * p.D;
+    if (S_b == 0) {
+        for (int d = tid; d < p.D; d += blockDim.x) out[d] = 0;
+        if (tid == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.Hq + qh] = -INFINITY;
+        return;
+    }
+    const int W = p.hdr[1];
+    const int start = p.ps[b] + h * S_b;
+    const int c0 = start / W, c1 = (start + S_b - 1) / W;
+    const int n = c1 - c0 + 1;
+    const int64_t base = static_cast<int64_t>(c0) + static_cast<int64_t>(b) * p.H + h;
+    const float* ml = p.rec_ml + (base * p.G + g) * 2;   // record k at ml + 2 k G
+    const float* ro = p.rec_o + (base * p.G + g) * p.D;  // record k at ro + k G D
+    __shared__ float w_s[kMaxWeights];
+    __shared__ float red[2][4];
+
+    float M = -INFINITY;
+    for (int k = tid; k < n; k += blockDim.x) M = fmaxf(M, ml[2 * k * p.G]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     if (lane == 0) red[0][warp] = M;
     __syncthreads();
     M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-    const float w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-    if (tid < kMaxSplits) w_s[tid] = w;
-    float lsum = w * ls;
+    float lsum = 0.0f;
+    for (int k = tid; k < n; k += blockDim.x) {
+        const float mk = ml[2 * k * p.G];
+        const float w = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
+        if (k < kMaxWeights) w_s[k] = w;
+        lsum += w * ml[2 * k * p.G + 1];
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
     if (lane == 0) red[1][warp] = lsum;
@@ -557,57 +765,48 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
             (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
     for (int d = tid; d < p.D; d += blockDim.x) {
         float acc = 0.0f;
-        for (int s = 0; s < n_act; ++s) {
-            const float ws = w_s[s];
-            if (ws != 0.0f) acc += ws * p.part_o[(row + s) * p.D + d];
+        for (int k = 0; k < n; ++k) {
+            float w;
+            if (k < kMaxWeights) {
+                w = w_s[k];
+            } else {
+                const float mk = ml[2 * k * p.G];
+                w = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
+            }
+            if (w != 0.0f) acc += w * ro[static_cast<int64_t>(k) * p.G * p.D + d];
         }
         const __nv_bfloat16 yb = __float2bfloat16_rn(acc * inv_l);
-        p.out[(static_cast<int64_t>(b) * p.Hq + qh) * p.D + d] =
-            *reinterpret_cast<const uint16_t*>(&yb);
+        out[d] = *reinterpret_cast<const uint16_t*>(&yb);
     }
 }
 
 // ------------------------------------------------------------------------------------------
-// Host side: split heuristic, workspace carving, V tensor map
+// Host side: grid, workspace carving
 // ------------------------------------------------------------------------------------------
-struct SplitPlan {
-    int num_splits;
-    int stages_per_split;
-};
-
-SplitPlan plan_splits(int batch, int H, int max_pages, int T, int max_num_splits) {
-    const int64_t max_tokens = static_cast<int64_t>(max_pages) * T;
-    const int max_stages =
-        static_cast<int>(std::max<int64_t>(1, (max_tokens + kStageTokens - 1) / kStageTokens));
-    int cap = max_num_splits > 0 ? max_num_splits : kMaxSplits;
-    cap = std::min(cap, max_stages);
-    int n;
-    if (max_num_splits > 0) {
-        n = cap;
-    } else {
-        // about four waves of four resident CTAs per SM
-        const int64_t target = static_cast<int64_t>(num_sms()) * 16;
-        const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(batch) * H);
-        n = static_cast<int>(std::min<int64_t>(cap, (target + pairs - 1) / pairs));
-        n = std::max(n, 1);
-    }
-    const int sps = (max_stages + n - 1) / n;
-    return SplitPlan{(max_stages + sps - 1) / sps, sps};
-}
-
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+int stage_tokens(int D) { return D == 256 ? 32 : 64; }
+int blocks_per_sm(int D) { return D == 64 ? 6 : 3; }
+
+// CTAs of the split kernel: one wave (automatic), or n runs per (sequence, KV head) pair.
+int64_t decode_ctas(int batch, int H, int D, int max_num_splits) {
+    if (max_num_splits > 0) return static_cast<int64_t>(max_num_splits) * batch * H;
+    return static_cast<int64_t>(num_sms()) * blocks_per_sm(D);
+}
+
 struct WsLayout {
-    size_t o, m, l, total;
+    size_t hdr, ps, ml, o, total;
 };
 
-WsLayout ws_layout(int batch, int Hq, int D, int S) {
-    const size_t rows = static_cast<size_t>(batch) * Hq * S;
+WsLayout ws_layout(int batch, int H, int Hq, int D, int64_t ctas) {
+    const size_t records = static_cast<size_t>(ctas) + static_cast<size_t>(batch) * H;
+    const size_t G = static_cast<size_t>(Hq / H);
     WsLayout w;
-    w.o = 0;
-    w.m = align256(rows * D * sizeof(float));
-    w.l = w.m + align256(rows * sizeof(float));
-    w.total = w.l + align256(rows * sizeof(float));
+    w.hdr = 0;
+    w.ps = 256;
+    w.ml = w.ps + align256((static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+    w.o = w.ml + align256(records * G * 2 * sizeof(float));
+    w.total = w.o + align256(records * G * D * sizeof(float));
     return w;
 }
 
@@ -621,14 +820,23 @@ bool decode_shape_ok(const nvfp4kv_layout* l, int Hq) {
     return G >= 1 && G <= kMaxGroup;
 }
 
+// The flat stage list, the token positions and the records index with 32-bit integers.
+bool decode_size_ok(int batch, int H, int D, int max_pages, int T, int64_t ctas) {
+    const int64_t max_tokens = static_cast<int64_t>(max_pages) * T;
+    const int64_t tok = stage_tokens(D);
+    const int64_t stages = (max_tokens + tok - 1) / tok * batch * H;
+    const int64_t lim = (int64_t{1} << 31) - 1;
+    return max_tokens < lim - tok && stages + ctas * kWarps < lim &&
+           ctas + static_cast<int64_t>(batch) * H < lim;
+}
+
 template <int D>
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams& p, int64_t ctas, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Geo<D>::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_splits, p.H, p.B);
-    decode_split_kernel<D><<<grid, kDecThreads, Geo<D>::SMEM, s>>>(p);
+    decode_split_kernel<D><<<static_cast<unsigned>(ctas), kDecThreads, Geo<D>::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -644,9 +852,10 @@ extern "C" size_t nvfp4_paged_decode_workspace_size(const nvfp4kv_layout* layout
     if (!layout_ok(layout) || batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0 ||
         max_num_splits < 0 || max_num_splits > kMaxSplits)
         return 0;
-    const SplitPlan plan = plan_splits(batch, layout->num_kv_heads, max_pages_per_seq,
-                                       layout->page_size, max_num_splits);
-    return ws_layout(batch, num_q_heads, layout->head_dim, plan.num_splits).total;
+    if (num_q_heads % layout->num_kv_heads != 0) return 0;
+    const int H = layout->num_kv_heads;
+    const int64_t ctas = decode_ctas(batch, H, layout->head_dim, max_num_splits);
+    return ws_layout(batch, H, num_q_heads, layout->head_dim, ctas).total;
 }
 
 extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
@@ -667,12 +876,13 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
     if (!aligned16(q) || !aligned16(k_data) || !aligned16(k_scales) || !aligned16(v_data) ||
         !aligned16(v_scales) || !aligned16(out))
         return NVFP4KV_ERR_INVALID_ARG;
-    if (batch > 65535 || layout->num_kv_heads > 65535 || num_q_heads > 65535)
-        return NVFP4KV_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_q_heads > 65535) return NVFP4KV_ERR_UNSUPPORTED;
     const int D = layout->head_dim;
-    const SplitPlan plan = plan_splits(batch, layout->num_kv_heads, max_pages_per_seq,
-                                       layout->page_size, max_num_splits);
-    const WsLayout wl = ws_layout(batch, num_q_heads, D, plan.num_splits);
+    const int H = layout->num_kv_heads;
+    const int T = layout->page_size;
+    const int64_t ctas = decode_ctas(batch, H, D, max_num_splits);
+    if (!decode_size_ok(batch, H, D, max_pages_per_seq, T, ctas)) return NVFP4KV_ERR_UNSUPPORTED;
+    const WsLayout wl = ws_layout(batch, H, num_q_heads, D, ctas);
     if (!workspace || workspace_bytes < wl.total || !aligned16(workspace))
         return NVFP4KV_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -684,47 +894,48 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
     p.vd = v_data;
     p.vs = v_scales;
     p.gk = k_global_scale;
-    p.gv = v_global_scale;
     p.page_table = page_table;
     p.seq_lens = seq_lens;
-    p.part_o = reinterpret_cast<float*>(ws + wl.o);
-    p.part_m = reinterpret_cast<float*>(ws + wl.m);
-    p.part_l = reinterpret_cast<float*>(ws + wl.l);
+    p.hdr = reinterpret_cast<int32_t*>(ws + wl.hdr);
+    p.ps = reinterpret_cast<int32_t*>(ws + wl.ps);
+    p.rec_ml = reinterpret_cast<float*>(ws + wl.ml);
+    p.rec_o = reinterpret_cast<float*>(ws + wl.o);
     p.status = status;
+    p.t_magic = UINT64_MAX / static_cast<uint64_t>(T) + 1;
     p.B = batch;
     p.Hq = num_q_heads;
-    p.H = layout->num_kv_heads;
-    p.G = num_q_heads / layout->num_kv_heads;
-    p.T = layout->page_size;
+    p.H = H;
+    p.G = num_q_heads / H;
+    p.T = T;
     p.pool_pages = pool_pages;
     p.max_pages = max_pages_per_seq;
-    p.num_splits = plan.num_splits;
-    p.stages_per_split = plan.stages_per_split;
+    p.min_w = (max_num_splits > 0) ? 1 : kWarps;
     p.sm_scale = sm_scale;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (D) {
-    case 64: e = launch_decode<64>(p, s); break;
-    case 128: e = launch_decode<128>(p, s); break;
-    default: e = launch_decode<256>(p, s); break;
+    case 64: e = launch_decode<64>(p, ctas, s); break;
+    case 128: e = launch_decode<128>(p, ctas, s); break;
+    default: e = launch_decode<256>(p, ctas, s); break;
     }
     if (e != cudaSuccess) return NVFP4KV_ERR_CUDA;
 
     CombineParams cp{};
-    cp.part_o = p.part_o;
-    cp.part_m = p.part_m;
-    cp.part_l = p.part_l;
+    cp.rec_o = p.rec_o;
+    cp.rec_ml = p.rec_ml;
+    cp.hdr = p.hdr;
+    cp.ps = p.ps;
     cp.seq_lens = seq_lens;
     cp.gv = v_global_scale;
     cp.out = static_cast<uint16_t*>(out);
     cp.lse = lse;
     cp.Hq = num_q_heads;
+    cp.H = H;
+    cp.G = p.G;
     cp.D = D;
-    cp.T = layout->page_size;
-    cp.max_pages = max_pages_per_seq;
-    cp.num_splits = plan.num_splits;
-    cp.stages_per_split = plan.stages_per_split;
+    cp.tok = stage_tokens(D);
+    cp.max_tokens = max_pages_per_seq * T;
     combine_kernel<<<dim3(num_q_heads, batch), 128, 0, s>>>(cp);
     return launch_status();
 }

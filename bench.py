@@ -18,6 +18,7 @@ Under torchrun each rank runs its own batch (weak scaling, no data-path collecti
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -32,6 +33,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 GB = 1e9
+# ncu summary of the decode call whose DRAM traffic is reported, valid while the decode
+# sources hash to the value recorded in it
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_split_kernel_long_context.md")
+DECODE_SOURCES = [os.path.join(ROOT, "nvfp4_paged_kv_gb300", "csrc", f)
+                  for f in ("decode.cu", "common.cuh")]
 METRIC = "NVFP4 paged decode-attn KV GB/s + quant/dequant GB/s, % of GB300 HBM peak"
 WORKLOAD = ("page round-trip 4096x32x8x128 K+V (amax, encode, decode->BF16, decode->FP8) + "
             "long-context decode 8 seqs U[32K,128K] 64q/8kv d128 page64 split-KV")
@@ -40,13 +46,15 @@ WORKLOAD = ("page round-trip 4096x32x8x128 K+V (amax, encode, decode->BF16, deco
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip per-kernel timings")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of untimed steps under the clock sampler before timing")
     ap.add_argument("--ref-pages", type=int, default=256,
                     help="reference arm: page round-trip pages per step")
     ap.add_argument("--ref-max-tokens", type=int, default=0,
@@ -103,7 +111,7 @@ def barrier(world):
 
 class ClockSampler:
     """nvidia-smi sampling during the timed region (SM clock, throttle reasons)."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -111,6 +119,11 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.path = None
+        self.t_load = None
+
+    def mark_load(self):
+        """Samples taken before this moment (sampler start-up, idle) are dropped."""
+        self.t_load = time.time()
 
     def __enter__(self):
         try:
@@ -142,8 +155,15 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) < 10:
+                    continue
+                try:
+                    t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    t = None
+                if self.t_load is not None and t is not None and t < self.t_load:
+                    continue
+                rows.append(parts[1:])
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
@@ -162,6 +182,28 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(x for x in smax if math.isfinite(x)) if smax else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+def decode_traffic():
+    """DRAM bytes (read + write) of one long-context decode call from the committed ncu
+    summary, or None when the decode sources changed since that capture."""
+    import hashlib
+    try:
+        h = hashlib.sha256()
+        for f in DECODE_SOURCES:
+            with open(f, "rb") as fh:
+                h.update(fh.read())
+        fields = {}
+        with open(DECODE_PROFILE) as fh:
+            for line in fh:
+                if ":" in line and line.startswith(("traffic_bytes_per_call", "sources_sha256")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("sources_sha256") == h.hexdigest():
+            return int(fields["traffic_bytes_per_call"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
 
 
 # ---------------------------------------------------------------------------- the path
@@ -494,7 +536,14 @@ def main():
           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
+        # keep the GPU loaded for about a second of sampling before the timed region, so the
+        # nvidia-smi samples (every 200 ms) see the clocks under this load
+        clk.mark_load()
+        t_end = time.time() + args.clock_window
+        while time.time() < t_end:
+            for _ in range(8):
+                path.step()
+            torch.cuda.synchronize()
         start.record()
         for i in range(args.steps):
             path.step(ev[i])
@@ -507,6 +556,7 @@ def main():
     step_bytes = path.step_bytes
     value = step_bytes * world / (ms_step * 1e-3) / GB
     clocks = clk.summary()
+    clocks["window"] = f"{args.clock_window:g} s of untimed steps, then the timed steps"
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -522,7 +572,7 @@ def main():
                      "achieved": round(path.bytes_decode / (dec_ms * 1e-3) / GB, 1),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(path.bytes_decode / (dec_ms * 1e-3) / GB / peak, 4),
-                     "traffic": None, "peak_kind": peak_kind,
+                     "traffic": decode_traffic(), "peak_kind": peak_kind,
                      "launch_ms": round(dec_ms, 4), "algorithmic_bytes": int(path.bytes_decode)},
         "clocks": clocks,
         "gpu_launches": path.launches_per_step * args.steps,

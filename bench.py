@@ -273,7 +273,7 @@ class Path:
                              + wl.B * wl.Hq * wl.D * 2 * 2                   # q in, out
                              + pt.numel() * 4 + wl.B * 4 + wl.B * wl.Hq * 4)  # table, lens, lse
         self.decode_tokens = wl.B
-        self.launches_per_step = 2 * 2 + 2 + 2 + 2 + 2   # amax(2 kernels) x2, q x2, dq x4, dec 2
+        self.launches_per_step = 2 * 2 + 2 + 4 + 1   # amax (2 kernels) x2, quantize x2, dequantize x4, decode 1
         torch.cuda.synchronize()
 
     # individual launches --------------------------------------------------------------
@@ -366,7 +366,7 @@ def kernel_table(path, peak):
     add("dequantize_V_fp8 token pairs (page round-trip)", lambda: path.dequantize_fp8(1),
         n * 1.5625, 1)
     wl = path.wl
-    add("decode (long context)", path.decode, path.bytes_decode, 2,
+    add("decode (long context)", path.decode, path.bytes_decode, 1,
         {"kv_tokens": wl.kv_tokens})
     res["decode (long context)"]["kv_tokens_per_s"] = round(
         wl.kv_tokens / (res["decode (long context)"]["ms"] * 1e-3), 1)
@@ -394,7 +394,7 @@ def kernel_table(path, peak):
     add("decode (decode batch 32x8192, GQA 4)",
         lambda: kv.nvfp4_paged_decode_attention(lay, q, kd, ks, gk, vd, vs, gv, pt, sl,
                                                 db.sm_scale, out, workspace=ws),
-        nbytes, 2)
+        nbytes, 1)
     r = res["decode (decode batch 32x8192, GQA 4)"]
     r["decode_tokens_per_s"] = round(db.B / (r["ms"] * 1e-3), 1)
     r["kv_tokens_per_s"] = round(db.kv_tokens / (r["ms"] * 1e-3), 1)
@@ -568,7 +568,7 @@ def main():
                    "frac_of_peak": round(value / world / peak, 4),
                    "peak_GB_s": peak, "peak_kind": peak_kind,
                    "long_context_seq_lens": path.wl.seq_lens},
-        "roofline": {"bound": "hbm", "kernel": "nvfp4_paged_decode_attention (split + combine)",
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (nvfp4_paged_decode_attention, one launch)",
                      "achieved": round(path.bytes_decode / (dec_ms * 1e-3) / GB, 1),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(path.bytes_decode / (dec_ms * 1e-3) / GB / peak, 4),

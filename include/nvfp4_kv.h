@@ -181,9 +181,10 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
  * A sequence of length 0 gives out = 0 and lse = -inf.
  *
  * Split-KV: the (sequence, KV head) pairs are cut into 64-token stages (32 at head_dim 256), the
- * stages of all pairs form one list, and the list is cut into equal runs, one per CTA of the
- * first kernel. Each (run, pair) piece leaves a partial (max, sum, unnormalised output) in the
- * workspace and a second kernel merges the partials of each (sequence, query head).
+ * stages of all pairs form one list, and the list is cut into equal runs, one per CTA. Each
+ * (run, pair) piece leaves a partial (max, sum, unnormalised output) in the workspace; the last
+ * CTA to finish a pair merges its partials and writes the outputs (one kernel launch). The
+ * workspace needs no initialisation: its counters carry a per-call tag.
  *   q              BF16 [batch][num_q_heads][D]
  *   k_data, k_scales   NVFP4 K pool in NVFP4KV_PACK_DIM_PAIRS (layout.packing is not read)
  *   v_data, v_scales   NVFP4 V pool in NVFP4KV_PACK_TOKEN_PAIRS

@@ -10,11 +10,12 @@
 // Design for GB300 (the SM120 kernel of the LMSYS page is prior art, not the blueprint):
 //  * Work is a flat list of stages: stage j of pair (sequence b, KV head h) covers tokens
 //    [TOK j, TOK j + TOK) of b (TOK = 64 tokens, 32 at head_dim 256), pairs in (b, h) order.
-//    One persistent wave of CTAs cuts the list into equal runs, so every SM streams the same
-//    number of bytes whatever the mix of sequence lengths (no tail of idle SMs). A run may
-//    cross pairs; each (CTA, pair) piece leaves one partial record, merged by the combine
-//    kernel. The record of CTA c for pair bh is record c + bh, so records never collide and
-//    their number is bounded by (CTAs + pairs) before any length is known.
+//    One persistent wave of CTAs cuts the list into equal runs, so every SM streams about the
+//    same number of bytes whatever the mix of sequence lengths. A run may cross pairs; each
+//    (CTA, pair) piece leaves one partial record c + bh, so records never collide and their
+//    number is bounded by (CTAs + pairs) before any length is known. The last CTA to finish a
+//    pair (counted with a per-pair counter that carries a per-call tag, so the workspace never
+//    needs clearing) merges the pair's records and writes the outputs: no second kernel.
 //  * A CTA has 4 warps; warp w takes stages w, w+4, ... of the piece. A stage is SUB MMA tiles
 //    of 16 tokens, streamed through a per-warp 2-slot shared-memory ring by asynchronous copies
 //    (cp.async, 16 bytes per lane, completion per warp by wait_group): the packed K rows,
@@ -31,10 +32,12 @@
 //    rescaling is rare. P^T moves to the B-operand layout with movmatrix.
 //  * O^T += V^^T P^T with head dims as M: V is stored token-pair packed, so every converted byte
 //    is one A-register (one head dim of two adjacent tokens) times the pair's two block scales.
-//  * at the end of a piece the 4 warps merge (max, sum, output) in shared memory and the CTA
-//    writes the record; the combine kernel merges the records of each (sequence, query head)
-//    by log-sum-exp and writes the BF16 output and the natural-log LSE.
+//  * at the end of a piece the 4 warps merge (max, sum, output) in shared memory; a piece that
+//    is a whole pair writes the BF16 output and the natural-log LSE directly, otherwise the CTA
+//    writes its record and the pair's last CTA merges the records by log-sum-exp.
 // Bytes per (token, KV head) at head_dim 128: 64 + 8 (K) + 64 + 8 (V) = 144.
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
@@ -51,7 +54,7 @@ constexpr int kSlots = 2;          // stages per warp ring
 constexpr int kMaxGroup = 8;
 constexpr int kMaxSplits = 64;     // bound of the caller-forced split count
 constexpr int kPageBuf = 256;      // page ids of a piece kept in shared memory
-constexpr int kMaxWeights = 1024;  // combine: merge weights cached in shared memory
+constexpr int kMaxRecW = 64;      // merge: weights of up to this many records kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -80,10 +83,11 @@ struct Geo {
     static constexpr int SUB_DIV = D / 64;      // data chunk i of a lane lies in sub-tile i / SUB_DIV
     static constexpr int SCH = SS / 16;         // 16-byte chunks of one scale pool
     static constexpr int SC_PER_LANE = 2 * SCH / 32;
-    static constexpr int BLOCKS_PER_SM = (D == 64) ? 6 : 3;
+    static constexpr int BLOCKS_PER_SM = (D == 64) ? 5 : 3;
     static_assert(DCH * 32 * 16 == SK && DCH == SUB * SUB_DIV, "copy split");
     static_assert(SC_PER_LANE * 32 == 2 * SCH, "scale copy split");
-    static_assert(kWarps * kMaxGroup * D * 4 <= SMEM, "merge buffer must fit in the rings");
+    static_assert((kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup + 2 * kMaxGroup) * 4 <= SMEM,
+                  "merge buffers must fit in the rings");
 };
 
 struct DecodeParams {
@@ -95,15 +99,46 @@ struct DecodeParams {
     const float* gk;
     const int32_t* page_table;
     const int32_t* seq_lens;
-    int32_t* hdr;       // [0] total stages, [1] stages per CTA (written by CTA 0)
-    int32_t* ps;        // [B + 1] first stage of each sequence's pairs (written by CTA 0)
+    const float* gv;
+    uint16_t* out;      // BF16 bits [B][Hq][D]
+    float* lse;         // [B][Hq] or null
+    unsigned long long* done;  // [B * H] tagged counts of finished pieces of each pair
     float* rec_o;       // [records][G][D] unnormalised output
     float* rec_ml;      // [records][G][2] running max (log2 domain), sum of exp2(x - max)
     int32_t* status;
     uint64_t t_magic;   // ceil(2^64 / T)
+    uint32_t nonce;     // tag of this call
     int32_t B, Hq, H, G, T, pool_pages, max_pages, min_w;
     float sm_scale;
 };
+
+// Tagged counter (tag in the high 32 bits, count in the low 32): add inc and return the count
+// before the add, treating a word whose tag is not this call's as a count of 0. `old` is the
+// value returned by a first atomicAdd. Tags grow from call to call, so a stale word is replaced
+// by one atomicMax (which never lowers an installed count); a word holding a larger tag
+// (garbage) falls back to a compare-and-swap loop. Only values returned by atomics are used:
+// a plain re-read could be served stale from L1.
+__device__ __forceinline__ uint32_t tagged_finish(unsigned long long* w, unsigned long long old,
+                                                  uint32_t nonce, uint32_t inc) {
+    if (static_cast<uint32_t>(old >> 32) == nonce) return static_cast<uint32_t>(old);
+    const unsigned long long base = static_cast<unsigned long long>(nonce) << 32;
+    atomicMax(w, base);
+    unsigned long long cur = atomicAdd(w, static_cast<unsigned long long>(inc));
+    if (static_cast<uint32_t>(cur >> 32) == nonce) return static_cast<uint32_t>(cur);
+    cur += inc;
+    for (int it = 0; it < 256; ++it) {
+        if (static_cast<uint32_t>(cur >> 32) == nonce) {
+            const unsigned long long o2 = atomicAdd(w, static_cast<unsigned long long>(inc));
+            if (static_cast<uint32_t>(o2 >> 32) == nonce) return static_cast<uint32_t>(o2);
+            cur = o2 + inc;
+            continue;
+        }
+        const unsigned long long seen = atomicCAS(w, cur, base | inc);
+        if (seen == cur) return 0;
+        cur = seen;
+    }
+    return 0xFFFFFFFFu;  // could not install the tag: report the pair as not finished
+}
 
 __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
@@ -199,6 +234,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
     __shared__ int page_ids[kPageBuf];
     __shared__ int scan_warp[kWarps];
     __shared__ int start_bp[2];  // pair walk start: sequence, its first stage
+    __shared__ int last_s;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -233,22 +269,21 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         if (w < warp) excl += scan_warp[w];
         total += scan_warp[w];
     }
+    // CTA c takes the run [c W, c W + W) of the stage list
     const int n_ctas = gridDim.x;
     const int W = max(p.min_w, max(1, (total + n_ctas - 1) / n_ctas));
-    const int s_begin = blockIdx.x * W;
-    const int s_end = min(total, s_begin + W);
     if (blockIdx.x == 0) {
-        int acc = excl;
+        // sequences without stages (length 0 or invalid): output 0, LSE -inf
         for (int b = b_lo; b < b_hi; ++b) {
-            p.ps[b] = acc;
-            acc += H * seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
-        }
-        if (tid == kDecThreads - 1) p.ps[p.B] = total;
-        if (tid == 0) {
-            p.hdr[0] = total;
-            p.hdr[1] = W;
+            if (seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK) != 0) continue;
+            uint16_t* ob = p.out + static_cast<int64_t>(b) * p.Hq * D;
+            for (int i = 0; i < p.Hq * D; ++i) ob[i] = 0;
+            if (p.lse)
+                for (int i = 0; i < p.Hq; ++i) p.lse[static_cast<int64_t>(b) * p.Hq + i] = -INFINITY;
         }
     }
+    const int s_begin = blockIdx.x * W;
+    const int s_end = min(total, s_begin + W);
     if (s_begin >= s_end) return;
     if (s_begin >= excl && s_begin < excl + local) {
         int acc = excl;
@@ -281,6 +316,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
     int S_b = seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
     int h = (s_begin - start_bp[1]) / S_b;
     int j = (s_begin - start_bp[1]) - h * S_b;
+    int pair_start = start_bp[1] + h * S_b;  // flat index of stage 0 of pair (b, h)
     int s = s_begin;
     bool first_piece = true;
     while (s < s_end) {
@@ -653,7 +689,11 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         }
         const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M0);
         const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M1);
-        float* so = reinterpret_cast<float*>(smem);  // [kWarps][kMaxGroup][D], over the rings
+        // over the drained rings: the warps' partial outputs [kWarps][kMaxGroup][D], then the
+        // merge weights of a pair's records [kMaxRecW][kMaxGroup] and merged (max, sum) per head
+        float* so = reinterpret_cast<float*>(smem);
+        float (*mw_s)[kMaxGroup] = reinterpret_cast<float (*)[kMaxGroup]>(so + kWarps * kMaxGroup * D);
+        float (*ml_s)[2] = reinterpret_cast<float (*)[2]>(so + kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup);
 #pragma unroll
         for (int m = 0; m < G_::KSTEPS; ++m) {
             const int d0 = rho * (D / 8) + 2 * m;
@@ -664,32 +704,160 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
             base[D + d0 + 1] = o[m][3] * f1;
         }
         __syncthreads();
-        const int64_t rec = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(b) * H + h;
-        float* ro = p.rec_o + rec * G * D;
-        for (int i = tid; i < G * D; i += kDecThreads) {
-            const int col = i / D, d = i - (i / D) * D;
-            float acc = 0.0f;
+        // CTAs c_first .. c_last cover the pair, each leaving record c + (b H + h); the last of
+        // them to finish merges the records
+        const int c_first = pair_start / W, c_last = (pair_start + S_b - 1) / W;
+        const int n_rec = c_last - c_first + 1;
+        const int64_t bh64 = static_cast<int64_t>(b) * H + h;
+        auto rec_index = [&](int k) -> int64_t { return c_first + k + bh64; };
+        const float gvs = __ldg(p.gv);
+        if (n_rec == 1) {
+            // the whole pair is this piece: normalise and write the output directly
+            if (tid < G) {
+                float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
-            ro[i] = acc;
-        }
-        if (tid < G) {
-            float M = -INFINITY;
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
+                float lsum = 0.0f;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
-            float lsum = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = red_m[w][tid];
-                if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
+                for (int w = 0; w < kWarps; ++w) {
+                    const float mw = red_m[w][tid];
+                    if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
+                }
+                ml_s[tid][0] = M;
+                ml_s[tid][1] = lsum;
+                if (p.lse)
+                    p.lse[static_cast<int64_t>(b) * p.Hq + h * G + tid] =
+                        (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
             }
-            p.rec_ml[(rec * G + tid) * 2] = M;
-            p.rec_ml[(rec * G + tid) * 2 + 1] = lsum;
+            __syncthreads();
+            uint16_t* ob = p.out + (static_cast<int64_t>(b) * p.Hq + h * G) * D;
+            for (int i = tid; i < G * D; i += kDecThreads) {
+                const int col = i / D, d = i - (i / D) * D;
+                float acc = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
+                const float ls = ml_s[col][1];
+                const __nv_bfloat16 yb = __float2bfloat16_rn(ls > 0.0f ? acc * (gvs / ls) : 0.0f);
+                ob[i] = *reinterpret_cast<const uint16_t*>(&yb);
+            }
+        } else {
+            const int64_t rec = blockIdx.x + bh64;
+            float* ro = p.rec_o + rec * G * D;
+            for (int i = tid; i < G * D; i += kDecThreads) {
+                const int col = i / D, d = i - (i / D) * D;
+                float acc = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
+                ro[i] = acc;
+            }
+            if (tid < G) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
+                float lsum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float mw = red_m[w][tid];
+                    if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
+                }
+                p.rec_ml[(rec * G + tid) * 2] = M;
+                p.rec_ml[(rec * G + tid) * 2 + 1] = lsum;
+            }
+            __syncthreads();  // the record is written ...
+            if (tid == 0) {
+                __threadfence();  // ... and visible before the count says so
+                unsigned long long* cnt = p.done + bh64;
+                const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
+                last_s = (k == static_cast<uint32_t>(n_rec - 1)) ? 1 : 0;
+            }
+            __syncthreads();
+            if (last_s) {
+                // every record of the pair is written: merge them (L2 reads, not L1)
+                __threadfence();
+                if (warp < G) {  // warp w: query heads w, w + 4
+                    for (int col = warp; col < G; col += kWarps) {
+                        float M = -INFINITY;
+                        for (int k = lane; k < n_rec; k += 32)
+                            M = fmaxf(M, __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2));
+#pragma unroll
+                        for (int o2 = 16; o2 > 0; o2 >>= 1)
+                            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o2));
+                        float lsum = 0.0f;
+                        for (int k = lane; k < n_rec; k += 32) {
+                            const float mk = __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);
+                            const float wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
+                            if (k < kMaxRecW) mw_s[k][col] = wk;
+                            lsum += wk * __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2 + 1);
+                        }
+#pragma unroll
+                        for (int o2 = 16; o2 > 0; o2 >>= 1)
+                            lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o2);
+                        if (lane == 0) {
+                            ml_s[col][0] = M;
+                            ml_s[col][1] = lsum;
+                            if (p.lse)
+                                p.lse[static_cast<int64_t>(b) * p.Hq + h * G + col] =
+                                    (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f
+                                                  : -INFINITY;
+                        }
+                    }
+                }
+                __syncthreads();
+                // thread tid owns outputs i = tid + kDecThreads q; records are read kRecUnroll
+                // at a time so that their L2 latencies overlap
+                constexpr int NQ = kMaxGroup * D / kDecThreads;
+                constexpr int kRecUnroll = 4;
+                float acc[NQ];
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) acc[q] = 0.0f;
+                for (int k0 = 0; k0 < n_rec; k0 += kRecUnroll) {
+                    float v[kRecUnroll][NQ];
+#pragma unroll
+                    for (int u = 0; u < kRecUnroll; ++u) {
+                        const int k = min(k0 + u, n_rec - 1);
+                        const float* rk = p.rec_o + rec_index(k) * G * D;
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q) {
+                            const int i = tid + kDecThreads * q;
+                            v[u][q] = (i < G * D) ? __ldcg(rk + i) : 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kRecUnroll; ++u) {
+                        const int k = k0 + u;
+                        if (k >= n_rec) break;
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q) {
+                            const int i = tid + kDecThreads * q;
+                            if (i >= G * D) continue;
+                            const int col = i / D;
+                            float wk;
+                            if (k < kMaxRecW) {
+                                wk = mw_s[k][col];
+                            } else {
+                                const float mk = __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);
+                                wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - ml_s[col][0]);
+                            }
+                            acc[q] += wk * v[u][q];
+                        }
+                    }
+                }
+                uint16_t* ob = p.out + (static_cast<int64_t>(b) * p.Hq + h * G) * D;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const int i = tid + kDecThreads * q;
+                    if (i >= G * D) continue;
+                    const float ls = ml_s[i / D][1];
+                    const __nv_bfloat16 yb = __float2bfloat16_rn(ls > 0.0f ? acc[q] * (gvs / ls) : 0.0f);
+                    ob[i] = *reinterpret_cast<const uint16_t*>(&yb);
+                }
+            }
         }
 
         // ---- next piece: the next pair with at least one stage
         s += j1 - j0;
         j = 0;
+        pair_start += S_b;
         if (s < s_end) {
             if (++h == H) {
                 h = 0;
@@ -703,90 +871,12 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
 }
 
 // ------------------------------------------------------------------------------------------
-// Combine: for the records R of (sequence b, query head qh),
-//   out = g_V sum_R 2^(m_R - M) o_R / sum_R 2^(m_R - M) l_R;  lse = ln 2 (M + log2 L).
-// ------------------------------------------------------------------------------------------
-struct CombineParams {
-    const float* rec_o;
-    const float* rec_ml;
-    const int32_t* hdr;
-    const int32_t* ps;
-    const int32_t* seq_lens;
-    const float* gv;
-    uint16_t* out;  // BF16 bits [B][Hq][D]
-    float* lse;     // [B][Hq] or null
-    int32_t Hq, H, G, D, tok, max_tokens;
-};
-
-__global__ void __launch_bounds__(128) combine_kernel(const CombineParams p) {
-    const int qh = blockIdx.x, b = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = qh / p.G, g = qh - h * p.G;
-    const int L = __ldg(p.seq_lens + b);
-    const int S_b = seq_stages(L, p.max_tokens, p.tok);
-    uint16_t* out = p.out + (static_cast<int64_t>(b) * p.Hq + qh) * p.D;
-    if (S_b == 0) {
-        for (int d = tid; d < p.D; d += blockDim.x) out[d] = 0;
-        if (tid == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.Hq + qh] = -INFINITY;
-        return;
-    }
-    const int W = p.hdr[1];
-    const int start = p.ps[b] + h * S_b;
-    const int c0 = start / W, c1 = (start + S_b - 1) / W;
-    const int n = c1 - c0 + 1;
-    const int64_t base = static_cast<int64_t>(c0) + static_cast<int64_t>(b) * p.H + h;
-    const float* ml = p.rec_ml + (base * p.G + g) * 2;   // record k at ml + 2 k G
-    const float* ro = p.rec_o + (base * p.G + g) * p.D;  // record k at ro + k G D
-    __shared__ float w_s[kMaxWeights];
-    __shared__ float red[2][4];
-
-    float M = -INFINITY;
-    for (int k = tid; k < n; k += blockDim.x) M = fmaxf(M, ml[2 * k * p.G]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    if (lane == 0) red[0][warp] = M;
-    __syncthreads();
-    M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-    float lsum = 0.0f;
-    for (int k = tid; k < n; k += blockDim.x) {
-        const float mk = ml[2 * k * p.G];
-        const float w = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-        if (k < kMaxWeights) w_s[k] = w;
-        lsum += w * ml[2 * k * p.G + 1];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
-    if (lane == 0) red[1][warp] = lsum;
-    __syncthreads();
-    lsum = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-    const float inv_l = (lsum > 0.0f) ? __ldg(p.gv) / lsum : 0.0f;
-    if (tid == 0 && p.lse)
-        p.lse[static_cast<int64_t>(b) * p.Hq + qh] =
-            (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
-    for (int d = tid; d < p.D; d += blockDim.x) {
-        float acc = 0.0f;
-        for (int k = 0; k < n; ++k) {
-            float w;
-            if (k < kMaxWeights) {
-                w = w_s[k];
-            } else {
-                const float mk = ml[2 * k * p.G];
-                w = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-            }
-            if (w != 0.0f) acc += w * ro[static_cast<int64_t>(k) * p.G * p.D + d];
-        }
-        const __nv_bfloat16 yb = __float2bfloat16_rn(acc * inv_l);
-        out[d] = *reinterpret_cast<const uint16_t*>(&yb);
-    }
-}
-
-// ------------------------------------------------------------------------------------------
 // Host side: grid, workspace carving
 // ------------------------------------------------------------------------------------------
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int stage_tokens(int D) { return D == 256 ? 32 : 64; }
-int blocks_per_sm(int D) { return D == 64 ? 6 : 3; }
+int blocks_per_sm(int D) { return D == 64 ? 5 : 3; }
 
 // CTAs of the split kernel: one wave (automatic), or n runs per (sequence, KV head) pair.
 int64_t decode_ctas(int batch, int H, int D, int max_num_splits) {
@@ -795,16 +885,17 @@ int64_t decode_ctas(int batch, int H, int D, int max_num_splits) {
 }
 
 struct WsLayout {
-    size_t hdr, ps, ml, o, total;
+    size_t done, ml, o, total;
 };
 
+// Records: one per (CTA, pair) it covers; bounded by CTAs + pairs because runs are consecutive
 WsLayout ws_layout(int batch, int H, int Hq, int D, int64_t ctas) {
-    const size_t records = static_cast<size_t>(ctas) + static_cast<size_t>(batch) * H;
+    const size_t pairs = static_cast<size_t>(batch) * H;
+    const size_t records = static_cast<size_t>(ctas) + pairs;
     const size_t G = static_cast<size_t>(Hq / H);
     WsLayout w;
-    w.hdr = 0;
-    w.ps = 256;
-    w.ml = w.ps + align256((static_cast<size_t>(batch) + 1) * sizeof(int32_t));
+    w.done = 0;
+    w.ml = align256(pairs * sizeof(unsigned long long));
     w.o = w.ml + align256(records * G * 2 * sizeof(float));
     w.total = w.o + align256(records * G * D * sizeof(float));
     return w;
@@ -828,6 +919,16 @@ bool decode_size_ok(int batch, int H, int D, int max_pages, int T, int64_t ctas)
     const int64_t lim = (int64_t{1} << 31) - 1;
     return max_tokens < lim - tok && stages + ctas * kWarps < lim &&
            ctas + static_cast<int64_t>(batch) * H < lim;
+}
+
+// One tag per call (all devices): counters of earlier calls never carry it. Tags grow from call
+// to call, which lets a stale counter be replaced by one atomicMax.
+uint32_t next_nonce() {
+    static std::atomic<uint32_t> counter{static_cast<uint32_t>(
+        std::chrono::steady_clock::now().time_since_epoch().count() & 0x3FFFFFFF) + 1u};
+    uint32_t n = counter.fetch_add(1) + 1;
+    if (n == 0) n = counter.fetch_add(1) + 1;
+    return n;
 }
 
 template <int D>
@@ -896,8 +997,11 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
     p.gk = k_global_scale;
     p.page_table = page_table;
     p.seq_lens = seq_lens;
-    p.hdr = reinterpret_cast<int32_t*>(ws + wl.hdr);
-    p.ps = reinterpret_cast<int32_t*>(ws + wl.ps);
+    p.gv = v_global_scale;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.done = reinterpret_cast<unsigned long long*>(ws + wl.done);
+    p.nonce = next_nonce();
     p.rec_ml = reinterpret_cast<float*>(ws + wl.ml);
     p.rec_o = reinterpret_cast<float*>(ws + wl.o);
     p.status = status;
@@ -921,21 +1025,5 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
     }
     if (e != cudaSuccess) return NVFP4KV_ERR_CUDA;
 
-    CombineParams cp{};
-    cp.rec_o = p.rec_o;
-    cp.rec_ml = p.rec_ml;
-    cp.hdr = p.hdr;
-    cp.ps = p.ps;
-    cp.seq_lens = seq_lens;
-    cp.gv = v_global_scale;
-    cp.out = static_cast<uint16_t*>(out);
-    cp.lse = lse;
-    cp.Hq = num_q_heads;
-    cp.H = H;
-    cp.G = p.G;
-    cp.D = D;
-    cp.tok = stage_tokens(D);
-    cp.max_tokens = max_pages_per_seq * T;
-    combine_kernel<<<dim3(num_q_heads, batch), 128, 0, s>>>(cp);
-    return launch_status();
+    return NVFP4KV_OK;
 }

@@ -50,6 +50,14 @@ __device__ __forceinline__ uint4 ld_stream_16B(const void* p) {
     return r;
 }
 
+__device__ __forceinline__ uint2 ld_stream_8B(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];"
+                 : "=r"(r.x), "=r"(r.y)
+                 : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t ld_stream_4B(const void* p) {
     uint32_t r;
     asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r) : "l"(p));
@@ -253,7 +261,9 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
 // one IEEE fp32 multiply, and rounded to the output type to nearest even (FP8 saturating).
 // A unit is 8 codes: half a block of one token (dim pairs: 4 code bytes + the block's scale,
 // 8 outputs of one token) or 8 head dims of a token pair (token pairs: 8 code bytes + the
-// pair's 2 scales, 8 outputs for each of the two tokens).
+// pair's 2 scales, 8 outputs for each of the two tokens). FP8 outputs are half as wide, so
+// there a unit is twice as large (one whole block; 16 dims of a token pair) and every store
+// is still 16 bytes.
 // ------------------------------------------------------------------------------------------
 struct DequantParams {
     const uint8_t* src_data;
@@ -269,8 +279,9 @@ struct DequantParams {
     int32_t bpp;            // blocks per page
     int32_t nb;             // blocks per token row
     uint64_t nb2_magic;     // div_magic(2 * nb)
+    uint64_t nb_magic;      // div_magic(nb)
     int32_t units;          // units per page
-    int32_t items_per_page; // ceil(units / kItemBlocks)
+    int32_t items_per_page; // ceil(units / units per item)
     int32_t* status;
 };
 
@@ -296,6 +307,7 @@ __device__ __forceinline__ void store8(void* dst, int64_t elem, const float (&y)
 
 template <int DST, int PACK>
 __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const DequantParams p) {
+    constexpr int kU = kBlocksPerThread;  // units per thread per item
     const float g = __ldg(p.g);
     const float mult = (DST == NVFP4KV_FP8_E4M3)
                            ? (p.dst_scale ? __fdiv_rn(g, __ldg(p.dst_scale)) : g)
@@ -312,8 +324,73 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
         }
         const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
         const int64_t dst_elem0 = static_cast<int64_t>(dp) * p.bpp * 16;
-        const int32_t u_begin = k * kItemBlocks + threadIdx.x;
-        if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+        const int32_t u_begin = k * kThreads * kU + threadIdx.x;
+        if constexpr (DST == NVFP4KV_FP8_E4M3) {
+            // one 16-byte load of codes (dim pairs: 8 bytes) per unit, 16-byte FP8 stores
+            uint4 code[kU];
+            uint32_t sc[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit < p.units) {
+                    if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+                        const uint2 c2 = ld_stream_8B(p.src_data + (src_blk0 + unit) * 8);
+                        code[u] = make_uint4(c2.x, c2.y, 0u, 0u);
+                        sc[u] = ld_stream_1B(p.src_scales + src_blk0 + unit) * 0x0101u;
+                    } else {
+                        code[u] = ld_stream_16B(p.src_data + src_blk0 * 8 + static_cast<int64_t>(unit) * 16);
+                        sc[u] = *reinterpret_cast<const uint16_t*>(p.src_scales + src_blk0 +
+                                                                   static_cast<int64_t>(unit) * 2);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int32_t unit = u_begin + u * kThreads;
+                if (unit >= p.units) continue;
+                const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
+                if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+                    // 16 values of one token: (s, s) times each code pair
+                    uint32_t v[8];
+                    e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
+                    e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
+                    uint32_t o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t a = hmul2_u32(v[2 * j], s2), b = hmul2_u32(v[2 * j + 1], s2);
+                        o[j] = f32x2_to_e4m3x2(__fmul_rn(f16_lo(a), mult), __fmul_rn(f16_hi(a), mult)) |
+                               (f32x2_to_e4m3x2(__fmul_rn(f16_lo(b), mult), __fmul_rn(f16_hi(b), mult))
+                                << 16);
+                    }
+                    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + dst_elem0 +
+                                              static_cast<int64_t>(unit) * 16) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                } else {
+                    // 16 head dims of tokens 2rp (low nibbles) and 2rp+1 (high nibbles)
+                    const uint32_t rp = fast_div(unit, p.nb_magic);
+                    const int32_t blk = unit - static_cast<int32_t>(rp) * p.nb;
+                    const uint32_t words[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
+                    uint32_t o0[4], o1[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t v[4];
+                        e2m1x8_to_f16x2x4(words[q], v);  // v[j]: dim 4q + j of (token 2rp, 2rp+1)
+                        const uint32_t a0 = hmul2_u32(v[0], s2), a1 = hmul2_u32(v[1], s2);
+                        const uint32_t a2 = hmul2_u32(v[2], s2), a3 = hmul2_u32(v[3], s2);
+                        o0[q] = f32x2_to_e4m3x2(__fmul_rn(f16_lo(a0), mult), __fmul_rn(f16_lo(a1), mult)) |
+                                (f32x2_to_e4m3x2(__fmul_rn(f16_lo(a2), mult), __fmul_rn(f16_lo(a3), mult))
+                                 << 16);
+                        o1[q] = f32x2_to_e4m3x2(__fmul_rn(f16_hi(a0), mult), __fmul_rn(f16_hi(a1), mult)) |
+                                (f32x2_to_e4m3x2(__fmul_rn(f16_hi(a2), mult), __fmul_rn(f16_hi(a3), mult))
+                                 << 16);
+                    }
+                    const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * rp) * p.nb * 16 + blk * 16;
+                    uint8_t* d8 = static_cast<uint8_t*>(p.dst);
+                    *reinterpret_cast<uint4*>(d8 + e0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+                    *reinterpret_cast<uint4*>(d8 + e0 + p.nb * 16) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                }
+            }
+        } else if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
             uint32_t code[kBlocksPerThread], sbyte[kBlocksPerThread];
 #pragma unroll
             for (int u = 0; u < kBlocksPerThread; ++u) {
@@ -390,8 +467,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
 // fp32(e4m3 * src_scale) is fp32(max|e4m3| * |src_scale|) because rounding is monotone.
 // ------------------------------------------------------------------------------------------
 constexpr int kAmaxThreads = 256;
-constexpr int kAmaxMaxCtas = 1024;
-constexpr int kAmaxLoads = 4;   // 16-byte loads per thread per item
+constexpr int kAmaxMaxCtas = 2048;
+constexpr int kAmaxLoads = 8;   // 16-byte loads per thread per item (128 bytes in flight)
 
 struct AmaxParams {
     const void* src;
@@ -544,7 +621,7 @@ extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
     p.items_per_page = static_cast<int32_t>((p.page_bytes + p.item_bytes - 1) / p.item_bytes);
     p.partial = static_cast<uint32_t*>(workspace);
     p.status = status;
-    int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 4);
+    int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
     if (grid > kAmaxMaxCtas) grid = kAmaxMaxCtas;
     switch (src_dtype) {
     case NVFP4KV_BF16:
@@ -671,8 +748,13 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     p.bpp = static_cast<int32_t>(bpp64);
     p.nb = layout->head_dim / 16;
     p.nb2_magic = div_magic(static_cast<uint32_t>(2 * p.nb));
-    // 8 codes per dim-pair unit (2 per block); 16 codes per token-pair unit (2 per block pair)
-    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp : 2 * p.bpp;
+    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
+    // BF16 / FP16 out: 8 codes per dim-pair unit (2 per block), 16 codes per token-pair unit
+    // (2 per block pair); FP8 out: a whole block, 32 codes per token-pair unit
+    if (dst_dtype == NVFP4KV_FP8_E4M3)
+        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
+    else
+        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp : 2 * p.bpp;
     p.items_per_page = (p.units + kItemBlocks - 1) / kItemBlocks;
     p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -419,6 +419,11 @@ def kernel_table(path, peak):
     add("extend chunk encode (128 pages)",
         lambda: kv.nvfp4_kv_quantize_pages(lay, chunk, g, pd, ps, dst_page_ids=chunk_dst),
         chunk.shape[0] * per * 2.5625 + chunk.shape[0] * 4, 1)
+    # fused extend write: the chunk read once, NVFP4 pages + its FP8 workspace copy written
+    wsc = torch.empty((chunk.shape[0], ex.H, ex.T, ex.D), dtype=u8, device=dev)
+    add("extend chunk write NVFP4 + FP8 workspace (128 pages)",
+        lambda: kv.nvfp4_kv_extend_write(lay, chunk, g, pd, ps, wsc, dst_page_ids=chunk_dst),
+        chunk.shape[0] * per * 3.5625 + chunk.shape[0] * 4, 1)
     del flush
     return res
 

@@ -168,6 +168,30 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
                                          int32_t* status, nvfp4kv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * Extend-path write of the current chunk (LMSYS page, "Path 2: Chunked prefill / Extend": the
+ * chunk's K/V are copied into the FP8 workspace that attention reads, and the cache keeps them
+ * as NVFP4). One pass over the chunk's 16-bit pages writes both, reading the chunk once:
+ *   NVFP4 pages: exactly as nvfp4_kv_quantize_pages (same codes and scales, same packing)
+ *   FP8 pages:   y = E4M3_rne_satfinite(fp32(x * fp32(1 / ws_scale))), layout [page][H][T][D]
+ *   src_dtype      NVFP4KV_BF16 or NVFP4KV_FP16 (anything else: NVFP4KV_ERR_UNSUPPORTED)
+ *   src, src_pool_pages, src_page_ids, global_scale, dst_data, dst_scales, dst_pool_pages,
+ *   dst_page_ids   as in nvfp4_kv_quantize_pages
+ *   ws_fp8         FP8 E4M3 workspace pool [ws_pool_pages][H][T][D], 16-byte aligned
+ *   ws_page_ids    workspace page of each source page (NULL = 0 .. num_pages-1)
+ *   ws_scale       device scalar (NULL = 1)
+ * A page id outside its pool sets NVFP4KV_STATUS_PAGE_OOB and that page is skipped in all three
+ * pools. Source and outputs must not overlap.
+ * ------------------------------------------------------------------------------------------ */
+nvfp4kv_status nvfp4_kv_extend_write(const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype,
+                                     const void* src, int32_t src_pool_pages,
+                                     const int32_t* src_page_ids, const float* global_scale,
+                                     uint8_t* dst_data, uint8_t* dst_scales,
+                                     int32_t dst_pool_pages, const int32_t* dst_page_ids,
+                                     uint8_t* ws_fp8, int32_t ws_pool_pages,
+                                     const int32_t* ws_page_ids, const float* ws_scale,
+                                     int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Paged GQA decode attention reading NVFP4 K/V directly from the cache (LMSYS page, "Path 3:
  * Decode" and "NVFP4 KV Decode Attention Kernel Implementation", Figure 3: BF16 queries, packed
  * K/V tiles and their E4M3 block scales staged in shared memory, e2m1x2 conversion in

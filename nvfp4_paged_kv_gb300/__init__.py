@@ -23,7 +23,7 @@ __all__ = [
     "STATUS_PAGE_OOB", "STATUS_BAD_SEQ_LEN",
     "STATUS_TIMEOUT", "NVFP4KVError", "load", "lib_path", "version",
     "nvfp4_kv_global_scale_workspace_size", "nvfp4_kv_compute_global_scale",
-    "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages",
+    "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages", "nvfp4_kv_extend_write",
     "nvfp4_paged_decode_workspace_size", "nvfp4_paged_decode_attention", "nvfp4_kv_round_f32",
     "nvfp4_paged_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
@@ -85,6 +85,8 @@ def load():
             "nvfp4_kv_global_scale_workspace_size": (SZ, []),
             "nvfp4_kv_compute_global_scale": (I32, [LP, I32, P, I32, P, I32, P, P, P, SZ, P, P]),
             "nvfp4_kv_quantize_pages": (I32, [LP, I32, P, I32, P, P, P, P, P, I32, P, I32, P, P]),
+            "nvfp4_kv_extend_write": (I32, [LP, I32, P, I32, P, P, P, P, I32, P, P, I32, P, P,
+                                            I32, P, P]),
             "nvfp4_kv_dequantize_pages": (I32, [LP, P, P, I32, P, P, I32, P, I32, P, P, I32, P,
                                                 P]),
             "nvfp4_paged_decode_workspace_size": (SZ, [LP, I32, I32, I32, I32]),
@@ -191,6 +193,24 @@ def nvfp4_kv_quantize_pages(layout: Layout, src: torch.Tensor, global_scale: tor
         _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), int(num_pages), _ptr(status),
         _stream(stream))
     _check("nvfp4_kv_quantize_pages", code)
+
+
+def nvfp4_kv_extend_write(layout: Layout, src: torch.Tensor, global_scale: torch.Tensor,
+                          dst_data: torch.Tensor, dst_scales: torch.Tensor, ws_fp8: torch.Tensor,
+                          *, src_dtype=None, src_page_ids=None, dst_page_ids=None,
+                          ws_page_ids=None, ws_scale=None, num_pages=None, status=None,
+                          stream=None):
+    """One pass over the chunk's 16-bit pages `src`: NVFP4 pages into (dst_data, dst_scales)
+    and the FP8 E4M3 workspace copy into `ws_fp8` ([pool, H, T, D] uint8)."""
+    lib = load()
+    if num_pages is None:
+        num_pages = src_page_ids.numel() if src_page_ids is not None else src.shape[0]
+    code = lib.nvfp4_kv_extend_write(
+        ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
+        _ids(src_page_ids), _ptr(global_scale), _ptr(dst_data), _ptr(dst_scales),
+        dst_data.shape[0], _ids(dst_page_ids), _ptr(ws_fp8), ws_fp8.shape[0],
+        _ids(ws_page_ids), _ptr(ws_scale), int(num_pages), _ptr(status), _stream(stream))
+    _check("nvfp4_kv_extend_write", code)
 
 
 def nvfp4_kv_dequantize_pages(layout: Layout, src_data: torch.Tensor, src_scales: torch.Tensor,

@@ -100,7 +100,22 @@ struct QuantParams {
     int32_t units;          // work units per page (blocks, or block pairs for token pairs)
     int32_t items_per_page; // ceil(units / kItemUnits)
     int32_t* status;
+    // extend write only: the FP8 E4M3 workspace copy of the source pages
+    uint8_t* ws;
+    const int32_t* ws_ids;
+    const float* ws_scale;  // y = E4M3(fp32(x * fp32(1 / ws_scale))); NULL: 1
+    int32_t ws_pool;
 };
+
+// FP8 E4M3 bytes (round to nearest even, saturating) of fp32(x[k] * m), k = 0 .. 15
+__device__ __forceinline__ uint4 fp8_block(const float (&x)[16], float m) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        w[q] = f32x2_to_e4m3x2(__fmul_rn(x[4 * q], m), __fmul_rn(x[4 * q + 1], m)) |
+               (f32x2_to_e4m3x2(__fmul_rn(x[4 * q + 2], m), __fmul_rn(x[4 * q + 3], m)) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 // One block of 16 source values as loaded: 32 bytes (16-bit sources) or 16 bytes (FP8).
 template <int SRC, bool A32>
@@ -167,7 +182,8 @@ __device__ __forceinline__ void pick_scale(const float (&x)[16], float g, float 
 // (one 256-bit load per block). PACK: NVFP4KV_PACK_DIM_PAIRS (a unit is one block of one token)
 // or NVFP4KV_PACK_TOKEN_PAIRS (a unit is the same block of tokens 2p and 2p+1; the E2M1 pair
 // conversion of (token 2p, token 2p+1) at one head dim is directly the interleaved byte).
-template <int SRC, bool A32, int PACK>
+// WS: also write the FP8 workspace copy of every source block (the extend path's fused write).
+template <int SRC, bool A32, int PACK, bool WS = false>
 __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantParams p) {
     constexpr int kUnitsPerThread = (PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? kBlocksPerThread / 2
                                                                         : kBlocksPerThread;
@@ -175,18 +191,23 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
     const float g = __ldg(p.g);
     const float d = __fmul_rn(6.0f, g);
     const float sscale = (SRC == NVFP4KV_FP8_E4M3 && p.src_scale) ? __ldg(p.src_scale) : 1.0f;
+    const float wm = (WS && p.ws_scale) ? __frcp_rn(__ldg(p.ws_scale)) : 1.0f;
     const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
     for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int32_t i = static_cast<int32_t>(item / p.items_per_page);
         const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
         const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
         const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
-        if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool) {
+        int32_t wp = 0;
+        if constexpr (WS) wp = p.ws_ids ? __ldg(p.ws_ids + i) : i;
+        if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool ||
+            (WS && (wp < 0 || wp >= p.ws_pool))) {
             if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
             continue;
         }
         const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
         const int64_t dst_blk0 = static_cast<int64_t>(dp) * p.bpp;
+        uint8_t* const ws_page = WS ? p.ws + static_cast<int64_t>(wp) * p.bpp * 16 : nullptr;
         const int32_t u_begin = k * kItemUnits + threadIdx.x;
         if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
             U8x32 raw[kUnitsPerThread];
@@ -214,6 +235,8 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
                 }
                 *reinterpret_cast<uint2*>(p.dst_data + (dst_blk0 + blk) * 8) = make_uint2(w0, w1);
                 p.dst_scales[dst_blk0 + blk] = static_cast<uint8_t>(sb);
+                if constexpr (WS)
+                    *reinterpret_cast<uint4*>(ws_page + static_cast<int64_t>(blk) * 16) = fp8_block(x, wm);
             }
         } else {
             U8x32 raw0[kUnitsPerThread], raw1[kUnitsPerThread];
@@ -249,6 +272,14 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
                 *reinterpret_cast<uint4*>(p.dst_data + o * 16) = make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint16_t*>(p.dst_scales + o * 2) =
                     static_cast<uint16_t>(s0 | (s1 << 8));
+                if constexpr (WS) {
+                    // the same block of tokens 2p and 2p+1 in the plain [token][dim] workspace
+                    const uint32_t row_pair = fast_div(unit, p.nb_magic);
+                    const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
+                    const int64_t wb = static_cast<int64_t>(2 * row_pair) * p.nb + b;
+                    *reinterpret_cast<uint4*>(ws_page + wb * 16) = fp8_block(x0, wm);
+                    *reinterpret_cast<uint4*>(ws_page + (wb + p.nb) * 16) = fp8_block(x1, wm);
+                }
             }
         }
     }
@@ -709,6 +740,73 @@ extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
     }
 #undef NVFP4KV_QPACK
 #undef NVFP4KV_QLAUNCH
+    return launch_status();
+}
+
+extern "C" nvfp4kv_status nvfp4_kv_extend_write(
+    const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype, const void* src,
+    int32_t src_pool_pages, const int32_t* src_page_ids, const float* global_scale,
+    uint8_t* dst_data, uint8_t* dst_scales, int32_t dst_pool_pages, const int32_t* dst_page_ids,
+    uint8_t* ws_fp8, int32_t ws_pool_pages, const int32_t* ws_page_ids, const float* ws_scale,
+    int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream) {
+    if (!layout_ok(layout) || num_pages < 0 || src_pool_pages < 0 || dst_pool_pages < 0 ||
+        ws_pool_pages < 0)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (src_dtype != NVFP4KV_BF16 && src_dtype != NVFP4KV_FP16) return NVFP4KV_ERR_UNSUPPORTED;
+    if (num_pages == 0) return NVFP4KV_OK;
+    if (!src || !global_scale || !dst_data || !dst_scales || !ws_fp8 || !aligned16(src) ||
+        !aligned16(dst_data) || !aligned16(dst_scales) || !aligned16(ws_fp8))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if ((!src_page_ids && src_pool_pages < num_pages) ||
+        (!dst_page_ids && dst_pool_pages < num_pages) ||
+        (!ws_page_ids && ws_pool_pages < num_pages))
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int pack = layout->packing;
+    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
+    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
+                          (layout->head_dim / 16);
+    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
+    QuantParams p{};
+    p.src = src;
+    p.src_ids = src_page_ids;
+    p.g = global_scale;
+    p.dst_data = dst_data;
+    p.dst_scales = dst_scales;
+    p.dst_ids = dst_page_ids;
+    p.src_pool = src_pool_pages;
+    p.dst_pool = dst_pool_pages;
+    p.num_pages = num_pages;
+    p.bpp = static_cast<int32_t>(bpp64);
+    p.nb = layout->head_dim / 16;
+    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
+    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
+    const int item_units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? kItemBlocks / 2 : kItemBlocks;
+    p.items_per_page = (p.units + item_units - 1) / item_units;
+    p.status = status;
+    p.ws = ws_fp8;
+    p.ws_ids = ws_page_ids;
+    p.ws_scale = ws_scale;
+    p.ws_pool = ws_pool_pages;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
+    const bool a32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
+#define NVFP4KV_XLAUNCH(SRC, A32)                                                             \
+    do {                                                                                     \
+        if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                                                \
+            quantize_pages_kernel<SRC, A32, NVFP4KV_PACK_TOKEN_PAIRS, true><<<grid, kThreads, 0, s>>>(p); \
+        else                                                                                 \
+            quantize_pages_kernel<SRC, A32, NVFP4KV_PACK_DIM_PAIRS, true><<<grid, kThreads, 0, s>>>(p);   \
+    } while (0)
+    if (src_dtype == NVFP4KV_BF16) {
+        if (a32) NVFP4KV_XLAUNCH(NVFP4KV_BF16, true);
+        else NVFP4KV_XLAUNCH(NVFP4KV_BF16, false);
+    } else {
+        if (a32) NVFP4KV_XLAUNCH(NVFP4KV_FP16, true);
+        else NVFP4KV_XLAUNCH(NVFP4KV_FP16, false);
+    }
+#undef NVFP4KV_XLAUNCH
     return launch_status();
 }
 

@@ -66,6 +66,7 @@ def _load():
                 "orc_tensor_amax": (d, [i, i, i, i, p, p, i, d]),
                 "orc_global_scale_from_amax": (d, [d]),
                 "orc_quantize_pages": (None, [i, i, i, i, i, p, p, d, d, p, p, p, i]),
+                "orc_cast_fp8_pages": (None, [i, i, i, i, p, p, d, p, p, i]),
                 "orc_dequantize_pages": (None, [i, i, i, i, p, p, p, d, i, p, p, d, i]),
                 "orc_paged_decode_attention": (None, [i, i, i, i, i, i, i, p, p, p, d, p, p, d,
                                                       p, i, p, d, p, p, p]),
@@ -209,6 +210,22 @@ def quantize_pages(src, dtype, H, D, T, g, num_dst_pages=None, src_page_ids=None
                                float(src_scale), float(g), _ptr(data), _ptr(scales), _ptr(dids),
                                int(num_pages))
     return data, scales
+
+
+def cast_fp8_pages(src, dtype, H, D, T, ws_scale=1.0, num_dst_pages=None, src_page_ids=None,
+                   dst_page_ids=None, num_pages=None):
+    """FP8 E4M3 copy of 16-bit pages (the extend path's workspace copy of the current chunk):
+    E4M3(fp32(x * fp32(1 / ws_scale))) bytes shaped [num_dst_pages, H, T, D]."""
+    src = _src_dtype(src, dtype)
+    sids, dids = _ids(src_page_ids), _ids(dst_page_ids)
+    if num_pages is None:
+        num_pages = len(sids) if sids is not None else src.size // (H * T * D)
+    if num_dst_pages is None:
+        num_dst_pages = int(dids.max()) + 1 if dids is not None and len(dids) else num_pages
+    out = np.zeros((num_dst_pages, H, T, D), dtype=np.uint8)
+    _load().orc_cast_fp8_pages(H, D, T, dtype, _ptr(src), _ptr(sids), float(ws_scale),
+                               _ptr(out), _ptr(dids), int(num_pages))
+    return out
 
 
 def dequantize_pages(data, scales, H, D, T, g, out_dtype=BF16, num_dst_pages=None,

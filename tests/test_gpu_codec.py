@@ -228,6 +228,65 @@ def test_extend_workload(kv, cuda):
     assert np.array_equal(got_d[untouched], pool_d[untouched])
 
 
+# ------------------------------------------------------------------------------ extend write
+
+@pytest.mark.parametrize("kind", ["bf16", "fp16"])
+@pytest.mark.parametrize("pack", [oracle.DIM_PAIRS, oracle.TOKEN_PAIRS])
+@pytest.mark.parametrize("ws_scale", [1.0, 0.375])
+def test_extend_write_parity(kv, cuda, kind, pack, ws_scale):
+    """One pass over a chunk's 16-bit pages (scattered sources, destinations and workspace
+    slots, a ragged page count): the NVFP4 pages equal both the oracle and the plain quantize
+    call, the FP8 workspace copy equals the oracle's E4M3(fp32(x * fp32(1 / ws_scale)))."""
+    P, H, T, D = 37, 2, 32, 128
+    src = _make_src(kind, P, H, T, D, seed=40 + pack).to(cuda)
+    bits = _src_bits(src)
+    odt = _odt(src)
+    lay = kv.Layout(H, D, T).with_packing(pack)
+    g = oracle.global_scale(bits, odt, H, D, T)
+    gs = _scalar(g, cuda)
+    rng = np.random.default_rng(7)
+    n = 29
+    sid = rng.permutation(P)[:n].astype(np.int32)
+    did = rng.permutation(48)[:n].astype(np.int32)
+    wid = rng.permutation(33)[:n].astype(np.int32)
+    ds, ss = oracle.pool_shapes(48, H, T, D, pack)
+    data = torch.zeros(ds, dtype=torch.uint8, device=cuda)
+    scales = torch.zeros(ss, dtype=torch.uint8, device=cuda)
+    ws = torch.zeros((33, H, T, D), dtype=torch.uint8, device=cuda)
+    t = lambda a: torch.from_numpy(a).to(cuda)  # noqa: E731
+    kv.nvfp4_kv_extend_write(lay, src, gs, data, scales, ws, src_page_ids=t(sid),
+                             dst_page_ids=t(did), ws_page_ids=t(wid),
+                             ws_scale=_scalar(ws_scale, cuda))
+    want_d, want_s = oracle.quantize_pages(bits, odt, H, D, T, g, num_dst_pages=48,
+                                           src_page_ids=sid, dst_page_ids=did, packing=pack)
+    want_ws = oracle.cast_fp8_pages(bits, odt, H, D, T, ws_scale=ws_scale, num_dst_pages=33,
+                                    src_page_ids=sid, dst_page_ids=wid)
+    assert np.array_equal(data.cpu().numpy(), want_d)
+    assert np.array_equal(scales.cpu().numpy(), want_s)
+    assert np.array_equal(ws.cpu().numpy(), want_ws)
+    # the NVFP4 half is exactly the plain quantize call
+    d2, s2 = torch.zeros_like(data), torch.zeros_like(scales)
+    kv.nvfp4_kv_quantize_pages(lay, src, gs, d2, s2, src_page_ids=t(sid), dst_page_ids=t(did))
+    assert torch.equal(d2, data) and torch.equal(s2, scales)
+
+
+def test_extend_write_flags_out_of_range_workspace_pages(kv, cuda):
+    """A workspace page id outside its pool skips that page in all three pools."""
+    P, H, T, D = 4, 2, 16, 64
+    src = _make_src("bf16", P, H, T, D, seed=9).to(cuda)
+    lay = kv.Layout(H, D, T)
+    gs = _scalar(0.25, cuda)
+    data = torch.zeros((P, H, T, D // 2), dtype=torch.uint8, device=cuda)
+    scales = torch.zeros((P, H, T, D // 16), dtype=torch.uint8, device=cuda)
+    ws = torch.zeros((P, H, T, D), dtype=torch.uint8, device=cuda)
+    wid = torch.tensor([0, 7, 2, 3], dtype=torch.int32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kv.nvfp4_kv_extend_write(lay, src, gs, data, scales, ws, ws_page_ids=wid, status=status)
+    assert int(status.item()) & kv.STATUS_PAGE_OOB
+    assert int(data[1].abs().sum()) == 0 and int(ws[1].abs().sum()) == 0
+    assert int(data[0].ne(0).sum()) > 0 and int(ws[0].ne(0).sum()) > 0
+
+
 # ------------------------------------------------------------------------------ faults
 
 def test_out_of_range_page_ids_are_flagged_and_skipped(kv, cuda):

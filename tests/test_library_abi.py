@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages",
+    for want in ("nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages", "nvfp4_kv_extend_write",
                  "nvfp4_paged_decode_attention", "nvfp4_paged_decode_workspace_size",
                  "nvfp4_kv_compute_global_scale", "nvfp4_kv_global_scale_workspace_size",
                  "nvfp4_kv_round_f32", "nvfp4kv_status_string", "nvfp4kv_version"):
@@ -80,6 +80,17 @@ def test_host_validation_rejects_bad_arguments(lib):
     dq = lib.nvfp4_kv_dequantize_pages
     assert dq(ctypes.byref(good), fake, fake, 1, None, fake, 9, fake, 1, None, None, 1, None,
               None) == 1
+    xw = lib.nvfp4_kv_extend_write
+    # FP8 source: unsupported (the workspace copy of an FP8 chunk is the chunk itself)
+    assert xw(ctypes.byref(good), 2, fake, 1, None, fake, fake, fake, 1, None, fake, 1, None,
+              None, 1, None, None) == 2
+    # missing workspace; misaligned workspace; zero pages is a no-op
+    assert xw(ctypes.byref(good), 0, fake, 1, None, fake, fake, fake, 1, None, None, 1, None,
+              None, 1, None, None) == 1
+    assert xw(ctypes.byref(good), 0, fake, 1, None, fake, fake, fake, 1, None, mis, 1,
+              None, None, 1, None, None) == 1
+    assert xw(ctypes.byref(good), 0, None, 0, None, None, None, None, 0, None, None, 0, None,
+              None, 0, None, None) == 0
     att = lib.nvfp4_paged_decode_attention
     args = [ctypes.byref(good), 2, 32, fake, fake, fake, fake, fake, fake, fake, 10, fake, 4,
             fake, 0.1, 0, fake, 1 << 20, fake, None, None, None]

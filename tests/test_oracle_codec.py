@@ -425,3 +425,71 @@ def test_token_pair_positions():
             byte = data[p, h, t // 2, 16 * blk + j]
             code = (byte >> 4) if t % 2 else (byte & 15)
             assert code == (15 if j == k else 0)
+
+
+# ------------------------------------------------------------------------------------------
+# FP8 workspace copy of a 16-bit chunk (LMSYS, "Path 2: Chunked prefill / Extend": the current
+# chunk's K/V are copied into the FP8 workspace the extend attention reads).
+# ------------------------------------------------------------------------------------------
+def _e4m3_finite():
+    return [b for b in range(256) if (b & 0x7F) != 0x7F]
+
+
+def _bf16_page(values, H=1, T=16, D=16):
+    """BF16 bit patterns of `values` (each exactly representable) laid out as one page."""
+    flat = np.zeros(H * T * D, dtype=np.uint16)
+    flat[:len(values)] = [oracle.bf16_bits(v) for v in values]
+    return flat.reshape(1, H, T, D), (H, T, D)
+
+
+def test_fp8_copy_is_the_identity_on_e4m3_values():
+    """Every finite E4M3 value is exact in BF16; with ws_scale = 1 its copy is its own byte
+    (zero keeps its sign)."""
+    codes = _e4m3_finite()
+    vals = [oracle.e4m3_value(b) for b in codes]
+    src, (H, T, D) = _bf16_page(vals)
+    out = oracle.cast_fp8_pages(src, oracle.BF16, H, D, T).reshape(-1)
+    assert list(out[:len(codes)]) == codes
+
+
+def test_fp8_copy_scales_by_the_reciprocal_of_ws_scale():
+    """ws_scale = 1/2 doubles every value: in the normal range the copy of v is exactly 2 v."""
+    vals = [oracle.e4m3_value(b) for b in _e4m3_finite()]
+    vals = [v for v in vals if 2 ** -6 <= abs(v) <= 224]
+    src, (H, T, D) = _bf16_page(vals)
+    out = oracle.cast_fp8_pages(src, oracle.BF16, H, D, T, ws_scale=0.5).reshape(-1)
+    assert all(oracle.e4m3_value(int(o)) == 2 * v for o, v in zip(out, vals))
+
+
+def test_fp8_copy_saturates_and_ties_to_even():
+    """|x| beyond 448 saturates to +-448 (0x7E / 0xFE); an exact midpoint between two E4M3
+    neighbours goes to the one with the even mantissa."""
+    vals = [1000.0, -1000.0, 464.0, 1.0625, 1.1875, -1.0625, 0.0]
+    src, (H, T, D) = _bf16_page(vals)
+    out = oracle.cast_fp8_pages(src, oracle.BF16, H, D, T).reshape(-1)[:len(vals)]
+    got = [oracle.e4m3_value(int(o)) for o in out]
+    assert got == [448.0, -448.0, 448.0, 1.0, 1.25, -1.0, 0.0]
+
+
+def test_fp8_copy_is_the_nearest_e4m3_value():
+    """Random FP16 inputs: the copy decodes to the E4M3 value nearest to x (brute force over the
+    whole grid), ties to the even code, within the finite range."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(256) * rng.choice([1e-3, 0.1, 1.0, 30.0], 256)).astype(np.float16)
+    grid = sorted({oracle.e4m3_value(b): b for b in _e4m3_finite() if b < 0x80}.items())
+    src = x.view(np.uint16).reshape(1, 1, 16, 16)
+    out = oracle.cast_fp8_pages(src, oracle.FP16, 1, 16, 16).reshape(-1)
+    for xi, o in zip(x.astype(np.float64), out):
+        a = abs(xi)
+        best = min(grid, key=lambda e: (abs(e[0] - a), e[1] & 1))  # nearest, then even code
+        assert oracle.e4m3_value(int(o)) == (best[0] if xi >= 0 else -best[0])
+
+
+def test_fp8_copy_follows_page_ids():
+    """Source page 2 of a pool goes to workspace page 0 and source page 0 to page 1."""
+    rng = np.random.default_rng(6)
+    pool = rng.integers(0, 0x3C00, size=(3, 2, 4, 16), dtype=np.uint16)  # FP16 in [0, 1)
+    out = oracle.cast_fp8_pages(pool, oracle.FP16, 2, 16, 4, src_page_ids=[2, 0],
+                                dst_page_ids=[0, 1])
+    one = oracle.cast_fp8_pages(pool, oracle.FP16, 2, 16, 4)
+    assert np.array_equal(out[0], one[2]) and np.array_equal(out[1], one[0])

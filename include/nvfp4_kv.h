@@ -170,12 +170,14 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
 /* ------------------------------------------------------------------------------------------
  * Extend-path write of the current chunk (LMSYS page, "Path 2: Chunked prefill / Extend": the
  * chunk's K/V are copied into the FP8 workspace that attention reads, and the cache keeps them
- * as NVFP4). One pass over the chunk's 16-bit pages writes both, reading the chunk once:
+ * as NVFP4). One pass over the chunk's pages writes both, reading the chunk once:
  *   NVFP4 pages: exactly as nvfp4_kv_quantize_pages (same codes and scales, same packing)
  *   FP8 pages:   y = E4M3_rne_satfinite(fp32(x * fp32(1 / ws_scale))), layout [page][H][T][D]
- *   src_dtype      NVFP4KV_BF16 or NVFP4KV_FP16 (anything else: NVFP4KV_ERR_UNSUPPORTED)
- *   src, src_pool_pages, src_page_ids, global_scale, dst_data, dst_scales, dst_pool_pages,
- *   dst_page_ids   as in nvfp4_kv_quantize_pages
+ * with x the source value (BF16 / FP16 exactly; FP8 as x = fp32(e4m3 * src_scale), so an FP8
+ * chunk written with ws_scale == src_scale gets its own bytes back).
+ *   src_dtype      NVFP4KV_BF16, NVFP4KV_FP16 or NVFP4KV_FP8_E4M3 (else NVFP4KV_ERR_UNSUPPORTED)
+ *   src, src_pool_pages, src_page_ids, src_scale, global_scale, dst_data, dst_scales,
+ *   dst_pool_pages, dst_page_ids   as in nvfp4_kv_quantize_pages
  *   ws_fp8         FP8 E4M3 workspace pool [ws_pool_pages][H][T][D], 16-byte aligned
  *   ws_page_ids    workspace page of each source page (NULL = 0 .. num_pages-1)
  *   ws_scale       device scalar (NULL = 1)
@@ -184,7 +186,8 @@ nvfp4kv_status nvfp4_kv_dequantize_pages(const nvfp4kv_layout* layout, const uin
  * ------------------------------------------------------------------------------------------ */
 nvfp4kv_status nvfp4_kv_extend_write(const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype,
                                      const void* src, int32_t src_pool_pages,
-                                     const int32_t* src_page_ids, const float* global_scale,
+                                     const int32_t* src_page_ids, const float* src_scale,
+                                     const float* global_scale,
                                      uint8_t* dst_data, uint8_t* dst_scales,
                                      int32_t dst_pool_pages, const int32_t* dst_page_ids,
                                      uint8_t* ws_fp8, int32_t ws_pool_pages,
@@ -264,6 +267,73 @@ nvfp4kv_status nvfp4_paged_decode_attention_noalloc(
     int32_t pool_pages, const int32_t* page_table, int32_t max_pages_per_seq,
     const int32_t* seq_lens, float sm_scale, int32_t max_num_splits, void* out, float* lse,
     int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Cold-page codec ("KV Cache Compression in TensorRT LLM", NVIDIA: "NVFP4 Cold-Page
+ * Compression", "How It Works", Figure 6 and Figure 7). A hot page lives on the GPU in 16 bits
+ * per value; a cold page is one fixed-size block per page, holding the NVFP4 data and block
+ * scales of K and V and, optionally, lossless bytes copied unchanged. Offload quantizes a batch
+ * of hot pages and writes their cold blocks in the same pass; onboard reads cold blocks and
+ * writes the dequantized hot pages in the same pass. The cold pool may be pinned host memory
+ * (cudaHostAlloc / cudaHostRegister, addressed through unified virtual addressing; the kernels
+ * then read or write it over the host link directly, with no separate copy) or device memory.
+ *
+ * Cold block of one page, byte offsets from its base (every offset a multiple of 16):
+ *   k_data    K codes, dim-pair packing [H][T][D/2] (byte j = dims 2j low, 2j+1 high nibble)
+ *   k_scales  K block scales [H][T][D/16], E4M3
+ *   v_data    V codes, dim-pair packing [H][T][D/2]
+ *   v_scales  V block scales [H][T][D/16]
+ *   extra     extra_bytes copied unchanged (e.g. state that must not be quantized)
+ * each part starting at the previous part's end rounded up to 16; `bytes` is the end of the
+ * extra part rounded up to 16. When H*T*D/16 is a multiple of 16 there is no padding and
+ * bytes = 2 * (9/16) * H*T*D + extra_bytes. Slot s of the cold pool starts at cold + s * bytes.
+ * The layout's `packing` field is ignored here (cold blocks always use dim pairs).
+ * ------------------------------------------------------------------------------------------ */
+typedef struct nvfp4kv_cold_block_layout {
+    int64_t k_data, k_scales, v_data, v_scales, extra, bytes;
+} nvfp4kv_cold_block_layout;
+
+/* Fills *out for `layout` and extra_bytes (>= 0, a multiple of 16). Host only. */
+nvfp4kv_status nvfp4_kv_cold_block_layout(const nvfp4kv_layout* layout, int32_t extra_bytes,
+                                          nvfp4kv_cold_block_layout* out);
+
+/* Offload: hot page hot_page_ids[i] -> cold slot cold_slot_ids[i], for i < num_pages.
+ *   hot_dtype          NVFP4KV_BF16 or NVFP4KV_FP16 (else NVFP4KV_ERR_UNSUPPORTED)
+ *   hot_k, hot_v       hot pools, page p of K at hot_k + p * hot_page_stride elements, laid out
+ *                      [H][T][D] (K and V may be two pools, or one pool holding both:
+ *                      hot_v = hot_k + H*T*D and hot_page_stride = 2*H*T*D); 16-byte aligned
+ *   hot_page_stride    elements between consecutive pages, >= H*T*D, a multiple of 8
+ *   hot_pool_pages, hot_page_ids   pages in each hot pool; ids (NULL = 0 .. num_pages-1)
+ *   k_global_scale, v_global_scale device scalars g of K and V (NULL = 1); codes and scales
+ *                      are exactly those of nvfp4_kv_quantize_pages with the same g
+ *   extra, extra_page_stride, extra_bytes   lossless bytes of hot page p at
+ *                      extra + p * extra_page_stride (16-byte aligned; stride a multiple of 16);
+ *                      extra_bytes = 0 (extra may be NULL) copies none
+ *   cold, cold_slots, cold_slot_ids  cold pool of cold_slots blocks (16-byte aligned); slots
+ *                      (NULL = 0 .. num_pages-1)
+ * A page id or slot outside its pool sets NVFP4KV_STATUS_PAGE_OOB and that page is skipped. */
+nvfp4kv_status nvfp4_kv_offload_pages(
+    const nvfp4kv_layout* layout, nvfp4kv_dtype hot_dtype, const void* hot_k, const void* hot_v,
+    int64_t hot_page_stride, int32_t hot_pool_pages, const int32_t* hot_page_ids,
+    const float* k_global_scale, const float* v_global_scale, const uint8_t* extra,
+    int64_t extra_page_stride, int32_t extra_bytes, uint8_t* cold, int32_t cold_slots,
+    const int32_t* cold_slot_ids, int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream);
+
+/* Onboard: cold slot cold_slot_ids[i] -> hot page hot_page_ids[i], for i < num_pages. Values
+ * are exactly those of nvfp4_kv_dequantize_pages (BF16 / FP16 output) with the same g; the
+ * extra bytes are copied back unchanged. Arguments as in nvfp4_kv_offload_pages. */
+nvfp4kv_status nvfp4_kv_onboard_pages(
+    const nvfp4kv_layout* layout, const uint8_t* cold, int32_t cold_slots,
+    const int32_t* cold_slot_ids, const float* k_global_scale, const float* v_global_scale,
+    nvfp4kv_dtype hot_dtype, void* hot_k, void* hot_v, int64_t hot_page_stride,
+    int32_t hot_pool_pages, const int32_t* hot_page_ids, uint8_t* extra,
+    int64_t extra_page_stride, int32_t extra_bytes, int32_t num_pages, int32_t* status,
+    nvfp4kv_stream_t stream);
+
+/* Device address of pinned host memory (cudaHostGetDevicePointer): the address to pass as
+ * `cold` when the cold pool is pinned host memory. NVFP4KV_ERR_INVALID_ARG if host_ptr is not
+ * pinned memory known to CUDA. Host only; enqueues nothing. */
+nvfp4kv_status nvfp4_kv_host_device_pointer(void* host_ptr, void** device_ptr);
 
 /* ------------------------------------------------------------------------------------------
  * The two roundings of the encoder on their own, for exhaustive verification over fp32 inputs:

@@ -26,6 +26,8 @@ __all__ = [
     "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages", "nvfp4_kv_extend_write",
     "nvfp4_paged_decode_workspace_size", "nvfp4_paged_decode_attention", "nvfp4_kv_round_f32",
     "nvfp4_paged_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "ColdBlockLayout", "nvfp4_kv_cold_block_layout", "nvfp4_kv_offload_pages",
+    "nvfp4_kv_onboard_pages",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20   # NVFP4KV_NOALLOC_SCRATCH_BYTES
 
@@ -50,6 +52,16 @@ class Layout(ctypes.Structure):
     def __repr__(self):
         return (f"Layout(num_kv_heads={self.num_kv_heads}, head_dim={self.head_dim}, "
                 f"page_size={self.page_size}, packing={self.packing})")
+
+
+class ColdBlockLayout(ctypes.Structure):
+    """Byte offsets of the parts of one cold block and its size (``nvfp4kv_cold_block_layout``)."""
+    _fields_ = [(n, ctypes.c_int64) for n in
+                ("k_data", "k_scales", "v_data", "v_scales", "extra", "bytes")]
+
+    def __repr__(self):
+        return "ColdBlockLayout(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in
+                                              self._fields_) + ")"
 
 
 class NVFP4KVError(RuntimeError):
@@ -78,6 +90,7 @@ def load():
                 "(python -c 'import __graft_entry__ as g; g.build()')")
         lib = ctypes.CDLL(_build.LIB)
         P, I32, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        I64 = ctypes.c_int64
         LP = ctypes.POINTER(Layout)
         sigs = {
             "nvfp4kv_status_string": (ctypes.c_char_p, [I32]),
@@ -85,14 +98,20 @@ def load():
             "nvfp4_kv_global_scale_workspace_size": (SZ, []),
             "nvfp4_kv_compute_global_scale": (I32, [LP, I32, P, I32, P, I32, P, P, P, SZ, P, P]),
             "nvfp4_kv_quantize_pages": (I32, [LP, I32, P, I32, P, P, P, P, P, I32, P, I32, P, P]),
-            "nvfp4_kv_extend_write": (I32, [LP, I32, P, I32, P, P, P, P, I32, P, P, I32, P, P,
-                                            I32, P, P]),
+            "nvfp4_kv_extend_write": (I32, [LP, I32, P, I32, P, P, P, P, P, I32, P, P, I32, P,
+                                            P, I32, P, P]),
             "nvfp4_kv_dequantize_pages": (I32, [LP, P, P, I32, P, P, I32, P, I32, P, P, I32, P,
                                                 P]),
             "nvfp4_paged_decode_workspace_size": (SZ, [LP, I32, I32, I32, I32]),
             "nvfp4_paged_decode_attention": (I32, [LP, I32, I32, P, P, P, P, P, P, P, I32, P,
                                                    I32, P, F, I32, P, SZ, P, P, P, P]),
             "nvfp4_kv_round_f32": (I32, [P, SZ, I32, P, P]),
+            "nvfp4_kv_cold_block_layout": (I32, [LP, I32, ctypes.POINTER(ColdBlockLayout)]),
+            "nvfp4_kv_offload_pages": (I32, [LP, I32, P, P, I64, I32, P, P, P, P, I64, I32, P,
+                                             I32, P, I32, P, P]),
+            "nvfp4_kv_onboard_pages": (I32, [LP, P, I32, P, P, P, I32, P, P, I64, I32, P, P,
+                                             I64, I32, I32, P, P]),
+            "nvfp4_kv_host_device_pointer": (I32, [P, ctypes.POINTER(ctypes.c_void_p)]),
             "nvfp4_paged_decode_attention_noalloc": (I32, [LP, I32, I32, P, P, P, P, P, P, P,
                                                            I32, P, I32, P, F, I32, P, P, P, P]),
         }
@@ -197,18 +216,19 @@ def nvfp4_kv_quantize_pages(layout: Layout, src: torch.Tensor, global_scale: tor
 
 def nvfp4_kv_extend_write(layout: Layout, src: torch.Tensor, global_scale: torch.Tensor,
                           dst_data: torch.Tensor, dst_scales: torch.Tensor, ws_fp8: torch.Tensor,
-                          *, src_dtype=None, src_page_ids=None, dst_page_ids=None,
-                          ws_page_ids=None, ws_scale=None, num_pages=None, status=None,
-                          stream=None):
-    """One pass over the chunk's 16-bit pages `src`: NVFP4 pages into (dst_data, dst_scales)
-    and the FP8 E4M3 workspace copy into `ws_fp8` ([pool, H, T, D] uint8)."""
+                          *, src_dtype=None, src_page_ids=None, src_scale=None,
+                          dst_page_ids=None, ws_page_ids=None, ws_scale=None, num_pages=None,
+                          status=None, stream=None):
+    """One pass over the chunk's pages `src` (BF16 / FP16, or FP8 E4M3 bytes read as
+    e4m3 * src_scale): NVFP4 pages into (dst_data, dst_scales) and the FP8 E4M3 workspace copy
+    into `ws_fp8` ([pool, H, T, D] uint8)."""
     lib = load()
     if num_pages is None:
         num_pages = src_page_ids.numel() if src_page_ids is not None else src.shape[0]
     code = lib.nvfp4_kv_extend_write(
         ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
-        _ids(src_page_ids), _ptr(global_scale), _ptr(dst_data), _ptr(dst_scales),
-        dst_data.shape[0], _ids(dst_page_ids), _ptr(ws_fp8), ws_fp8.shape[0],
+        _ids(src_page_ids), _ptr(src_scale), _ptr(global_scale), _ptr(dst_data),
+        _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), _ptr(ws_fp8), ws_fp8.shape[0],
         _ids(ws_page_ids), _ptr(ws_scale), int(num_pages), _ptr(status), _stream(stream))
     _check("nvfp4_kv_extend_write", code)
 
@@ -288,3 +308,94 @@ def nvfp4_kv_round_f32(x: torch.Tensor, target: int, out: torch.Tensor, stream=N
     code = load().nvfp4_kv_round_f32(_ptr(x), x.numel(), int(target), _ptr(out),
                                      _stream(stream))
     _check("nvfp4_kv_round_f32", code)
+
+
+# ------------------------------------------------------------------------------ cold pages
+
+def nvfp4_kv_cold_block_layout(layout: Layout, extra_bytes: int = 0) -> ColdBlockLayout:
+    """Offsets and size of one cold block for `layout` with `extra_bytes` lossless bytes."""
+    out = ColdBlockLayout()
+    _check("nvfp4_kv_cold_block_layout",
+           load().nvfp4_kv_cold_block_layout(ctypes.byref(layout), int(extra_bytes),
+                                             ctypes.byref(out)))
+    return out
+
+
+def _paged_ptr(t: torch.Tensor):
+    """Pointer and page stride (elements) of a [pages, ...] CUDA tensor whose pages are each
+    contiguous (pages may be strided, e.g. the K or V half of one combined pool)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("hot pools must be CUDA tensors")
+    if not t[0].is_contiguous():
+        raise ValueError("each page of a hot pool must be contiguous")
+    return t.data_ptr(), t.stride(0)
+
+
+def _cold_ptr(t: torch.Tensor):
+    """Device address of a cold pool: a CUDA tensor, or pinned host memory (its device alias)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor, got {type(t)}")
+    if not t.is_contiguous():
+        raise ValueError("the cold pool must be contiguous")
+    if t.is_cuda:
+        return t.data_ptr()
+    if not t.is_pinned():
+        raise ValueError("a host cold pool must be pinned memory")
+    dev = ctypes.c_void_p()
+    _check("nvfp4_kv_host_device_pointer",
+           load().nvfp4_kv_host_device_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(dev)))
+    return dev.value
+
+
+def _extra_args(extra, extra_bytes):
+    if extra is None or extra_bytes == 0:
+        return None, 0, 0
+    if not extra.is_cuda or not extra[0].is_contiguous():
+        raise ValueError("extra must be a CUDA tensor [pages, bytes] with contiguous rows")
+    return extra.data_ptr(), extra.stride(0) * extra.element_size(), int(extra_bytes)
+
+
+def nvfp4_kv_offload_pages(layout: Layout, hot_k: torch.Tensor, hot_v: torch.Tensor,
+                           cold: torch.Tensor, *, k_global_scale=None, v_global_scale=None,
+                           hot_page_ids=None, cold_slot_ids=None, extra=None, extra_bytes=0,
+                           num_pages=None, hot_dtype=None, status=None, stream=None):
+    """Quantize hot pages (BF16 / FP16 [pages, H, T, D]) into cold blocks of `cold`
+    ([slots, block bytes] uint8, device or pinned host memory) in one pass."""
+    lib = load()
+    bl = nvfp4_kv_cold_block_layout(layout, extra_bytes)
+    kp, ks = _paged_ptr(hot_k)
+    vp, vs = _paged_ptr(hot_v)
+    if ks != vs:
+        raise ValueError("hot_k and hot_v must have the same page stride")
+    if num_pages is None:
+        num_pages = hot_page_ids.numel() if hot_page_ids is not None else hot_k.shape[0]
+    ep, es, eb = _extra_args(extra, extra_bytes)
+    code = lib.nvfp4_kv_offload_pages(
+        ctypes.byref(layout), _dtype_code(hot_k, hot_dtype), kp, vp, ks, hot_k.shape[0],
+        _ids(hot_page_ids), _ptr(k_global_scale), _ptr(v_global_scale), ep, es, eb,
+        _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids), int(num_pages),
+        _ptr(status), _stream(stream))
+    _check("nvfp4_kv_offload_pages", code)
+
+
+def nvfp4_kv_onboard_pages(layout: Layout, cold: torch.Tensor, hot_k: torch.Tensor,
+                           hot_v: torch.Tensor, *, k_global_scale=None, v_global_scale=None,
+                           cold_slot_ids=None, hot_page_ids=None, extra=None, extra_bytes=0,
+                           num_pages=None, hot_dtype=None, status=None, stream=None):
+    """Dequantize cold blocks of `cold` into hot pages (BF16 / FP16) in one pass."""
+    lib = load()
+    bl = nvfp4_kv_cold_block_layout(layout, extra_bytes)
+    kp, ks = _paged_ptr(hot_k)
+    vp, vs = _paged_ptr(hot_v)
+    if ks != vs:
+        raise ValueError("hot_k and hot_v must have the same page stride")
+    if num_pages is None:
+        num_pages = cold_slot_ids.numel() if cold_slot_ids is not None else cold.numel() // bl.bytes
+    ep, es, eb = _extra_args(extra, extra_bytes)
+    code = lib.nvfp4_kv_onboard_pages(
+        ctypes.byref(layout), _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids),
+        _ptr(k_global_scale), _ptr(v_global_scale), _dtype_code(hot_k, hot_dtype), kp, vp, ks,
+        hot_k.shape[0], _ids(hot_page_ids), ep, es, eb, int(num_pages), _ptr(status),
+        _stream(stream))
+    _check("nvfp4_kv_onboard_pages", code)
+

@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "codec_core.cuh"
 #include "common.cuh"
 #include "host_util.h"
 
@@ -25,63 +26,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBlocksPerThread = 4;                      // 16-value blocks per thread per item
 constexpr int kItemBlocks = kThreads * kBlocksPerThread; // blocks per work item
-
-// ------------------------------------------------------------------------------------------
-// Streaming loads / stores
-// ------------------------------------------------------------------------------------------
-struct U8x32 {
-    uint32_t w[8];
-};
-
-__device__ __forceinline__ U8x32 ld_stream_32B(const void* p) {
-    U8x32 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
-                   "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint4 ld_stream_16B(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint2 ld_stream_8B(const void* p) {
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];"
-                 : "=r"(r.x), "=r"(r.y)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ld_stream_4B(const void* p) {
-    uint32_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ld_stream_1B(const void* p) {
-    uint16_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
-}
-
-// ------------------------------------------------------------------------------------------
-// Encode one block of 16 exact fp32 values x:
-//   a  = max |x_i|                                          (exact)
-//   s  = E4M3_rne_satfinite(fp32(a / d)), d = fp32(6 g)      one IEEE division
-//   r  = fp32(1 / fp32(s g)), or 0 when s g == 0             one IEEE reciprocal
-//   c_i = E2M1_rne_satfinite(fp32(x_i * r)), sign kept
-// ------------------------------------------------------------------------------------------
-// n / d for n * d < 2^40 with a 64-bit multiply: magic = ceil(2^40 / d).
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint64_t magic) {
-    return static_cast<uint32_t>((static_cast<uint64_t>(n) * magic) >> 40);
-}
-inline uint64_t div_magic(uint32_t d) { return ((uint64_t{1} << 40) + d - 1) / d; }
 
 struct QuantParams {
     const void* src;
@@ -115,67 +59,6 @@ __device__ __forceinline__ uint4 fp8_block(const float (&x)[16], float m) {
         w[q] = f32x2_to_e4m3x2(__fmul_rn(x[4 * q], m), __fmul_rn(x[4 * q + 1], m)) |
                (f32x2_to_e4m3x2(__fmul_rn(x[4 * q + 2], m), __fmul_rn(x[4 * q + 3], m)) << 16);
     return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// One block of 16 source values as loaded: 32 bytes (16-bit sources) or 16 bytes (FP8).
-template <int SRC, bool A32>
-__device__ __forceinline__ U8x32 load_raw(const void* src, int64_t blk) {
-    U8x32 raw;
-    if constexpr (SRC == NVFP4KV_FP8_E4M3) {
-        const uint4 v = ld_stream_16B(static_cast<const uint8_t*>(src) + blk * 16);
-        raw.w[0] = v.x;
-        raw.w[1] = v.y;
-        raw.w[2] = v.z;
-        raw.w[3] = v.w;
-    } else {
-        const uint8_t* a = static_cast<const uint8_t*>(src) + blk * 32;
-        if constexpr (A32) {
-            raw = ld_stream_32B(a);
-        } else {
-            const uint4 lo = ld_stream_16B(a), hi = ld_stream_16B(a + 16);
-            raw = U8x32{{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w}};
-        }
-    }
-    return raw;
-}
-
-// The 16 values as exact fp32 (BF16 / FP16 widening is exact; FP8 sources are
-// x = fp32(e4m3 * src_scale)).
-template <int SRC>
-__device__ __forceinline__ void widen(const U8x32& raw, float sscale, float (&x)[16]) {
-    if constexpr (SRC == NVFP4KV_FP8_E4M3) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t h[2];
-            e4m3x4_to_f16x2x2(raw.w[j], h);
-            x[4 * j + 0] = __fmul_rn(f16_lo(h[0]), sscale);
-            x[4 * j + 1] = __fmul_rn(f16_hi(h[0]), sscale);
-            x[4 * j + 2] = __fmul_rn(f16_lo(h[1]), sscale);
-            x[4 * j + 3] = __fmul_rn(f16_hi(h[1]), sscale);
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if constexpr (SRC == NVFP4KV_BF16) {
-                x[2 * j] = bf16_lo(raw.w[j]);
-                x[2 * j + 1] = bf16_hi(raw.w[j]);
-            } else {
-                x[2 * j] = f16_lo(raw.w[j]);
-                x[2 * j + 1] = f16_hi(raw.w[j]);
-            }
-        }
-    }
-}
-
-// Block scale pick of one block: s, and r = fp32(1 / fp32(s g)) (0 when s g == 0).
-__device__ __forceinline__ void pick_scale(const float (&x)[16], float g, float d,
-                                           uint32_t& sbyte, float& r) {
-    float a = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(x[k]));
-    sbyte = f32x2_to_e4m3x2(__fdiv_rn(a, d), 0.0f) & 0xFFu;
-    const float sg = __fmul_rn(e4m3_to_f32(sbyte), g);
-    r = (sg == 0.0f) ? 0.0f : __frcp_rn(sg);
 }
 
 // SRC: NVFP4KV_BF16, NVFP4KV_FP16 or NVFP4KV_FP8_E4M3. A32: a 16-bit source is 32-byte aligned
@@ -745,14 +628,15 @@ extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
 
 extern "C" nvfp4kv_status nvfp4_kv_extend_write(
     const nvfp4kv_layout* layout, nvfp4kv_dtype src_dtype, const void* src,
-    int32_t src_pool_pages, const int32_t* src_page_ids, const float* global_scale,
-    uint8_t* dst_data, uint8_t* dst_scales, int32_t dst_pool_pages, const int32_t* dst_page_ids,
-    uint8_t* ws_fp8, int32_t ws_pool_pages, const int32_t* ws_page_ids, const float* ws_scale,
+    int32_t src_pool_pages, const int32_t* src_page_ids, const float* src_scale,
+    const float* global_scale, uint8_t* dst_data, uint8_t* dst_scales, int32_t dst_pool_pages,
+    const int32_t* dst_page_ids, uint8_t* ws_fp8, int32_t ws_pool_pages, const int32_t* ws_page_ids, const float* ws_scale,
     int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream) {
     if (!layout_ok(layout) || num_pages < 0 || src_pool_pages < 0 || dst_pool_pages < 0 ||
         ws_pool_pages < 0)
         return NVFP4KV_ERR_INVALID_ARG;
-    if (src_dtype != NVFP4KV_BF16 && src_dtype != NVFP4KV_FP16) return NVFP4KV_ERR_UNSUPPORTED;
+    if (src_dtype != NVFP4KV_BF16 && src_dtype != NVFP4KV_FP16 && src_dtype != NVFP4KV_FP8_E4M3)
+        return NVFP4KV_ERR_UNSUPPORTED;
     if (num_pages == 0) return NVFP4KV_OK;
     if (!src || !global_scale || !dst_data || !dst_scales || !ws_fp8 || !aligned16(src) ||
         !aligned16(dst_data) || !aligned16(dst_scales) || !aligned16(ws_fp8))
@@ -771,6 +655,7 @@ extern "C" nvfp4kv_status nvfp4_kv_extend_write(
     QuantParams p{};
     p.src = src;
     p.src_ids = src_page_ids;
+    p.src_scale = src_scale;
     p.g = global_scale;
     p.dst_data = dst_data;
     p.dst_scales = dst_scales;
@@ -802,9 +687,11 @@ extern "C" nvfp4kv_status nvfp4_kv_extend_write(
     if (src_dtype == NVFP4KV_BF16) {
         if (a32) NVFP4KV_XLAUNCH(NVFP4KV_BF16, true);
         else NVFP4KV_XLAUNCH(NVFP4KV_BF16, false);
-    } else {
+    } else if (src_dtype == NVFP4KV_FP16) {
         if (a32) NVFP4KV_XLAUNCH(NVFP4KV_FP16, true);
         else NVFP4KV_XLAUNCH(NVFP4KV_FP16, false);
+    } else {
+        NVFP4KV_XLAUNCH(NVFP4KV_FP8_E4M3, false);
     }
 #undef NVFP4KV_XLAUNCH
     return launch_status();

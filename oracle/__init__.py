@@ -66,7 +66,7 @@ def _load():
                 "orc_tensor_amax": (d, [i, i, i, i, p, p, i, d]),
                 "orc_global_scale_from_amax": (d, [d]),
                 "orc_quantize_pages": (None, [i, i, i, i, i, p, p, d, d, p, p, p, i]),
-                "orc_cast_fp8_pages": (None, [i, i, i, i, p, p, d, p, p, i]),
+                "orc_cast_fp8_pages": (None, [i, i, i, i, p, p, d, d, p, p, i]),
                 "orc_dequantize_pages": (None, [i, i, i, i, p, p, p, d, i, p, p, d, i]),
                 "orc_paged_decode_attention": (None, [i, i, i, i, i, i, i, p, p, p, d, p, p, d,
                                                       p, i, p, d, p, p, p]),
@@ -213,9 +213,10 @@ def quantize_pages(src, dtype, H, D, T, g, num_dst_pages=None, src_page_ids=None
 
 
 def cast_fp8_pages(src, dtype, H, D, T, ws_scale=1.0, num_dst_pages=None, src_page_ids=None,
-                   dst_page_ids=None, num_pages=None):
-    """FP8 E4M3 copy of 16-bit pages (the extend path's workspace copy of the current chunk):
-    E4M3(fp32(x * fp32(1 / ws_scale))) bytes shaped [num_dst_pages, H, T, D]."""
+                   dst_page_ids=None, num_pages=None, src_scale=1.0):
+    """FP8 E4M3 copy of source pages (the extend path's workspace copy of the current chunk):
+    E4M3(fp32(x * fp32(1 / ws_scale))) bytes shaped [num_dst_pages, H, T, D]; an FP8 source
+    is read as x = fp32(e4m3 * src_scale)."""
     src = _src_dtype(src, dtype)
     sids, dids = _ids(src_page_ids), _ids(dst_page_ids)
     if num_pages is None:
@@ -223,8 +224,8 @@ def cast_fp8_pages(src, dtype, H, D, T, ws_scale=1.0, num_dst_pages=None, src_pa
     if num_dst_pages is None:
         num_dst_pages = int(dids.max()) + 1 if dids is not None and len(dids) else num_pages
     out = np.zeros((num_dst_pages, H, T, D), dtype=np.uint8)
-    _load().orc_cast_fp8_pages(H, D, T, dtype, _ptr(src), _ptr(sids), float(ws_scale),
-                               _ptr(out), _ptr(dids), int(num_pages))
+    _load().orc_cast_fp8_pages(H, D, T, dtype, _ptr(src), _ptr(sids), float(src_scale),
+                               float(ws_scale), _ptr(out), _ptr(dids), int(num_pages))
     return out
 
 
@@ -286,3 +287,82 @@ def paged_decode_attention_bf16(q_bf16, k_bf16, v_bf16, page_table, seq_lens, sm
     _load().orc_paged_decode_attention_bf16(B, Hq, H, D, T, _ptr(q), _ptr(k), _ptr(v), _ptr(pt),
                                             pt.shape[1], _ptr(sl), float(sm_scale), _ptr(out))
     return out
+
+
+# ------------------------------------------------------------------------------ cold pages
+# "KV Cache Compression in TensorRT LLM" (NVIDIA), "NVFP4 Cold-Page Compression": a cold page
+# is one fixed-size block per page holding the NVFP4 data, the block scales and the lossless
+# bytes (Figure 6); encode happens on the way out, decode on the way back (Figure 7). The block
+# order taken here: K codes (dim pairs), K scales, V codes, V scales, extra bytes, each part
+# starting at the previous part's end rounded up to 16 bytes.
+
+def cold_block_layout(H, D, T, extra_bytes=0):
+    """Byte offsets of the parts of one cold block and its size."""
+    def up16(x):
+        return (x + 15) // 16 * 16
+    n = H * T * D
+    off = {"k_data": 0}
+    off["k_scales"] = up16(n // 2)
+    off["v_data"] = off["k_scales"] + up16(n // 16)
+    off["v_scales"] = off["v_data"] + up16(n // 2)
+    off["extra"] = off["v_scales"] + up16(n // 16)
+    off["bytes"] = off["extra"] + int(extra_bytes)
+    return off
+
+
+def cold_offload(k, v, dtype, H, D, T, g_k, g_v, num_slots, hot_page_ids=None,
+                 cold_slot_ids=None, extra=None, extra_bytes=0, num_pages=None):
+    """Cold blocks [num_slots, bytes] (uint8, zero where nothing is written) of hot pages
+    hot_page_ids[i] -> slots cold_slot_ids[i]: the K and V pages encoded exactly as
+    quantize_pages (dim pairs) with g_k / g_v, placed by cold_block_layout, and
+    extra[hot page, :extra_bytes] copied unchanged."""
+    lay = cold_block_layout(H, D, T, extra_bytes)
+    hids = _ids(hot_page_ids)
+    sids = _ids(cold_slot_ids)
+    if num_pages is None:
+        num_pages = len(hids) if hids is not None else k.size // (H * T * D)
+    kd, ks = quantize_pages(k, dtype, H, D, T, g_k, src_page_ids=hids, num_pages=num_pages)
+    vd, vs = quantize_pages(v, dtype, H, D, T, g_v, src_page_ids=hids, num_pages=num_pages)
+    n = H * T * D
+    blocks = np.zeros((num_slots, lay["bytes"]), dtype=np.uint8)
+    for i in range(num_pages):
+        s = int(sids[i]) if sids is not None else i
+        hp = int(hids[i]) if hids is not None else i
+        b = blocks[s]
+        b[lay["k_data"]:lay["k_data"] + n // 2] = kd[i].reshape(-1)
+        b[lay["k_scales"]:lay["k_scales"] + n // 16] = ks[i].reshape(-1)
+        b[lay["v_data"]:lay["v_data"] + n // 2] = vd[i].reshape(-1)
+        b[lay["v_scales"]:lay["v_scales"] + n // 16] = vs[i].reshape(-1)
+        if extra_bytes:
+            b[lay["extra"]:lay["extra"] + extra_bytes] = extra[hp, :extra_bytes]
+    return blocks
+
+
+def cold_onboard(blocks, H, D, T, g_k, g_v, out_dtype, num_hot_pages, cold_slot_ids=None,
+                 hot_page_ids=None, extra_bytes=0, num_pages=None):
+    """(k, v, extra) hot pools [num_hot_pages, H, T, D] (16-bit patterns) and
+    [num_hot_pages, extra_bytes] written from cold slots cold_slot_ids[i] into hot pages
+    hot_page_ids[i]: the block's K and V parts decoded exactly as dequantize_pages."""
+    lay = cold_block_layout(H, D, T, extra_bytes)
+    sids = _ids(cold_slot_ids)
+    hids = _ids(hot_page_ids)
+    if num_pages is None:
+        num_pages = len(sids) if sids is not None else blocks.shape[0]
+    n = H * T * D
+    slot = [int(sids[i]) if sids is not None else i for i in range(num_pages)]
+    part = lambda name, size, shape: np.stack(  # noqa: E731
+        [blocks[s, lay[name]:lay[name] + size].reshape(shape) for s in slot]) if slot else \
+        np.zeros((0,) + shape, np.uint8)
+    kd = part("k_data", n // 2, (H, T, D // 2))
+    ks = part("k_scales", n // 16, (H, T, D // 16))
+    vd = part("v_data", n // 2, (H, T, D // 2))
+    vs = part("v_scales", n // 16, (H, T, D // 16))
+    k = dequantize_pages(kd, ks, H, D, T, g_k, out_dtype, num_dst_pages=num_hot_pages,
+                         dst_page_ids=hids, num_pages=num_pages)
+    v = dequantize_pages(vd, vs, H, D, T, g_v, out_dtype, num_dst_pages=num_hot_pages,
+                         dst_page_ids=hids, num_pages=num_pages)
+    ex = np.zeros((num_hot_pages, extra_bytes), dtype=np.uint8)
+    for i, s in enumerate(slot):
+        hp = int(hids[i]) if hids is not None else i
+        ex[hp] = blocks[s, lay["extra"]:lay["extra"] + extra_bytes]
+    return k, v, ex

@@ -38,7 +38,7 @@
  *   R6 decode: v = e2m1(c) * e4m3(s) (exact), then fp32(v * g), then the output rounding.
  *   R7 global scale: g = fp32(amax_tensor / 2688) (2688 = 448 * 6); g = 1 if that is 0.
  *   R8 FP8 output: E4M3_rne_satfinite(fp32(v * fp32(g / out_scale))), sign kept.
- *   R9 FP8 workspace copy of a 16-bit chunk (extend path): E4M3_rne_satfinite(fp32(x * m)),
+ *   R9 FP8 workspace copy of a chunk (extend path): E4M3_rne_satfinite(fp32(x * m)),
  *      m = fp32(1 / ws_scale), sign kept; pages keep the plain [page][head][token][dim] order.
  *
  * Build: plain C99, no SIMD intrinsics, -ffp-contract=off (no fused multiply-add), optional
@@ -406,22 +406,23 @@ void orc_quantize_pages(int H, int D, int T, int packing, int src_dtype, const v
 }
 
 /*
- * FP8 workspace copy of 16-bit source pages. R9.
- * [LMSYS Path 2]: the current chunk's K/V are copied into the FP8 workspace that the extend
- * attention reads (and, separately, written to the NVFP4 cache: orc_quantize_pages).
+ * FP8 workspace copy of source pages (BF16, FP16, or FP8 read as x = fp32(e4m3 * src_scale)).
+ * R9. [LMSYS Path 2]: the current chunk's K/V are copied into the FP8 workspace that the
+ * extend attention reads (and, separately, written to the NVFP4 cache: orc_quantize_pages).
  */
 void orc_cast_fp8_pages(int H, int D, int T, int src_dtype, const void* src,
-                        const int32_t* src_page_ids, double ws_scale, uint8_t* dst,
-                        const int32_t* dst_page_ids, int num_pages)
+                        const int32_t* src_page_ids, double src_scale, double ws_scale,
+                        uint8_t* dst, const int32_t* dst_page_ids, int num_pages)
 {
     size_t page_elems = (size_t)H * T * D;
     double m = fp32(1.0 / fp32(ws_scale)); /* FP32 scalar and its FP32 reciprocal */
+    double ss = fp32(src_scale);
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < num_pages; ++i) {
         size_t sp = (size_t)(src_page_ids ? src_page_ids[i] : i);
         size_t dp = (size_t)(dst_page_ids ? dst_page_ids[i] : i);
         for (size_t e = 0; e < page_elems; ++e) {
-            double x = load_src(src_dtype, src, sp * page_elems + e, 1.0);
+            double x = load_src(src_dtype, src, sp * page_elems + e, ss);
             dst[dp * page_elems + e] = e4m3_encode(fp32(x * m));
         }
     }

@@ -230,19 +230,23 @@ def test_extend_workload(kv, cuda):
 
 # ------------------------------------------------------------------------------ extend write
 
-@pytest.mark.parametrize("kind", ["bf16", "fp16"])
+@pytest.mark.parametrize("kind", ["bf16", "fp16", "fp8"])
 @pytest.mark.parametrize("pack", [oracle.DIM_PAIRS, oracle.TOKEN_PAIRS])
 @pytest.mark.parametrize("ws_scale", [1.0, 0.375])
 def test_extend_write_parity(kv, cuda, kind, pack, ws_scale):
-    """One pass over a chunk's 16-bit pages (scattered sources, destinations and workspace
-    slots, a ragged page count): the NVFP4 pages equal both the oracle and the plain quantize
-    call, the FP8 workspace copy equals the oracle's E4M3(fp32(x * fp32(1 / ws_scale)))."""
+    """One pass over a chunk's pages (scattered sources, destinations and workspace slots, a
+    ragged page count): the NVFP4 pages equal both the oracle and the plain quantize call, the
+    FP8 workspace copy equals the oracle's E4M3(fp32(x * fp32(1 / ws_scale))), x read from FP8
+    sources as fp32(e4m3 * src_scale)."""
     P, H, T, D = 37, 2, 32, 128
     src = _make_src(kind, P, H, T, D, seed=40 + pack).to(cuda)
     bits = _src_bits(src)
     odt = _odt(src)
     lay = kv.Layout(H, D, T).with_packing(pack)
-    g = oracle.global_scale(bits, odt, H, D, T)
+    src_scale = float(np.float32(0.375)) if kind == "fp8" else 1.0
+    sst = _scalar(src_scale, cuda) if kind == "fp8" else None
+    sdt = kv.FP8_E4M3 if kind == "fp8" else None
+    g = oracle.global_scale(bits, odt, H, D, T, src_scale=src_scale)
     gs = _scalar(g, cuda)
     rng = np.random.default_rng(7)
     n = 29
@@ -255,19 +259,24 @@ def test_extend_write_parity(kv, cuda, kind, pack, ws_scale):
     ws = torch.zeros((33, H, T, D), dtype=torch.uint8, device=cuda)
     t = lambda a: torch.from_numpy(a).to(cuda)  # noqa: E731
     kv.nvfp4_kv_extend_write(lay, src, gs, data, scales, ws, src_page_ids=t(sid),
-                             dst_page_ids=t(did), ws_page_ids=t(wid),
-                             ws_scale=_scalar(ws_scale, cuda))
+                             dst_page_ids=t(did), ws_page_ids=t(wid), src_scale=sst,
+                             ws_scale=_scalar(ws_scale, cuda), src_dtype=sdt)
     want_d, want_s = oracle.quantize_pages(bits, odt, H, D, T, g, num_dst_pages=48,
-                                           src_page_ids=sid, dst_page_ids=did, packing=pack)
+                                           src_page_ids=sid, dst_page_ids=did,
+                                           src_scale=src_scale, packing=pack)
     want_ws = oracle.cast_fp8_pages(bits, odt, H, D, T, ws_scale=ws_scale, num_dst_pages=33,
-                                    src_page_ids=sid, dst_page_ids=wid)
+                                    src_page_ids=sid, dst_page_ids=wid, src_scale=src_scale)
     assert np.array_equal(data.cpu().numpy(), want_d)
     assert np.array_equal(scales.cpu().numpy(), want_s)
     assert np.array_equal(ws.cpu().numpy(), want_ws)
     # the NVFP4 half is exactly the plain quantize call
     d2, s2 = torch.zeros_like(data), torch.zeros_like(scales)
-    kv.nvfp4_kv_quantize_pages(lay, src, gs, d2, s2, src_page_ids=t(sid), dst_page_ids=t(did))
+    kv.nvfp4_kv_quantize_pages(lay, src, gs, d2, s2, src_page_ids=t(sid), dst_page_ids=t(did),
+                               src_scale=sst, src_dtype=sdt)
     assert torch.equal(d2, data) and torch.equal(s2, scales)
+    if kind == "fp8" and ws_scale == src_scale:
+        # an FP8 chunk written at its own scale is copied byte for byte
+        assert torch.equal(ws[t(wid).long()], src[t(sid).long()])
 
 
 def test_extend_write_flags_out_of_range_workspace_pages(kv, cuda):

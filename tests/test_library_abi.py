@@ -29,6 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages", "nvfp4_kv_extend_write",
+                 "nvfp4_kv_cold_block_layout", "nvfp4_kv_offload_pages", "nvfp4_kv_onboard_pages",
+                 "nvfp4_kv_host_device_pointer",
                  "nvfp4_paged_decode_attention", "nvfp4_paged_decode_workspace_size",
                  "nvfp4_kv_compute_global_scale", "nvfp4_kv_global_scale_workspace_size",
                  "nvfp4_kv_round_f32", "nvfp4kv_status_string", "nvfp4kv_version"):
@@ -81,16 +83,37 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert dq(ctypes.byref(good), fake, fake, 1, None, fake, 9, fake, 1, None, None, 1, None,
               None) == 1
     xw = lib.nvfp4_kv_extend_write
-    # FP8 source: unsupported (the workspace copy of an FP8 chunk is the chunk itself)
-    assert xw(ctypes.byref(good), 2, fake, 1, None, fake, fake, fake, 1, None, fake, 1, None,
-              None, 1, None, None) == 2
+    # unknown source dtype
+    assert xw(ctypes.byref(good), 7, fake, 1, None, None, fake, fake, fake, 1, None, fake, 1,
+              None, None, 1, None, None) == 2
     # missing workspace; misaligned workspace; zero pages is a no-op
-    assert xw(ctypes.byref(good), 0, fake, 1, None, fake, fake, fake, 1, None, None, 1, None,
-              None, 1, None, None) == 1
-    assert xw(ctypes.byref(good), 0, fake, 1, None, fake, fake, fake, 1, None, mis, 1,
+    assert xw(ctypes.byref(good), 0, fake, 1, None, None, fake, fake, fake, 1, None, None, 1,
               None, None, 1, None, None) == 1
-    assert xw(ctypes.byref(good), 0, None, 0, None, None, None, None, 0, None, None, 0, None,
-              None, 0, None, None) == 0
+    assert xw(ctypes.byref(good), 2, fake, 1, None, None, fake, fake, fake, 1, None, mis, 1,
+              None, None, 1, None, None) == 1
+    assert xw(ctypes.byref(good), 0, None, 0, None, None, None, None, None, 0, None, None, 0,
+              None, None, 0, None, None) == 0
+    off = lib.nvfp4_kv_offload_pages
+    hot_stride = 8 * 64 * 128
+    # FP8 hot pool: unsupported; null cold pool; misaligned hot pool; page stride below a page;
+    # extra bytes without an extra pointer; zero pages is a no-op
+    assert off(ctypes.byref(good), 2, fake, fake, hot_stride, 1, None, None, None, None, 0, 0,
+               fake, 1, None, 1, None, None) == 2
+    assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None, None, 0, 0,
+               None, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, mis, fake, hot_stride, 1, None, None, None, None, 0, 0,
+               fake, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, fake, fake, hot_stride - 8, 1, None, None, None, None, 0,
+               0, fake, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None, None, 16, 16,
+               fake, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, None, None, 0, 0, None, None, None, None, 0, 0, None, 0,
+               None, 0, None, None) == 0
+    on = lib.nvfp4_kv_onboard_pages
+    assert on(ctypes.byref(good), None, 1, None, None, None, 0, fake, fake, hot_stride, 1, None,
+              None, 0, 0, 1, None, None) == 1
+    assert on(ctypes.byref(good), fake, 1, None, None, None, 2, fake, fake, hot_stride, 1, None,
+              None, 0, 0, 1, None, None) == 2
     att = lib.nvfp4_paged_decode_attention
     args = [ctypes.byref(good), 2, 32, fake, fake, fake, fake, fake, fake, fake, 10, fake, 4,
             fake, 0.1, 0, fake, 1 << 20, fake, None, None, None]
@@ -120,3 +143,22 @@ def test_workspace_sizes(lib):
     n64 = kv.nvfp4_paged_decode_workspace_size(lay, 4, 32, 4096, 64)
     assert n64 >= 64 * 4 * 32 * (128 + 2) * 4
     assert kv.nvfp4_paged_decode_workspace_size(lay, 4, 32, 4096, 65) == 0
+
+
+def test_cold_block_layout_matches_its_definition(lib):
+    """The library's cold block offsets equal the oracle's, written from the same definition
+    (K codes, K scales, V codes, V scales, extra, each part at the previous end rounded up
+    to 16), including shapes that need padding; a bad extra size is rejected."""
+    import nvfp4_paged_kv_gb300 as kv
+    import oracle
+    fields = ("k_data", "k_scales", "v_data", "v_scales", "extra", "bytes")
+    for H, D, T, extra in ((8, 128, 32, 0), (8, 128, 64, 4096), (1, 16, 1, 32), (3, 80, 5, 16)):
+        bl = kv.nvfp4_kv_cold_block_layout(kv.Layout(H, D, T), extra)
+        ref = oracle.cold_block_layout(H, D, T, extra)
+        assert [getattr(bl, f) for f in fields] == [ref[f] for f in fields]
+    out = kv.ColdBlockLayout()
+    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 128, 32)), 8,
+                                          ctypes.byref(out)) == 1
+    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 120, 32)), 0,
+                                          ctypes.byref(out)) == 1
+

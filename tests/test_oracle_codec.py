@@ -493,3 +493,30 @@ def test_fp8_copy_follows_page_ids():
                                 dst_page_ids=[0, 1])
     one = oracle.cast_fp8_pages(pool, oracle.FP16, 2, 16, 4)
     assert np.array_equal(out[0], one[2]) and np.array_equal(out[1], one[0])
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37, 3.0, 2.0 ** -5])
+def test_fp8_copy_of_an_fp8_chunk_with_its_own_scale_is_the_identity(scale):
+    """An FP8 chunk read as x = fp32(e * s) and written with ws_scale = s gets its own bytes back:
+    fp32(x * fp32(1 / s)) is e to within a few fp32 ulps, which E4M3 rounding removes (every e is
+    a grid point; 448 stays 448 under saturation). Negative zero keeps its sign."""
+    codes = np.array(_e4m3_finite(), dtype=np.uint8)
+    n = 16 * ((len(codes) + 15) // 16)
+    page = np.zeros(n, dtype=np.uint8)
+    page[:len(codes)] = codes
+    out = oracle.cast_fp8_pages(page.reshape(1, 1, n // 16, 16), oracle.FP8_E4M3, 1, 16, n // 16,
+                                src_scale=scale, ws_scale=scale).reshape(-1)
+    assert list(out[:len(codes)]) == list(codes)
+
+
+def test_fp8_copy_of_an_fp8_chunk_rescales_by_src_over_ws():
+    """src_scale 2, ws_scale 1: the copy of e is exactly E4M3(2 e), i.e. 2 e in the normal range
+    and 448 (saturated) above 224."""
+    codes = [b for b in _e4m3_finite() if b < 0x80 and oracle.e4m3_value(b) >= 2 ** -6]
+    n = 16 * ((len(codes) + 15) // 16)
+    page = np.zeros(n, dtype=np.uint8)
+    page[:len(codes)] = codes
+    out = oracle.cast_fp8_pages(page.reshape(1, 1, n // 16, 16), oracle.FP8_E4M3, 1, 16, n // 16,
+                                src_scale=2.0).reshape(-1)
+    for c, o in zip(codes, out):
+        assert oracle.e4m3_value(int(o)) == min(2 * oracle.e4m3_value(c), 448.0)

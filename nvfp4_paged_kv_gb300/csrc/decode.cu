@@ -86,7 +86,7 @@ struct Geo {
     static constexpr int BLOCKS_PER_SM = (D == 64) ? 5 : 3;
     static_assert(DCH * 32 * 16 == SK && DCH == SUB * SUB_DIV, "copy split");
     static_assert(SC_PER_LANE * 32 == 2 * SCH, "scale copy split");
-    static_assert((kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup + 2 * kMaxGroup) * 4 <= SMEM,
+    static_assert((kWarps * kMaxGroup * D + 2 * kMaxRecW * kMaxGroup + 2 * kMaxGroup) * 4 <= SMEM,
                   "merge buffers must fit in the rings");
 };
 
@@ -690,10 +690,13 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M0);
         const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M1);
         // over the drained rings: the warps' partial outputs [kWarps][kMaxGroup][D], then the
-        // merge weights of a pair's records [kMaxRecW][kMaxGroup] and merged (max, sum) per head
+        // merge weights of a pair's records [kMaxRecW][kMaxGroup], merged (max, sum) per head, and the
+        // records' sums [kMaxRecW][kMaxGroup]
         float* so = reinterpret_cast<float*>(smem);
         float (*mw_s)[kMaxGroup] = reinterpret_cast<float (*)[kMaxGroup]>(so + kWarps * kMaxGroup * D);
         float (*ml_s)[2] = reinterpret_cast<float (*)[2]>(so + kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup);
+        float (*lw_s)[kMaxGroup] = reinterpret_cast<float (*)[kMaxGroup]>(
+            so + kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup + 2 * kMaxGroup);
 #pragma unroll
         for (int m = 0; m < G_::KSTEPS; ++m) {
             const int d0 = rho * (D / 8) + 2 * m;
@@ -772,22 +775,55 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
             }
             __syncthreads();
             if (last_s) {
-                // every record of the pair is written: merge them (L2 reads, not L1)
+                // every record of the pair is written: merge them (L2 reads, not L1). The (max,
+                // sum) pairs of up to kMaxRecW records are staged in shared memory by one round
+                // of loads while the first records' outputs are already in flight.
                 __threadfence();
+                constexpr int NQ = kMaxGroup * D / kDecThreads;
+                constexpr int kRecUnroll = 8;
+                const int n_fast = min(n_rec, kMaxRecW);
+                for (int idx = tid; idx < n_fast * G; idx += kDecThreads) {
+                    const int k = idx / G, col = idx - (idx / G) * G;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                        p.rec_ml + (rec_index(k) * G + col) * 2));
+                    mw_s[k][col] = ml.x;
+                    lw_s[k][col] = ml.y;
+                }
+                float v[kRecUnroll][NQ];
+                auto load_recs = [&](int k0) {
+#pragma unroll
+                    for (int u = 0; u < kRecUnroll; ++u) {
+                        const int k = min(k0 + u, n_rec - 1);
+                        const float* rk = p.rec_o + rec_index(k) * G * D;
+#pragma unroll
+                        for (int q = 0; q < NQ; ++q) {
+                            const int i = tid + kDecThreads * q;
+                            v[u][q] = (i < G * D) ? __ldcg(rk + i) : 0.0f;
+                        }
+                    }
+                };
+                load_recs(0);
+                __syncthreads();
                 if (warp < G) {  // warp w: query heads w, w + 4
                     for (int col = warp; col < G; col += kWarps) {
+                        auto m_of = [&](int k) {
+                            return k < n_fast ? mw_s[k][col]
+                                              : __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);
+                        };
                         float M = -INFINITY;
-                        for (int k = lane; k < n_rec; k += 32)
-                            M = fmaxf(M, __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2));
+                        for (int k = lane; k < n_rec; k += 32) M = fmaxf(M, m_of(k));
 #pragma unroll
                         for (int o2 = 16; o2 > 0; o2 >>= 1)
                             M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o2));
                         float lsum = 0.0f;
                         for (int k = lane; k < n_rec; k += 32) {
-                            const float mk = __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);
+                            const float mk = m_of(k);
+                            const float lk = k < n_fast
+                                                 ? lw_s[k][col]
+                                                 : __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2 + 1);
                             const float wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-                            if (k < kMaxRecW) mw_s[k][col] = wk;
-                            lsum += wk * __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2 + 1);
+                            if (k < n_fast) mw_s[k][col] = wk;  // this lane alone reads entry k
+                            lsum += wk * lk;
                         }
 #pragma unroll
                         for (int o2 = 16; o2 > 0; o2 >>= 1)
@@ -803,25 +839,12 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                     }
                 }
                 __syncthreads();
-                // thread tid owns outputs i = tid + kDecThreads q; records are read kRecUnroll
-                // at a time so that their L2 latencies overlap
-                constexpr int NQ = kMaxGroup * D / kDecThreads;
-                constexpr int kRecUnroll = 4;
+                // thread tid owns outputs i = tid + kDecThreads q; kRecUnroll records at a time
                 float acc[NQ];
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) acc[q] = 0.0f;
                 for (int k0 = 0; k0 < n_rec; k0 += kRecUnroll) {
-                    float v[kRecUnroll][NQ];
-#pragma unroll
-                    for (int u = 0; u < kRecUnroll; ++u) {
-                        const int k = min(k0 + u, n_rec - 1);
-                        const float* rk = p.rec_o + rec_index(k) * G * D;
-#pragma unroll
-                        for (int q = 0; q < NQ; ++q) {
-                            const int i = tid + kDecThreads * q;
-                            v[u][q] = (i < G * D) ? __ldcg(rk + i) : 0.0f;
-                        }
-                    }
+                    if (k0 > 0) load_recs(k0);
 #pragma unroll
                     for (int u = 0; u < kRecUnroll; ++u) {
                         const int k = k0 + u;
@@ -832,7 +855,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                             if (i >= G * D) continue;
                             const int col = i / D;
                             float wk;
-                            if (k < kMaxRecW) {
+                            if (k < n_fast) {
                                 wk = mw_s[k][col];
                             } else {
                                 const float mk = __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);

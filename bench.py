@@ -432,49 +432,57 @@ def kernel_table(path, peak):
 def cold_table(path, flush, timer, pages=2048):
     """Cold-page codec over the host link: offload (encode fused with the write of the cold
     blocks into pinned host memory) and onboard (decode fused with the read back), for `pages`
-    pages of the round-trip workload (K and V, 32 tokens x 8 heads x 128 dims per page). Each
-    line carries the measured time of a plain copy of the same cold bytes over the same link
-    (the bound) and of a plain copy of the uncompressed 16-bit pages (what a codec that only
-    concatenates the pools would move)."""
+    pages of the round-trip workload (K and V, 32 tokens x 8 heads x 128 dims per page), with
+    the RoPE part of K (head dims 64..127) quantized like the rest, kept at 16 bits, or stored
+    as two NVFP4 components. Each line carries the measured time of a plain copy of the same
+    cold bytes over the same link (the bound) and of a plain copy of the uncompressed 16-bit
+    pages (what a codec that only concatenates the pools would move)."""
     import torch
     kv, rt = path.kv, path.rt
     H, T, D = rt.H, rt.T, rt.D
     lay = kv.Layout(H, D, T)
-    bl = kv.nvfp4_kv_cold_block_layout(lay)
     n = min(pages, rt.P)
     hk, hv = path.k[:n], path.v[:n]
     gk, gv = path.rt_out[0]["g"], path.rt_out[1]["g"]
-    cold_h = torch.empty((n, bl.bytes), dtype=torch.uint8).pin_memory()
-    cold_d = torch.empty((n, bl.bytes), dtype=torch.uint8, device=path.dev)
     hot_h = torch.empty((2, n, H, T, D), dtype=torch.bfloat16).pin_memory()
     back_k, back_v = torch.empty_like(hk), torch.empty_like(hv)
-    cold_bytes = n * bl.bytes
     hot_bytes = 2 * n * H * T * D * 2
-    t_off = timer(lambda: kv.nvfp4_kv_offload_pages(lay, hk, hv, cold_h, k_global_scale=gk,
-                                                    v_global_scale=gv), flush)
-    t_on = timer(lambda: kv.nvfp4_kv_onboard_pages(lay, cold_h, back_k, back_v,
-                                                   k_global_scale=gk, v_global_scale=gv), flush)
-    t_d2h = timer(lambda: cold_h.copy_(cold_d, non_blocking=True), flush)
-    t_h2d = timer(lambda: cold_d.copy_(cold_h, non_blocking=True), flush)
     t_d2h_hot = timer(lambda: (hot_h[0].copy_(hk, non_blocking=True),
                                hot_h[1].copy_(hv, non_blocking=True)), flush)
     t_h2d_hot = timer(lambda: (back_k.copy_(hot_h[0], non_blocking=True),
                                back_v.copy_(hot_h[1], non_blocking=True)), flush)
     out = {}
-    for name, t, t_copy, t_hot, direction in (
-            ("cold offload K+V -> pinned host (%d pages)" % n, t_off, t_d2h, t_d2h_hot, "d2h"),
-            ("cold onboard pinned host -> K+V (%d pages)" % n, t_on, t_h2d, t_h2d_hot, "h2d")):
-        out[name] = {
-            "ms": round(t, 4), "bound": "host link (" + direction + ")",
-            "link_bytes": int(cold_bytes), "hbm_bytes": int(hot_bytes),
-            "link_GB_s": round(cold_bytes / (t * 1e-3) / GB, 1),
-            "plain_copy_ms": round(t_copy, 4),
-            "plain_copy_GB_s": round(cold_bytes / (t_copy * 1e-3) / GB, 1),
-            "frac_of_plain_copy": round(t_copy / t, 4),
-            "uncompressed_copy_ms": round(t_hot, 4),
-            "speedup_vs_uncompressed_copy": round(t_hot / t, 3),
-            "launches": 1}
-    del cold_h, cold_d, hot_h, back_k, back_v
+    for label, rope in (("", None), (", RoPE dims kept 16-bit", kv.ColdRope(kv.ROPE_SKIP, 64, 64)),
+                        (", RoPE dims 2FP4", kv.ColdRope(kv.ROPE_2FP4, 64, 64))):
+        bl = kv.nvfp4_kv_cold_block_layout(lay, 0, rope)
+        cold_h = torch.empty((n, bl.bytes), dtype=torch.uint8).pin_memory()
+        cold_d = torch.empty((n, bl.bytes), dtype=torch.uint8, device=path.dev)
+        cold_bytes = n * bl.bytes
+        t_off = timer(lambda: kv.nvfp4_kv_offload_pages(lay, hk, hv, cold_h, k_global_scale=gk,
+                                                        v_global_scale=gv, rope=rope), flush)
+        t_on = timer(lambda: kv.nvfp4_kv_onboard_pages(lay, cold_h, back_k, back_v,
+                                                       k_global_scale=gk, v_global_scale=gv,
+                                                       rope=rope), flush)
+        t_d2h = timer(lambda: cold_h.copy_(cold_d, non_blocking=True), flush)
+        t_h2d = timer(lambda: cold_d.copy_(cold_h, non_blocking=True), flush)
+        for name, t, t_copy, t_hot, direction in (
+                ("cold offload K+V -> pinned host (%d pages%s)" % (n, label), t_off, t_d2h,
+                 t_d2h_hot, "d2h"),
+                ("cold onboard pinned host -> K+V (%d pages%s)" % (n, label), t_on, t_h2d,
+                 t_h2d_hot, "h2d")):
+            out[name] = {
+                "ms": round(t, 4), "bound": "host link (" + direction + ")",
+                "link_bytes": int(cold_bytes), "hbm_bytes": int(hot_bytes),
+                "bits_per_value": round(cold_bytes * 8 / (2 * n * H * T * D), 4),
+                "link_GB_s": round(cold_bytes / (t * 1e-3) / GB, 1),
+                "plain_copy_ms": round(t_copy, 4),
+                "plain_copy_GB_s": round(cold_bytes / (t_copy * 1e-3) / GB, 1),
+                "frac_of_plain_copy": round(t_copy / t, 4),
+                "uncompressed_copy_ms": round(t_hot, 4),
+                "speedup_vs_uncompressed_copy": round(t_hot / t, 3),
+                "launches": 1}
+        del cold_h, cold_d
+    del hot_h, back_k, back_v
     return out
 
 

@@ -278,23 +278,54 @@ nvfp4kv_status nvfp4_paged_decode_attention_noalloc(
  * (cudaHostAlloc / cudaHostRegister, addressed through unified virtual addressing; the kernels
  * then read or write it over the host link directly, with no separate copy) or device memory.
  *
- * Cold block of one page, byte offsets from its base (every offset a multiple of 16):
- *   k_data    K codes, dim-pair packing [H][T][D/2] (byte j = dims 2j low, 2j+1 high nibble)
- *   k_scales  K block scales [H][T][D/16], E4M3
- *   v_data    V codes, dim-pair packing [H][T][D/2]
- *   v_scales  V block scales [H][T][D/16]
- *   extra     extra_bytes copied unchanged (e.g. state that must not be quantized)
- * each part starting at the previous part's end rounded up to 16; `bytes` is the end of the
- * extra part rounded up to 16. When H*T*D/16 is a multiple of 16 there is no padding and
+ * The position-encoded (RoPE) part of K (the same page, "The RoPE part of K"): head dims
+ * [first_dim, first_dim + dims) of every K vector, both multiples of 16. Three modes:
+ *   NVFP4KV_ROPE_QUANTIZE  quantized like the rest (the default; also rope == NULL)
+ *   NVFP4KV_ROPE_SKIP      kept at the hot page's 16-bit precision
+ *   NVFP4KV_ROPE_2FP4      two NVFP4 components: c1 encodes x as usual; with v1 = e2m1(c1) *
+ *                          e4m3(s1), the residual r = fp32(x - fp32(v1 g)) is encoded the same
+ *                          way (same g) into c2; decode is fp32(fp32(v1 g) + fp32(v2 g)),
+ *                          then the 16-bit rounding
+ *
+ * Cold block of one page, byte offsets from its base (every offset a multiple of 16); K's
+ * blocks split into the N = D - dims other head dims and the R = dims RoPE dims of each row:
+ *   k_data        K codes of the other dims, dim-pair packing [H][T][N/2] (byte j = dims 2j
+ *                 low, 2j+1 high nibble, counted within the other dims in order)
+ *   k_scales      their block scales [H][T][N/16], E4M3
+ *   k_rope        SKIP: the RoPE values [H][T][R] (16-bit); 2FP4: codes of c1 [H][T][R/2]
+ *   k_rope_scales 2FP4: block scales of c1 [H][T][R/16]
+ *   k_rope2       2FP4: codes of c2 [H][T][R/2]
+ *   k_rope2_scales 2FP4: block scales of c2 [H][T][R/16]
+ *   v_data        V codes, dim-pair packing [H][T][D/2]
+ *   v_scales      V block scales [H][T][D/16]
+ *   extra         extra_bytes copied unchanged (e.g. state that must not be quantized)
+ * each part starting at the previous part's end rounded up to 16 (parts a mode does not use are
+ * -1 and take no room; with QUANTIZE, N = D); `bytes` is the end of the extra part. When
+ * H*T*D/16 is a multiple of 16 and QUANTIZE is used there is no padding and
  * bytes = 2 * (9/16) * H*T*D + extra_bytes. Slot s of the cold pool starts at cold + s * bytes.
  * The layout's `packing` field is ignored here (cold blocks always use dim pairs).
  * ------------------------------------------------------------------------------------------ */
+typedef enum nvfp4kv_rope_mode {
+    NVFP4KV_ROPE_QUANTIZE = 0,
+    NVFP4KV_ROPE_SKIP = 1,
+    NVFP4KV_ROPE_2FP4 = 2
+} nvfp4kv_rope_mode;
+
+typedef struct nvfp4kv_cold_rope {
+    int32_t mode;       /* nvfp4kv_rope_mode */
+    int32_t first_dim;  /* multiple of 16 */
+    int32_t dims;       /* multiple of 16, > 0, first_dim + dims <= head_dim (<= 2048) */
+} nvfp4kv_cold_rope;
+
 typedef struct nvfp4kv_cold_block_layout {
-    int64_t k_data, k_scales, v_data, v_scales, extra, bytes;
+    int64_t k_data, k_scales, k_rope, k_rope_scales, k_rope2, k_rope2_scales;
+    int64_t v_data, v_scales, extra, bytes;
 } nvfp4kv_cold_block_layout;
 
-/* Fills *out for `layout` and extra_bytes (>= 0, a multiple of 16). Host only. */
-nvfp4kv_status nvfp4_kv_cold_block_layout(const nvfp4kv_layout* layout, int32_t extra_bytes,
+/* Fills *out for `layout`, the RoPE option (NULL = QUANTIZE) and extra_bytes (>= 0, a multiple
+ * of 16). Host only. */
+nvfp4kv_status nvfp4_kv_cold_block_layout(const nvfp4kv_layout* layout,
+                                          const nvfp4kv_cold_rope* rope, int32_t extra_bytes,
                                           nvfp4kv_cold_block_layout* out);
 
 /* Offload: hot page hot_page_ids[i] -> cold slot cold_slot_ids[i], for i < num_pages.
@@ -306,6 +337,7 @@ nvfp4kv_status nvfp4_kv_cold_block_layout(const nvfp4kv_layout* layout, int32_t 
  *   hot_pool_pages, hot_page_ids   pages in each hot pool; ids (NULL = 0 .. num_pages-1)
  *   k_global_scale, v_global_scale device scalars g of K and V (NULL = 1); codes and scales
  *                      are exactly those of nvfp4_kv_quantize_pages with the same g
+ *   rope               host pointer, the RoPE part of K and its mode (NULL = QUANTIZE)
  *   extra, extra_page_stride, extra_bytes   lossless bytes of hot page p at
  *                      extra + p * extra_page_stride (16-byte aligned; stride a multiple of 16);
  *                      extra_bytes = 0 (extra may be NULL) copies none
@@ -315,17 +347,19 @@ nvfp4kv_status nvfp4_kv_cold_block_layout(const nvfp4kv_layout* layout, int32_t 
 nvfp4kv_status nvfp4_kv_offload_pages(
     const nvfp4kv_layout* layout, nvfp4kv_dtype hot_dtype, const void* hot_k, const void* hot_v,
     int64_t hot_page_stride, int32_t hot_pool_pages, const int32_t* hot_page_ids,
-    const float* k_global_scale, const float* v_global_scale, const uint8_t* extra,
-    int64_t extra_page_stride, int32_t extra_bytes, uint8_t* cold, int32_t cold_slots,
-    const int32_t* cold_slot_ids, int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream);
+    const float* k_global_scale, const float* v_global_scale, const nvfp4kv_cold_rope* rope,
+    const uint8_t* extra, int64_t extra_page_stride, int32_t extra_bytes, uint8_t* cold,
+    int32_t cold_slots, const int32_t* cold_slot_ids, int32_t num_pages, int32_t* status,
+    nvfp4kv_stream_t stream);
 
 /* Onboard: cold slot cold_slot_ids[i] -> hot page hot_page_ids[i], for i < num_pages. Values
- * are exactly those of nvfp4_kv_dequantize_pages (BF16 / FP16 output) with the same g; the
- * extra bytes are copied back unchanged. Arguments as in nvfp4_kv_offload_pages. */
+ * are exactly those of nvfp4_kv_dequantize_pages (BF16 / FP16 output) with the same g (RoPE
+ * part: SKIP copies it back, 2FP4 decodes as above); the extra bytes are copied back
+ * unchanged. Arguments as in nvfp4_kv_offload_pages, with the same `rope`. */
 nvfp4kv_status nvfp4_kv_onboard_pages(
     const nvfp4kv_layout* layout, const uint8_t* cold, int32_t cold_slots,
     const int32_t* cold_slot_ids, const float* k_global_scale, const float* v_global_scale,
-    nvfp4kv_dtype hot_dtype, void* hot_k, void* hot_v, int64_t hot_page_stride,
+    const nvfp4kv_cold_rope* rope, nvfp4kv_dtype hot_dtype, void* hot_k, void* hot_v, int64_t hot_page_stride,
     int32_t hot_pool_pages, const int32_t* hot_page_ids, uint8_t* extra,
     int64_t extra_page_stride, int32_t extra_bytes, int32_t num_pages, int32_t* status,
     nvfp4kv_stream_t stream);

@@ -26,7 +26,8 @@ __all__ = [
     "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages", "nvfp4_kv_extend_write",
     "nvfp4_paged_decode_workspace_size", "nvfp4_paged_decode_attention", "nvfp4_kv_round_f32",
     "nvfp4_paged_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "ColdBlockLayout", "nvfp4_kv_cold_block_layout", "nvfp4_kv_offload_pages",
+    "ColdBlockLayout", "ColdRope", "ROPE_QUANTIZE", "ROPE_SKIP", "ROPE_2FP4",
+    "nvfp4_kv_cold_block_layout", "nvfp4_kv_offload_pages",
     "nvfp4_kv_onboard_pages",
 ]
 NOALLOC_SCRATCH_BYTES = 32 << 20   # NVFP4KV_NOALLOC_SCRATCH_BYTES
@@ -54,10 +55,23 @@ class Layout(ctypes.Structure):
                 f"page_size={self.page_size}, packing={self.packing})")
 
 
+ROPE_QUANTIZE, ROPE_SKIP, ROPE_2FP4 = 0, 1, 2   # nvfp4kv_rope_mode
+
+
+class ColdRope(ctypes.Structure):
+    """The RoPE part of K (head dims [first_dim, first_dim + dims)) and how a cold block keeps
+    it (``nvfp4kv_cold_rope``)."""
+    _fields_ = [("mode", ctypes.c_int32), ("first_dim", ctypes.c_int32), ("dims", ctypes.c_int32)]
+
+    def __init__(self, mode: int = ROPE_QUANTIZE, first_dim: int = 0, dims: int = 0):
+        super().__init__(int(mode), int(first_dim), int(dims))
+
+
 class ColdBlockLayout(ctypes.Structure):
     """Byte offsets of the parts of one cold block and its size (``nvfp4kv_cold_block_layout``)."""
     _fields_ = [(n, ctypes.c_int64) for n in
-                ("k_data", "k_scales", "v_data", "v_scales", "extra", "bytes")]
+                ("k_data", "k_scales", "k_rope", "k_rope_scales", "k_rope2", "k_rope2_scales",
+                 "v_data", "v_scales", "extra", "bytes")]
 
     def __repr__(self):
         return "ColdBlockLayout(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in
@@ -106,10 +120,10 @@ def load():
             "nvfp4_paged_decode_attention": (I32, [LP, I32, I32, P, P, P, P, P, P, P, I32, P,
                                                    I32, P, F, I32, P, SZ, P, P, P, P]),
             "nvfp4_kv_round_f32": (I32, [P, SZ, I32, P, P]),
-            "nvfp4_kv_cold_block_layout": (I32, [LP, I32, ctypes.POINTER(ColdBlockLayout)]),
-            "nvfp4_kv_offload_pages": (I32, [LP, I32, P, P, I64, I32, P, P, P, P, I64, I32, P,
-                                             I32, P, I32, P, P]),
-            "nvfp4_kv_onboard_pages": (I32, [LP, P, I32, P, P, P, I32, P, P, I64, I32, P, P,
+            "nvfp4_kv_cold_block_layout": (I32, [LP, P, I32, ctypes.POINTER(ColdBlockLayout)]),
+            "nvfp4_kv_offload_pages": (I32, [LP, I32, P, P, I64, I32, P, P, P, P, P, I64, I32,
+                                             P, I32, P, I32, P, P]),
+            "nvfp4_kv_onboard_pages": (I32, [LP, P, I32, P, P, P, P, I32, P, P, I64, I32, P, P,
                                              I64, I32, I32, P, P]),
             "nvfp4_kv_host_device_pointer": (I32, [P, ctypes.POINTER(ctypes.c_void_p)]),
             "nvfp4_paged_decode_attention_noalloc": (I32, [LP, I32, I32, P, P, P, P, P, P, P,
@@ -312,12 +326,18 @@ def nvfp4_kv_round_f32(x: torch.Tensor, target: int, out: torch.Tensor, stream=N
 
 # ------------------------------------------------------------------------------ cold pages
 
-def nvfp4_kv_cold_block_layout(layout: Layout, extra_bytes: int = 0) -> ColdBlockLayout:
-    """Offsets and size of one cold block for `layout` with `extra_bytes` lossless bytes."""
+def _rope_ref(rope):
+    return None if rope is None else ctypes.byref(rope)
+
+
+def nvfp4_kv_cold_block_layout(layout: Layout, extra_bytes: int = 0,
+                               rope: Optional[ColdRope] = None) -> ColdBlockLayout:
+    """Offsets and size of one cold block for `layout` with `extra_bytes` lossless bytes and
+    the RoPE option `rope` (None: the RoPE part is quantized like the rest)."""
     out = ColdBlockLayout()
     _check("nvfp4_kv_cold_block_layout",
-           load().nvfp4_kv_cold_block_layout(ctypes.byref(layout), int(extra_bytes),
-                                             ctypes.byref(out)))
+           load().nvfp4_kv_cold_block_layout(ctypes.byref(layout), _rope_ref(rope),
+                                             int(extra_bytes), ctypes.byref(out)))
     return out
 
 
@@ -358,11 +378,12 @@ def _extra_args(extra, extra_bytes):
 def nvfp4_kv_offload_pages(layout: Layout, hot_k: torch.Tensor, hot_v: torch.Tensor,
                            cold: torch.Tensor, *, k_global_scale=None, v_global_scale=None,
                            hot_page_ids=None, cold_slot_ids=None, extra=None, extra_bytes=0,
-                           num_pages=None, hot_dtype=None, status=None, stream=None):
+                           rope: Optional[ColdRope] = None, num_pages=None, hot_dtype=None,
+                           status=None, stream=None):
     """Quantize hot pages (BF16 / FP16 [pages, H, T, D]) into cold blocks of `cold`
     ([slots, block bytes] uint8, device or pinned host memory) in one pass."""
     lib = load()
-    bl = nvfp4_kv_cold_block_layout(layout, extra_bytes)
+    bl = nvfp4_kv_cold_block_layout(layout, extra_bytes, rope)
     kp, ks = _paged_ptr(hot_k)
     vp, vs = _paged_ptr(hot_v)
     if ks != vs:
@@ -372,8 +393,8 @@ def nvfp4_kv_offload_pages(layout: Layout, hot_k: torch.Tensor, hot_v: torch.Ten
     ep, es, eb = _extra_args(extra, extra_bytes)
     code = lib.nvfp4_kv_offload_pages(
         ctypes.byref(layout), _dtype_code(hot_k, hot_dtype), kp, vp, ks, hot_k.shape[0],
-        _ids(hot_page_ids), _ptr(k_global_scale), _ptr(v_global_scale), ep, es, eb,
-        _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids), int(num_pages),
+        _ids(hot_page_ids), _ptr(k_global_scale), _ptr(v_global_scale), _rope_ref(rope), ep, es,
+        eb, _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids), int(num_pages),
         _ptr(status), _stream(stream))
     _check("nvfp4_kv_offload_pages", code)
 
@@ -381,10 +402,11 @@ def nvfp4_kv_offload_pages(layout: Layout, hot_k: torch.Tensor, hot_v: torch.Ten
 def nvfp4_kv_onboard_pages(layout: Layout, cold: torch.Tensor, hot_k: torch.Tensor,
                            hot_v: torch.Tensor, *, k_global_scale=None, v_global_scale=None,
                            cold_slot_ids=None, hot_page_ids=None, extra=None, extra_bytes=0,
-                           num_pages=None, hot_dtype=None, status=None, stream=None):
+                           rope: Optional[ColdRope] = None, num_pages=None, hot_dtype=None,
+                           status=None, stream=None):
     """Dequantize cold blocks of `cold` into hot pages (BF16 / FP16) in one pass."""
     lib = load()
-    bl = nvfp4_kv_cold_block_layout(layout, extra_bytes)
+    bl = nvfp4_kv_cold_block_layout(layout, extra_bytes, rope)
     kp, ks = _paged_ptr(hot_k)
     vp, vs = _paged_ptr(hot_v)
     if ks != vs:
@@ -394,7 +416,8 @@ def nvfp4_kv_onboard_pages(layout: Layout, cold: torch.Tensor, hot_k: torch.Tens
     ep, es, eb = _extra_args(extra, extra_bytes)
     code = lib.nvfp4_kv_onboard_pages(
         ctypes.byref(layout), _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids),
-        _ptr(k_global_scale), _ptr(v_global_scale), _dtype_code(hot_k, hot_dtype), kp, vp, ks,
+        _ptr(k_global_scale), _ptr(v_global_scale), _rope_ref(rope),
+        _dtype_code(hot_k, hot_dtype), kp, vp, ks,
         hot_k.shape[0], _ids(hot_page_ids), ep, es, eb, int(num_pages), _ptr(status),
         _stream(stream))
     _check("nvfp4_kv_onboard_pages", code)

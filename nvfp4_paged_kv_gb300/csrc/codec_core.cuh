@@ -128,4 +128,31 @@ __device__ __forceinline__ void pick_scale(const float (&x)[16], float g, float 
     r = (sg == 0.0f) ? 0.0f : __frcp_rn(sg);
 }
 
+// E2M1 codes of fp32(x_i * r), round to nearest even, saturating, sign kept, packed two per byte
+// (value 2j in the low nibble of byte j).
+__device__ __forceinline__ uint2 pack_e2m1_block(const float (&x)[16], float r) {
+    uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w0 |= f32x2_to_e2m1x2(__fmul_rn(x[2 * j], r), __fmul_rn(x[2 * j + 1], r)) << (8 * j);
+        w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r)) << (8 * j);
+    }
+    return make_uint2(w0, w1);
+}
+
+// The 16 values e2m1(c_i) * e4m3(s) of one block (8 code bytes, scale byte), exact: the FP16
+// conversions are exact and the products have at most 6 significant bits.
+__device__ __forceinline__ void block_values(uint2 code, uint32_t sbyte, float (&v)[16]) {
+    const uint32_t s2 = e4m3x2_to_f16x2(sbyte * 0x0101u);
+    uint32_t h[8];
+    e2m1x8_to_f16x2x4(code.x, *reinterpret_cast<uint32_t(*)[4]>(h));
+    e2m1x8_to_f16x2x4(code.y, *reinterpret_cast<uint32_t(*)[4]>(h + 4));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t e = hmul2_u32(h[j], s2);
+        v[2 * j] = f16_lo(e);
+        v[2 * j + 1] = f16_hi(e);
+    }
+}
+
 }  // namespace nvfp4kv

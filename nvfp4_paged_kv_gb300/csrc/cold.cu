@@ -11,7 +11,11 @@
 // the same block encode (codec_core.cuh) and the same exact FP16 decode products.
 //
 // Work items: (page, tensor, chunk of kChunk blocks) for K and V, then (page, chunk of
-// kExtraChunk bytes) for the lossless part. A CTA takes items in a grid-stride loop.
+// kExtraChunk bytes) for the lossless part. A CTA takes items in a grid-stride loop. When the
+// RoPE part of K is kept apart (the same page, "The RoPE part of K": kept at 16 bits, or two
+// NVFP4 components of which the second encodes the first one's rounding error), K is cut into
+// items of whole token rows instead, a multiple of 16 rows, so that each of K's split scale
+// regions starts on a 16-byte boundary in every item.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -30,6 +34,10 @@ constexpr int kExtraChunk = kColdThreads * 16 * kExtraVecs;
 
 struct ColdParams {
     const uint8_t* hot[2];      // K and V hot pools (bytes); onboard writes through them
+    // RoPE part of K (rope_mode != 0): blocks [rb, rb + nbr) of each row of nb blocks
+    int32_t rope_mode, nb, rb, nbr, nbn, rows, rows_per_item, k_items;
+    uint64_t nb_magic;
+    int64_t off_rope, off_rope_s, off_rope2, off_rope2_s;
     int64_t hot_stride;         // bytes between consecutive hot pages
     int32_t hot_pool;
     const int32_t* hot_ids;
@@ -57,19 +65,177 @@ struct ItemPos {
     int32_t chunk;
 };
 
+// Items of a page: K (k_items), V (chunks), extra (extra_items).
 __device__ __forceinline__ ItemPos item_pos(const ColdParams& p, int64_t item) {
-    const int32_t per_page = 2 * p.chunks + p.extra_items;
+    const int32_t per_page = p.k_items + p.chunks + p.extra_items;
     ItemPos r;
     r.page = static_cast<int32_t>(item / per_page);
     const int32_t q = static_cast<int32_t>(item - static_cast<int64_t>(r.page) * per_page);
-    if (q < 2 * p.chunks) {
-        r.tensor = q >= p.chunks ? 1 : 0;
-        r.chunk = q - r.tensor * p.chunks;
+    if (q < p.k_items) {
+        r.tensor = 0;
+        r.chunk = q;
+    } else if (q < p.k_items + p.chunks) {
+        r.tensor = 1;
+        r.chunk = q - p.k_items;
     } else {
         r.tensor = 2;
-        r.chunk = q - 2 * p.chunks;
+        r.chunk = q - p.k_items - p.chunks;
     }
     return r;
+}
+
+// Copy n bytes of shared memory to dst (dst 16-byte aligned): 16-byte stores, then the tail.
+__device__ __forceinline__ void smem_to_global(uint8_t* dst, const uint8_t* s, int32_t n) {
+    const int32_t nv = n >> 4;
+    for (int32_t v = threadIdx.x; v < nv; v += kColdThreads)
+        *reinterpret_cast<uint4*>(dst + v * 16) = *reinterpret_cast<const uint4*>(s + v * 16);
+    for (int32_t j = nv * 16 + static_cast<int32_t>(threadIdx.x); j < n; j += kColdThreads)
+        dst[j] = s[j];
+}
+// The reverse (src 16-byte aligned).
+__device__ __forceinline__ void global_to_smem(uint8_t* s, const uint8_t* src, int32_t n) {
+    const int32_t nv = n >> 4;
+    for (int32_t v = threadIdx.x; v < nv; v += kColdThreads)
+        *reinterpret_cast<uint4*>(s + v * 16) = *reinterpret_cast<const uint4*>(src + v * 16);
+    for (int32_t j = nv * 16 + static_cast<int32_t>(threadIdx.x); j < n; j += kColdThreads)
+        s[j] = src[j];
+}
+
+// Where block col of a row goes: the other dims (index within the row's N/16 blocks) or the
+// RoPE dims (index within the row's R/16 blocks).
+__device__ __forceinline__ bool rope_col(const ColdParams& p, int32_t col, int32_t& idx) {
+    if (col >= p.rb && col < p.rb + p.nbr) {
+        idx = col - p.rb;
+        return true;
+    }
+    idx = col < p.rb ? col : col - p.nbr;
+    return false;
+}
+
+// Offload of one K item of whole rows when the RoPE part is kept apart (MODE 1: 16-bit copy,
+// MODE 2: two NVFP4 components).
+template <int SRC, int MODE>
+__device__ __forceinline__ void offload_k_rows(const ColdParams& p, uint8_t* blk_base,
+                                               const uint8_t* src, float g, int32_t chunk,
+                                               uint8_t* s_n, uint8_t* s_r1, uint8_t* s_r2) {
+    const float d = __fmul_rn(6.0f, g);
+    const int32_t row0 = chunk * p.rows_per_item;
+    const int32_t nrows = min(p.rows_per_item, p.rows - row0);
+    const int32_t nblk = nrows * p.nb;
+    uint8_t* const kd = blk_base + p.off_data[0] + static_cast<int64_t>(row0) * p.nbn * 8;
+    uint8_t* const kr = blk_base + p.off_rope +
+                        static_cast<int64_t>(row0) * p.nbr * (MODE == NVFP4KV_ROPE_SKIP ? 32 : 8);
+    uint8_t* const kr2 = blk_base + p.off_rope2 + static_cast<int64_t>(row0) * p.nbr * 8;
+    for (int32_t b = threadIdx.x; b < nblk; b += kColdThreads) {
+        const int32_t r = static_cast<int32_t>(fast_div(static_cast<uint32_t>(b), p.nb_magic));
+        const int32_t col = b - r * p.nb;
+        const int64_t sblk = static_cast<int64_t>(row0) * p.nb + b;
+        int32_t idx;
+        const bool rope = rope_col(p, col, idx);
+        if (rope && MODE == NVFP4KV_ROPE_SKIP) {
+            const uint8_t* a = src + sblk * 32;
+            const uint4 lo = ld_stream_16B(a), hi = ld_stream_16B(a + 16);
+            uint8_t* q = kr + static_cast<int64_t>(r * p.nbr + idx) * 32;
+            *reinterpret_cast<uint4*>(q) = lo;
+            *reinterpret_cast<uint4*>(q + 16) = hi;
+            continue;
+        }
+        float x[16];
+        widen<SRC>(load_raw<SRC, false>(src, sblk), 1.0f, x);
+        uint32_t sb;
+        float rcp;
+        pick_scale(x, g, d, sb, rcp);
+        const uint2 c1 = pack_e2m1_block(x, rcp);
+        if (!rope) {
+            const int32_t ni = r * p.nbn + idx;
+            *reinterpret_cast<uint2*>(kd + static_cast<int64_t>(ni) * 8) = c1;
+            s_n[ni] = static_cast<uint8_t>(sb);
+            continue;
+        }
+        if constexpr (MODE == NVFP4KV_ROPE_2FP4) {
+            // second component: the first one's rounding error r = fp32(x - fp32(v1 g))
+            float v1[16], res[16];
+            block_values(c1, sb, v1);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) res[k] = __fsub_rn(x[k], __fmul_rn(v1[k], g));
+            uint32_t sb2;
+            float rcp2;
+            pick_scale(res, g, d, sb2, rcp2);
+            const uint2 c2 = pack_e2m1_block(res, rcp2);
+            const int32_t ri = r * p.nbr + idx;
+            *reinterpret_cast<uint2*>(kr + static_cast<int64_t>(ri) * 8) = c1;
+            *reinterpret_cast<uint2*>(kr2 + static_cast<int64_t>(ri) * 8) = c2;
+            s_r1[ri] = static_cast<uint8_t>(sb);
+            s_r2[ri] = static_cast<uint8_t>(sb2);
+        }
+    }
+    __syncthreads();
+    smem_to_global(blk_base + p.off_scales[0] + static_cast<int64_t>(row0) * p.nbn, s_n,
+                   nrows * p.nbn);
+    if constexpr (MODE == NVFP4KV_ROPE_2FP4) {
+        smem_to_global(blk_base + p.off_rope_s + static_cast<int64_t>(row0) * p.nbr, s_r1,
+                       nrows * p.nbr);
+        smem_to_global(blk_base + p.off_rope2_s + static_cast<int64_t>(row0) * p.nbr, s_r2,
+                       nrows * p.nbr);
+    }
+    __syncthreads();
+}
+
+// Onboard of one K item of whole rows when the RoPE part is kept apart.
+template <int DST, int MODE>
+__device__ __forceinline__ void onboard_k_rows(const ColdParams& p, const uint8_t* blk_base,
+                                               uint8_t* dst, float g, int32_t chunk,
+                                               uint8_t* s_n, uint8_t* s_r1, uint8_t* s_r2) {
+    const int32_t row0 = chunk * p.rows_per_item;
+    const int32_t nrows = min(p.rows_per_item, p.rows - row0);
+    const int32_t nblk = nrows * p.nb;
+    global_to_smem(s_n, blk_base + p.off_scales[0] + static_cast<int64_t>(row0) * p.nbn,
+                   nrows * p.nbn);
+    if constexpr (MODE == NVFP4KV_ROPE_2FP4) {
+        global_to_smem(s_r1, blk_base + p.off_rope_s + static_cast<int64_t>(row0) * p.nbr,
+                       nrows * p.nbr);
+        global_to_smem(s_r2, blk_base + p.off_rope2_s + static_cast<int64_t>(row0) * p.nbr,
+                       nrows * p.nbr);
+    }
+    __syncthreads();
+    const uint8_t* const kd = blk_base + p.off_data[0] + static_cast<int64_t>(row0) * p.nbn * 8;
+    const uint8_t* const kr = blk_base + p.off_rope +
+                              static_cast<int64_t>(row0) * p.nbr * (MODE == NVFP4KV_ROPE_SKIP ? 32 : 8);
+    const uint8_t* const kr2 = blk_base + p.off_rope2 + static_cast<int64_t>(row0) * p.nbr * 8;
+    for (int32_t b = threadIdx.x; b < nblk; b += kColdThreads) {
+        const int32_t r = static_cast<int32_t>(fast_div(static_cast<uint32_t>(b), p.nb_magic));
+        const int32_t col = b - r * p.nb;
+        uint8_t* const q = dst + (static_cast<int64_t>(row0) * p.nb + b) * 32;
+        int32_t idx;
+        const bool rope = rope_col(p, col, idx);
+        float y[16];
+        if (!rope) {
+            const int32_t ni = r * p.nbn + idx;
+            block_values(*reinterpret_cast<const uint2*>(kd + static_cast<int64_t>(ni) * 8), s_n[ni], y);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) y[k] = __fmul_rn(y[k], g);
+        } else if constexpr (MODE == NVFP4KV_ROPE_SKIP) {
+            const uint8_t* a = kr + static_cast<int64_t>(r * p.nbr + idx) * 32;
+            *reinterpret_cast<uint4*>(q) = *reinterpret_cast<const uint4*>(a);
+            *reinterpret_cast<uint4*>(q + 16) = *reinterpret_cast<const uint4*>(a + 16);
+            continue;
+        } else {
+            const int32_t ri = r * p.nbr + idx;
+            float v2[16];
+            block_values(*reinterpret_cast<const uint2*>(kr + static_cast<int64_t>(ri) * 8), s_r1[ri], y);
+            block_values(*reinterpret_cast<const uint2*>(kr2 + static_cast<int64_t>(ri) * 8), s_r2[ri], v2);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) y[k] = __fadd_rn(__fmul_rn(y[k], g), __fmul_rn(v2[k], g));
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = (DST == NVFP4KV_BF16) ? pack_bf16x2(y[2 * j], y[2 * j + 1])
+                                         : pack_f16x2(y[2 * j], y[2 * j + 1]);
+        *reinterpret_cast<uint4*>(q) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(q + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    __syncthreads();
 }
 
 // Bounds of the item's page ids; false (and the status bit) when either is outside its pool.
@@ -99,13 +265,16 @@ __device__ __forceinline__ void copy_extra(const uint8_t* src, uint8_t* dst, int
     }
 }
 
-// Offload. SRC: NVFP4KV_BF16 or NVFP4KV_FP16.
-template <int SRC>
+// Offload. SRC: NVFP4KV_BF16 or NVFP4KV_FP16; MODE: how the RoPE part of K is kept.
+template <int SRC, int MODE>
 __global__ void __launch_bounds__(kColdThreads) cold_offload_kernel(const ColdParams p) {
     __shared__ __align__(16) uint8_t s_sc[kChunk];
+    __shared__ __align__(16) uint8_t s_r1[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
+    __shared__ __align__(16) uint8_t s_r2[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
     const float gk = p.g[0] ? __ldg(p.g[0]) : 1.0f;
     const float gv = p.g[1] ? __ldg(p.g[1]) : 1.0f;
-    const int64_t total = static_cast<int64_t>(p.num_pages) * (2 * p.chunks + p.extra_items);
+    const int64_t total =
+        static_cast<int64_t>(p.num_pages) * (p.k_items + p.chunks + p.extra_items);
     for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
         const ItemPos ip = item_pos(p, item);
         int32_t hp, cs;
@@ -121,6 +290,12 @@ __global__ void __launch_bounds__(kColdThreads) cold_offload_kernel(const ColdPa
         const float g = t ? gv : gk;
         const float d = __fmul_rn(6.0f, g);
         const uint8_t* src = p.hot[t] + static_cast<int64_t>(hp) * p.hot_stride;
+        if constexpr (MODE != NVFP4KV_ROPE_QUANTIZE) {
+            if (t == 0) {
+                offload_k_rows<SRC, MODE>(p, blk_base, src, g, ip.chunk, s_sc, s_r1, s_r2);
+                continue;
+            }
+        }
         const int32_t b0 = ip.chunk * kChunk;
         const int32_t n = min(kChunk, p.bpp - b0);
         U8x32 raw[kColdUnits];
@@ -163,12 +338,15 @@ __global__ void __launch_bounds__(kColdThreads) cold_offload_kernel(const ColdPa
 
 // Onboard. DST: NVFP4KV_BF16 or NVFP4KV_FP16. v = e2m1 * e4m3 is exact in FP16; the output is
 // the 16-bit rounding of fp32(v * g).
-template <int DST>
+template <int DST, int MODE>
 __global__ void __launch_bounds__(kColdThreads) cold_onboard_kernel(const ColdParams p) {
     __shared__ __align__(16) uint8_t s_sc[kChunk];
+    __shared__ __align__(16) uint8_t s_r1[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
+    __shared__ __align__(16) uint8_t s_r2[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
     const float gk = p.g[0] ? __ldg(p.g[0]) : 1.0f;
     const float gv = p.g[1] ? __ldg(p.g[1]) : 1.0f;
-    const int64_t total = static_cast<int64_t>(p.num_pages) * (2 * p.chunks + p.extra_items);
+    const int64_t total =
+        static_cast<int64_t>(p.num_pages) * (p.k_items + p.chunks + p.extra_items);
     for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
         const ItemPos ip = item_pos(p, item);
         int32_t hp, cs;
@@ -183,6 +361,14 @@ __global__ void __launch_bounds__(kColdThreads) cold_onboard_kernel(const ColdPa
         }
         const int t = ip.tensor;
         const float g = t ? gv : gk;
+        if constexpr (MODE != NVFP4KV_ROPE_QUANTIZE) {
+            if (t == 0) {
+                onboard_k_rows<DST, MODE>(
+                    p, blk_base, const_cast<uint8_t*>(p.hot[0]) + static_cast<int64_t>(hp) * p.hot_stride,
+                    g, ip.chunk, s_sc, s_r1, s_r2);
+                continue;
+            }
+        }
         const int32_t b0 = ip.chunk * kChunk;
         const int32_t n = min(kChunk, p.bpp - b0);
         const uint8_t* const data = blk_base + p.off_data[t] + static_cast<int64_t>(b0) * 8;
@@ -225,16 +411,43 @@ __global__ void __launch_bounds__(kColdThreads) cold_onboard_kernel(const ColdPa
 
 inline int64_t round16(int64_t x) { return (x + 15) & ~int64_t{15}; }
 
-bool cold_layout(const nvfp4kv_layout* l, int32_t extra_bytes, nvfp4kv_cold_block_layout* o) {
-    if (!layout_ok(l) || extra_bytes < 0 || (extra_bytes & 15)) return false;
-    const int64_t vals = static_cast<int64_t>(l->num_kv_heads) * l->page_size * l->head_dim;
-    const int64_t db = vals / 2, sb = vals / 16;
-    o->k_data = 0;
-    o->k_scales = round16(db);
-    o->v_data = o->k_scales + round16(sb);
-    o->v_scales = o->v_data + round16(db);
-    o->extra = o->v_scales + round16(sb);
-    o->bytes = o->extra + extra_bytes;
+// RoPE option: mode, first dim, dims; false if malformed.
+bool rope_ok(const nvfp4kv_layout* l, const nvfp4kv_cold_rope* r) {
+    if (!r || r->mode == NVFP4KV_ROPE_QUANTIZE) return true;
+    if (r->mode != NVFP4KV_ROPE_SKIP && r->mode != NVFP4KV_ROPE_2FP4) return false;
+    return r->first_dim >= 0 && r->dims > 0 && (r->first_dim % 16) == 0 && (r->dims % 16) == 0 &&
+           r->first_dim + r->dims <= l->head_dim && l->head_dim <= 2048;
+}
+
+bool cold_layout(const nvfp4kv_layout* l, const nvfp4kv_cold_rope* rope, int32_t extra_bytes,
+                 nvfp4kv_cold_block_layout* o) {
+    if (!layout_ok(l) || extra_bytes < 0 || (extra_bytes & 15) || !rope_ok(l, rope)) return false;
+    const int mode = rope ? rope->mode : NVFP4KV_ROPE_QUANTIZE;
+    const int64_t rows = static_cast<int64_t>(l->num_kv_heads) * l->page_size;
+    const int64_t vals = rows * l->head_dim;
+    const int64_t R = (mode == NVFP4KV_ROPE_QUANTIZE) ? 0 : rope->dims;
+    const int64_t kvals = rows * (l->head_dim - R), rvals = rows * R;
+    int64_t at = 0;
+    auto part = [&](int64_t bytes) {
+        const int64_t off = at;
+        at = round16(at + bytes);
+        return off;
+    };
+    o->k_data = part(kvals / 2);
+    o->k_scales = part(kvals / 16);
+    o->k_rope = o->k_rope_scales = o->k_rope2 = o->k_rope2_scales = -1;
+    if (mode == NVFP4KV_ROPE_SKIP) {
+        o->k_rope = part(rvals * 2);
+    } else if (mode == NVFP4KV_ROPE_2FP4) {
+        o->k_rope = part(rvals / 2);
+        o->k_rope_scales = part(rvals / 16);
+        o->k_rope2 = part(rvals / 2);
+        o->k_rope2_scales = part(rvals / 16);
+    }
+    o->v_data = part(vals / 2);
+    o->v_scales = part(vals / 16);
+    o->extra = at;
+    o->bytes = at + extra_bytes;
     return true;
 }
 
@@ -242,11 +455,12 @@ bool cold_layout(const nvfp4kv_layout* l, int32_t extra_bytes, nvfp4kv_cold_bloc
 nvfp4kv_status setup(ColdParams& p, const nvfp4kv_layout* layout, nvfp4kv_dtype hot_dtype,
                      const void* hot_k, const void* hot_v, int64_t hot_page_stride,
                      int32_t hot_pool_pages, const int32_t* hot_page_ids, const float* gk,
-                     const float* gv, const uint8_t* extra, int64_t extra_page_stride,
+                     const float* gv, const nvfp4kv_cold_rope* rope, const uint8_t* extra,
+                     int64_t extra_page_stride,
                      int32_t extra_bytes, const uint8_t* cold, int32_t cold_slots,
                      const int32_t* cold_slot_ids, int32_t num_pages, int32_t* status) {
     nvfp4kv_cold_block_layout bl;
-    if (!cold_layout(layout, extra_bytes, &bl) || num_pages < 0 || hot_pool_pages < 0 ||
+    if (!cold_layout(layout, rope, extra_bytes, &bl) || num_pages < 0 || hot_pool_pages < 0 ||
         cold_slots < 0)
         return NVFP4KV_ERR_INVALID_ARG;
     if (hot_dtype != NVFP4KV_BF16 && hot_dtype != NVFP4KV_FP16) return NVFP4KV_ERR_UNSUPPORTED;
@@ -284,6 +498,22 @@ nvfp4kv_status setup(ColdParams& p, const nvfp4kv_layout* layout, nvfp4kv_dtype 
     p.cold_ids = cold_slot_ids;
     p.bpp = static_cast<int32_t>(vals / 16);
     p.chunks = (p.bpp + kChunk - 1) / kChunk;
+    p.rope_mode = rope ? rope->mode : NVFP4KV_ROPE_QUANTIZE;
+    p.nb = layout->head_dim / 16;
+    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
+    p.rows = layout->num_kv_heads * layout->page_size;
+    p.k_items = p.chunks;
+    if (p.rope_mode != NVFP4KV_ROPE_QUANTIZE) {
+        p.rb = rope->first_dim / 16;
+        p.nbr = rope->dims / 16;
+        p.nbn = p.nb - p.nbr;
+        p.rows_per_item = max(16, (kChunk / p.nb) / 16 * 16);
+        p.k_items = (p.rows + p.rows_per_item - 1) / p.rows_per_item;
+        p.off_rope = bl.k_rope;
+        p.off_rope_s = bl.k_rope_scales;
+        p.off_rope2 = bl.k_rope2;
+        p.off_rope2_s = bl.k_rope2_scales;
+    }
     p.extra_items = (extra_bytes + kExtraChunk - 1) / kExtraChunk;
     p.num_pages = num_pages;
     p.status = status;
@@ -291,7 +521,8 @@ nvfp4kv_status setup(ColdParams& p, const nvfp4kv_layout* layout, nvfp4kv_dtype 
 }
 
 int cold_grid(const ColdParams& p) {
-    const int64_t items = static_cast<int64_t>(p.num_pages) * (2 * p.chunks + p.extra_items);
+    const int64_t items =
+        static_cast<int64_t>(p.num_pages) * (p.k_items + p.chunks + p.extra_items);
     const int64_t cap = static_cast<int64_t>(num_sms()) * 4;
     return static_cast<int>(items < cap ? (items < 1 ? 1 : items) : cap);
 }
@@ -302,50 +533,74 @@ int cold_grid(const ColdParams& p) {
 using namespace nvfp4kv;
 
 extern "C" nvfp4kv_status nvfp4_kv_cold_block_layout(const nvfp4kv_layout* layout,
+                                                     const nvfp4kv_cold_rope* rope,
                                                      int32_t extra_bytes,
                                                      nvfp4kv_cold_block_layout* out) {
     if (!out) return NVFP4KV_ERR_INVALID_ARG;
-    return cold_layout(layout, extra_bytes, out) ? NVFP4KV_OK : NVFP4KV_ERR_INVALID_ARG;
+    return cold_layout(layout, rope, extra_bytes, out) ? NVFP4KV_OK : NVFP4KV_ERR_INVALID_ARG;
 }
 
 extern "C" nvfp4kv_status nvfp4_kv_offload_pages(
     const nvfp4kv_layout* layout, nvfp4kv_dtype hot_dtype, const void* hot_k, const void* hot_v,
     int64_t hot_page_stride, int32_t hot_pool_pages, const int32_t* hot_page_ids,
-    const float* k_global_scale, const float* v_global_scale, const uint8_t* extra,
-    int64_t extra_page_stride, int32_t extra_bytes, uint8_t* cold, int32_t cold_slots,
-    const int32_t* cold_slot_ids, int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream) {
+    const float* k_global_scale, const float* v_global_scale, const nvfp4kv_cold_rope* rope,
+    const uint8_t* extra, int64_t extra_page_stride, int32_t extra_bytes, uint8_t* cold,
+    int32_t cold_slots, const int32_t* cold_slot_ids, int32_t num_pages, int32_t* status,
+    nvfp4kv_stream_t stream) {
     ColdParams p;
     const nvfp4kv_status st =
         setup(p, layout, hot_dtype, hot_k, hot_v, hot_page_stride, hot_pool_pages, hot_page_ids,
-              k_global_scale, v_global_scale, extra, extra_page_stride, extra_bytes, cold,
+              k_global_scale, v_global_scale, rope, extra, extra_page_stride, extra_bytes, cold,
               cold_slots, cold_slot_ids, num_pages, status);
     if (st != NVFP4KV_OK || num_pages == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = cold_grid(p);
+#define NVFP4KV_OFF(SRC)                                                                      \
+    do {                                                                                      \
+        if (p.rope_mode == NVFP4KV_ROPE_SKIP)                                                 \
+            cold_offload_kernel<SRC, NVFP4KV_ROPE_SKIP><<<grid, kColdThreads, 0, s>>>(p);     \
+        else if (p.rope_mode == NVFP4KV_ROPE_2FP4)                                            \
+            cold_offload_kernel<SRC, NVFP4KV_ROPE_2FP4><<<grid, kColdThreads, 0, s>>>(p);     \
+        else                                                                                  \
+            cold_offload_kernel<SRC, NVFP4KV_ROPE_QUANTIZE><<<grid, kColdThreads, 0, s>>>(p); \
+    } while (0)
     if (hot_dtype == NVFP4KV_BF16)
-        cold_offload_kernel<NVFP4KV_BF16><<<cold_grid(p), kColdThreads, 0, s>>>(p);
+        NVFP4KV_OFF(NVFP4KV_BF16);
     else
-        cold_offload_kernel<NVFP4KV_FP16><<<cold_grid(p), kColdThreads, 0, s>>>(p);
+        NVFP4KV_OFF(NVFP4KV_FP16);
+#undef NVFP4KV_OFF
     return launch_status();
 }
 
 extern "C" nvfp4kv_status nvfp4_kv_onboard_pages(
     const nvfp4kv_layout* layout, const uint8_t* cold, int32_t cold_slots,
     const int32_t* cold_slot_ids, const float* k_global_scale, const float* v_global_scale,
-    nvfp4kv_dtype hot_dtype, void* hot_k, void* hot_v, int64_t hot_page_stride,
-    int32_t hot_pool_pages, const int32_t* hot_page_ids, uint8_t* extra,
+    const nvfp4kv_cold_rope* rope, nvfp4kv_dtype hot_dtype, void* hot_k, void* hot_v,
+    int64_t hot_page_stride, int32_t hot_pool_pages, const int32_t* hot_page_ids, uint8_t* extra,
     int64_t extra_page_stride, int32_t extra_bytes, int32_t num_pages, int32_t* status,
     nvfp4kv_stream_t stream) {
     ColdParams p;
     const nvfp4kv_status st =
         setup(p, layout, hot_dtype, hot_k, hot_v, hot_page_stride, hot_pool_pages, hot_page_ids,
-              k_global_scale, v_global_scale, extra, extra_page_stride, extra_bytes, cold,
+              k_global_scale, v_global_scale, rope, extra, extra_page_stride, extra_bytes, cold,
               cold_slots, cold_slot_ids, num_pages, status);
     if (st != NVFP4KV_OK || num_pages == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = cold_grid(p);
+#define NVFP4KV_ON(DST)                                                                      \
+    do {                                                                                     \
+        if (p.rope_mode == NVFP4KV_ROPE_SKIP)                                                \
+            cold_onboard_kernel<DST, NVFP4KV_ROPE_SKIP><<<grid, kColdThreads, 0, s>>>(p);    \
+        else if (p.rope_mode == NVFP4KV_ROPE_2FP4)                                           \
+            cold_onboard_kernel<DST, NVFP4KV_ROPE_2FP4><<<grid, kColdThreads, 0, s>>>(p);    \
+        else                                                                                 \
+            cold_onboard_kernel<DST, NVFP4KV_ROPE_QUANTIZE><<<grid, kColdThreads, 0, s>>>(p); \
+    } while (0)
     if (hot_dtype == NVFP4KV_BF16)
-        cold_onboard_kernel<NVFP4KV_BF16><<<cold_grid(p), kColdThreads, 0, s>>>(p);
+        NVFP4KV_ON(NVFP4KV_BF16);
     else
-        cold_onboard_kernel<NVFP4KV_FP16><<<cold_grid(p), kColdThreads, 0, s>>>(p);
+        NVFP4KV_ON(NVFP4KV_FP16);
+#undef NVFP4KV_ON
     return launch_status();
 }
 

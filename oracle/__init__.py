@@ -67,6 +67,8 @@ def _load():
                 "orc_global_scale_from_amax": (d, [d]),
                 "orc_quantize_pages": (None, [i, i, i, i, i, p, p, d, d, p, p, p, i]),
                 "orc_cast_fp8_pages": (None, [i, i, i, i, p, p, d, d, p, p, i]),
+                "orc_encode_2fp4_blocks": (None, [i, i, p, d, p, p, p, p]),
+                "orc_decode_2fp4_blocks": (None, [i, p, p, p, p, d, i, p]),
                 "orc_dequantize_pages": (None, [i, i, i, i, p, p, p, d, i, p, p, d, i]),
                 "orc_paged_decode_attention": (None, [i, i, i, i, i, i, i, p, p, p, d, p, p, d,
                                                       p, i, p, d, p, p, p]),
@@ -292,77 +294,180 @@ def paged_decode_attention_bf16(q_bf16, k_bf16, v_bf16, page_table, seq_lens, sm
 # ------------------------------------------------------------------------------ cold pages
 # "KV Cache Compression in TensorRT LLM" (NVIDIA), "NVFP4 Cold-Page Compression": a cold page
 # is one fixed-size block per page holding the NVFP4 data, the block scales and the lossless
-# bytes (Figure 6); encode happens on the way out, decode on the way back (Figure 7). The block
-# order taken here: K codes (dim pairs), K scales, V codes, V scales, extra bytes, each part
-# starting at the previous part's end rounded up to 16 bytes.
+# bytes (Figure 6); encode happens on the way out, decode on the way back (Figure 7); the
+# position-encoded (RoPE) part of K may be quantized like the rest, kept at its original
+# precision, or stored as two FP4 components ("The RoPE part of K"). The block order taken
+# here: K codes of the other head dims (dim pairs), their scales, the RoPE part (SKIP: the
+# 16-bit values; 2FP4: codes and scales of the first, then of the second component), V codes,
+# V scales, extra bytes, each part starting at the previous part's end rounded up to 16 bytes.
 
-def cold_block_layout(H, D, T, extra_bytes=0):
-    """Byte offsets of the parts of one cold block and its size."""
+ROPE_QUANTIZE, ROPE_SKIP, ROPE_2FP4 = 0, 1, 2
+
+
+def encode_2fp4_blocks(x_bits, dtype, g):
+    """Two-component encoding (R10 of nvfp4_oracle.c) of blocks of 16 consecutive 16-bit
+    values: (codes1 [n, 8], scales1 [n], codes2 [n, 8], scales2 [n])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1)
+    n = x.size // 16
+    c1 = np.zeros((n, 8), np.uint8)
+    c2 = np.zeros((n, 8), np.uint8)
+    s1 = np.zeros(n, np.uint8)
+    s2 = np.zeros(n, np.uint8)
+    _load().orc_encode_2fp4_blocks(n, int(dtype), _ptr(x), float(g), _ptr(c1), _ptr(s1),
+                                   _ptr(c2), _ptr(s2))
+    return c1, s1, c2, s2
+
+
+def decode_2fp4_blocks(c1, s1, c2, s2, g, out_dtype=BF16):
+    """16-bit patterns [n, 16] of two-component blocks (R10)."""
+    c1, c2 = (np.ascontiguousarray(a, dtype=np.uint8) for a in (c1, c2))
+    s1, s2 = (np.ascontiguousarray(a, dtype=np.uint8) for a in (s1, s2))
+    n = s1.size
+    out = np.zeros((n, 16), np.uint16)
+    _load().orc_decode_2fp4_blocks(n, _ptr(c1), _ptr(s1), _ptr(c2), _ptr(s2), float(g),
+                                   int(out_dtype), _ptr(out))
+    return out
+
+
+def cold_block_layout(H, D, T, extra_bytes=0, rope=None):
+    """Byte offsets of the parts of one cold block and its size; rope = (mode, first_dim,
+    dims) or None (quantized like the rest). Parts a mode does not use are -1."""
     def up16(x):
         return (x + 15) // 16 * 16
-    n = H * T * D
-    off = {"k_data": 0}
-    off["k_scales"] = up16(n // 2)
-    off["v_data"] = off["k_scales"] + up16(n // 16)
-    off["v_scales"] = off["v_data"] + up16(n // 2)
-    off["extra"] = off["v_scales"] + up16(n // 16)
-    off["bytes"] = off["extra"] + int(extra_bytes)
+    mode = ROPE_QUANTIZE if rope is None else rope[0]
+    R = 0 if mode == ROPE_QUANTIZE else rope[2]
+    rows = H * T
+    off = {}
+    at = 0
+
+    def part(name, nbytes):
+        nonlocal at
+        off[name] = at
+        at = up16(at + nbytes)
+    part("k_data", rows * (D - R) // 2)
+    part("k_scales", rows * (D - R) // 16)
+    for name in ("k_rope", "k_rope_scales", "k_rope2", "k_rope2_scales"):
+        off[name] = -1
+    if mode == ROPE_SKIP:
+        part("k_rope", rows * R * 2)
+    elif mode == ROPE_2FP4:
+        part("k_rope", rows * R // 2)
+        part("k_rope_scales", rows * R // 16)
+        part("k_rope2", rows * R // 2)
+        part("k_rope2_scales", rows * R // 16)
+    part("v_data", rows * D // 2)
+    part("v_scales", rows * D // 16)
+    off["extra"] = at
+    off["bytes"] = at + int(extra_bytes)
     return off
 
 
+def _rope_cols(D, rope):
+    """(other head dims, RoPE head dims) of a K vector."""
+    mode = ROPE_QUANTIZE if rope is None else rope[0]
+    if mode == ROPE_QUANTIZE:
+        return np.arange(D), np.arange(0)
+    rc = np.arange(rope[1], rope[1] + rope[2])
+    return np.setdiff1d(np.arange(D), rc), rc
+
+
 def cold_offload(k, v, dtype, H, D, T, g_k, g_v, num_slots, hot_page_ids=None,
-                 cold_slot_ids=None, extra=None, extra_bytes=0, num_pages=None):
+                 cold_slot_ids=None, extra=None, extra_bytes=0, num_pages=None, rope=None):
     """Cold blocks [num_slots, bytes] (uint8, zero where nothing is written) of hot pages
-    hot_page_ids[i] -> slots cold_slot_ids[i]: the K and V pages encoded exactly as
-    quantize_pages (dim pairs) with g_k / g_v, placed by cold_block_layout, and
-    extra[hot page, :extra_bytes] copied unchanged."""
-    lay = cold_block_layout(H, D, T, extra_bytes)
+    hot_page_ids[i] -> slots cold_slot_ids[i]: K's other dims and V encoded exactly as
+    quantize_pages (dim pairs) with g_k / g_v, the RoPE part of K as `rope` says, placed by
+    cold_block_layout, and extra[hot page, :extra_bytes] copied unchanged."""
+    lay = cold_block_layout(H, D, T, extra_bytes, rope)
     hids = _ids(hot_page_ids)
     sids = _ids(cold_slot_ids)
     if num_pages is None:
         num_pages = len(hids) if hids is not None else k.size // (H * T * D)
-    kd, ks = quantize_pages(k, dtype, H, D, T, g_k, src_page_ids=hids, num_pages=num_pages)
+    k = np.ascontiguousarray(k, dtype=np.uint16).reshape(-1, H, T, D)
+    hot = hids if hids is not None else np.arange(num_pages, dtype=np.int32)
+    kp = k[hot[:num_pages]]                               # [n, H, T, D] in batch order
+    oc, rc = _rope_cols(D, rope)
+    mode = ROPE_QUANTIZE if rope is None else rope[0]
+    N, R = oc.size, rc.size
+    if N:
+        kd, ks = quantize_pages(np.ascontiguousarray(kp[..., oc]), dtype, H, N, T, g_k)
     vd, vs = quantize_pages(v, dtype, H, D, T, g_v, src_page_ids=hids, num_pages=num_pages)
-    n = H * T * D
+    if mode == ROPE_2FP4:
+        r1, rs1, r2, rs2 = encode_2fp4_blocks(np.ascontiguousarray(kp[..., rc]), dtype, g_k)
+        per = H * T * R // 16
+    rows = H * T
     blocks = np.zeros((num_slots, lay["bytes"]), dtype=np.uint8)
+
+    def put(b, name, arr):
+        a = np.ascontiguousarray(arr).view(np.uint8).reshape(-1)
+        b[lay[name]:lay[name] + a.size] = a
     for i in range(num_pages):
         s = int(sids[i]) if sids is not None else i
-        hp = int(hids[i]) if hids is not None else i
+        hp = int(hot[i])
         b = blocks[s]
-        b[lay["k_data"]:lay["k_data"] + n // 2] = kd[i].reshape(-1)
-        b[lay["k_scales"]:lay["k_scales"] + n // 16] = ks[i].reshape(-1)
-        b[lay["v_data"]:lay["v_data"] + n // 2] = vd[i].reshape(-1)
-        b[lay["v_scales"]:lay["v_scales"] + n // 16] = vs[i].reshape(-1)
+        if N:
+            put(b, "k_data", kd[i])
+            put(b, "k_scales", ks[i])
+        if mode == ROPE_SKIP:
+            put(b, "k_rope", kp[i][..., rc].reshape(rows, R))
+        elif mode == ROPE_2FP4:
+            put(b, "k_rope", r1[i * per:(i + 1) * per])
+            put(b, "k_rope_scales", rs1[i * per:(i + 1) * per])
+            put(b, "k_rope2", r2[i * per:(i + 1) * per])
+            put(b, "k_rope2_scales", rs2[i * per:(i + 1) * per])
+        put(b, "v_data", vd[i])
+        put(b, "v_scales", vs[i])
         if extra_bytes:
             b[lay["extra"]:lay["extra"] + extra_bytes] = extra[hp, :extra_bytes]
     return blocks
 
 
 def cold_onboard(blocks, H, D, T, g_k, g_v, out_dtype, num_hot_pages, cold_slot_ids=None,
-                 hot_page_ids=None, extra_bytes=0, num_pages=None):
+                 hot_page_ids=None, extra_bytes=0, num_pages=None, rope=None):
     """(k, v, extra) hot pools [num_hot_pages, H, T, D] (16-bit patterns) and
     [num_hot_pages, extra_bytes] written from cold slots cold_slot_ids[i] into hot pages
-    hot_page_ids[i]: the block's K and V parts decoded exactly as dequantize_pages."""
-    lay = cold_block_layout(H, D, T, extra_bytes)
+    hot_page_ids[i]: the block's NVFP4 parts decoded exactly as dequantize_pages, the RoPE part
+    of K copied back (SKIP) or decoded as two components (2FP4)."""
+    lay = cold_block_layout(H, D, T, extra_bytes, rope)
     sids = _ids(cold_slot_ids)
     hids = _ids(hot_page_ids)
     if num_pages is None:
         num_pages = len(sids) if sids is not None else blocks.shape[0]
-    n = H * T * D
+    oc, rc = _rope_cols(D, rope)
+    mode = ROPE_QUANTIZE if rope is None else rope[0]
+    N, R = oc.size, rc.size
+    rows = H * T
     slot = [int(sids[i]) if sids is not None else i for i in range(num_pages)]
-    part = lambda name, size, shape: np.stack(  # noqa: E731
-        [blocks[s, lay[name]:lay[name] + size].reshape(shape) for s in slot]) if slot else \
-        np.zeros((0,) + shape, np.uint8)
-    kd = part("k_data", n // 2, (H, T, D // 2))
-    ks = part("k_scales", n // 16, (H, T, D // 16))
-    vd = part("v_data", n // 2, (H, T, D // 2))
-    vs = part("v_scales", n // 16, (H, T, D // 16))
-    k = dequantize_pages(kd, ks, H, D, T, g_k, out_dtype, num_dst_pages=num_hot_pages,
-                         dst_page_ids=hids, num_pages=num_pages)
+    hot = [int(hids[i]) if hids is not None else i for i in range(num_pages)]
+
+    def part(name, size, shape, dt=np.uint8):
+        if not slot:
+            return np.zeros((0,) + shape, dt)
+        return np.stack([blocks[s, lay[name]:lay[name] + size].view(dt).reshape(shape)
+                         for s in slot])
+    k = np.zeros((num_hot_pages, H, T, D), np.uint16)
+    if N:
+        kd = part("k_data", rows * N // 2, (H, T, N // 2))
+        ks = part("k_scales", rows * N // 16, (H, T, N // 16))
+        kn = dequantize_pages(kd, ks, H, N, T, g_k, out_dtype, num_pages=num_pages)
+        for i in range(num_pages):
+            k[hot[i]][..., oc] = kn[i]
+    if mode == ROPE_SKIP:
+        kr = part("k_rope", rows * R * 2, (H, T, R), np.uint16)
+        for i in range(num_pages):
+            k[hot[i]][..., rc] = kr[i]
+    elif mode == ROPE_2FP4:
+        nb = rows * R // 16
+        for i, s in enumerate(slot):
+            g = lambda name, sz: blocks[s, lay[name]:lay[name] + sz]  # noqa: E731
+            y = decode_2fp4_blocks(g("k_rope", nb * 8).reshape(nb, 8), g("k_rope_scales", nb),
+                                   g("k_rope2", nb * 8).reshape(nb, 8), g("k_rope2_scales", nb),
+                                   g_k, out_dtype)
+            k[hot[i]][..., rc] = y.reshape(H, T, R)
+    vd = part("v_data", rows * D // 2, (H, T, D // 2))
+    vs = part("v_scales", rows * D // 16, (H, T, D // 16))
     v = dequantize_pages(vd, vs, H, D, T, g_v, out_dtype, num_dst_pages=num_hot_pages,
                          dst_page_ids=hids, num_pages=num_pages)
     ex = np.zeros((num_hot_pages, extra_bytes), dtype=np.uint8)
     for i, s in enumerate(slot):
-        hp = int(hids[i]) if hids is not None else i
-        ex[hp] = blocks[s, lay["extra"]:lay["extra"] + extra_bytes]
+        ex[hot[i]] = blocks[s, lay["extra"]:lay["extra"] + extra_bytes]
     return k, v, ex

@@ -38,6 +38,10 @@
  *   R6 decode: v = e2m1(c) * e4m3(s) (exact), then fp32(v * g), then the output rounding.
  *   R7 global scale: g = fp32(amax_tensor / 2688) (2688 = 448 * 6); g = 1 if that is 0.
  *   R8 FP8 output: E4M3_rne_satfinite(fp32(v * fp32(g / out_scale))), sign kept.
+ *   R10 two-component (2FP4) encoding of the RoPE part of K in a cold page: c1 = the encoding
+ *      of x (R4, R5); with v1 = e2m1(c1) * e4m3(s1), the residual r = fp32(x - fp32(v1 g)) is
+ *      encoded the same way with the same g into c2; decode = fp32(fp32(v1 g) + fp32(v2 g)),
+ *      then the 16-bit rounding.
  *   R9 FP8 workspace copy of a chunk (extend path): E4M3_rne_satfinite(fp32(x * m)),
  *      m = fp32(1 / ws_scale), sign kept; pages keep the plain [page][head][token][dim] order.
  *
@@ -426,6 +430,55 @@ void orc_cast_fp8_pages(int H, int D, int T, int src_dtype, const void* src,
             dst[dp * page_elems + e] = e4m3_encode(fp32(x * m));
         }
     }
+}
+
+/*
+ * Two-component encoding of n_blocks blocks of 16 consecutive 16-bit source values. R10.
+ * [TRTLLM "The RoPE part of K"]: the RoPE part can be stored as two FP4 components, the
+ * second holding the first one's rounding error. Codes are packed two per byte, value 2j of a
+ * block in the low nibble of byte j (8 bytes per block); one scale byte per block.
+ */
+void orc_encode_2fp4_blocks(int n_blocks, int src_dtype, const void* src, double g,
+                            uint8_t* codes1, uint8_t* scales1, uint8_t* codes2, uint8_t* scales2)
+{
+    g = fp32(g);
+    for (int blk = 0; blk < n_blocks; ++blk) {
+        double x[16], r[16];
+        int c1[16], c2[16];
+        uint8_t s1, s2;
+        for (int k = 0; k < 16; ++k)
+            x[k] = load_src(src_dtype, src, (size_t)blk * 16 + k, 1.0);
+        encode_block(x, g, c1, &s1);
+        for (int k = 0; k < 16; ++k) {
+            double v1 = e2m1_value(c1[k]) * e4m3_value(s1); /* exact */
+            r[k] = fp32(x[k] - fp32(v1 * g));
+        }
+        encode_block(r, g, c2, &s2);
+        for (int j = 0; j < 8; ++j) {
+            codes1[(size_t)blk * 8 + j] = (uint8_t)(c1[2 * j] | (c1[2 * j + 1] << 4));
+            codes2[(size_t)blk * 8 + j] = (uint8_t)(c2[2 * j] | (c2[2 * j + 1] << 4));
+        }
+        scales1[blk] = s1;
+        scales2[blk] = s2;
+    }
+}
+
+/* Decode of the two-component blocks into 16-bit bit patterns (ORC_BF16 / ORC_FP16). R10. */
+void orc_decode_2fp4_blocks(int n_blocks, const uint8_t* codes1, const uint8_t* scales1,
+                            const uint8_t* codes2, const uint8_t* scales2, double g,
+                            int out_dtype, uint16_t* out)
+{
+    g = fp32(g);
+    for (int blk = 0; blk < n_blocks; ++blk)
+        for (int k = 0; k < 16; ++k) {
+            uint8_t b1 = codes1[(size_t)blk * 8 + k / 2], b2 = codes2[(size_t)blk * 8 + k / 2];
+            int c1 = (k & 1) ? (b1 >> 4) : (b1 & 15), c2 = (k & 1) ? (b2 >> 4) : (b2 & 15);
+            double v1 = e2m1_value(c1) * e4m3_value(scales1[blk]);
+            double v2 = e2m1_value(c2) * e4m3_value(scales2[blk]);
+            double y = fp32(fp32(v1 * g) + fp32(v2 * g));
+            out[(size_t)blk * 16 + k] = (out_dtype == ORC_BF16) ? bf16_bits(bf16_round(y))
+                                                                  : fp16_bits(fp16_round(y));
+        }
 }
 
 /*

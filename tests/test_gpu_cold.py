@@ -158,3 +158,50 @@ def test_cold_codec_rejects_bad_arguments(kv, cuda):
     cold = torch.zeros((2, bl.bytes), dtype=torch.uint8, device=cuda)
     with pytest.raises(kv.NVFP4KVError):  # FP8 hot pool
         kv.nvfp4_kv_offload_pages(lay, k, k, cold, hot_dtype=kv.FP8_E4M3)
+
+
+# (H, T, D, first_dim, dims): RoPE dims in the middle, two row items with a ragged second, the
+# whole head, a three-row page
+ROPE_CASES = [(2, 16, 128, 64, 64), (4, 64, 144, 16, 32), (2, 8, 64, 0, 64), (1, 3, 80, 32, 16)]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("case", ROPE_CASES)
+@pytest.mark.parametrize("kind", ["bf16", "fp16"])
+def test_rope_modes_parity(kv, cuda, mode, case, kind):
+    """The RoPE part of K kept at 16 bits (SKIP) or as two NVFP4 components (2FP4): cold blocks
+    byte for byte and onboarded pages bit for bit against the oracle, through pinned host
+    memory, scattered pages and slots."""
+    H, T, D, first, dims = case
+    P, slots, n = 7, 9, 5
+    k = _pages(kind, P, H, T, D, seed=90).to(cuda)
+    v = _pages(kind, P, H, T, D, seed=91).to(cuda)
+    odt = oracle.BF16 if kind == "bf16" else oracle.FP16
+    g_k = oracle.global_scale(_bits(k), odt, H, D, T)
+    g_v = oracle.global_scale(_bits(v), odt, H, D, T)
+    rng = np.random.default_rng(5)
+    hot = rng.permutation(P)[:n].astype(np.int32)
+    slot = rng.permutation(slots)[:n].astype(np.int32)
+    lay = kv.Layout(H, D, T)
+    rope = kv.ColdRope(mode, first, dims)
+    bl = kv.nvfp4_kv_cold_block_layout(lay, 0, rope)
+    cold = torch.zeros((slots, bl.bytes), dtype=torch.uint8).pin_memory()
+    t = lambda a: torch.from_numpy(a).to(cuda)  # noqa: E731
+    gk, gv = _scalar(g_k, cuda), _scalar(g_v, cuda)
+    kv.nvfp4_kv_offload_pages(lay, k, v, cold, k_global_scale=gk, v_global_scale=gv,
+                              hot_page_ids=t(hot), cold_slot_ids=t(slot), rope=rope)
+    torch.cuda.synchronize()
+    want = oracle.cold_offload(_bits(k), _bits(v), odt, H, D, T, g_k, g_v, slots,
+                               hot_page_ids=hot, cold_slot_ids=slot, rope=(mode, first, dims))
+    assert np.array_equal(cold.numpy(), want)
+    k2, v2 = torch.zeros_like(k), torch.zeros_like(v)
+    kv.nvfp4_kv_onboard_pages(lay, cold, k2, v2, k_global_scale=gk, v_global_scale=gv,
+                              cold_slot_ids=t(slot), hot_page_ids=t(hot), rope=rope)
+    torch.cuda.synchronize()
+    wk, wv, _ = oracle.cold_onboard(want, H, D, T, g_k, g_v, odt, P, cold_slot_ids=slot,
+                                    hot_page_ids=hot, rope=(mode, first, dims))
+    assert np.array_equal(_bits(k2), wk)
+    assert np.array_equal(_bits(v2), wv)
+    if mode == 1:
+        rc = slice(first, first + dims)
+        assert torch.equal(k2[t(hot).long()][..., rc], k[t(hot).long()][..., rc])

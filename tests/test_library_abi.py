@@ -96,24 +96,28 @@ def test_host_validation_rejects_bad_arguments(lib):
     off = lib.nvfp4_kv_offload_pages
     hot_stride = 8 * 64 * 128
     # FP8 hot pool: unsupported; null cold pool; misaligned hot pool; page stride below a page;
-    # extra bytes without an extra pointer; zero pages is a no-op
-    assert off(ctypes.byref(good), 2, fake, fake, hot_stride, 1, None, None, None, None, 0, 0,
-               fake, 1, None, 1, None, None) == 2
-    assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None, None, 0, 0,
-               None, 1, None, 1, None, None) == 1
-    assert off(ctypes.byref(good), 0, mis, fake, hot_stride, 1, None, None, None, None, 0, 0,
-               fake, 1, None, 1, None, None) == 1
-    assert off(ctypes.byref(good), 0, fake, fake, hot_stride - 8, 1, None, None, None, None, 0,
+    # extra bytes without an extra pointer; a malformed RoPE option; zero pages is a no-op
+    assert off(ctypes.byref(good), 2, fake, fake, hot_stride, 1, None, None, None, None, None, 0,
+               0, fake, 1, None, 1, None, None) == 2
+    assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None, None, None, 0,
+               0, None, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, mis, fake, hot_stride, 1, None, None, None, None, None, 0,
                0, fake, 1, None, 1, None, None) == 1
-    assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None, None, 16, 16,
-               fake, 1, None, 1, None, None) == 1
-    assert off(ctypes.byref(good), 0, None, None, 0, 0, None, None, None, None, 0, 0, None, 0,
-               None, 0, None, None) == 0
+    assert off(ctypes.byref(good), 0, fake, fake, hot_stride - 8, 1, None, None, None, None,
+               None, 0, 0, fake, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None, None, None,
+               16, 16, fake, 1, None, 1, None, None) == 1
+    for bad in (kv.ColdRope(kv.ROPE_SKIP, 8, 64), kv.ColdRope(kv.ROPE_2FP4, 96, 64),
+                kv.ColdRope(kv.ROPE_SKIP, 0, 0), kv.ColdRope(7, 0, 16)):
+        assert off(ctypes.byref(good), 0, fake, fake, hot_stride, 1, None, None, None,
+                   ctypes.byref(bad), None, 0, 0, fake, 1, None, 1, None, None) == 1
+    assert off(ctypes.byref(good), 0, None, None, 0, 0, None, None, None, None, None, 0, 0,
+               None, 0, None, 0, None, None) == 0
     on = lib.nvfp4_kv_onboard_pages
-    assert on(ctypes.byref(good), None, 1, None, None, None, 0, fake, fake, hot_stride, 1, None,
-              None, 0, 0, 1, None, None) == 1
-    assert on(ctypes.byref(good), fake, 1, None, None, None, 2, fake, fake, hot_stride, 1, None,
-              None, 0, 0, 1, None, None) == 2
+    assert on(ctypes.byref(good), None, 1, None, None, None, None, 0, fake, fake, hot_stride, 1,
+              None, None, 0, 0, 1, None, None) == 1
+    assert on(ctypes.byref(good), fake, 1, None, None, None, None, 2, fake, fake, hot_stride, 1,
+              None, None, 0, 0, 1, None, None) == 2
     att = lib.nvfp4_paged_decode_attention
     args = [ctypes.byref(good), 2, 32, fake, fake, fake, fake, fake, fake, fake, 10, fake, 4,
             fake, 0.1, 0, fake, 1 << 20, fake, None, None, None]
@@ -147,18 +151,25 @@ def test_workspace_sizes(lib):
 
 def test_cold_block_layout_matches_its_definition(lib):
     """The library's cold block offsets equal the oracle's, written from the same definition
-    (K codes, K scales, V codes, V scales, extra, each part at the previous end rounded up
-    to 16), including shapes that need padding; a bad extra size is rejected."""
+    (K codes, K scales, the RoPE part as its mode keeps it, V codes, V scales, extra, each part
+    at the previous end rounded up to 16), including shapes that need padding; a bad extra size
+    or RoPE option is rejected."""
     import nvfp4_paged_kv_gb300 as kv
     import oracle
-    fields = ("k_data", "k_scales", "v_data", "v_scales", "extra", "bytes")
+    fields = ("k_data", "k_scales", "k_rope", "k_rope_scales", "k_rope2", "k_rope2_scales",
+              "v_data", "v_scales", "extra", "bytes")
     for H, D, T, extra in ((8, 128, 32, 0), (8, 128, 64, 4096), (1, 16, 1, 32), (3, 80, 5, 16)):
-        bl = kv.nvfp4_kv_cold_block_layout(kv.Layout(H, D, T), extra)
-        ref = oracle.cold_block_layout(H, D, T, extra)
-        assert [getattr(bl, f) for f in fields] == [ref[f] for f in fields]
+        for rope in (None, (kv.ROPE_SKIP, 0, 16), (kv.ROPE_2FP4, D - 16, 16),
+                     (kv.ROPE_2FP4, 0, D), (kv.ROPE_QUANTIZE, 0, 0)):
+            cr = None if rope is None else kv.ColdRope(*rope)
+            bl = kv.nvfp4_kv_cold_block_layout(kv.Layout(H, D, T), extra, cr)
+            ref = oracle.cold_block_layout(H, D, T, extra, rope)
+            assert [getattr(bl, f) for f in fields] == [ref[f] for f in fields], (H, D, T, rope)
     out = kv.ColdBlockLayout()
-    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 128, 32)), 8,
+    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 128, 32)), None, 8,
                                           ctypes.byref(out)) == 1
-    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 120, 32)), 0,
+    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 120, 32)), None, 0,
                                           ctypes.byref(out)) == 1
-
+    bad = kv.ColdRope(kv.ROPE_SKIP, 120, 16)
+    assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 128, 32)),
+                                          ctypes.byref(bad), 0, ctypes.byref(out)) == 1

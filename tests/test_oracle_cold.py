@@ -112,3 +112,107 @@ def test_cold_offload_leaves_other_slots_untouched():
                                hot_page_ids=[2, 0], cold_slot_ids=[3, 0])
     assert not some[1].any() and not some[2].any()
     assert np.array_equal(some[3], all_blocks[2]) and np.array_equal(some[0], all_blocks[0])
+
+
+# ---------------------------------------------------------------- the RoPE part of K
+
+def _codes_values(codes, scales):
+    """Exact block values e2m1(c) * e4m3(s) of packed codes [n, 8] and scales [n]: [n, 16]."""
+    lo = (codes & 15).astype(int)
+    hi = (codes >> 4).astype(int)
+    c = np.stack([lo, hi], axis=-1).reshape(codes.shape[0], 16)
+    e = np.vectorize(oracle.e2m1_value)(c)
+    s = np.vectorize(oracle.e4m3_value)(scales.astype(int))
+    return e * s[:, None]
+
+
+def _f32(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def test_2fp4_is_exact_on_the_grid():
+    """Blocks s * (E2M1 grid) with g = 1: the first component is exact, so the residual is 0,
+    the second component is all +0 codes with scale 0, and decoding returns x (a -0 comes back
+    as +0: the decode sums -0 and +0)."""
+    rng = np.random.default_rng(21)
+    bits, x = _grid_pages(rng, 2, 1, 4, 32)
+    c1, s1, c2, s2 = oracle.encode_2fp4_blocks(bits, oracle.BF16, 1.0)
+    assert not c2.any() and not s2.any()
+    y = oracle.decode_2fp4_blocks(c1, s1, c2, s2, 1.0, oracle.BF16)
+    plus_zero = np.where(bits == 0x8000, 0, bits)
+    assert np.array_equal(y.reshape(-1), plus_zero.reshape(-1))
+    assert np.array_equal(_codes_values(c1, s1).reshape(-1), x.reshape(-1))
+
+
+@pytest.mark.parametrize("g", [1.0, 0.0123])
+def test_2fp4_second_component_encodes_the_first_ones_error(g):
+    """Random BF16 blocks: the residual is r = fp32(x - fp32(v1 g)); the second component is the
+    plain encoding of r (scale E4M3(amax(r) / fp32(6 g)), each code the nearest E2M1 value of
+    fp32(r / fp32(s2 g)) by brute force), and the two-component value is never farther from x
+    than the first component alone (0 is on the E2M1 grid)."""
+    rng = np.random.default_rng(22)
+    x = (rng.standard_normal((64, 16)) * rng.choice([1e-2, 1.0, 40.0], (64, 1))).astype(np.float32)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)          # truncate to BF16
+    xv = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    c1, s1, c2, s2 = oracle.encode_2fp4_blocks(bits, oracle.BF16, g)
+    gf = float(np.float32(g))
+    y1 = _f32(_codes_values(c1, s1) * gf)
+    r = _f32(xv - y1)
+    d = float(np.float32(6.0 * gf))
+    grid = [oracle.e2m1_value(c) for c in range(16)]
+    for b in range(64):
+        s_expect = oracle.e4m3_encode(float(np.float32(np.abs(r[b]).max() / d)))
+        assert s2[b] == s_expect
+        sg = float(np.float32(oracle.e4m3_value(int(s2[b])) * gf))
+        rcp = 0.0 if sg == 0.0 else float(np.float32(1.0 / sg))
+        for k in range(16):
+            q = float(np.float32(r[b, k] * rcp))
+            code = (c2[b, k // 2] >> (4 * (k & 1))) & 15
+            best = min(abs(q - e) for e in grid[:8]) if q >= 0 else min(abs(q - e) for e in grid[8:])
+            assert abs(q - grid[code]) == best or abs(q) > 6
+    y2 = _f32(y1 + _f32(_codes_values(c2, s2) * gf))
+    assert np.all(np.abs(xv - y2) <= np.abs(xv - y1) * (1 + 2 ** -20) + 1e-30)
+    assert np.abs(xv - y2).mean() < 0.25 * np.abs(xv - y1).mean()
+
+
+def test_skip_rope_block_bytes_by_hand():
+    """SKIP keeps the RoPE dims as 16-bit values at k_rope + (row R + d - first) * 2: a page that
+    is zero except one BF16 value 1.5 (0x3FC0) at (head 1, token 3, dim first + 5) shows exactly
+    there; the other dims' codes and scales are all zero."""
+    H, T, D, first, R = 2, 4, 64, 32, 16
+    k = np.zeros((1, H, T, D), np.uint16)
+    v = np.zeros((1, H, T, D), np.uint16)
+    k[0, 1, 3, first + 5] = 0x3FC0
+    rope = (oracle.ROPE_SKIP, first, R)
+    blocks = oracle.cold_offload(k, v, oracle.BF16, H, D, T, 1.0, 1.0, 1, rope=rope)
+    lay = oracle.cold_block_layout(H, D, T, 0, rope)
+    want = np.zeros(lay["bytes"], np.uint8)
+    off = lay["k_rope"] + ((1 * T + 3) * R + 5) * 2
+    want[off], want[off + 1] = 0xC0, 0x3F
+    assert np.array_equal(blocks[0], want)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_rope_round_trip(mode):
+    """SKIP returns the RoPE dims bit for bit; 2FP4 returns decode_2fp4 of them; the other dims
+    are what a plain NVFP4 round trip of those dims gives, whatever the RoPE mode."""
+    rng = np.random.default_rng(23)
+    P, H, T, D, first, R = 3, 2, 8, 64, 16, 32
+    k = (rng.standard_normal((P, H, T, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    v = (rng.standard_normal((P, H, T, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    rope = (mode, first, R)
+    g = 0.01
+    blocks = oracle.cold_offload(k, v, oracle.BF16, H, D, T, g, g, P, rope=rope)
+    kk, vv, _ = oracle.cold_onboard(blocks, H, D, T, g, g, oracle.BF16, P, rope=rope)
+    rc = np.arange(first, first + R)
+    oc = np.setdiff1d(np.arange(D), rc)
+    if mode == 1:
+        assert np.array_equal(kk[..., rc], k[..., rc])
+    else:
+        c1, s1, c2, s2 = oracle.encode_2fp4_blocks(np.ascontiguousarray(k[..., rc]), oracle.BF16, g)
+        assert np.array_equal(kk[..., rc].reshape(-1),
+                              oracle.decode_2fp4_blocks(c1, s1, c2, s2, g).reshape(-1))
+    kd, ks = oracle.quantize_pages(np.ascontiguousarray(k[..., oc]), oracle.BF16, H, D - R, T, g)
+    assert np.array_equal(kk[..., oc], oracle.dequantize_pages(kd, ks, H, D - R, T, g))
+    vd, vs = oracle.quantize_pages(v, oracle.BF16, H, D, T, g)
+    assert np.array_equal(vv, oracle.dequantize_pages(vd, vs, H, D, T, g))

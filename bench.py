@@ -486,6 +486,71 @@ def cold_table(path, flush, timer, pages=2048):
     return out
 
 
+def scale_stats(kv, lay, x, g_t):
+    """Encode BF16 pages x ([P, H, T, D]) with the global scale in g_t (device scalar) and decode
+    them back to BF16, both through the library; return the error and the scale-range counts:
+    blocks whose E4M3 scale rounds to 0 (every value of the block decodes to 0), blocks whose
+    scale is subnormal (below 2^-6: fewer than 4 significant bits), blocks whose scale saturates
+    (amax / (6 g) above 464, the midpoint between 448 and the next E4M3 step, so rounding alone
+    would not bring it to 448), and the values the range clips (|x| above 7 * 448 g, the
+    midpoint beyond the largest code 6 at the largest scale)."""
+    import torch
+    P, H, T, D = x.shape
+    u8 = torch.uint8
+    data = torch.empty((P, H, T, D // 2), dtype=u8, device=x.device)
+    scales = torch.empty((P, H, T, D // 16), dtype=u8, device=x.device)
+    kv.nvfp4_kv_quantize_pages(lay, x, g_t, data, scales)
+    y = torch.empty_like(x)
+    kv.nvfp4_kv_dequantize_pages(lay, data, scales, g_t, y)
+    g = float(g_t.item())
+    xf, yf = x.float().view(-1, 16), y.float().view(-1, 16)
+    err = xf - yf
+    amax = xf.abs().amax(1)
+    s = scales.view(-1).to(torch.int32)
+    nz = amax > 0
+    lim = 7.0 * 448.0 * g
+    rel_blk = (err.abs().amax(1)[nz] / amax[nz])
+    return {
+        "g": g,
+        "blocks": int(xf.shape[0]),
+        "rel_rmse": float(err.pow(2).sum().sqrt() / xf.pow(2).sum().sqrt()),
+        "mean_block_rel_max_err": float(rel_blk.mean()),
+        "blocks_zero_scale": int(((s == 0) & nz).sum()),
+        "blocks_subnormal_scale": int((((s & 0x78) == 0) & (s != 0)).sum()),
+        "blocks_saturated_scale": int((amax / (6.0 * g) > 464.0).sum()),
+        "values_clipped": int((xf.abs() > lim).sum()),
+    }
+
+
+def global_scale_study(path):
+    """Error and scale-range counts of the unit global scale (g = 1) against the calibrated one
+    (g = amax / 2688) on the synthetic distributions."""
+    import torch
+    import synthetic
+    kv, dev = path.kv, path.dev
+    cases = {}
+    rt = path.rt
+    lay = kv.Layout(rt.H, rt.D, rt.T)
+    gen = synthetic.gen(7, device=dev)
+    cases["N(0,1), 1% blocks x1e3, 1% x1e-3 (round-trip K, 4096 pages)"] = (path.k, lay)
+    db = synthetic.decode_batch()
+    cases["N(0,1), K channels 13/42/77/118 x20 (decode K, 1024 pages)"] = (
+        synthetic.kv_pages_bf16(1024, db.H, db.T, db.D, gen, k_outliers=True, device=dev),
+        kv.Layout(db.H, db.D, db.T))
+    cases["N(0,1) (V, 1024 pages)"] = (
+        synthetic.kv_pages_bf16(1024, db.H, db.T, db.D, gen, device=dev),
+        kv.Layout(db.H, db.D, db.T))
+    out = {}
+    for name, (x, ly) in cases.items():
+        g_cal = torch.empty(1, dtype=torch.float32, device=dev)
+        kv.nvfp4_kv_compute_global_scale(ly, x, g_cal)
+        g_one = torch.ones(1, dtype=torch.float32, device=dev)
+        out[name] = {"unit": scale_stats(kv, ly, x, g_one),
+                     "calibrated": scale_stats(kv, ly, x, g_cal)}
+    torch.cuda.synchronize()
+    return out
+
+
 # ---------------------------------------------------------------------------- CPU baseline
 
 def oracle_sample(seed=0, pages=1024, decode_seqs=1, max_tokens=None):
@@ -642,6 +707,7 @@ def main():
     }
     if not args.no_kernels and rank == 0:
         result["kernels"] = kernel_table(path, peak)
+        result["global_scale_study"] = global_scale_study(path)
     if not args.no_e2e:
         result["e2e"] = e2e(path, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

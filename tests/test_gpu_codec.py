@@ -336,3 +336,38 @@ def test_zero_pages_and_zero_tensor(kv, cuda):
     gs.zero_()
     kv.nvfp4_kv_compute_global_scale(lay, z, gs)
     assert gs.item() == 1.0
+
+
+# ------------------------------------------------------------------------------ scale study
+
+@pytest.mark.parametrize("calibrated", [False, True])
+def test_global_scale_study_counts_match_the_oracle(kv, cuda, calibrated):
+    """The benchmark's global-scale study (error and scale-range counts of g = 1 against
+    g = amax / 2688) computed through the library equals the same statistics of the oracle's
+    codes and decoded values on a sample with x1e3 and x1e-3 blocks."""
+    import bench
+    P, H, T, D = 16, 2, 16, 64
+    x = synthetic.outlier_blocks_bf16(P, H, T, D, synthetic.gen(33), frac_big=0.02,
+                                      frac_small=0.05).to(cuda)
+    lay = kv.Layout(H, D, T)
+    bits = _src_bits(x)
+    g = oracle.global_scale(bits, oracle.BF16, H, D, T) if calibrated else 1.0
+    st = bench.scale_stats(kv, lay, x, _scalar(g, cuda))
+    d, s = oracle.quantize_pages(bits, oracle.BF16, H, D, T, g)
+    y = oracle.dequantize_pages(d, s, H, D, T, g)
+    xs = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(-1, 16)
+    ys = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64).reshape(-1, 16)
+    sb = s.reshape(-1).astype(int)
+    amax = np.abs(xs).max(1)
+    nz = amax > 0
+    assert st["blocks_zero_scale"] == int(((sb == 0) & nz).sum())
+    assert st["blocks_subnormal_scale"] == int((((sb & 0x78) == 0) & (sb != 0)).sum())
+    assert st["blocks_saturated_scale"] == int((amax / (6 * g) > 464).sum())
+    assert st["values_clipped"] == int((np.abs(xs) > 7 * 448 * g).sum())
+    err = xs - ys
+    want = np.sqrt((err ** 2).sum()) / np.sqrt((xs ** 2).sum())
+    assert abs(st["rel_rmse"] - want) <= 1e-5 * want + 1e-12
+    if calibrated:
+        assert st["blocks_saturated_scale"] == 0 and st["values_clipped"] == 0
+    else:
+        assert st["blocks_saturated_scale"] > 0 and st["blocks_zero_scale"] > 0

@@ -273,7 +273,7 @@ class Path:
                              + wl.B * wl.Hq * wl.D * 2 * 2                   # q in, out
                              + pt.numel() * 4 + wl.B * 4 + wl.B * wl.Hq * 4)  # table, lens, lse
         self.decode_tokens = wl.B
-        self.launches_per_step = 2 * 2 + 2 + 4 + 1   # amax (2 kernels) x2, quantize x2, dequantize x4, decode 1
+        self.launches_per_step = 2 + 2 + 4 + 1   # amax x2, quantize x2, dequantize x4, decode 1
         torch.cuda.synchronize()
 
     # individual launches --------------------------------------------------------------
@@ -356,7 +356,7 @@ def kernel_table(path, peak):
         res[name] = d
 
     n = path.rt.P * path.rt.H * path.rt.T * path.rt.D
-    add("amax_K (page round-trip)", lambda: path.amax(0), n * 2, 2)
+    add("amax_K (page round-trip)", lambda: path.amax(0), n * 2, 1)
     add("quantize_K dim pairs (page round-trip)", lambda: path.quantize(0), n * 2.5625, 1)
     add("quantize_V token pairs (page round-trip)", lambda: path.quantize(1), n * 2.5625, 1)
     add("dequantize_K_bf16 (page round-trip)", lambda: path.dequantize_bf16(0), n * 2.5625, 1)

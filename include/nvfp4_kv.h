@@ -114,8 +114,10 @@ int32_t nvfp4kv_version(void);
  *   src_page_ids   [num_pages] page ids into src (NULL = 0 .. num_pages-1)
  *   src_scale      FP8 sources only: device scalar, x = fp32(e4m3 * src_scale) (NULL = 1)
  *   global_scale_out  device float written with g
- *   workspace      device scratch of nvfp4_kv_global_scale_workspace_size() bytes
- * num_pages == 0 writes g = 1.
+ *   workspace      device scratch of nvfp4_kv_global_scale_workspace_size() bytes (16): a
+ *                  tagged maximum and a tagged count; never needs clearing; calls that can
+ *                  overlap on the GPU must not share it
+ * One launch: the CTA that finishes last writes g. num_pages == 0 writes g = 1.
  * ------------------------------------------------------------------------------------------ */
 size_t nvfp4_kv_global_scale_workspace_size(void);
 

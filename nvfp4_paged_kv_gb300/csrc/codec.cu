@@ -173,11 +173,10 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
 // cvt.rn.f16x2.e4m3x2 are exact, and the product has at most 6 significant bits), widened to
 // fp32 exactly, multiplied by g (BF16 / FP16 out) or m = fp32(g / dst_scale) (FP8 out) with
 // one IEEE fp32 multiply, and rounded to the output type to nearest even (FP8 saturating).
-// A unit is 8 codes: half a block of one token (dim pairs: 4 code bytes + the block's scale,
-// 8 outputs of one token) or 8 head dims of a token pair (token pairs: 8 code bytes + the
-// pair's 2 scales, 8 outputs for each of the two tokens). FP8 outputs are half as wide, so
-// there a unit is twice as large (one whole block; 16 dims of a token pair) and every store
-// is still 16 bytes.
+// A unit is one block of one token (dim pairs: 8 code bytes + the block's scale, 16 outputs,
+// one 32-byte store) or 8 head dims of a token pair (token pairs: 8 code bytes + the pair's 2
+// scales, 8 outputs for each of the two tokens). FP8 outputs are half as wide: a dim-pair unit
+// stores 16 bytes, a token-pair unit covers 16 dims of the pair.
 // ------------------------------------------------------------------------------------------
 struct DequantParams {
     const uint8_t* src_data;
@@ -262,9 +261,9 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
             for (int u = 0; u < kU; ++u) {
                 const int32_t unit = u_begin + u * kThreads;
                 if (unit >= p.units) continue;
-                const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
                 if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
                     // 16 values of one token: (s, s) times each code pair
+                    const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
                     uint32_t v[8];
                     e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
                     e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
@@ -280,6 +279,7 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
                                               static_cast<int64_t>(unit) * 16) =
                         make_uint4(o[0], o[1], o[2], o[3]);
                 } else {
+                    const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
                     // 16 head dims of tokens 2rp (low nibbles) and 2rp+1 (high nibbles)
                     const uint32_t rp = fast_div(unit, p.nb_magic);
                     const int32_t blk = unit - static_cast<int32_t>(rp) * p.nb;
@@ -305,13 +305,15 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
                 }
             }
         } else if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
-            uint32_t code[kBlocksPerThread], sbyte[kBlocksPerThread];
+            // a unit is one block: 8 code bytes and its scale in, 16 outputs (32 bytes) out
+            uint2 code[kBlocksPerThread];
+            uint32_t sbyte[kBlocksPerThread];
 #pragma unroll
             for (int u = 0; u < kBlocksPerThread; ++u) {
                 const int32_t unit = u_begin + u * kThreads;
                 if (unit < p.units) {
-                    code[u] = ld_stream_4B(p.src_data + (src_blk0 * 2 + unit) * 4);
-                    sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + (unit >> 1));
+                    code[u] = ld_stream_8B(p.src_data + (src_blk0 + unit) * 8);
+                    sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + unit);
                 }
             }
 #pragma unroll
@@ -319,16 +321,17 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
                 const int32_t unit = u_begin + u * kThreads;
                 if (unit >= p.units) continue;
                 const uint32_t s2 = e4m3x2_to_f16x2(sbyte[u] * 0x0101u);  // (s, s)
-                uint32_t v[4];
-                e2m1x8_to_f16x2x4(code[u], v);
-                float y[8];
+                uint32_t v[8];
+                e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
+                e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
+                uint32_t o[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 8; ++j) {
                     const uint32_t v2 = hmul2_u32(v[j], s2);
-                    y[2 * j] = __fmul_rn(f16_lo(v2), mult);
-                    y[2 * j + 1] = __fmul_rn(f16_hi(v2), mult);
+                    const float lo = __fmul_rn(f16_lo(v2), mult), hi = __fmul_rn(f16_hi(v2), mult);
+                    o[j] = (DST == NVFP4KV_BF16) ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
                 }
-                store8<DST>(p.dst, dst_elem0 + static_cast<int64_t>(unit) * 8, y);
+                st_global_32B(static_cast<uint8_t*>(p.dst) + (dst_elem0 + static_cast<int64_t>(unit) * 16) * 2, o);
             }
         } else {
             uint2 code[kBlocksPerThread];
@@ -376,9 +379,10 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
 // ------------------------------------------------------------------------------------------
 // Tensor amax and global scale. Non-negative IEEE values order like their bit patterns, so the
 // maximum of |x| is taken on the sign-cleared 16-bit (BF16 / FP16) or 8-bit (FP8) patterns with
-// SIMD unsigned maxima; one partial per CTA goes to the workspace and a one-CTA kernel
-// finishes: g = fp32(amax / 2688), or 1 when that is 0. For FP8 sources the maximum of
-// fp32(e4m3 * src_scale) is fp32(max|e4m3| * |src_scale|) because rounding is monotone.
+// SIMD unsigned maxima; each CTA raises a tagged maximum word in the workspace and bumps a
+// tagged count, and the CTA that completes the count writes g = fp32(amax / 2688), or 1 when
+// that is 0: one launch, and the workspace never needs clearing. For FP8 sources the maximum
+// of fp32(e4m3 * src_scale) is fp32(max|e4m3| * |src_scale|) because rounding is monotone.
 // ------------------------------------------------------------------------------------------
 constexpr int kAmaxThreads = 256;
 constexpr int kAmaxMaxCtas = 2048;
@@ -392,9 +396,45 @@ struct AmaxParams {
     int64_t page_bytes;   // bytes of one page (a multiple of 16)
     int32_t items_per_page;
     int32_t item_bytes;   // kAmaxThreads * 16 * kAmaxLoads
-    uint32_t* partial;    // [gridDim.x] max pattern per CTA
+    unsigned long long* word;  // [0] tagged maximum pattern, [1] tagged count of finished CTAs
+    uint32_t nonce;       // tag of this call
+    const float* src_scale;
+    float* out;
     int32_t* status;
 };
+
+// g of the maximum magnitude pattern r: fp32(amax / 2688), 1 when that is 0. FP8 sources:
+// amax = fp32(max|e4m3| * |src_scale|) (rounding is monotone).
+template <int SRC>
+__device__ __forceinline__ float global_scale_of(uint32_t r, const float* src_scale) {
+    float amax;
+    if constexpr (SRC == NVFP4KV_FP8_E4M3) {
+        amax = __fmul_rn(e4m3_to_f32(r), fabsf(src_scale ? *src_scale : 1.0f));
+    } else if constexpr (SRC == NVFP4KV_BF16) {
+        amax = __uint_as_float(r << 16);
+    } else {
+        amax = __half2float(__ushort_as_half(static_cast<uint16_t>(r)));
+    }
+    const float g = __fdiv_rn(amax, 2688.0f);
+    return (g == 0.0f) ? 1.0f : g;
+}
+
+// Raise the tagged maximum (tag in the high 32 bits) to r. Tags grow from call to call, so a
+// word of an earlier call is replaced by the first atomicMax; a word holding a larger tag
+// (garbage) is installed over with a bounded compare-and-swap loop.
+__device__ __forceinline__ void tagged_max(unsigned long long* w, uint32_t nonce, uint32_t r) {
+    const unsigned long long v = (static_cast<unsigned long long>(nonce) << 32) | r;
+    unsigned long long old = atomicMax(w, v);
+    for (int it = 0; it < 256 && static_cast<uint32_t>(old >> 32) > nonce; ++it) {
+        const unsigned long long seen = atomicCAS(w, old, v);
+        if (seen == old) return;
+        old = seen;
+        if (static_cast<uint32_t>(old >> 32) <= nonce) {
+            atomicMax(w, v);
+            return;
+        }
+    }
+}
 
 template <int SRC>
 __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) {
@@ -446,34 +486,19 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) 
     if (threadIdx.x == 0) {
         uint32_t r = 0u;
         for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
-        p.partial[blockIdx.x] = r;
-    }
-}
-
-template <int SRC>
-__global__ void global_scale_finish_kernel(const uint32_t* partial, int32_t n,
-                                           const float* src_scale, float* out) {
-    uint32_t m = 0u;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, partial[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    __shared__ uint32_t red[32];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t r = 0u;
-        for (int w = 0; w < (blockDim.x + 31) / 32; ++w) r = max(r, red[w]);
-        float amax;
-        if constexpr (SRC == NVFP4KV_FP8_E4M3) {
-            const float e = e4m3_to_f32(r);
-            amax = __fmul_rn(e, fabsf(src_scale ? *src_scale : 1.0f));
-        } else if constexpr (SRC == NVFP4KV_BF16) {
-            amax = __uint_as_float(r << 16);
-        } else {
-            amax = __half2float(__ushort_as_half(static_cast<uint16_t>(r)));
+        // the CTA's maximum into the call's tagged maximum, then the count; the CTA that
+        // completes the count writes g
+        tagged_max(p.word, p.nonce, r);
+        __threadfence();
+        const uint32_t k = tagged_finish(p.word + 1, atomicAdd(p.word + 1, 1ull), p.nonce, 1);
+        if (k == gridDim.x - 1) {
+            __threadfence();
+            const unsigned long long w = atomicAdd(p.word, 0ull);
+            const uint32_t best = (static_cast<uint32_t>(w >> 32) == p.nonce)
+                                      ? static_cast<uint32_t>(w)
+                                      : 0u;
+            *p.out = global_scale_of<SRC>(best, p.src_scale);
         }
-        const float g = __fdiv_rn(amax, 2688.0f);
-        *out = (g == 0.0f) ? 1.0f : g;
     }
 }
 
@@ -502,7 +527,7 @@ int grid_for(int64_t items, int ctas_per_sm) {
 using namespace nvfp4kv;
 
 extern "C" size_t nvfp4_kv_global_scale_workspace_size(void) {
-    return static_cast<size_t>(kAmaxMaxCtas) * sizeof(uint32_t);
+    return 2 * sizeof(unsigned long long);
 }
 
 extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
@@ -533,26 +558,17 @@ extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
     p.page_bytes = elems * static_cast<int64_t>(dtype_bytes(src_dtype));
     p.item_bytes = kAmaxThreads * 16 * kAmaxLoads;
     p.items_per_page = static_cast<int32_t>((p.page_bytes + p.item_bytes - 1) / p.item_bytes);
-    p.partial = static_cast<uint32_t*>(workspace);
+    p.word = static_cast<unsigned long long*>(workspace);
+    p.nonce = next_nonce();
+    p.src_scale = src_scale;
+    p.out = global_scale_out;
     p.status = status;
     int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
     if (grid > kAmaxMaxCtas) grid = kAmaxMaxCtas;
     switch (src_dtype) {
-    case NVFP4KV_BF16:
-        amax_kernel<NVFP4KV_BF16><<<grid, kAmaxThreads, 0, s>>>(p);
-        global_scale_finish_kernel<NVFP4KV_BF16><<<1, 1024, 0, s>>>(p.partial, grid, src_scale,
-                                                                    global_scale_out);
-        break;
-    case NVFP4KV_FP16:
-        amax_kernel<NVFP4KV_FP16><<<grid, kAmaxThreads, 0, s>>>(p);
-        global_scale_finish_kernel<NVFP4KV_FP16><<<1, 1024, 0, s>>>(p.partial, grid, src_scale,
-                                                                    global_scale_out);
-        break;
-    default:
-        amax_kernel<NVFP4KV_FP8_E4M3><<<grid, kAmaxThreads, 0, s>>>(p);
-        global_scale_finish_kernel<NVFP4KV_FP8_E4M3><<<1, 1024, 0, s>>>(
-            p.partial, grid, src_scale, global_scale_out);
-        break;
+    case NVFP4KV_BF16: amax_kernel<NVFP4KV_BF16><<<grid, kAmaxThreads, 0, s>>>(p); break;
+    case NVFP4KV_FP16: amax_kernel<NVFP4KV_FP16><<<grid, kAmaxThreads, 0, s>>>(p); break;
+    default: amax_kernel<NVFP4KV_FP8_E4M3><<<grid, kAmaxThreads, 0, s>>>(p); break;
     }
     return launch_status();
 }
@@ -734,12 +750,12 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     p.nb = layout->head_dim / 16;
     p.nb2_magic = div_magic(static_cast<uint32_t>(2 * p.nb));
     p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
-    // BF16 / FP16 out: 8 codes per dim-pair unit (2 per block), 16 codes per token-pair unit
-    // (2 per block pair); FP8 out: a whole block, 32 codes per token-pair unit
+    // BF16 / FP16 out: a block per dim-pair unit, 16 codes per token-pair unit (2 per block
+    // pair); FP8 out: a block per dim-pair unit, 32 codes per token-pair unit
     if (dst_dtype == NVFP4KV_FP8_E4M3)
         p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
     else
-        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp : 2 * p.bpp;
+        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp : p.bpp;
     p.items_per_page = (p.units + kItemBlocks - 1) / kItemBlocks;
     p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -155,4 +155,17 @@ __device__ __forceinline__ void block_values(uint2 code, uint32_t sbyte, float (
     }
 }
 
+// 32 bytes to global memory with one 256-bit store when p is 32-byte aligned (a warp then
+// writes whole 32-byte sectors with each instruction), else as two 16-byte stores.
+__device__ __forceinline__ void st_global_32B(void* p, const uint32_t (&w)[8]) {
+    if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else {
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p) + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
 }  // namespace nvfp4kv

@@ -232,8 +232,7 @@ __device__ __forceinline__ void onboard_k_rows(const ColdParams& p, const uint8_
         for (int j = 0; j < 8; ++j)
             o[j] = (DST == NVFP4KV_BF16) ? pack_bf16x2(y[2 * j], y[2 * j + 1])
                                          : pack_f16x2(y[2 * j], y[2 * j + 1]);
-        *reinterpret_cast<uint4*>(q) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(q + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+        st_global_32B(q, o);
     }
     __syncthreads();
 }
@@ -401,9 +400,7 @@ __global__ void __launch_bounds__(kColdThreads) cold_onboard_kernel(const ColdPa
                 const float lo = __fmul_rn(f16_lo(e), g), hi = __fmul_rn(f16_hi(e), g);
                 o[j] = (DST == NVFP4KV_BF16) ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
             }
-            uint8_t* q = dst + static_cast<int64_t>(b0 + b) * 32;
-            *reinterpret_cast<uint4*>(q) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(q + 16) = make_uint4(o[4], o[5], o[6], o[7]);
+            st_global_32B(dst + static_cast<int64_t>(b0 + b) * 32, o);
         }
         __syncthreads();
     }

@@ -17,6 +17,34 @@ constexpr int kNumSmsDefault = 152;
 // ------------------------------------------------------------------------------------------
 // Status word
 // ------------------------------------------------------------------------------------------
+// Tagged counter (tag in the high 32 bits, count in the low 32): add inc and return the count
+// before the add, treating a word whose tag is not this call's as a count of 0. `old` is the
+// value returned by a first atomicAdd. Tags grow from call to call, so a stale word is replaced
+// by one atomicMax (which never lowers an installed count); a word holding a larger tag
+// (garbage) falls back to a compare-and-swap loop. Only values returned by atomics are used:
+// a plain re-read could be served stale from L1.
+__device__ __forceinline__ uint32_t tagged_finish(unsigned long long* w, unsigned long long old,
+                                                  uint32_t nonce, uint32_t inc) {
+    if (static_cast<uint32_t>(old >> 32) == nonce) return static_cast<uint32_t>(old);
+    const unsigned long long base = static_cast<unsigned long long>(nonce) << 32;
+    atomicMax(w, base);
+    unsigned long long cur = atomicAdd(w, static_cast<unsigned long long>(inc));
+    if (static_cast<uint32_t>(cur >> 32) == nonce) return static_cast<uint32_t>(cur);
+    cur += inc;
+    for (int it = 0; it < 256; ++it) {
+        if (static_cast<uint32_t>(cur >> 32) == nonce) {
+            const unsigned long long o2 = atomicAdd(w, static_cast<unsigned long long>(inc));
+            if (static_cast<uint32_t>(o2 >> 32) == nonce) return static_cast<uint32_t>(o2);
+            cur = o2 + inc;
+            continue;
+        }
+        const unsigned long long seen = atomicCAS(w, cur, base | inc);
+        if (seen == cur) return 0;
+        cur = seen;
+    }
+    return 0xFFFFFFFFu;  // could not install the tag: report the pair as not finished
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     if (status) atomicOr(status, bit);
 }

@@ -112,34 +112,6 @@ struct DecodeParams {
     float sm_scale;
 };
 
-// Tagged counter (tag in the high 32 bits, count in the low 32): add inc and return the count
-// before the add, treating a word whose tag is not this call's as a count of 0. `old` is the
-// value returned by a first atomicAdd. Tags grow from call to call, so a stale word is replaced
-// by one atomicMax (which never lowers an installed count); a word holding a larger tag
-// (garbage) falls back to a compare-and-swap loop. Only values returned by atomics are used:
-// a plain re-read could be served stale from L1.
-__device__ __forceinline__ uint32_t tagged_finish(unsigned long long* w, unsigned long long old,
-                                                  uint32_t nonce, uint32_t inc) {
-    if (static_cast<uint32_t>(old >> 32) == nonce) return static_cast<uint32_t>(old);
-    const unsigned long long base = static_cast<unsigned long long>(nonce) << 32;
-    atomicMax(w, base);
-    unsigned long long cur = atomicAdd(w, static_cast<unsigned long long>(inc));
-    if (static_cast<uint32_t>(cur >> 32) == nonce) return static_cast<uint32_t>(cur);
-    cur += inc;
-    for (int it = 0; it < 256; ++it) {
-        if (static_cast<uint32_t>(cur >> 32) == nonce) {
-            const unsigned long long o2 = atomicAdd(w, static_cast<unsigned long long>(inc));
-            if (static_cast<uint32_t>(o2 >> 32) == nonce) return static_cast<uint32_t>(o2);
-            cur = o2 + inc;
-            continue;
-        }
-        const unsigned long long seen = atomicCAS(w, cur, base | inc);
-        if (seen == cur) return 0;
-        cur = seen;
-    }
-    return 0xFFFFFFFFu;  // could not install the tag: report the pair as not finished
-}
-
 __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
     const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
                               *reinterpret_cast<const __half2*>(&b));
@@ -942,16 +914,6 @@ bool decode_size_ok(int batch, int H, int D, int max_pages, int T, int64_t ctas)
     const int64_t lim = (int64_t{1} << 31) - 1;
     return max_tokens < lim - tok && stages + ctas * kWarps < lim &&
            ctas + static_cast<int64_t>(batch) * H < lim;
-}
-
-// One tag per call (all devices): counters of earlier calls never carry it. Tags grow from call
-// to call, which lets a stale counter be replaced by one atomicMax.
-uint32_t next_nonce() {
-    static std::atomic<uint32_t> counter{static_cast<uint32_t>(
-        std::chrono::steady_clock::now().time_since_epoch().count() & 0x3FFFFFFF) + 1u};
-    uint32_t n = counter.fetch_add(1) + 1;
-    if (n == 0) n = counter.fetch_add(1) + 1;
-    return n;
 }
 
 template <int D>

@@ -2,6 +2,8 @@
 // error mapping. No device code here.
 #pragma once
 
+#include <atomic>
+#include <chrono>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -39,6 +41,16 @@ inline int num_sms() {
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+// One tag per call (all devices): counters of earlier calls never carry it. Tags grow from call
+// to call, which lets a stale counter be replaced by one atomicMax.
+inline uint32_t next_nonce() {
+    static std::atomic<uint32_t> counter{static_cast<uint32_t>(
+        std::chrono::steady_clock::now().time_since_epoch().count() & 0x3FFFFFFF) + 1u};
+    uint32_t n = counter.fetch_add(1) + 1;
+    if (n == 0) n = counter.fetch_add(1) + 1;
+    return n;
 }
 
 inline nvfp4kv_status launch_status() {

@@ -128,7 +128,7 @@ def test_quantize_parity(kv, cuda, kind, shape, ids, pack):
 
 @pytest.mark.parametrize("out_kind", ["bf16", "fp16", "fp8"])
 @pytest.mark.parametrize("shape", [(9, 3, 16, 48), (40, 8, 32, 128), (1, 1, 1, 16),
-                                   (3, 2, 2, 256)])
+                                   (3, 2, 2, 256), (5, 1, 3, 80)])
 @pytest.mark.parametrize("pack", [0, 1])
 def test_dequantize_parity(kv, cuda, out_kind, shape, pack):
     P, H, T, D = shape
@@ -371,3 +371,25 @@ def test_global_scale_study_counts_match_the_oracle(kv, cuda, calibrated):
         assert st["blocks_saturated_scale"] == 0 and st["values_clipped"] == 0
     else:
         assert st["blocks_saturated_scale"] > 0 and st["blocks_zero_scale"] > 0
+
+
+def test_global_scale_workspace_needs_no_clearing(kv, cuda):
+    """One launch computes g through a tagged maximum and a tagged count in the workspace: g is
+    right whatever the workspace holds (all ones, random bytes, the previous call's words), for
+    calls that alternate between tensors of different maxima."""
+    H, T, D = 2, 16, 64
+    xs = [synthetic.outlier_blocks_bf16(9, H, T, D, synthetic.gen(s), big=b).to(cuda)
+          for s, b in ((41, 1e3), (42, 3.0), (43, 50.0))]
+    lay = kv.Layout(H, D, T)
+    want = [oracle.global_scale(_src_bits(x), oracle.BF16, H, D, T) for x in xs]
+    ws = torch.empty(kv.nvfp4_kv_global_scale_workspace_size(), dtype=torch.uint8, device=cuda)
+    out = torch.empty(1, dtype=torch.float32, device=cuda)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    for trial in range(12):
+        if trial == 0:
+            ws.fill_(0xFF)
+        elif trial % 4 == 1:
+            ws.copy_(torch.randint(0, 256, ws.shape, generator=gen, dtype=torch.uint8))
+        i = trial % 3
+        kv.nvfp4_kv_compute_global_scale(lay, xs[i], out, workspace=ws)
+        assert out.item() == want[i], (trial, out.item(), want[i])

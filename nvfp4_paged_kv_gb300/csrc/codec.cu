@@ -116,10 +116,10 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
                     w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r))
                           << (8 * j);
                 }
-                *reinterpret_cast<uint2*>(p.dst_data + (dst_blk0 + blk) * 8) = make_uint2(w0, w1);
-                p.dst_scales[dst_blk0 + blk] = static_cast<uint8_t>(sb);
+                st_cs(p.dst_data + (dst_blk0 + blk) * 8, make_uint2(w0, w1));
+                st_cs_u8(p.dst_scales + dst_blk0 + blk, sb);
                 if constexpr (WS)
-                    *reinterpret_cast<uint4*>(ws_page + static_cast<int64_t>(blk) * 16) = fp8_block(x, wm);
+                    st_cs(ws_page + static_cast<int64_t>(blk) * 16, fp8_block(x, wm));
             }
         } else {
             U8x32 raw0[kUnitsPerThread], raw1[kUnitsPerThread];
@@ -152,16 +152,15 @@ __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantPar
                                  << (8 * (e & 3));
                 // unit index = (row pair, block): data at unit * 16, scales at unit * 2
                 const int64_t o = dst_blk0 / 2 + unit;
-                *reinterpret_cast<uint4*>(p.dst_data + o * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint16_t*>(p.dst_scales + o * 2) =
-                    static_cast<uint16_t>(s0 | (s1 << 8));
+                st_cs(p.dst_data + o * 16, make_uint4(w[0], w[1], w[2], w[3]));
+                st_cs_u16(p.dst_scales + o * 2, s0 | (s1 << 8));
                 if constexpr (WS) {
                     // the same block of tokens 2p and 2p+1 in the plain [token][dim] workspace
                     const uint32_t row_pair = fast_div(unit, p.nb_magic);
                     const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
                     const int64_t wb = static_cast<int64_t>(2 * row_pair) * p.nb + b;
-                    *reinterpret_cast<uint4*>(ws_page + wb * 16) = fp8_block(x0, wm);
-                    *reinterpret_cast<uint4*>(ws_page + (wb + p.nb) * 16) = fp8_block(x1, wm);
+                    st_cs(ws_page + wb * 16, fp8_block(x0, wm));
+                    st_cs(ws_page + (wb + p.nb) * 16, fp8_block(x1, wm));
                 }
             }
         }
@@ -204,7 +203,7 @@ __device__ __forceinline__ void store8(void* dst, int64_t elem, const float (&y)
         uint2 o;
         o.x = f32x2_to_e4m3x2(y[0], y[1]) | (f32x2_to_e4m3x2(y[2], y[3]) << 16);
         o.y = f32x2_to_e4m3x2(y[4], y[5]) | (f32x2_to_e4m3x2(y[6], y[7]) << 16);
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + elem) = o;
+        st_cs(static_cast<uint8_t*>(dst) + elem, o);
     } else {
         uint4 o;
         if constexpr (DST == NVFP4KV_BF16) {
@@ -214,7 +213,7 @@ __device__ __forceinline__ void store8(void* dst, int64_t elem, const float (&y)
             o = make_uint4(pack_f16x2(y[0], y[1]), pack_f16x2(y[2], y[3]),
                            pack_f16x2(y[4], y[5]), pack_f16x2(y[6], y[7]));
         }
-        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst) + elem * 2) = o;
+        st_cs(static_cast<uint8_t*>(dst) + elem * 2, o);
     }
 }
 
@@ -275,9 +274,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
                                (f32x2_to_e4m3x2(__fmul_rn(f16_lo(b), mult), __fmul_rn(f16_hi(b), mult))
                                 << 16);
                     }
-                    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + dst_elem0 +
-                                              static_cast<int64_t>(unit) * 16) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
+                    st_cs(static_cast<uint8_t*>(p.dst) + dst_elem0 + static_cast<int64_t>(unit) * 16,
+                          make_uint4(o[0], o[1], o[2], o[3]));
                 } else {
                     const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
                     // 16 head dims of tokens 2rp (low nibbles) and 2rp+1 (high nibbles)
@@ -300,8 +298,8 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
                     }
                     const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * rp) * p.nb * 16 + blk * 16;
                     uint8_t* d8 = static_cast<uint8_t*>(p.dst);
-                    *reinterpret_cast<uint4*>(d8 + e0) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-                    *reinterpret_cast<uint4*>(d8 + e0 + p.nb * 16) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                    st_cs(d8 + e0, make_uint4(o0[0], o0[1], o0[2], o0[3]));
+                    st_cs(d8 + e0 + p.nb * 16, make_uint4(o1[0], o1[1], o1[2], o1[3]));
                 }
             }
         } else if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {

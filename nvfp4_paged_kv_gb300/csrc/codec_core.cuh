@@ -159,13 +159,34 @@ __device__ __forceinline__ void block_values(uint2 code, uint32_t sbyte, float (
 // writes whole 32-byte sectors with each instruction), else as two 16-byte stores.
 __device__ __forceinline__ void st_global_32B(void* p, const uint32_t (&w)[8]) {
     if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
-        asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
+        asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
                      "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                      : "memory");
     } else {
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p) + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+        asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(static_cast<uint8_t*>(p) + 16),
+                     "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
     }
+}
+
+// Streaming stores (.cs: the lines are evicted first from L2, as outputs of this pass are not
+// read again by it).
+__device__ __forceinline__ void st_cs(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cs(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_cs_u16(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(v)) : "memory");
+}
+__device__ __forceinline__ void st_cs_u8(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "h"(static_cast<uint16_t>(v)) : "memory");
 }
 
 }  // namespace nvfp4kv

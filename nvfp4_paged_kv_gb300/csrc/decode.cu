@@ -162,16 +162,21 @@ __device__ __forceinline__ uint32_t v_swz(int pr, int x) {
     return static_cast<uint32_t>(pr * D + ((((x >> 4) ^ (pr & Geo<D>::SWZ))) << 4) + (x & 15));
 }
 
-// 16-byte asynchronous copy global -> shared, with compile-time offsets on both addresses.
+// 16-byte asynchronous copy global -> shared, with compile-time offsets on both addresses, under
+// the L2 policy `pol` (evict-first for the K/V stream: each byte is read once per call, so its
+// lines are the first to go and other lines, such as outputs still waiting to be written back,
+// are not pushed out by it).
 template <int OFF_S, int OFF_G>
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src),
-                 "n"(OFF_S), "n"(OFF_G)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0+%2], [%1+%3], 16, %4;" ::"r"(dst),
+                 "l"(src), "n"(OFF_S), "n"(OFF_G), "l"(pol)
                  : "memory");
 }
 // The same with a source size of 16 or 0 bytes (0: the 16 bytes are zero-filled, nothing read).
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(bytes), "l"(pol)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -314,6 +319,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         const int64_t page_rows = static_cast<int64_t>(H) * T;
         const bool page_aligned = (T % TOK) == 0;
         auto issue_stage = [&](int js, uint32_t slot) {
+            const uint64_t kv_pol = l2_policy_evict_first();
             const int t0 = js * TOK;
             const int nval = min(TOK, L - t0);
             int64_t row0[G_::SUB];  // token row of each sub-tile in its pool, -1: not real
@@ -349,8 +355,8 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                 const uint8_t* vsrc = p.vd + doff;
                 static_for<G_::DCH>([&](auto I) {
                     constexpr int i = decltype(I)::value;
-                    cp_async16<G_::K_OFF + 512 * i, 512 * i>(slot + 16 * lane, ksrc);
-                    cp_async16<0, 512 * i>(slot + v_dst[i], vsrc);
+                    cp_async16<G_::K_OFF + 512 * i, 512 * i>(slot + 16 * lane, ksrc, kv_pol);
+                    cp_async16<0, 512 * i>(slot + v_dst[i], vsrc, kv_pol);
                 });
                 const int64_t soff = row0[0] * G_::NB;
 #pragma unroll
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                     const bool kpool = jc < G_::SCH;
                     const int jj = kpool ? jc : jc - G_::SCH;
                     cp_async16<0, 0>(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
-                                     (kpool ? p.ks : p.vs) + soff + 16 * jj);
+                                     (kpool ? p.ks : p.vs) + soff + 16 * jj, kv_pol);
                 }
             } else {
 #pragma unroll
@@ -369,8 +375,8 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                     const bool ok = row0[u] >= 0;
                     const int64_t off = ok ? row0[u] * (D / 2) + 16 * jj : 0;
                     cp_async16_zfill(slot + G_::K_OFF + 16 * (lane + 32 * i), p.kd + off,
-                                     ok ? 16u : 0u);
-                    cp_async16_zfill(slot + v_dst[i], p.vd + off, ok ? 16u : 0u);
+                                     ok ? 16u : 0u, kv_pol);
+                    cp_async16_zfill(slot + v_dst[i], p.vd + off, ok ? 16u : 0u, kv_pol);
                 }
 #pragma unroll
                 for (int k = 0; k < G_::SC_PER_LANE; ++k) {
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                     const bool ok = ru >= 0;
                     const int64_t off = ok ? ru * G_::NB + 16 * (jj - u * (D / 16)) : 0;
                     cp_async16_zfill(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
-                                     (kpool ? p.ks : p.vs) + off, ok ? 16u : 0u);
+                                     (kpool ? p.ks : p.vs) + off, ok ? 16u : 0u, kv_pol);
                 }
             }
             if (lane == 0) sts_u32(slot + G_::HDR_OFF, okbits | (static_cast<uint32_t>(nval) << 8));
@@ -752,7 +758,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                 // of loads while the first records' outputs are already in flight.
                 __threadfence();
                 constexpr int NQ = kMaxGroup * D / kDecThreads;
-                constexpr int kRecUnroll = 8;
+                constexpr int kRecUnroll = NQ >= 16 ? 2 : 8;  // record values in flight: 32 or 64
                 const int n_fast = min(n_rec, kMaxRecW);
                 for (int idx = tid; idx < n_fast * G; idx += kDecThreads) {
                     const int k = idx / G, col = idx - (idx / G) * G;

@@ -133,7 +133,8 @@ nvfp4kv_status nvfp4_kv_compute_global_scale(const nvfp4kv_layout* layout,
  * Encode pages to NVFP4 (block amax -> E4M3 scale pick -> E2M1 round-to-nearest-even -> pack).
  * LMSYS page, "Path 1: Initial prefill" and "Path 2: Chunked prefill / Extend" (the current
  * K/V is quantized and written into the NVFP4 cache); TensorRT LLM page, "How It Works"
- * ("Encode and decode, fused with the copy": a batch of pages per call, on the caller's stream).
+ * (the paragraph on the fused encode and decode: a batch of pages per call, on the caller's
+ * stream).
  *   src / src_page_ids / src_pool_pages   as above (BF16, FP16 or FP8 E4M3 pages)
  *   src_scale      FP8 sources: device scalar (NULL = 1); ignored for 16-bit sources
  *   global_scale   device scalar g (> 0)

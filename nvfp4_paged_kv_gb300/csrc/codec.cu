@@ -5,8 +5,8 @@
 // ("Accelerating Long-Context and Agentic Inference with NVFP4 KV Cache", LMSYS: introduction,
 // Figure 1; "KV Cache Compression in TensorRT LLM", NVIDIA: "NVFP4 Cold-Page Compression",
 // Figure 6). Encode and decode run on a batch of pages per call on the caller's stream, as the
-// TensorRT LLM codec does ("How It Works": the cache manager calls the codec with batches of
-// pages on its own stream); the extend path's FP8 workspace fill is the FP8-output decode
+// TensorRT LLM codec does ("How It Works": the cache manager hands the codec a batch of pages
+// at a time, on a stream of the manager's); the extend path's FP8 workspace fill is the FP8-output decode
 // (LMSYS, "Path 2: Chunked prefill / Extend").
 //
 // All three kernels stream HBM once: every byte of input is loaded with one coalesced vector

@@ -1,11 +1,11 @@
-// Split-KV paged GQA decode attention over NVFP4 K/V for sm_103a, plus the combine pass.
+// Split-KV paged GQA decode attention over NVFP4 K/V for sm_103a, its merge in the same launch.
 //
 // What it computes ("Accelerating Long-Context and Agentic Inference with NVFP4 KV Cache",
 // LMSYS: "Path 3: Decode", "NVFP4 KV Decode Attention Kernel Implementation", Figure 3): for
 // each sequence and query head, softmax(sm_scale q.K^T) V over the sequence's tokens, with K
 // and V read in their packed NVFP4 form straight from the paged cache and dequantized in
-// registers. The global K/V scales are folded into the score scale and the final output
-// ("supplied through the attention BMM scaling parameters").
+// registers. The global K/V scales are folded into the score scale and the final output (the
+// page applies them through the attention matmuls' scaling parameters).
 //
 // Design for GB300 (the SM120 kernel of the LMSYS page is prior art, not the blueprint):
 //  * Work is a flat list of stages: stage j of pair (sequence b, KV head h) covers tokens

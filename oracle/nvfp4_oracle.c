@@ -113,7 +113,7 @@ static double fp16_round(double y)
 
 /* ------------------------------------------------------------------------------------------ */
 /* E2M1 (FP4): sign, 2 exponent bits (bias 1), 1 mantissa bit, no inf / NaN.                   */
-/* [LMSYS intro, Figure 1]: "four-bit E2M1 values". Magnitudes by code 0..7:                   */
+/* [LMSYS intro, Figure 1]: the values are 4-bit E2M1. Magnitudes by code 0..7:                */
 /* 0, 0.5, 1, 1.5, 2, 3, 4, 6.                                                                 */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -140,7 +140,7 @@ static int e2m1_encode(double y)
 
 /* ------------------------------------------------------------------------------------------ */
 /* E4M3 ("fn" variant): bias 7, no inf, NaN = S.1111.111, largest finite 448,                  */
-/* smallest normal 2^-6, subnormal step 2^-9. [LMSYS intro]: "an FP8 scale for each block".    */
+/* smallest normal 2^-6, subnormal step 2^-9. [LMSYS intro]: each block has an FP8 scale.      */
 /* ------------------------------------------------------------------------------------------ */
 
 static double e4m3_value(uint8_t b)
@@ -319,7 +319,7 @@ void orc_e4m3_encode_f32(const float* x, size_t n, uint8_t* out)
 
 /* ------------------------------------------------------------------------------------------ */
 /* Global (tensor) scale. R7.                                                                  */
-/* [LMSYS intro]: "an additional FP32 tensor-level scale"; [LMSYS "Limitations"]: the          */
+/* [LMSYS intro]: one more scale, FP32, per tensor; [LMSYS "Limitations"]: the                 */
 /* experiments used 1.0, and calibration may reduce overflow / underflow. The calibrated       */
 /* rule maps the tensor maximum to the top of both grids: amax / (448 * 6).                    */
 /* ------------------------------------------------------------------------------------------ */
@@ -371,7 +371,7 @@ static void encode_block(const double* x, double g, int* c, uint8_t* scale_out)
 
 /*
  * Quantize pages (K or V of one layer) to NVFP4.
- * [TRTLLM "How It Works", "Encode and decode, fused with the copy"]: a batch of pages goes
+ * [TRTLLM "How It Works", the paragraph on the fused encode and decode]: a batch of pages goes
  * through one encoder; [LMSYS Path 1 / Path 2]: the current K/V is quantized and written into
  * the NVFP4 cache. Layout R3; src pages are [page][H][T][D] in src_dtype.
  */

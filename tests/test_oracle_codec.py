@@ -287,8 +287,8 @@ def _values(bits, dtype, scale=1.0):
 def test_round_trips_do_not_accumulate_error(dtype, g_mode):
     """Every finite value of the source dtype, (i) alone in a block and (ii) among random
     values, through 4 round trips ("KV Cache Compression in TensorRT LLM", Evaluation >
-    Accuracy, Figure 15: the distance to the original stays the one-trip quantization error and
-    the distance to the previous trip is zero from the second trip on).
+    Accuracy, Figure 15: after the first trip the error against the original does not grow, and
+    trips two and later return exactly the previous trip's values).
 
     Under the round-to-nearest scale pick this holds exactly for every block whose E4M3 block
     scale is zero or a normal number. A block whose scale is subnormal (amax < 6 g 2^-6) may

@@ -434,6 +434,26 @@ def kernel_table(path, peak):
     add("extend chunk write NVFP4 + FP8 workspace (128 pages)",
         lambda: kv.nvfp4_kv_extend_write(lay, chunk, g, pd, ps, wsc, dst_page_ids=chunk_dst),
         chunk.shape[0] * per * 3.5625 + chunk.shape[0] * 4, 1)
+    # the same two chunk calls as a serving loop issues them, back to back over 12 rotating
+    # chunks (the K and V chunks of 6 layers: 201 MB of inputs, more than L2), per launch
+    nrot = 12
+    chunks = [synthetic.kv_pages_bf16(chunk.shape[0], ex.H, ex.T, ex.D,
+                                      synthetic.gen(50 + r, device=dev), device=dev)
+              for r in range(nrot)]
+    wss = [torch.empty_like(wsc) for _ in range(nrot)]
+    for name, fn, bpv in (
+            ("extend chunk encode (128 pages, 12 chunks back to back)",
+             lambda r: kv.nvfp4_kv_quantize_pages(lay, chunks[r], g, pd, ps,
+                                                  dst_page_ids=chunk_dst), 2.5625),
+            ("extend chunk write NVFP4 + FP8 workspace (128 pages, 12 chunks back to back)",
+             lambda r: kv.nvfp4_kv_extend_write(lay, chunks[r], g, pd, ps, wss[r],
+                                                dst_page_ids=chunk_dst), 3.5625)):
+        ms = time_kernel(lambda: [fn(r) for r in range(nrot)], flush) / nrot
+        nbytes = chunk.shape[0] * per * bpv + chunk.shape[0] * 4
+        gbs = nbytes / (ms * 1e-3) / GB
+        res[name] = {"ms": round(ms, 4), "bytes": int(nbytes), "GB_s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4), "launches": nrot}
+    del chunks, wss
     res.update(cold_table(path, flush, time_kernel))
     del flush
     return res

@@ -68,6 +68,7 @@ __device__ __forceinline__ uint4 fp8_block(const float (&x)[16], float m) {
 // WS: also write the FP8 workspace copy of every source block (the extend path's fused write).
 template <int SRC, bool A32, int PACK, bool WS = false>
 __global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantParams p) {
+    pdl_enter();
     constexpr int kUnitsPerThread = (PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? kBlocksPerThread / 2
                                                                         : kBlocksPerThread;
     constexpr int kItemUnits = kThreads * kUnitsPerThread;
@@ -219,6 +220,7 @@ __device__ __forceinline__ void store8(void* dst, int64_t elem, const float (&y)
 
 template <int DST, int PACK>
 __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const DequantParams p) {
+    pdl_enter();
     constexpr int kU = kBlocksPerThread;  // units per thread per item
     const float g = __ldg(p.g);
     const float mult = (DST == NVFP4KV_FP8_E4M3)
@@ -436,6 +438,7 @@ __device__ __forceinline__ void tagged_max(unsigned long long* w, uint32_t nonce
 
 template <int SRC>
 __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) {
+    pdl_enter();
     const uint32_t mask = (SRC == NVFP4KV_FP8_E4M3) ? 0x7F7F7F7Fu : 0x7FFF7FFFu;
     uint32_t m = 0u;
     const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
@@ -500,7 +503,10 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) 
     }
 }
 
-__global__ void write_one_kernel(float* out) { *out = 1.0f; }
+__global__ void write_one_kernel(float* out) {
+    pdl_enter();
+    *out = 1.0f;
+}
 
 // ------------------------------------------------------------------------------------------
 // The encoder's two roundings on their own (exhaustive verification over fp32 inputs).
@@ -538,7 +544,7 @@ extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
         return NVFP4KV_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (num_pages == 0) {
-        write_one_kernel<<<1, 1, 0, s>>>(global_scale_out);
+        launch_pdl(write_one_kernel, 1, 1, 0, s, global_scale_out);
         return launch_status();
     }
     if (!src || !aligned16(src)) return NVFP4KV_ERR_INVALID_ARG;
@@ -564,9 +570,9 @@ extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
     int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
     if (grid > kAmaxMaxCtas) grid = kAmaxMaxCtas;
     switch (src_dtype) {
-    case NVFP4KV_BF16: amax_kernel<NVFP4KV_BF16><<<grid, kAmaxThreads, 0, s>>>(p); break;
-    case NVFP4KV_FP16: amax_kernel<NVFP4KV_FP16><<<grid, kAmaxThreads, 0, s>>>(p); break;
-    default: amax_kernel<NVFP4KV_FP8_E4M3><<<grid, kAmaxThreads, 0, s>>>(p); break;
+    case NVFP4KV_BF16: launch_pdl(amax_kernel<NVFP4KV_BF16>, grid, kAmaxThreads, 0, s, p); break;
+    case NVFP4KV_FP16: launch_pdl(amax_kernel<NVFP4KV_FP16>, grid, kAmaxThreads, 0, s, p); break;
+    default: launch_pdl(amax_kernel<NVFP4KV_FP8_E4M3>, grid, kAmaxThreads, 0, s, p); break;
     }
     return launch_status();
 }
@@ -616,7 +622,7 @@ extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
     const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
     const bool a32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
 #define NVFP4KV_QLAUNCH(SRC, A32, PK) \
-    quantize_pages_kernel<SRC, A32, PK><<<grid, kThreads, 0, s>>>(p)
+    launch_pdl(quantize_pages_kernel<SRC, A32, PK>, grid, kThreads, 0, s, p)
 #define NVFP4KV_QPACK(SRC, A32)                                          \
     do {                                                                  \
         if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                             \
@@ -694,9 +700,9 @@ extern "C" nvfp4kv_status nvfp4_kv_extend_write(
 #define NVFP4KV_XLAUNCH(SRC, A32)                                                             \
     do {                                                                                     \
         if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                                                \
-            quantize_pages_kernel<SRC, A32, NVFP4KV_PACK_TOKEN_PAIRS, true><<<grid, kThreads, 0, s>>>(p); \
+            launch_pdl(quantize_pages_kernel<SRC, A32, NVFP4KV_PACK_TOKEN_PAIRS, true>, grid, kThreads, 0, s, p); \
         else                                                                                 \
-            quantize_pages_kernel<SRC, A32, NVFP4KV_PACK_DIM_PAIRS, true><<<grid, kThreads, 0, s>>>(p);   \
+            launch_pdl(quantize_pages_kernel<SRC, A32, NVFP4KV_PACK_DIM_PAIRS, true>, grid, kThreads, 0, s, p);   \
     } while (0)
     if (src_dtype == NVFP4KV_BF16) {
         if (a32) NVFP4KV_XLAUNCH(NVFP4KV_BF16, true);
@@ -761,9 +767,9 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
 #define NVFP4KV_DQLAUNCH(DST)                                                                \
     do {                                                                                      \
         if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                                                 \
-            dequantize_pages_kernel<DST, NVFP4KV_PACK_TOKEN_PAIRS><<<grid, kThreads, 0, s>>>(p); \
+            launch_pdl(dequantize_pages_kernel<DST, NVFP4KV_PACK_TOKEN_PAIRS>, grid, kThreads, 0, s, p); \
         else                                                                                  \
-            dequantize_pages_kernel<DST, NVFP4KV_PACK_DIM_PAIRS><<<grid, kThreads, 0, s>>>(p);   \
+            launch_pdl(dequantize_pages_kernel<DST, NVFP4KV_PACK_DIM_PAIRS>, grid, kThreads, 0, s, p);   \
     } while (0)
     switch (dst_dtype) {
     case NVFP4KV_BF16: NVFP4KV_DQLAUNCH(NVFP4KV_BF16); break;

@@ -267,6 +267,7 @@ __device__ __forceinline__ void copy_extra(const uint8_t* src, uint8_t* dst, int
 // Offload. SRC: NVFP4KV_BF16 or NVFP4KV_FP16; MODE: how the RoPE part of K is kept.
 template <int SRC, int MODE>
 __global__ void __launch_bounds__(kColdThreads) cold_offload_kernel(const ColdParams p) {
+    pdl_enter();
     __shared__ __align__(16) uint8_t s_sc[kChunk];
     __shared__ __align__(16) uint8_t s_r1[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
     __shared__ __align__(16) uint8_t s_r2[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
@@ -339,6 +340,7 @@ __global__ void __launch_bounds__(kColdThreads) cold_offload_kernel(const ColdPa
 // the 16-bit rounding of fp32(v * g).
 template <int DST, int MODE>
 __global__ void __launch_bounds__(kColdThreads) cold_onboard_kernel(const ColdParams p) {
+    pdl_enter();
     __shared__ __align__(16) uint8_t s_sc[kChunk];
     __shared__ __align__(16) uint8_t s_r1[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
     __shared__ __align__(16) uint8_t s_r2[MODE == NVFP4KV_ROPE_2FP4 ? kChunk : 16];
@@ -555,11 +557,11 @@ extern "C" nvfp4kv_status nvfp4_kv_offload_pages(
 #define NVFP4KV_OFF(SRC)                                                                      \
     do {                                                                                      \
         if (p.rope_mode == NVFP4KV_ROPE_SKIP)                                                 \
-            cold_offload_kernel<SRC, NVFP4KV_ROPE_SKIP><<<grid, kColdThreads, 0, s>>>(p);     \
+            launch_pdl(cold_offload_kernel<SRC, NVFP4KV_ROPE_SKIP>, grid, kColdThreads, 0, s, p);     \
         else if (p.rope_mode == NVFP4KV_ROPE_2FP4)                                            \
-            cold_offload_kernel<SRC, NVFP4KV_ROPE_2FP4><<<grid, kColdThreads, 0, s>>>(p);     \
+            launch_pdl(cold_offload_kernel<SRC, NVFP4KV_ROPE_2FP4>, grid, kColdThreads, 0, s, p);     \
         else                                                                                  \
-            cold_offload_kernel<SRC, NVFP4KV_ROPE_QUANTIZE><<<grid, kColdThreads, 0, s>>>(p); \
+            launch_pdl(cold_offload_kernel<SRC, NVFP4KV_ROPE_QUANTIZE>, grid, kColdThreads, 0, s, p); \
     } while (0)
     if (hot_dtype == NVFP4KV_BF16)
         NVFP4KV_OFF(NVFP4KV_BF16);
@@ -587,11 +589,11 @@ extern "C" nvfp4kv_status nvfp4_kv_onboard_pages(
 #define NVFP4KV_ON(DST)                                                                      \
     do {                                                                                     \
         if (p.rope_mode == NVFP4KV_ROPE_SKIP)                                                \
-            cold_onboard_kernel<DST, NVFP4KV_ROPE_SKIP><<<grid, kColdThreads, 0, s>>>(p);    \
+            launch_pdl(cold_onboard_kernel<DST, NVFP4KV_ROPE_SKIP>, grid, kColdThreads, 0, s, p);    \
         else if (p.rope_mode == NVFP4KV_ROPE_2FP4)                                           \
-            cold_onboard_kernel<DST, NVFP4KV_ROPE_2FP4><<<grid, kColdThreads, 0, s>>>(p);    \
+            launch_pdl(cold_onboard_kernel<DST, NVFP4KV_ROPE_2FP4>, grid, kColdThreads, 0, s, p);    \
         else                                                                                 \
-            cold_onboard_kernel<DST, NVFP4KV_ROPE_QUANTIZE><<<grid, kColdThreads, 0, s>>>(p); \
+            launch_pdl(cold_onboard_kernel<DST, NVFP4KV_ROPE_QUANTIZE>, grid, kColdThreads, 0, s, p); \
     } while (0)
     if (hot_dtype == NVFP4KV_BF16)
         NVFP4KV_ON(NVFP4KV_BF16);

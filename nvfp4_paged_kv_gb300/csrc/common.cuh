@@ -45,6 +45,14 @@ __device__ __forceinline__ uint32_t tagged_finish(unsigned long long* w, unsigne
     return 0xFFFFFFFFu;  // could not install the tag: report the pair as not finished
 }
 
+// Programmatic dependent launch: wait until the previous grid on the stream has completed and
+// its memory is visible (a no-op when the launch did not allow overlap), then let the next grid
+// be scheduled.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     if (status) atomicOr(status, bit);
 }

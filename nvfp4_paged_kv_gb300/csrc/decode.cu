@@ -203,6 +203,7 @@ __device__ __forceinline__ int seq_stages(int L, int max_tokens, int tok) {
 template <int D>
 __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
     decode_split_kernel(const DecodeParams p) {
+    pdl_enter();
     using G_ = Geo<D>;
     constexpr int TOK = G_::TOK;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -928,7 +929,9 @@ cudaError_t launch_decode(const DecodeParams& p, int64_t ctas, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Geo<D>::SMEM);
     if (e != cudaSuccess) return e;
-    decode_split_kernel<D><<<static_cast<unsigned>(ctas), kDecThreads, Geo<D>::SMEM, s>>>(p);
+    e = launch_pdl(decode_split_kernel<D>, static_cast<unsigned>(ctas), kDecThreads,
+                   static_cast<size_t>(Geo<D>::SMEM), s, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/nvfp4_kv.h"
@@ -51,6 +52,26 @@ inline uint32_t next_nonce() {
     uint32_t n = counter.fetch_add(1) + 1;
     if (n == 0) n = counter.fetch_add(1) + 1;
     return n;
+}
+
+// Launch with programmatic dependent launch allowed: the grid may be scheduled while the
+// previous kernel on the stream drains; every kernel of this library waits for the previous
+// grid (griddepcontrol.wait) before its first global memory access, so data dependencies on the
+// stream are kept.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 inline nvfp4kv_status launch_status() {

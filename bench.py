@@ -347,6 +347,33 @@ def time_kernel(fn, flush, reps=15):
     return statistics.median(ts)
 
 
+def error_vs_unquantized(q, k, v, pt, sl, out, sm_scale):
+    """What NVFP4 costs in accuracy: the decode output (NVFP4 K/V) against attention over the
+    unquantized BF16 K/V pages, computed here in plain PyTorch fp32 on the device (a reporting
+    reference, not part of the path)."""
+    import torch
+    B, Hq, D = q.shape
+    H, T = k.shape[1], k.shape[2]
+    G = Hq // H
+    diffs, refs = [], []
+    for b in range(B):
+        L = int(sl[b])
+        n = (L + T - 1) // T
+        ids = pt[b, :n].long()
+        kb = k[ids].permute(1, 0, 2, 3).reshape(H, n * T, D)[:, :L].float()
+        vb = v[ids].permute(1, 0, 2, 3).reshape(H, n * T, D)[:, :L].float()
+        qb = q[b].float().reshape(H, G, D)
+        s = torch.einsum("hgd,htd->hgt", qb, kb) * sm_scale
+        ref = torch.einsum("hgt,htd->hgd", torch.softmax(s, dim=-1), vb).reshape(Hq, D)
+        diffs.append((out[b].float() - ref).flatten())
+        refs.append(ref.flatten())
+    d = torch.cat(diffs)
+    rf = torch.cat(refs)
+    return {"vs": "attention over the unquantized BF16 K/V (PyTorch fp32)",
+            "max_abs": round(float(d.abs().max()), 6), "mean_abs": round(float(d.abs().mean()), 6),
+            "rel_rmse": round(float(d.pow(2).mean().sqrt() / rf.pow(2).mean().sqrt()), 6)}
+
+
 def kernel_table(path, peak):
     """Per-kernel achieved GB/s (L2 flushed before every launch), plus the decode-batch
     workload and the extend workload as extra single-kernel cases."""
@@ -395,10 +422,13 @@ def kernel_table(path, peak):
     kv.nvfp4_kv_compute_global_scale(lay, v, gv)
     kv.nvfp4_kv_quantize_pages(lay, k, gk, kd, ks)
     kv.nvfp4_kv_quantize_pages(lay.with_packing(kv.PACK_TOKEN_PAIRS), v, gv, vd, vs)
-    del k, v
     out = torch.empty((db.B, db.Hq, db.D), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(kv.nvfp4_paged_decode_workspace_size(lay, db.B, db.Hq, pt.shape[1], 0),
                      dtype=u8, device=dev)
+    kv.nvfp4_paged_decode_attention(lay, q, kd, ks, gk, vd, vs, gv, pt, sl, db.sm_scale, out,
+                                    workspace=ws)
+    qerr = error_vs_unquantized(q, k, v, pt, sl, out, db.sm_scale)
+    del k, v
     nbytes = db.kv_tokens * db.H * (db.D + db.D // 8) + db.B * db.Hq * db.D * 4 + \
         pt.numel() * 4 + db.B * 4
     add("decode (decode batch 32x8192, GQA 4)",
@@ -408,6 +438,7 @@ def kernel_table(path, peak):
     r = res["decode (decode batch 32x8192, GQA 4)"]
     r["decode_tokens_per_s"] = round(db.B / (r["ms"] * 1e-3), 1)
     r["kv_tokens_per_s"] = round(db.kv_tokens / (r["ms"] * 1e-3), 1)
+    r["error_vs_unquantized_bf16"] = qerr
     del kd, ks, vd, vs, q, out, ws
     # extend workload: gather + dequantize a 1024-page prefix into FP8, encode a 128-page chunk
     ex = synthetic.ExtendWorkload(seed=2)

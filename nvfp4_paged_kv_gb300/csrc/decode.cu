@@ -35,6 +35,10 @@
 //  * at the end of a piece the 4 warps merge (max, sum, output) in shared memory; a piece that
 //    is a whole pair writes the BF16 output and the natural-log LSE directly, otherwise the CTA
 //    writes its record and the pair's last CTA merges the records by log-sum-exp.
+//  * a piece boundary inside a run holds up the CTA as little as possible: the next piece's
+//    page ids are loaded into registers while the current piece streams, and the record's count
+//    is bumped by one lane while the CTA already streams the next piece; the outcome is read at
+//    that piece's end, where the CTA merges the pair if its count completed it.
 // Bytes per (token, KV head) at head_dim 128: 64 + 8 (K) + 64 + 8 (V) = 144.
 #include <atomic>
 #include <chrono>
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
     __shared__ int scan_warp[kWarps];
     __shared__ int start_bp[2];  // pair walk start: sequence, its first stage
     __shared__ int last_s;
+    __shared__ int pend_s[5];  // a pair whose count was bumped at the previous boundary: last?, b, h, start, stages
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
             acc += n;
         }
     }
+    if (tid == 0) pend_s[0] = 0;
     __syncthreads();
 
     // ------------------------------------------------ per-lane constants
@@ -304,11 +310,36 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         const int first_page = (j0 * TOK) / T;
         const int n_pages = (tok_end + T - 1) / T - first_page;
         const int32_t* pt_row = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-        if (!first_piece) __syncthreads();  // the previous merge is done with the rings
+        if (first_piece) {
+            for (int i = tid; i < n_pages && i < kPageBuf; i += kDecThreads)
+                page_ids[i] = __ldg(pt_row + first_page + i);
+            __syncthreads();
+        }
+        // (later pieces: their page ids were put in place before the previous piece's last barrier)
         first_piece = false;
-        for (int i = tid; i < n_pages && i < kPageBuf; i += kDecThreads)
-            page_ids[i] = __ldg(pt_row + first_page + i);
-        __syncthreads();
+        // the next piece of the run (the pair after (b, h), from its stage 0) and its page ids,
+        // loaded now so that they are in registers when this piece ends
+        const bool has_next = s + (j1 - j0) < s_end;
+        int nid[2] = {0, 0};
+        int nn_pages = 0;
+        if (has_next) {
+            int nb = b, nh = h + 1, nS = S_b;
+            if (nh == H) {
+                nh = 0;
+                do {
+                    ++nb;
+                    nS = seq_stages(__ldg(p.seq_lens + nb), max_tokens, TOK);
+                } while (nS == 0);
+            }
+            const int nj1 = min(nS, s_end - (pair_start + S_b));
+            nn_pages = (min(nj1 * TOK, __ldg(p.seq_lens + nb)) + T - 1) / T;
+            const int32_t* npt = p.page_table + static_cast<int64_t>(nb) * p.max_pages;
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int i = tid + q2 * kDecThreads;
+                if (i < nn_pages && i < kPageBuf) nid[q2] = __ldg(npt + i);
+            }
+        }
         auto page_of = [&](int pidx) {
             const int k = pidx - first_page;
             const int pg = (k < kPageBuf) ? page_ids[k] : __ldg(pt_row + pidx);
@@ -660,6 +691,9 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
             red_l[warp][2 * c + 1] = l1;
         }
         __syncthreads();  // every warp is done with its ring: the rings hold the merge buffer
+        // the outcome of the count bumped at the previous boundary (written before this barrier)
+        const int pend_last = pend_s[0];
+        const int pend_b = pend_s[1], pend_h = pend_s[2], pend_ps = pend_s[3], pend_S = pend_s[4];
         float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
@@ -693,6 +727,113 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         const int64_t bh64 = static_cast<int64_t>(b) * H + h;
         auto rec_index = [&](int k) -> int64_t { return c_first + k + bh64; };
         const float gvs = __ldg(p.gv);
+        // merge the records of pair (mb, mh) once all of them are written (by the CTA whose
+        // count completed them), writing its output and LSE
+        auto merge_records = [&](int mb, int mh, int mps, int mS) {
+            const int c_first_m = mps / W, c_last_m = (mps + mS - 1) / W;
+            const int n_rec_m = c_last_m - c_first_m + 1;
+            const int64_t bh_m = static_cast<int64_t>(mb) * H + mh;
+            auto rec_index_m = [&](int k) -> int64_t { return c_first_m + k + bh_m; };
+            // every record of the pair is written: merge them (L2 reads, not L1). The (max,
+            // sum) pairs of up to kMaxRecW records are staged in shared memory by one round
+            // of loads while the first records' outputs are already in flight.
+            __threadfence();
+            constexpr int NQ = kMaxGroup * D / kDecThreads;
+            constexpr int kRecUnroll = NQ >= 16 ? 2 : 8;  // record values in flight: 32 or 64
+            const int n_fast = min(n_rec_m, kMaxRecW);
+            for (int idx = tid; idx < n_fast * G; idx += kDecThreads) {
+                const int k = idx / G, col = idx - (idx / G) * G;
+                const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                    p.rec_ml + (rec_index_m(k) * G + col) * 2));
+                mw_s[k][col] = ml.x;
+                lw_s[k][col] = ml.y;
+            }
+            float v[kRecUnroll][NQ];
+            auto load_recs = [&](int k0) {
+#pragma unroll
+                for (int u = 0; u < kRecUnroll; ++u) {
+                    const int k = min(k0 + u, n_rec_m - 1);
+                    const float* rk = p.rec_o + rec_index_m(k) * G * D;
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        const int i = tid + kDecThreads * q;
+                        v[u][q] = (i < G * D) ? __ldcg(rk + i) : 0.0f;
+                    }
+                }
+            };
+            load_recs(0);
+            __syncthreads();
+            if (warp < G) {  // warp w: query heads w, w + 4
+                for (int col = warp; col < G; col += kWarps) {
+                    auto m_of = [&](int k) {
+                        return k < n_fast ? mw_s[k][col]
+                                          : __ldcg(p.rec_ml + (rec_index_m(k) * G + col) * 2);
+                    };
+                    float M = -INFINITY;
+                    for (int k = lane; k < n_rec_m; k += 32) M = fmaxf(M, m_of(k));
+#pragma unroll
+                    for (int o2 = 16; o2 > 0; o2 >>= 1)
+                        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o2));
+                    float lsum = 0.0f;
+                    for (int k = lane; k < n_rec_m; k += 32) {
+                        const float mk = m_of(k);
+                        const float lk = k < n_fast
+                                             ? lw_s[k][col]
+                                             : __ldcg(p.rec_ml + (rec_index_m(k) * G + col) * 2 + 1);
+                        const float wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
+                        if (k < n_fast) mw_s[k][col] = wk;  // this lane alone reads entry k
+                        lsum += wk * lk;
+                    }
+#pragma unroll
+                    for (int o2 = 16; o2 > 0; o2 >>= 1)
+                        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o2);
+                    if (lane == 0) {
+                        ml_s[col][0] = M;
+                        ml_s[col][1] = lsum;
+                        if (p.lse)
+                            p.lse[static_cast<int64_t>(mb) * p.Hq + mh * G + col] =
+                                (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f
+                                              : -INFINITY;
+                    }
+                }
+            }
+            __syncthreads();
+            // thread tid owns outputs i = tid + kDecThreads q; kRecUnroll records at a time
+            float acc[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) acc[q] = 0.0f;
+            for (int k0 = 0; k0 < n_rec_m; k0 += kRecUnroll) {
+                if (k0 > 0) load_recs(k0);
+#pragma unroll
+                for (int u = 0; u < kRecUnroll; ++u) {
+                    const int k = k0 + u;
+                    if (k >= n_rec_m) break;
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        const int i = tid + kDecThreads * q;
+                        if (i >= G * D) continue;
+                        const int col = i / D;
+                        float wk;
+                        if (k < n_fast) {
+                            wk = mw_s[k][col];
+                        } else {
+                            const float mk = __ldcg(p.rec_ml + (rec_index_m(k) * G + col) * 2);
+                            wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - ml_s[col][0]);
+                        }
+                        acc[q] += wk * v[u][q];
+                    }
+                }
+            }
+            uint16_t* ob = p.out + (static_cast<int64_t>(mb) * p.Hq + mh * G) * D;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const int i = tid + kDecThreads * q;
+                if (i >= G * D) continue;
+                const float ls = ml_s[i / D][1];
+                const __nv_bfloat16 yb = __float2bfloat16_rn(ls > 0.0f ? acc[q] * (gvs / ls) : 0.0f);
+                ob[i] = *reinterpret_cast<const uint16_t*>(&yb);
+            }
+        };
         if (n_rec == 1) {
             // the whole pair is this piece: normalise and write the output directly
             if (tid < G) {
@@ -745,115 +886,46 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                 p.rec_ml[(rec * G + tid) * 2] = M;
                 p.rec_ml[(rec * G + tid) * 2 + 1] = lsum;
             }
-            __syncthreads();  // the record is written ...
-            if (tid == 0) {
-                __threadfence();  // ... and visible before the count says so
-                unsigned long long* cnt = p.done + bh64;
-                const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
-                last_s = (k == static_cast<uint32_t>(n_rec - 1)) ? 1 : 0;
+        }
+        if (has_next) {
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int i = tid + q2 * kDecThreads;
+                if (i < nn_pages && i < kPageBuf) page_ids[i] = nid[q2];
             }
-            __syncthreads();
-            if (last_s) {
-                // every record of the pair is written: merge them (L2 reads, not L1). The (max,
-                // sum) pairs of up to kMaxRecW records are staged in shared memory by one round
-                // of loads while the first records' outputs are already in flight.
-                __threadfence();
-                constexpr int NQ = kMaxGroup * D / kDecThreads;
-                constexpr int kRecUnroll = NQ >= 16 ? 2 : 8;  // record values in flight: 32 or 64
-                const int n_fast = min(n_rec, kMaxRecW);
-                for (int idx = tid; idx < n_fast * G; idx += kDecThreads) {
-                    const int k = idx / G, col = idx - (idx / G) * G;
-                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-                        p.rec_ml + (rec_index(k) * G + col) * 2));
-                    mw_s[k][col] = ml.x;
-                    lw_s[k][col] = ml.y;
+        }
+        __syncthreads();  // outputs / record written, merge buffer read, next page ids in place
+        if (pend_last) {
+            merge_records(pend_b, pend_h, pend_ps, pend_S);
+            __syncthreads();  // the merge is done with the rings
+        }
+        if (n_rec > 1) {
+            if (has_next) {
+                // publish the record without holding up the next piece: one lane of the last
+                // warp makes it visible and bumps the count; the outcome is read at the next
+                // piece's end, where a completed pair is merged
+                if (warp == kWarps - 1 && lane == 0) {
+                    __threadfence();
+                    unsigned long long* cnt = p.done + bh64;
+                    const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
+                    pend_s[0] = (k == static_cast<uint32_t>(n_rec - 1)) ? 1 : 0;
+                    pend_s[1] = b;
+                    pend_s[2] = h;
+                    pend_s[3] = pair_start;
+                    pend_s[4] = S_b;
                 }
-                float v[kRecUnroll][NQ];
-                auto load_recs = [&](int k0) {
-#pragma unroll
-                    for (int u = 0; u < kRecUnroll; ++u) {
-                        const int k = min(k0 + u, n_rec - 1);
-                        const float* rk = p.rec_o + rec_index(k) * G * D;
-#pragma unroll
-                        for (int q = 0; q < NQ; ++q) {
-                            const int i = tid + kDecThreads * q;
-                            v[u][q] = (i < G * D) ? __ldcg(rk + i) : 0.0f;
-                        }
-                    }
-                };
-                load_recs(0);
-                __syncthreads();
-                if (warp < G) {  // warp w: query heads w, w + 4
-                    for (int col = warp; col < G; col += kWarps) {
-                        auto m_of = [&](int k) {
-                            return k < n_fast ? mw_s[k][col]
-                                              : __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);
-                        };
-                        float M = -INFINITY;
-                        for (int k = lane; k < n_rec; k += 32) M = fmaxf(M, m_of(k));
-#pragma unroll
-                        for (int o2 = 16; o2 > 0; o2 >>= 1)
-                            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o2));
-                        float lsum = 0.0f;
-                        for (int k = lane; k < n_rec; k += 32) {
-                            const float mk = m_of(k);
-                            const float lk = k < n_fast
-                                                 ? lw_s[k][col]
-                                                 : __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2 + 1);
-                            const float wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-                            if (k < n_fast) mw_s[k][col] = wk;  // this lane alone reads entry k
-                            lsum += wk * lk;
-                        }
-#pragma unroll
-                        for (int o2 = 16; o2 > 0; o2 >>= 1)
-                            lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o2);
-                        if (lane == 0) {
-                            ml_s[col][0] = M;
-                            ml_s[col][1] = lsum;
-                            if (p.lse)
-                                p.lse[static_cast<int64_t>(b) * p.Hq + h * G + col] =
-                                    (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f
-                                                  : -INFINITY;
-                        }
-                    }
+            } else {
+                if (tid == 0) {
+                    __threadfence();  // the record is visible before the count says so
+                    unsigned long long* cnt = p.done + bh64;
+                    const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
+                    last_s = (k == static_cast<uint32_t>(n_rec - 1)) ? 1 : 0;
                 }
                 __syncthreads();
-                // thread tid owns outputs i = tid + kDecThreads q; kRecUnroll records at a time
-                float acc[NQ];
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) acc[q] = 0.0f;
-                for (int k0 = 0; k0 < n_rec; k0 += kRecUnroll) {
-                    if (k0 > 0) load_recs(k0);
-#pragma unroll
-                    for (int u = 0; u < kRecUnroll; ++u) {
-                        const int k = k0 + u;
-                        if (k >= n_rec) break;
-#pragma unroll
-                        for (int q = 0; q < NQ; ++q) {
-                            const int i = tid + kDecThreads * q;
-                            if (i >= G * D) continue;
-                            const int col = i / D;
-                            float wk;
-                            if (k < n_fast) {
-                                wk = mw_s[k][col];
-                            } else {
-                                const float mk = __ldcg(p.rec_ml + (rec_index(k) * G + col) * 2);
-                                wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - ml_s[col][0]);
-                            }
-                            acc[q] += wk * v[u][q];
-                        }
-                    }
-                }
-                uint16_t* ob = p.out + (static_cast<int64_t>(b) * p.Hq + h * G) * D;
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const int i = tid + kDecThreads * q;
-                    if (i >= G * D) continue;
-                    const float ls = ml_s[i / D][1];
-                    const __nv_bfloat16 yb = __float2bfloat16_rn(ls > 0.0f ? acc[q] * (gvs / ls) : 0.0f);
-                    ob[i] = *reinterpret_cast<const uint16_t*>(&yb);
-                }
+                if (last_s) merge_records(b, h, pair_start, S_b);
             }
+        } else if (has_next && warp == kWarps - 1 && lane == 0) {
+            pend_s[0] = 0;
         }
 
         // ---- next piece: the next pair with at least one stage

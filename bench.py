@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip per-kernel timings")
     ap.add_argument("--clock-window", type=float, default=1.0,
@@ -768,6 +769,8 @@ def main():
         "clocks": clocks,
         "gpu_launches": path.launches_per_step * args.steps,
     }
+    if not args.no_graph:
+        result["graph"] = graph_replay(path, args, world, step_bytes, peak)
     if not args.no_kernels and rank == 0:
         result["kernels"] = kernel_table(path, peak)
         result["global_scale_study"] = global_scale_study(path)
@@ -784,6 +787,32 @@ def main():
                                   "seconds": round(t, 2)}
     if rank == 0:
         print(json.dumps(result))
+
+
+def graph_replay(path, args, world, step_bytes, peak):
+    """The same step captured once in a CUDA graph and replayed (the 9 launches of a step go
+    to the GPU as one graph launch); reported beside the eager number, not instead of it."""
+    import torch
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        path.step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        graph.replay()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = dist_max(start.elapsed_time(end), world) / args.steps
+    value = step_bytes * world / (ms * 1e-3) / GB
+    del graph
+    return {"value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "frac_of_peak": round(value / world / peak, 4)}
 
 
 def e2e(path, args, world):

@@ -115,8 +115,11 @@ int32_t nvfp4kv_version(void);
  *   src_scale      FP8 sources only: device scalar, x = fp32(e4m3 * src_scale) (NULL = 1)
  *   global_scale_out  device float written with g
  *   workspace      device scratch of nvfp4_kv_global_scale_workspace_size() bytes (16): a
- *                  tagged maximum and a tagged count; never needs clearing; calls that can
- *                  overlap on the GPU must not share it
+ *                  tagged maximum and a tagged count; never needs clearing (a word left by
+ *                  another call or holding garbage is replaced through its tag), and the CTA
+ *                  that finishes last sets both words back to 0, so a replayed CUDA graph that
+ *                  repeats a captured call (same tag) starts clean; calls that can overlap on
+ *                  the GPU must not share it
  * One launch: the CTA that finishes last writes g. num_pages == 0 writes g = 1.
  * ------------------------------------------------------------------------------------------ */
 size_t nvfp4_kv_global_scale_workspace_size(void);
@@ -214,7 +217,9 @@ nvfp4kv_status nvfp4_kv_extend_write(const nvfp4kv_layout* layout, nvfp4kv_dtype
  * stages of all pairs form one list, and the list is cut into equal runs, one per CTA. Each
  * (run, pair) piece leaves a partial (max, sum, unnormalised output) in the workspace; the last
  * CTA to finish a pair merges its partials and writes the outputs (one kernel launch). The
- * workspace needs no initialisation: its counters carry a per-call tag.
+ * workspace needs no initialisation: its counters carry a per-call tag, and the CTA that merges
+ * a pair sets that pair's counter back to 0, so a replayed CUDA graph that repeats a captured
+ * call (same tag) starts clean.
  *   q              BF16 [batch][num_q_heads][D]
  *   k_data, k_scales   NVFP4 K pool in NVFP4KV_PACK_DIM_PAIRS (layout.packing is not read)
  *   v_data, v_scales   NVFP4 V pool in NVFP4KV_PACK_TOKEN_PAIRS

@@ -499,6 +499,10 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) 
                                       ? static_cast<uint32_t>(w)
                                       : 0u;
             *p.out = global_scale_of<SRC>(best, p.src_scale);
+            // every CTA has counted: both words go back to 0, so a replay of the same launch
+            // (a captured CUDA graph, same tag) starts clean
+            atomicExch(p.word, 0ull);
+            atomicExch(p.word + 1, 0ull);
         }
     }
 }

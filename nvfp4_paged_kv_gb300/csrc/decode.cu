@@ -738,6 +738,9 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
             // sum) pairs of up to kMaxRecW records are staged in shared memory by one round
             // of loads while the first records' outputs are already in flight.
             __threadfence();
+            // every CTA of the pair has counted, so the count can go back to 0: a replay of the
+            // same launch (a captured CUDA graph, same tag) starts from a clean word
+            if (tid == 0) atomicExch(p.done + bh_m, 0ull);
             constexpr int NQ = kMaxGroup * D / kDecThreads;
             constexpr int kRecUnroll = NQ >= 16 ? 2 : 8;  // record values in flight: 32 or 64
             const int n_fast = min(n_rec_m, kMaxRecW);

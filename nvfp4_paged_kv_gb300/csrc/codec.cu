@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const Dequan
 // of fp32(e4m3 * src_scale) is fp32(max|e4m3| * |src_scale|) because rounding is monotone.
 // ------------------------------------------------------------------------------------------
 constexpr int kAmaxThreads = 256;
-constexpr int kAmaxMaxCtas = 2048;
 constexpr int kAmaxLoads = 8;   // 16-byte loads per thread per item (128 bytes in flight)
 
 struct AmaxParams {
@@ -571,13 +570,17 @@ extern "C" nvfp4kv_status nvfp4_kv_compute_global_scale(
     p.src_scale = src_scale;
     p.out = global_scale_out;
     p.status = status;
-    int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
-    if (grid > kAmaxMaxCtas) grid = kAmaxMaxCtas;
+    // one wave of resident CTAs: each CTA reads its items and raises the maximum once (a CTA
+    // that waited for a slot would read its whole share after the others have finished)
+    const int64_t items = static_cast<int64_t>(num_pages) * p.items_per_page;
+#define NVFP4KV_ALAUNCH(SRC) \
+    launch_pdl(amax_kernel<SRC>, wave_grid<amax_kernel<SRC>>(items, kAmaxThreads), kAmaxThreads, 0, s, p)
     switch (src_dtype) {
-    case NVFP4KV_BF16: launch_pdl(amax_kernel<NVFP4KV_BF16>, grid, kAmaxThreads, 0, s, p); break;
-    case NVFP4KV_FP16: launch_pdl(amax_kernel<NVFP4KV_FP16>, grid, kAmaxThreads, 0, s, p); break;
-    default: launch_pdl(amax_kernel<NVFP4KV_FP8_E4M3>, grid, kAmaxThreads, 0, s, p); break;
+    case NVFP4KV_BF16: NVFP4KV_ALAUNCH(NVFP4KV_BF16); break;
+    case NVFP4KV_FP16: NVFP4KV_ALAUNCH(NVFP4KV_FP16); break;
+    default: NVFP4KV_ALAUNCH(NVFP4KV_FP8_E4M3); break;
     }
+#undef NVFP4KV_ALAUNCH
     return launch_status();
 }
 

@@ -54,6 +54,29 @@ inline uint32_t next_nonce() {
     return n;
 }
 
+// CTAs of `Kernel` (with `threads` threads and `smem` bytes of dynamic shared memory) that fit on
+// one SM at once, asked of the runtime once per kernel (at least 1).
+template <auto Kernel>
+inline int resident_ctas(int threads, size_t smem) {
+    static const int n = [&] {
+        int v = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, Kernel, threads, smem) != cudaSuccess ||
+            v < 1)
+            v = 1;
+        return v;
+    }();
+    return n;
+}
+
+// Grid of a grid-strided kernel over `items` work items: one full wave of resident CTAs (no CTA
+// waits for a slot and then runs its share of items after the others have finished), or fewer
+// CTAs when there are fewer items.
+template <auto Kernel>
+inline int wave_grid(int64_t items, int threads, size_t smem = 0) {
+    const int64_t cap = static_cast<int64_t>(num_sms()) * resident_ctas<Kernel>(threads, smem);
+    return static_cast<int>(items < cap ? (items < 1 ? 1 : items) : cap);
+}
+
 // Launch with programmatic dependent launch allowed: the grid may be scheduled while the
 // previous kernel on the stream drains; every kernel of this library waits for the previous
 // grid (griddepcontrol.wait) before its first global memory access, so data dependencies on the

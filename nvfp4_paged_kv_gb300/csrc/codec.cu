@@ -66,8 +66,18 @@ __device__ __forceinline__ uint4 fp8_block(const float (&x)[16], float m) {
 // or NVFP4KV_PACK_TOKEN_PAIRS (a unit is the same block of tokens 2p and 2p+1; the E2M1 pair
 // conversion of (token 2p, token 2p+1) at one head dim is directly the interleaved byte).
 // WS: also write the FP8 workspace copy of every source block (the extend path's fused write).
+// CTAs per SM the register budget must allow: 4 for the plain encode (64 registers; the
+// dim-pair variant would take 70 and fit only 3, and 4 means a third more loads in flight:
+// 56.0 -> 53.3 us on 268 MB of BF16), 3 for the FP16 token-pair encode (held at 64 it spills
+// heavily), none (0) for the extend write, whose variants keep the compiler's own choice.
+template <int SRC, int PACK, bool WS>
+constexpr int quantize_min_ctas() {
+    return WS ? 0 : ((SRC == NVFP4KV_FP16 && PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? 3 : 4);
+}
+
 template <int SRC, bool A32, int PACK, bool WS = false>
-__global__ void __launch_bounds__(kThreads) quantize_pages_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, quantize_min_ctas<SRC, PACK, WS>())
+    quantize_pages_kernel(const QuantParams p) {
     pdl_enter();
     constexpr int kUnitsPerThread = (PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? kBlocksPerThread / 2
                                                                         : kBlocksPerThread;

@@ -780,7 +780,11 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     p.items_per_page = (p.units + kItemBlocks - 1) / kItemBlocks;
     p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
+    // up to 32 CTAs per SM, several waves of short-lived CTAs (one or two 32 KB items each): the
+    // block scheduler then hands the remaining items to whichever SM frees a slot first, which
+    // evens out the SMs' different streaming rates (BF16 out 57.3 -> 53.2 us, FP8 out 34.8 ->
+    // 32.8 us on 4096 pages against 8 CTAs per SM)
+    const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 32);
 #define NVFP4KV_DQLAUNCH(DST)                                                                \
     do {                                                                                      \
         if (pack == NVFP4KV_PACK_TOKEN_PAIRS)                                                 \

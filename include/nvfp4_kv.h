@@ -25,7 +25,8 @@
  *   reduces over head dims for Q.K (dim pairs feed its matmul directly) and over tokens for P.V
  *   (token pairs feed it directly).
  *   16/8-bit pages (BF16 / FP16 / FP8 E4M3 sources and outputs): [pool_pages][H][T][D]
- *   The two NVFP4 pools are read together by attention (TensorRT LLM page, Figure 6: "two pools").
+ *   The two NVFP4 pools are read together by attention (TensorRT LLM page, Figure 6: the codes
+ *   and the scales sit in separate pools).
  *
  * Numerics (all bit-exact and reproducible; g is the FP32 tensor scale):
  *   encode  a = max |x| over the block; s = E4M3_rne_satfinite(fp32(a / fp32(6 g)));
@@ -42,7 +43,10 @@
  *   - Every pointer except `layout` is device memory owned by the caller; the library never
  *     allocates, frees or synchronises. Work is enqueued on `stream` (may be 0) and returns
  *     without waiting; scalars that come from earlier GPU work (global scales) are passed by
- *     device pointer so a sequence of calls needs no host round trip.
+ *     device pointer so a sequence of calls needs no host round trip, and such a sequence can be
+ *     captured into a CUDA graph and replayed. Kernels are launched with programmatic dependent
+ *     launch: each waits for the earlier work on the stream to complete before it touches
+ *     memory (stream order is kept), while its launch overlaps the end of the previous kernel.
  *   - The return value reports host-side validation (NVFP4KV_ERR_INVALID_ARG /
  *     NVFP4KV_ERR_UNSUPPORTED / NVFP4KV_ERR_WORKSPACE) and launch failures (NVFP4KV_ERR_CUDA).
  *     On an error nothing is enqueued.

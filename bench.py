@@ -883,10 +883,28 @@ def e2e(path, args, world):
     torch.cuda.synchronize()
     barrier(world)
     ms = dist_max(a.elapsed_time(b), world) / n
+
+    # the host link as these pinned buffers see it, alone: one copy each way of the largest
+    # input and output buffers (context for the figure above, which is bound by this link)
+    def link_gbs(stream, dst, src):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)    # warm
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return round(src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / GB, 1)
+
+    big_in = max(range(len(h_in)), key=lambda i: h_in[i].numel() * h_in[i].element_size())
+    big_out = max(range(len(h_out[0])), key=lambda i: h_out[0][i].numel() * h_out[0][i].element_size())
+    h2d_gbs = link_gbs(s_in, ins_of(path)[big_in], h_in[big_in])
+    d2h_gbs = link_gbs(s_out, h_out[0][big_out], outs_of(path)[big_out])
     return {"value": round(path.step_bytes * world / (ms * 1e-3) / GB, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 3), "pipelined": "2 buffer sets, 3 streams",
-            "resident": "the long-context NVFP4 cache (filled once by the encoder)"}
+            "resident": "the long-context NVFP4 cache (filled once by the encoder)",
+            "link_alone_GB_s": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
 def profile_case(kv, dev, case):

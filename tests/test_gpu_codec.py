@@ -79,7 +79,8 @@ def test_rounding_exhaustive_fp32(kv, cuda, target):
 
 @pytest.mark.parametrize("kind", ["bf16", "fp16", "fp8"])
 @pytest.mark.parametrize("shape", [(7, 3, 5, 48), (33, 8, 32, 128), (5, 2, 64, 256),
-                                   (1, 1, 1, 16), (300, 2, 16, 64), (6, 3, 6, 48)])
+                                   (1, 1, 1, 16), (300, 2, 16, 64), (6, 3, 6, 48),
+                                   (9, 2, 256, 128)])
 @pytest.mark.parametrize("ids", [False, True])
 @pytest.mark.parametrize("pack", [0, 1])
 def test_quantize_parity(kv, cuda, kind, shape, ids, pack):

@@ -129,7 +129,7 @@ def test_quantize_parity(kv, cuda, kind, shape, ids, pack):
 
 @pytest.mark.parametrize("out_kind", ["bf16", "fp16", "fp8"])
 @pytest.mark.parametrize("shape", [(9, 3, 16, 48), (40, 8, 32, 128), (1, 1, 1, 16),
-                                   (3, 2, 2, 256), (5, 1, 3, 80)])
+                                   (3, 2, 2, 256), (5, 1, 3, 80), (9, 2, 256, 128)])
 @pytest.mark.parametrize("pack", [0, 1])
 def test_dequantize_parity(kv, cuda, out_kind, shape, pack):
     P, H, T, D = shape

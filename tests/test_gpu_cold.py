@@ -39,7 +39,7 @@ def _scalar(x, dev):
 
 # (H, T, D): small; 2304 blocks per tensor (two work items, ragged second); 15 blocks per
 # tensor (every part padded to 16 bytes)
-SHAPES = [(2, 16, 64), (4, 64, 144), (1, 3, 80)]
+SHAPES = [(2, 16, 64), (4, 64, 144), (1, 3, 80), (8, 32, 128)]
 
 
 @pytest.mark.parametrize("kind", ["bf16", "fp16"])

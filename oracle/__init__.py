@@ -33,53 +33,65 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-           "-Wall", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_to(_SRC, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def compile_to(src: str, out: str) -> str:
+    """Compile an oracle C source (this one, or a copy with a deliberate mistake planted by the
+    tests that check the pins catch it) to the shared library `out`, with the oracle's flags."""
+    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-Wall", "-shared", "-fPIC", src, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def bind(path: str):
+    """The oracle library at `path` with the argument types of every exported function."""
+    lib = ctypes.CDLL(path)
+    d, i, p, sz = ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    sig = {
+        "orc_max_threads": (i, []),
+        "orc_set_threads": (None, [i]),
+        "orc_round_to_format": (d, [d, i, i]),
+        "orc_fp32": (d, [d]),
+        "orc_bf16_round": (d, [d]),
+        "orc_fp16_round": (d, [d]),
+        "orc_e2m1_value": (d, [i]),
+        "orc_e2m1_encode": (i, [d]),
+        "orc_e4m3_value": (d, [i]),
+        "orc_e4m3_encode": (i, [d]),
+        "orc_bf16_value": (d, [i]),
+        "orc_bf16_bits": (i, [d]),
+        "orc_fp16_value": (d, [i]),
+        "orc_fp16_bits": (i, [d]),
+        "orc_e2m1_encode_f32": (None, [p, sz, p]),
+        "orc_e4m3_encode_f32": (None, [p, sz, p]),
+        "orc_tensor_amax": (d, [i, i, i, i, p, p, i, d]),
+        "orc_global_scale_from_amax": (d, [d]),
+        "orc_quantize_pages": (None, [i, i, i, i, i, p, p, d, d, p, p, p, i]),
+        "orc_cast_fp8_pages": (None, [i, i, i, i, p, p, d, d, p, p, i]),
+        "orc_encode_2fp4_blocks": (None, [i, i, p, d, p, p, p, p]),
+        "orc_decode_2fp4_blocks": (None, [i, p, p, p, p, d, i, p]),
+        "orc_dequantize_pages": (None, [i, i, i, i, p, p, p, d, i, p, p, d, i]),
+        "orc_paged_decode_attention": (None, [i, i, i, i, i, i, i, p, p, p, d, p, p, d,
+                                              p, i, p, d, p, p, p]),
+        "orc_paged_decode_attention_bf16": (None, [i, i, i, i, i, p, p, p, p, i, p,
+                                                   d, p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            d, i, p, sz = ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
-            sig = {
-                "orc_max_threads": (i, []),
-                "orc_set_threads": (None, [i]),
-                "orc_round_to_format": (d, [d, i, i]),
-                "orc_fp32": (d, [d]),
-                "orc_bf16_round": (d, [d]),
-                "orc_fp16_round": (d, [d]),
-                "orc_e2m1_value": (d, [i]),
-                "orc_e2m1_encode": (i, [d]),
-                "orc_e4m3_value": (d, [i]),
-                "orc_e4m3_encode": (i, [d]),
-                "orc_bf16_value": (d, [i]),
-                "orc_bf16_bits": (i, [d]),
-                "orc_fp16_value": (d, [i]),
-                "orc_fp16_bits": (i, [d]),
-                "orc_e2m1_encode_f32": (None, [p, sz, p]),
-                "orc_e4m3_encode_f32": (None, [p, sz, p]),
-                "orc_tensor_amax": (d, [i, i, i, i, p, p, i, d]),
-                "orc_global_scale_from_amax": (d, [d]),
-                "orc_quantize_pages": (None, [i, i, i, i, i, p, p, d, d, p, p, p, i]),
-                "orc_cast_fp8_pages": (None, [i, i, i, i, p, p, d, d, p, p, i]),
-                "orc_encode_2fp4_blocks": (None, [i, i, p, d, p, p, p, p]),
-                "orc_decode_2fp4_blocks": (None, [i, p, p, p, p, d, i, p]),
-                "orc_dequantize_pages": (None, [i, i, i, i, p, p, p, d, i, p, p, d, i]),
-                "orc_paged_decode_attention": (None, [i, i, i, i, i, i, i, p, p, p, d, p, p, d,
-                                                      p, i, p, d, p, p, p]),
-                "orc_paged_decode_attention_bf16": (None, [i, i, i, i, i, p, p, p, p, i, p,
-                                                           d, p]),
-            }
-            for name, (res, args) in sig.items():
-                fn = getattr(lib, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = lib
+            _lib = bind(build())
     return _lib
 
 

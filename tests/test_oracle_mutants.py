@@ -6,13 +6,16 @@ it, and runs a battery of the pin tests: at least one of them must fail. The mis
 kinds a reader of the pages could make: a rounding tie broken the wrong way, the nibble order
 swapped, a factor of the scale pick dropped, the global scale left out of the reciprocal or of
 the decode, the wrong global-scale constant, no saturation of the block scale, the softmax
-scale dropped, the wrong query-head to KV-head map, the LSE in the wrong logarithm."""
+scale dropped, the wrong query-head to KV-head map, the LSE in the wrong logarithm, the FP8
+workspace copy scaled the wrong way, the two tokens of a token pair swapped, the two-component
+(2FP4) residual taken with the wrong sign."""
 import numpy as np
 import pytest
 
 import oracle
 import test_oracle_attention as ta
 import test_oracle_codec as tc
+import test_oracle_cold as tco
 import test_oracle_format as tf
 
 MUTANTS = [
@@ -42,6 +45,13 @@ MUTANTS = [
      [("            int h = qh / G;", "            int h = qh % H;")]),
     ("LSE in log2",
      [("lse[(size_t)b * Hq + qh] = zmax + log(l);", "lse[(size_t)b * Hq + qh] = zmax + log2(l);")]),
+    ("FP8 workspace copy multiplied by ws_scale instead of its reciprocal",
+     [("    double m = fp32(1.0 / fp32(ws_scale)); /* FP32 scalar and its FP32 reciprocal */",
+       "    double m = fp32(ws_scale);")]),
+    ("token pairs: the two tokens of a pair swapped",
+     [("        *hi = t & 1;", "        *hi = (t + 1) & 1;")]),
+    ("2FP4 residual with the wrong sign",
+     [("            r[k] = fp32(x[k] - fp32(v1 * g));", "            r[k] = fp32(x[k] + fp32(v1 * g));")]),
 ]
 
 BATTERY = [
@@ -62,6 +72,9 @@ BATTERY = [
     (ta.test_gqa_head_mapping, ()),
     (ta.test_two_tokens_closed_form, ()),
     (ta.test_dominant_score_selects_its_value, ()),
+    (tc.test_fp8_copy_scales_by_the_reciprocal_of_ws_scale, ()),
+    (tc.test_token_pair_positions, ()),
+    (tco.test_2fp4_second_component_encodes_the_first_ones_error, (0.0123,)),
 ]
 
 

@@ -9,6 +9,7 @@ PyTorch is used for device memory and streams only.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -155,12 +156,27 @@ def _ptr(t: Optional[torch.Tensor]):
     return t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
-    if stream is None:
-        return torch.cuda.current_stream().cuda_stream
-    if isinstance(stream, torch.cuda.Stream):
-        return stream.cuda_stream
-    return int(stream)
+@contextlib.contextmanager
+def _on_device(tensors, stream):
+    """Make the device of the call's CUDA tensors current for the library call and yield the
+    stream handle to pass: `stream` if given (it must be a stream of that device), else that
+    device's current torch stream. The library sizes grids for the current device and launches on
+    the given stream, so a call whose tensors live on another GPU than the current one must not
+    go out on the current device's stream."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor) and t.is_cuda}
+    if len(devs) > 1:
+        raise ValueError("all CUDA tensors of one call must be on one device, got "
+                         + ", ".join(sorted(str(d) for d in devs)))
+    dev = devs.pop() if devs else torch.device("cuda", torch.cuda.current_device())
+    if isinstance(stream, torch.cuda.Stream) and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device} but the tensors are on {dev}")
+    with torch.cuda.device(dev):
+        if stream is None:
+            yield torch.cuda.current_stream(dev).cuda_stream
+        elif isinstance(stream, torch.cuda.Stream):
+            yield stream.cuda_stream
+        else:
+            yield int(stream)
 
 
 def _check(fn: str, code: int):
@@ -203,10 +219,11 @@ def nvfp4_kv_compute_global_scale(layout: Layout, src: torch.Tensor, out: torch.
     if workspace is None:
         workspace = torch.empty(nvfp4_kv_global_scale_workspace_size(), dtype=torch.uint8,
                                 device=src.device)
-    code = lib.nvfp4_kv_compute_global_scale(
-        ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
-        _ids(src_page_ids), int(num_pages), _ptr(src_scale), _ptr(out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    with _on_device((src, out, src_page_ids, src_scale, workspace, status), stream) as s:
+        code = lib.nvfp4_kv_compute_global_scale(
+            ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
+            _ids(src_page_ids), int(num_pages), _ptr(src_scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(status), s)
     _check("nvfp4_kv_compute_global_scale", code)
     return out
 
@@ -220,11 +237,13 @@ def nvfp4_kv_quantize_pages(layout: Layout, src: torch.Tensor, global_scale: tor
     lib = load()
     if num_pages is None:
         num_pages = src_page_ids.numel() if src_page_ids is not None else src.shape[0]
-    code = lib.nvfp4_kv_quantize_pages(
-        ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
-        _ids(src_page_ids), _ptr(src_scale), _ptr(global_scale), _ptr(dst_data),
-        _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), int(num_pages), _ptr(status),
-        _stream(stream))
+    with _on_device((src, global_scale, dst_data, dst_scales, src_page_ids, dst_page_ids,
+                     src_scale, status), stream) as s:
+        code = lib.nvfp4_kv_quantize_pages(
+            ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
+            _ids(src_page_ids), _ptr(src_scale), _ptr(global_scale), _ptr(dst_data),
+            _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), int(num_pages), _ptr(status),
+            s)
     _check("nvfp4_kv_quantize_pages", code)
 
 
@@ -239,11 +258,13 @@ def nvfp4_kv_extend_write(layout: Layout, src: torch.Tensor, global_scale: torch
     lib = load()
     if num_pages is None:
         num_pages = src_page_ids.numel() if src_page_ids is not None else src.shape[0]
-    code = lib.nvfp4_kv_extend_write(
-        ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
-        _ids(src_page_ids), _ptr(src_scale), _ptr(global_scale), _ptr(dst_data),
-        _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), _ptr(ws_fp8), ws_fp8.shape[0],
-        _ids(ws_page_ids), _ptr(ws_scale), int(num_pages), _ptr(status), _stream(stream))
+    with _on_device((src, global_scale, dst_data, dst_scales, ws_fp8, src_page_ids, dst_page_ids,
+                     ws_page_ids, src_scale, ws_scale, status), stream) as s:
+        code = lib.nvfp4_kv_extend_write(
+            ctypes.byref(layout), _dtype_code(src, src_dtype), _ptr(src), src.shape[0],
+            _ids(src_page_ids), _ptr(src_scale), _ptr(global_scale), _ptr(dst_data),
+            _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), _ptr(ws_fp8), ws_fp8.shape[0],
+            _ids(ws_page_ids), _ptr(ws_scale), int(num_pages), _ptr(status), s)
     _check("nvfp4_kv_extend_write", code)
 
 
@@ -255,11 +276,13 @@ def nvfp4_kv_dequantize_pages(layout: Layout, src_data: torch.Tensor, src_scales
     lib = load()
     if num_pages is None:
         num_pages = src_page_ids.numel() if src_page_ids is not None else src_data.shape[0]
-    code = lib.nvfp4_kv_dequantize_pages(
-        ctypes.byref(layout), _ptr(src_data), _ptr(src_scales), src_data.shape[0],
-        _ids(src_page_ids), _ptr(global_scale), _dtype_code(dst, dst_dtype), _ptr(dst),
-        dst.shape[0], _ids(dst_page_ids), _ptr(dst_scale), int(num_pages), _ptr(status),
-        _stream(stream))
+    with _on_device((src_data, src_scales, global_scale, dst, src_page_ids, dst_page_ids,
+                     dst_scale, status), stream) as s:
+        code = lib.nvfp4_kv_dequantize_pages(
+            ctypes.byref(layout), _ptr(src_data), _ptr(src_scales), src_data.shape[0],
+            _ids(src_page_ids), _ptr(global_scale), _dtype_code(dst, dst_dtype), _ptr(dst),
+            dst.shape[0], _ids(dst_page_ids), _ptr(dst_scale), int(num_pages), _ptr(status),
+            s)
     _check("nvfp4_kv_dequantize_pages", code)
 
 
@@ -285,12 +308,14 @@ def nvfp4_paged_decode_attention(layout: Layout, q: torch.Tensor, k_data, k_scal
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("page_table and seq_lens must be int32")
-    code = lib.nvfp4_paged_decode_attention(
-        ctypes.byref(layout), B, Hq, _ptr(q), _ptr(k_data), _ptr(k_scales),
-        _ptr(k_global_scale), _ptr(v_data), _ptr(v_scales), _ptr(v_global_scale),
-        k_data.shape[0], _ptr(page_table), maxp, _ptr(seq_lens), float(sm_scale),
-        int(max_num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    with _on_device((q, k_data, k_scales, k_global_scale, v_data, v_scales, v_global_scale,
+                     page_table, seq_lens, out, lse, workspace, status), stream) as s:
+        code = lib.nvfp4_paged_decode_attention(
+            ctypes.byref(layout), B, Hq, _ptr(q), _ptr(k_data), _ptr(k_scales),
+            _ptr(k_global_scale), _ptr(v_data), _ptr(v_scales), _ptr(v_global_scale),
+            k_data.shape[0], _ptr(page_table), maxp, _ptr(seq_lens), float(sm_scale),
+            int(max_num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(out), _ptr(lse), _ptr(status), s)
     _check("nvfp4_paged_decode_attention", code)
     return out
 
@@ -307,20 +332,23 @@ def nvfp4_paged_decode_attention_noalloc(layout: Layout, q: torch.Tensor, k_data
     B, Hq, _ = q.shape
     if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("page_table and seq_lens must be int32")
-    code = lib.nvfp4_paged_decode_attention_noalloc(
-        ctypes.byref(layout), B, Hq, _ptr(q), _ptr(k_data), _ptr(k_scales),
-        _ptr(k_global_scale), _ptr(v_data), _ptr(v_scales), _ptr(v_global_scale),
-        k_data.shape[0], _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
-        float(sm_scale), int(max_num_splits), _ptr(out), _ptr(lse), _ptr(status),
-        _stream(stream))
+    with _on_device((q, k_data, k_scales, k_global_scale, v_data, v_scales, v_global_scale,
+                     page_table, seq_lens, out, lse, status), stream) as s:
+        code = lib.nvfp4_paged_decode_attention_noalloc(
+            ctypes.byref(layout), B, Hq, _ptr(q), _ptr(k_data), _ptr(k_scales),
+            _ptr(k_global_scale), _ptr(v_data), _ptr(v_scales), _ptr(v_global_scale),
+            k_data.shape[0], _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
+            float(sm_scale), int(max_num_splits), _ptr(out), _ptr(lse), _ptr(status),
+            s)
     _check("nvfp4_paged_decode_attention_noalloc", code)
     return out
 
 
 def nvfp4_kv_round_f32(x: torch.Tensor, target: int, out: torch.Tensor, stream=None):
     """target 0: E2M1 codes, target 1: E4M3 bytes, of fp32 inputs (one byte each)."""
-    code = load().nvfp4_kv_round_f32(_ptr(x), x.numel(), int(target), _ptr(out),
-                                     _stream(stream))
+    with _on_device((x, out), stream) as s:
+        code = load().nvfp4_kv_round_f32(_ptr(x), x.numel(), int(target), _ptr(out),
+                                         s)
     _check("nvfp4_kv_round_f32", code)
 
 
@@ -391,11 +419,13 @@ def nvfp4_kv_offload_pages(layout: Layout, hot_k: torch.Tensor, hot_v: torch.Ten
     if num_pages is None:
         num_pages = hot_page_ids.numel() if hot_page_ids is not None else hot_k.shape[0]
     ep, es, eb = _extra_args(extra, extra_bytes)
-    code = lib.nvfp4_kv_offload_pages(
-        ctypes.byref(layout), _dtype_code(hot_k, hot_dtype), kp, vp, ks, hot_k.shape[0],
-        _ids(hot_page_ids), _ptr(k_global_scale), _ptr(v_global_scale), _rope_ref(rope), ep, es,
-        eb, _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids), int(num_pages),
-        _ptr(status), _stream(stream))
+    with _on_device((hot_k, hot_v, cold, k_global_scale, v_global_scale, hot_page_ids,
+                     cold_slot_ids, extra, status), stream) as s:
+        code = lib.nvfp4_kv_offload_pages(
+            ctypes.byref(layout), _dtype_code(hot_k, hot_dtype), kp, vp, ks, hot_k.shape[0],
+            _ids(hot_page_ids), _ptr(k_global_scale), _ptr(v_global_scale), _rope_ref(rope), ep, es,
+            eb, _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids), int(num_pages),
+            _ptr(status), s)
     _check("nvfp4_kv_offload_pages", code)
 
 
@@ -414,11 +444,13 @@ def nvfp4_kv_onboard_pages(layout: Layout, cold: torch.Tensor, hot_k: torch.Tens
     if num_pages is None:
         num_pages = cold_slot_ids.numel() if cold_slot_ids is not None else cold.numel() // bl.bytes
     ep, es, eb = _extra_args(extra, extra_bytes)
-    code = lib.nvfp4_kv_onboard_pages(
-        ctypes.byref(layout), _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids),
-        _ptr(k_global_scale), _ptr(v_global_scale), _rope_ref(rope),
-        _dtype_code(hot_k, hot_dtype), kp, vp, ks,
-        hot_k.shape[0], _ids(hot_page_ids), ep, es, eb, int(num_pages), _ptr(status),
-        _stream(stream))
+    with _on_device((cold, hot_k, hot_v, k_global_scale, v_global_scale, cold_slot_ids,
+                     hot_page_ids, extra, status), stream) as s:
+        code = lib.nvfp4_kv_onboard_pages(
+            ctypes.byref(layout), _cold_ptr(cold), cold.numel() // bl.bytes, _ids(cold_slot_ids),
+            _ptr(k_global_scale), _ptr(v_global_scale), _rope_ref(rope),
+            _dtype_code(hot_k, hot_dtype), kp, vp, ks,
+            hot_k.shape[0], _ids(hot_page_ids), ep, es, eb, int(num_pages), _ptr(status),
+            s)
     _check("nvfp4_kv_onboard_pages", code)
 

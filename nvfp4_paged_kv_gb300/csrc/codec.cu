@@ -430,19 +430,22 @@ __device__ __forceinline__ float global_scale_of(uint32_t r, const float* src_sc
 
 // Raise the tagged maximum (tag in the high 32 bits) to r. Tags grow from call to call, so a
 // word of an earlier call is replaced by the first atomicMax; a word holding a larger tag
-// (garbage) is installed over with a bounded compare-and-swap loop.
-__device__ __forceinline__ void tagged_max(unsigned long long* w, uint32_t nonce, uint32_t r) {
+// (garbage) is installed over with a bounded compare-and-swap loop. Returns false when that
+// loop ran out without installing r.
+__device__ __forceinline__ bool tagged_max(unsigned long long* w, uint32_t nonce, uint32_t r) {
     const unsigned long long v = (static_cast<unsigned long long>(nonce) << 32) | r;
     unsigned long long old = atomicMax(w, v);
-    for (int it = 0; it < 256 && static_cast<uint32_t>(old >> 32) > nonce; ++it) {
+    if (static_cast<uint32_t>(old >> 32) <= nonce) return true;
+    for (int it = 0; it < 256; ++it) {
         const unsigned long long seen = atomicCAS(w, old, v);
-        if (seen == old) return;
+        if (seen == old) return true;
         old = seen;
         if (static_cast<uint32_t>(old >> 32) <= nonce) {
             atomicMax(w, v);
-            return;
+            return true;
         }
     }
+    return false;
 }
 
 template <int SRC>
@@ -498,9 +501,10 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) 
         for (int w = 0; w < kAmaxThreads / 32; ++w) r = max(r, red[w]);
         // the CTA's maximum into the call's tagged maximum, then the count; the CTA that
         // completes the count writes g
-        tagged_max(p.word, p.nonce, r);
+        if (!tagged_max(p.word, p.nonce, r)) flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
         __threadfence();
         const uint32_t k = tagged_finish(p.word + 1, atomicAdd(p.word + 1, 1ull), p.nonce, 1);
+        if (k == kTagGiveUp) flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
         if (k == gridDim.x - 1) {
             __threadfence();
             const unsigned long long w = atomicAdd(p.word, 0ull);

@@ -1,6 +1,7 @@
-// Device helpers shared by the NVFP4 kernels (sm_103a): FP4/FP8 conversions, bulk async copies,
-// mbarriers, warp-level MMA. Every conversion here is the hardware instruction named in its
-// comment; the exact numerics of each kernel are stated next to the kernel.
+// Device helpers shared by the NVFP4 kernels (sm_103a): the tagged counters and status word of a
+// call, programmatic dependent launch, FP4/FP8/FP16 conversions, warp-level MMA and the L2
+// eviction policy of streamed loads. Every conversion here is the hardware instruction named in
+// its comment; the exact numerics of each kernel are stated next to the kernel.
 #pragma once
 
 #include <cstdint>
@@ -12,11 +13,14 @@
 
 namespace nvfp4kv {
 
-constexpr int kNumSmsDefault = 152;
-
 // ------------------------------------------------------------------------------------------
 // Status word
 // ------------------------------------------------------------------------------------------
+// Returned by tagged_finish when its bounded compare-and-swap loop could not install the call's
+// tag (the word held a larger tag and kept changing): the unit that counted is then never
+// completed, and the kernel ORs NVFP4KV_STATUS_TIMEOUT into the caller's status word.
+constexpr uint32_t kTagGiveUp = 0xFFFFFFFFu;
+
 // Tagged counter (tag in the high 32 bits, count in the low 32): add inc and return the count
 // before the add, treating a word whose tag is not this call's as a count of 0. `old` is the
 // value returned by a first atomicAdd. Tags grow from call to call, so a stale word is replaced
@@ -42,7 +46,7 @@ __device__ __forceinline__ uint32_t tagged_finish(unsigned long long* w, unsigne
         if (seen == cur) return 0;
         cur = seen;
     }
-    return 0xFFFFFFFFu;  // could not install the tag: report the pair as not finished
+    return kTagGiveUp;  // could not install the tag: the caller reports NVFP4KV_STATUS_TIMEOUT
 }
 
 // Programmatic dependent launch: wait until the previous grid on the stream has completed and
@@ -60,14 +64,6 @@ __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
 // ------------------------------------------------------------------------------------------
 // Conversions
 // ------------------------------------------------------------------------------------------
-
-// Two E2M1 codes (low nibble -> low half) to two exact FP16 values: cvt.rn.f16x2.e2m1x2.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
-    uint32_t out;
-    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-        : "=r"(out) : "r"(byte_in_low_bits));
-    return out;
-}
 
 // The four bytes of w, each as two E2M1 codes -> FP16 pair (o[k] from byte k). The bytes are
 // split with a vector move into 8-bit registers, which the conversions read directly (no shifts).
@@ -144,12 +140,6 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     return out;
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t out;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(out) : "r"(a), "r"(b), "r"(sel));
-    return out;
-}
-
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -176,74 +166,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return y;
 }
 
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t smem_addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(smem_addr));
-}
-
-// ------------------------------------------------------------------------------------------
-// Shared memory, mbarriers and bulk async copies (TMA, 1-D)
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar_addr), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for phase `parity` of an mbarrier, giving up after `limit_ns` nanoseconds.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint64_t limit_ns) {
-    const uint32_t addr = smem_u32(bar);
-    if (mbar_try_wait(addr, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(addr, parity)) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
-    }
-}
-
-// 1-D bulk copy global -> shared, completion counted in bytes on `bar`; L2 evict-first hint
-// (the K/V pages are streamed once per call).
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
-                                         uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;\n" ::"r"(smem_u32(smem_dst)),
-        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
+// L2 eviction policy for data that is read once per call: its lines are the first to go.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -24,7 +24,8 @@ std::vector<void*> g_scratch_addr;  // device address of g_decode_scratch, per d
 
 // Device address of the scratch on the current device. In host code the array's name is only a
 // host-side stand-in, so the address comes from cudaGetSymbolAddress, once per device, with
-// that device current.
+// that device current. The address is kept until the process exits; cudaDeviceReset ends the
+// context that owns the array, after which this entry point must not be used on that device.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -53,6 +54,15 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention_noalloc(
     const size_t need = nvfp4_paged_decode_workspace_size(layout, batch, num_q_heads,
                                                           max_pages_per_seq, max_num_splits);
     if (need > NVFP4KV_NOALLOC_SCRATCH_BYTES) return NVFP4KV_ERR_WORKSPACE;
+    // The scratch address is that of the current device's copy of the array: a stream of another
+    // device would run the kernel against memory of the wrong GPU.
+    if (stream != nullptr) {
+        int cur = 0, sdev = 0;
+        if (cudaGetDevice(&cur) != cudaSuccess ||
+            cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+            return NVFP4KV_ERR_CUDA;
+        if (sdev != cur) return NVFP4KV_ERR_INVALID_ARG;
+    }
     void* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return NVFP4KV_ERR_CUDA;
     // Same kernels and split plan as the workspace entry point; every partial the combine pass

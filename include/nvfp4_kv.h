@@ -50,10 +50,18 @@
  *   - The return value reports host-side validation (NVFP4KV_ERR_INVALID_ARG /
  *     NVFP4KV_ERR_UNSUPPORTED / NVFP4KV_ERR_WORKSPACE) and launch failures (NVFP4KV_ERR_CUDA).
  *     On an error nothing is enqueued.
- *   - Data-dependent faults found on the device (a page id outside [0, pool_pages), a sequence
- *     length outside [0, max_pages_per_seq * T], a pipeline wait that ran out) are OR-ed into the
- *     caller's `status` word (optional, int32 device memory, NVFP4KV_STATUS_* bits); the
- *     offending page / sequence is skipped and nothing traps. The caller clears the word.
+ *   - Data-dependent faults found on the device are OR-ed into the caller's `status` word
+ *     (optional, int32 device memory, NVFP4KV_STATUS_* bits) and nothing traps; the caller
+ *     clears the word. A page id outside [0, pool_pages) (PAGE_OOB) or a sequence length outside
+ *     [0, max_pages_per_seq * T] (BAD_SEQ_LEN) skips the offending page / sequence. TIMEOUT: the
+ *     tagged words of a workspace (a per-call tag in the high 32 bits) are installed over a word
+ *     holding a larger tag (garbage) by a compare-and-swap loop bounded at 256 rounds; if that
+ *     loop runs out (other CTAs kept changing the word), the count it served never completes,
+ *     so the affected (sequence, KV head) pair of a decode call keeps its previous output and
+ *     LSE, and a global-scale call may leave g unwritten or too small. No kernel spins on a flag
+ *     or a barrier; the decode's asynchronous copies complete without polling.
+ *   - `stream` must belong to the current device (or be 0), and every pointer must be memory
+ *     that device can address: grids are sized for the current device.
  *   - Buffers must be 16-byte aligned; sources and destinations must not overlap.
  *   - Inputs must be finite. Unused slots of a page (past the end of a sequence) are never read
  *     by attention; the codec encodes every slot of every listed page.
@@ -82,7 +90,7 @@ typedef enum nvfp4kv_status {
 /* Bits OR-ed into the optional device status word. */
 #define NVFP4KV_STATUS_PAGE_OOB 0x1      /* a page id was outside [0, pool_pages): skipped        */
 #define NVFP4KV_STATUS_BAD_SEQ_LEN 0x2   /* seq_len < 0 or > max_pages_per_seq * T: seq skipped   */
-#define NVFP4KV_STATUS_TIMEOUT 0x4       /* reserved for bounded waits; no current kernel sets it  */
+#define NVFP4KV_STATUS_TIMEOUT 0x4       /* a bounded retry loop on a workspace word gave up       */
 
 typedef enum nvfp4kv_packing {
     NVFP4KV_PACK_DIM_PAIRS = 0,   /* a byte holds two head dims of one token (K cache)          */
@@ -218,12 +226,13 @@ nvfp4kv_status nvfp4_kv_extend_write(const nvfp4kv_layout* layout, nvfp4kv_dtype
  * A sequence of length 0 gives out = 0 and lse = -inf.
  *
  * Split-KV: the (sequence, KV head) pairs are cut into 64-token stages (32 at head_dim 256), the
- * stages of all pairs form one list, and the list is cut into equal runs, one per CTA. Each
- * (run, pair) piece leaves a partial (max, sum, unnormalised output) in the workspace; the last
- * CTA to finish a pair merges its partials and writes the outputs (one kernel launch). The
- * workspace needs no initialisation: its counters carry a per-call tag, and the CTA that merges
- * a pair sets that pair's counter back to 0, so a replayed CUDA graph that repeats a captured
- * call (same tag) starts clean.
+ * stages of all pairs form one list, and the list is cut into equal runs, one per warp (one CTA
+ * per SM). Each (run, pair) piece of a pair split over several runs leaves a partial (max, sum,
+ * unnormalised output) in the workspace and bumps the pair's counter; the CTA whose warp
+ * completes the count merges the pair's partials after its own runs and writes the outputs (one
+ * kernel launch). The workspace needs no initialisation: its counters carry a per-call tag, and
+ * the CTA that merges a pair sets that pair's counter back to 0, so a replayed CUDA graph that
+ * repeats a captured call (same tag) starts clean.
  *   q              BF16 [batch][num_q_heads][D]
  *   k_data, k_scales   NVFP4 K pool in NVFP4KV_PACK_DIM_PAIRS (layout.packing is not read)
  *   v_data, v_scales   NVFP4 V pool in NVFP4KV_PACK_TOKEN_PAIRS
@@ -231,7 +240,7 @@ nvfp4kv_status nvfp4_kv_extend_write(const nvfp4kv_layout* layout, nvfp4kv_dtype
  *   page_table     int32 [batch][max_pages_per_seq] device
  *   seq_lens       int32 [batch] device; 0 <= seq_len <= max_pages_per_seq * T
  *   sm_scale       softmax scale (e.g. 1/sqrt(D))
- *   max_num_splits 0 = automatic: one wave of CTAs on the device (runs of at least 4 stages);
+ *   max_num_splits 0 = automatic: one run per warp of one CTA per SM;
  *                  n in 1..64: n * batch * num_kv_heads runs (n runs per pair when all
  *                  sequences have the same length)
  *   workspace      device scratch of nvfp4_paged_decode_workspace_size(...) bytes
@@ -266,7 +275,10 @@ nvfp4kv_status nvfp4_paged_decode_attention(
  *   - A call whose workspace need (nvfp4_paged_decode_workspace_size with the same arguments)
  *     exceeds NVFP4KV_NOALLOC_SCRATCH_BYTES returns NVFP4KV_ERR_WORKSPACE and enqueues nothing.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture.
+ *     with that device current); make that first call before any stream capture. The address
+ *     is kept for the life of the process: after cudaDeviceReset (which ends the context that
+ *     owns the array) the call must not be used on that device again.
+ *   - `stream` must be 0 or a stream of the current device, else NVFP4KV_ERR_INVALID_ARG.
  *   - Every call on a device shares the one array and leaves its contents behind. Calls that
  *     can overlap on the GPU (different streams without ordering between them) race on it.
  * ------------------------------------------------------------------------------------------ */

@@ -1,4 +1,4 @@
-// Split-KV paged GQA decode attention over NVFP4 K/V for sm_103a, its merge in the same launch.
+// Split-KV paged GQA decode attention over NVFP4 K/V for sm_103a, and its combine pass.
 //
 // What it computes ("Accelerating Long-Context and Agentic Inference with NVFP4 KV Cache",
 // LMSYS: "Path 3: Decode", "NVFP4 KV Decode Attention Kernel Implementation", Figure 3): for
@@ -10,18 +10,24 @@
 // Design for GB300 (the SM120 kernel of the LMSYS page is prior art, not the blueprint):
 //  * Work is a flat list of stages: stage j of pair (sequence b, KV head h) covers tokens
 //    [TOK j, TOK j + TOK) of b (TOK = 64 tokens, 32 at head_dim 256), pairs in (b, h) order.
-//    One persistent wave of CTAs cuts the list into equal runs, so every SM streams about the
-//    same number of bytes whatever the mix of sequence lengths. A run may cross pairs; each
-//    (CTA, pair) piece leaves one partial record c + bh, so records never collide and their
-//    number is bounded by (CTAs + pairs) before any length is known. The last CTA to finish a
-//    pair (counted with a per-pair counter that carries a per-call tag, so the workspace never
-//    needs clearing) merges the pair's records and writes the outputs: no second kernel.
-//  * A CTA has 4 warps; warp w takes stages w, w+4, ... of the piece. A stage is SUB MMA tiles
-//    of 16 tokens, streamed through a per-warp 2-slot shared-memory ring by asynchronous copies
-//    (cp.async, 16 bytes per lane, completion per warp by wait_group): the packed K rows,
-//    token-pair packed V rows and both scale pools of a stage are four contiguous runs of its
-//    page. Sub-tiles whose page id is out of range or that lie past the sequence end are
-//    zero-filled, and a small slot header tells the consumer which sub-tiles are real.
+//    One persistent CTA per SM runs (12 warps at head_dim 128, 16 at 64, 8 at 256: all warps
+//    of an SM are equally old, so none is favoured by the schedulers), and the list is cut into
+//    equal runs, one per warp, so every warp streams the same number of bytes whatever the mix
+//    of sequence lengths. A run may cross pairs; each (warp, pair) piece of a pair that is
+//    split over several warps leaves one partial record gw + bh (gw the warp's run, bh the
+//    pair), so records never collide and their number is bounded by runs + pairs before any
+//    length is known.
+//  * Every warp is an independent pipeline: after the stage prefix and the query cache fill at
+//    the start, no barrier ties the warps of a CTA together. A warp streams its run through its
+//    own ring of two shared-memory slots with asynchronous copies (cp.async, 16 bytes per lane,
+//    completion per warp by wait_group), straight across pair boundaries: the packed K rows,
+//    the token-pair packed V rows and both scale pools of a stage are four contiguous runs of
+//    its page. The page ids come from a 32-entry register window of the page table (one id per
+//    lane) whose successor is loaded a window ahead; the queries of the pairs the CTA touches
+//    (consecutive pairs, so one contiguous slice of q) are staged in shared memory at the
+//    start. A small header in each slot tells the consumer which sub-tiles are real, where the
+//    piece starts and ends and which pair it belongs to, so a pair boundary costs no wait for
+//    global memory.
 //  * S^T = K^ Q^T runs on the tensor cores with tokens as M = 16 and the GQA query group as
 //    N = 8 (mma.sync m16n8k16, FP16 in, FP32 accumulate). K is stored dim-pair packed, so every
 //    converted byte (cvt.rn.f16x2.e2m1x2) is one A-register: two adjacent head dims of one
@@ -32,16 +38,13 @@
 //    rescaling is rare. P^T moves to the B-operand layout with movmatrix.
 //  * O^T += V^^T P^T with head dims as M: V is stored token-pair packed, so every converted byte
 //    is one A-register (one head dim of two adjacent tokens) times the pair's two block scales.
-//  * at the end of a piece the 4 warps merge (max, sum, output) in shared memory; a piece that
-//    is a whole pair writes the BF16 output and the natural-log LSE directly, otherwise the CTA
-//    writes its record and the pair's last CTA merges the records by log-sum-exp.
-//  * a piece boundary inside a run holds up the CTA as little as possible: the next piece's
-//    page ids are loaded into registers while the current piece streams, and the record's count
-//    is bumped by one lane while the CTA already streams the next piece; the outcome is read at
-//    that piece's end, where the CTA merges the pair if its count completed it.
+//  * at the end of a piece the warp writes the BF16 output and the natural-log LSE directly
+//    when the piece is the whole pair, otherwise its record (from registers); the warp holding
+//    a split pair's first stage also writes the pair's descriptors (record range, tagged with
+//    the call). A second, small kernel (launched behind the first with programmatic dependent
+//    launch) merges the records of every split pair by log-sum-exp, one CTA per (pair, query
+//    head), and clears the descriptors it used.
 // Bytes per (token, KV head) at head_dim 128: 64 + 8 (K) + 64 + 8 (V) = 144.
-#include <atomic>
-#include <chrono>
 #include <cstdint>
 #include <utility>
 #include <cuda_runtime.h>
@@ -52,15 +55,12 @@
 namespace nvfp4kv {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kDecThreads = kWarps * 32;
-constexpr int kSlots = 2;          // stages per warp ring
 constexpr int kMaxGroup = 8;
 constexpr int kMaxSplits = 64;     // bound of the caller-forced split count
-constexpr int kPageBuf = 256;      // page ids of a piece kept in shared memory
-constexpr int kMaxRecW = 64;      // merge: weights of up to this many records kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kFirst = 1u, kLast = 2u;  // slot header flags: first / last stage of a piece
+constexpr int kSmemPerSm = 233472;           // shared memory of an SM (228 KiB)
 
 template <int D>
 struct Geo {
@@ -74,10 +74,16 @@ struct Geo {
     static constexpr int V_OFF = SK;
     static constexpr int KS_OFF = SK + SV;
     static constexpr int VS_OFF = KS_OFF + SS;
-    static constexpr int HDR_OFF = VS_OFF + SS;  // slot header: real sub-tiles, tokens
-    static constexpr int SLOT = HDR_OFF + 16;
-    static constexpr int RING = kSlots * SLOT;  // per warp
-    static constexpr int SMEM = kWarps * RING;
+    static constexpr int HDR_OFF = VS_OFF + SS;  // slot header (8 words)
+    static constexpr int SLOT = HDR_OFF + 32;
+    static constexpr int SLOTS = 2;              // ring slots per warp: one in flight, one computed
+    // warps of the one CTA per SM (register budget: 16 x 32 x 128, 12 x 32 x 170, 8 x 32 x 255)
+    static constexpr int WARPS = (D == 64) ? 16 : (D == 128 ? 12 : 8);
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr int RING = SLOTS * SLOT;     // per warp
+    static constexpr int QCACHE = (D == 128) ? 8192 : 16384;  // queries of the CTA's pairs
+    static constexpr int Q_OFF = WARPS * RING;
+    static constexpr int SMEM = Q_OFF + QCACHE;
     static constexpr int KSTEPS = D / 16;       // k-steps of S^T = K Q^T
     static constexpr int CHUNK = D / 8;         // bytes of a row one quad lane owns
     static constexpr int CW = CHUNK / 4;        // ... as 32-bit words
@@ -87,14 +93,10 @@ struct Geo {
     static constexpr int SUB_DIV = D / 64;      // data chunk i of a lane lies in sub-tile i / SUB_DIV
     static constexpr int SCH = SS / 16;         // 16-byte chunks of one scale pool
     static constexpr int SC_PER_LANE = 2 * SCH / 32;
-    // CTAs per SM: head_dim 64 at 4 (the register budget of 5 held it at 96 registers, and 4 at
-    // 121 registers decodes a 32 x 8192 batch 18 % faster), 256 at 2 (232 registers, no spills;
-    // 2-3 % faster than 3 with spills), 128 at 3
-    static constexpr int BLOCKS_PER_SM = (D == 64) ? 4 : (D == 256 ? 2 : 3);
     static_assert(DCH * 32 * 16 == SK && DCH == SUB * SUB_DIV, "copy split");
     static_assert(SC_PER_LANE * 32 == 2 * SCH, "scale copy split");
-    static_assert((kWarps * kMaxGroup * D + 2 * kMaxRecW * kMaxGroup + 2 * kMaxGroup) * 4 <= SMEM,
-                  "merge buffers must fit in the rings");
+    static_assert(SLOT % 16 == 0 && RING % 16 == 0, "16-byte aligned slots");
+    static_assert(SMEM + 1024 + 512 <= kSmemPerSm, "shared memory budget");
 };
 
 struct DecodeParams {
@@ -115,7 +117,7 @@ struct DecodeParams {
     int32_t* status;
     uint64_t t_magic;   // ceil(2^64 / T)
     uint32_t nonce;     // tag of this call
-    int32_t B, Hq, H, G, T, pool_pages, max_pages, min_w;
+    int32_t B, Hq, H, G, T, pool_pages, max_pages, num_runs;
     float sm_scale;
 };
 
@@ -152,14 +154,11 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
 // Shared-memory offset of byte x of token-pair row pr of a stage's V rows: 16-byte chunks are
@@ -186,6 +185,10 @@ __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, 
                  "l"(src), "r"(bytes), "l"(pol)
                  : "memory");
 }
+// 16-byte asynchronous copy with the default L2 policy (the queries: read once per piece).
+__device__ __forceinline__ void cp_async16_plain(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -207,20 +210,289 @@ __device__ __forceinline__ int seq_stages(int L, int max_tokens, int tok) {
     return (L > 0 && L <= max_tokens) ? (L + tok - 1) / tok : 0;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Merge the records of pair (b, h) (pieces of runs gf .. gl, records gf + bh .. gl + bh, one
+// contiguous block) by log-sum-exp and write its outputs; the whole CTA, after its runs. The
+// block is staged in shared memory by asynchronous copies (one round trip), the (max, sum) of
+// each query head reduced by one warp per head, and the weighted sum of the records' outputs
+// split over the threads: thread t takes one float4 column of the G x D outputs and every R-th
+// record of the chunk, R = threads / columns.
 template <int D>
-__global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
-    decode_split_kernel(const DecodeParams p) {
+__device__ __forceinline__ void merge_pair(const DecodeParams& p, int b, int h, int ps, int S,
+                                           int W, uint8_t* smem) {
+    using G_ = Geo<D>;
+    constexpr int NT = G_::THREADS;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = p.G;
+    const int gf = ps / W, gl = (ps + S - 1) / W;
+    const int n = gl - gf + 1;
+    const int64_t bh = static_cast<int64_t>(b) * p.H + h;
+    const int64_t rec0 = gf + bh;
+    __threadfence();  // the count said every record is written: read them after it
+    if (tid == 0) atomicExch(p.done + bh, 0ull);  // a replay with the same tag starts from 0
+    const int rec_bytes = G * D * 4;
+    // shared memory: records' outputs [KC][G][D], (max, sum) [KC][G], weights [KC][G],
+    // per-head running max / sum / rescale [8] x 3, partial sums [NT] float4
+    constexpr int kStage = G_::Q_OFF - (NT * 16 + 3 * kMaxGroup * 4) - 2048;
+    const int KC = min(n, min(64, kStage / (rec_bytes + G * 12)));
+    float* o_s = reinterpret_cast<float*>(smem);
+    float2* ml_s = reinterpret_cast<float2*>(smem + KC * rec_bytes);
+    float* w_s = reinterpret_cast<float*>(smem + KC * (rec_bytes + G * 8));
+    float* hd_s = reinterpret_cast<float*>(smem + kStage);  // M, L, rescale per head
+    float4* part_s = reinterpret_cast<float4*>(smem + kStage + 3 * kMaxGroup * 4);
+    const int C4 = G * D / 4;                    // float4 columns of the outputs
+    // columns per thread when there are more columns than threads (head_dim 256, 8 heads), else
+    // R = threads / columns groups of records per column
+    constexpr int CPT = (kMaxGroup * D / 4 + NT - 1) / NT;
+    const int R = max(1, NT / C4);
+    const int grp = (R > 1) ? tid / C4 : 0;
+    const int col0 = (R > 1) ? tid % C4 : tid;
+    if (tid < G) {
+        hd_s[tid] = -INFINITY;
+        hd_s[kMaxGroup + tid] = 0.0f;
+    }
+    float4 acc[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    for (int k0 = 0; k0 < n; k0 += KC) {
+        const int nk = min(KC, n - k0);
+        // stage the chunk's records: outputs and (max, sum), both contiguous in global memory
+        {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.rec_o + (rec0 + k0) * G * D);
+            const int nc = nk * rec_bytes / 16;
+            for (int i = tid; i < nc; i += NT) cp_async16_plain(s_base + 16 * i, src + 16 * i);
+            const float* msrc = p.rec_ml + (rec0 + k0) * G * 2;
+            for (int i = tid; i < nk * G; i += NT) ml_s[i] = __ldcg(reinterpret_cast<const float2*>(msrc) + i);
+            cp_async_commit();
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        // per head: the chunk's maximum, the running maximum, weights and sum
+        if (warp < G) {
+            const int g = warp;
+            float mx = -INFINITY;
+            for (int k = lane; k < nk; k += 32) mx = fmaxf(mx, ml_s[k * G + g].x);
+            mx = warp_max(mx);
+            const float Mo = hd_s[g];
+            const float Mn = fmaxf(Mo, mx);
+            float s = 0.0f;
+            for (int k = lane; k < nk; k += 32) {
+                const float2 ml = ml_s[k * G + g];
+                const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - Mn);
+                w_s[k * G + g] = w;
+                s += w * ml.y;
+            }
+            s = warp_sum(s);
+            __syncwarp();
+            if (lane == 0) {
+                const float a = (Mo == -INFINITY) ? 0.0f : exp2f(Mo - Mn);
+                hd_s[g] = Mn;
+                hd_s[kMaxGroup + g] = hd_s[kMaxGroup + g] * a + s;
+                hd_s[2 * kMaxGroup + g] = a;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int col = col0 + NT * j;
+            if (grp >= R || col >= C4) continue;
+            const int g_col = col * 4 / D;
+            const float a = hd_s[2 * kMaxGroup + g_col];
+            float4 v4 = acc[j];
+            v4.x *= a;
+            v4.y *= a;
+            v4.z *= a;
+            v4.w *= a;
+            for (int k = grp; k < nk; k += R) {
+                const float w = w_s[k * G + g_col];
+                const float4 v = reinterpret_cast<const float4*>(o_s + k * G * D)[col];
+                v4.x += w * v.x;
+                v4.y += w * v.y;
+                v4.z += w * v.z;
+                v4.w += w * v.w;
+            }
+            acc[j] = v4;
+        }
+        __syncthreads();  // the chunk's buffers are free
+    }
+    // sum the record groups (R > 1 only when every column has one thread per group), normalise
+    if (R > 1) {
+        if (grp < R) part_s[tid] = acc[0];
+        __syncthreads();
+        if (grp == 0) {
+            for (int r = 1; r < R; ++r) {
+                const float4 v = part_s[col0 + r * C4];
+                acc[0].x += v.x;
+                acc[0].y += v.y;
+                acc[0].z += v.z;
+                acc[0].w += v.w;
+            }
+        }
+    }
+    const float gvs = __ldg(p.gv);
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const int col = col0 + NT * j;
+        if (grp != 0 || col >= C4) continue;
+        const int g_col = col * 4 / D;
+        const float L = hd_s[kMaxGroup + g_col];
+        const float f = L > 0.0f ? gvs / L : 0.0f;
+        uint2 o;
+        o.x = pack_bf16x2(acc[j].x * f, acc[j].y * f);
+        o.y = pack_bf16x2(acc[j].z * f, acc[j].w * f);
+        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(b) * p.Hq + h * G) * D + 4 * col) = o;
+    }
+    if (tid < G && p.lse) {
+        const float L = hd_s[kMaxGroup + tid];
+        p.lse[static_cast<int64_t>(b) * p.Hq + h * G + tid] =
+            L > 0.0f ? (hd_s[tid] + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();  // shared memory is reused by the next pair
+}
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ int align16i(int x) { return (x + 15) & ~15; }
+
+// Merge pending pairs pend[first], pend[first + 1], ... together, as many as fit in shared memory
+// at once (whole CTA, after its runs): the records' outputs and (max, sum) pairs of all of them
+// are staged by asynchronous copies in one round trip; then one warp per (pair, query head)
+// reduces the maxima and sums and turns the records' maxima into weights, and every thread takes
+// float4 columns of the outputs. Returns how many pairs were merged (0 when the first pair alone
+// does not fit: the caller merges it by chunks).
+template <int D>
+__device__ __forceinline__ int merge_batch(const DecodeParams& p, const int (*pend)[4], int first,
+                                           int n_pend, int W, uint8_t* smem) {
+    using G_ = Geo<D>;
+    constexpr int NT = G_::THREADS, NW = G_::WARPS;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = p.G;
+    const int rec_bytes = G * D * 4;
+    // per pair: outputs n x rec_bytes, (max, sum) n x G x 8, weights n x G x 4, (M, L) G x 8
+    auto bytes_of = [&](int n) {
+        return n * rec_bytes + align16i(n * G * 8) + align16i(n * G * 4) + align16i(G * 8);
+    };
+    int cnt = 0, used = 0;
+    for (int i = first; i < n_pend; ++i) {
+        const int n = (pend[i][2] + pend[i][3] - 1) / W - pend[i][2] / W + 1;
+        const int need = bytes_of(n);
+        if (used + need > G_::SMEM) break;
+        used += need;
+        ++cnt;
+    }
+    if (cnt == 0) return 0;
+    __threadfence();  // the counts said every record is written: read them after it
+    const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    // stage every record of the batch
+    {
+        int off = 0;
+        for (int i = first; i < first + cnt; ++i) {
+            const int ps = pend[i][2], S = pend[i][3];
+            const int gf = ps / W, n = (ps + S - 1) / W - gf + 1;
+            const int64_t bh = static_cast<int64_t>(pend[i][0]) * p.H + pend[i][1];
+            const int64_t rec0 = gf + bh;
+            if (tid == 0) atomicExch(p.done + bh, 0ull);  // a replay with the same tag starts from 0
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p.rec_o + rec0 * G * D);
+            const int nc = n * rec_bytes / 16;
+            for (int c = tid; c < nc; c += NT) cp_async16_plain(s_base + off + 16 * c, src + 16 * c);
+            off += n * rec_bytes;
+            const float* msrc = p.rec_ml + rec0 * G * 2;
+            for (int c = tid; c < n * G; c += NT) cp_async8(s_base + off + 8 * c, msrc + 2 * c);
+            off += align16i(n * G * 8) + align16i(n * G * 4) + align16i(G * 8);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+    }
+    __syncthreads();
+    // one warp per (pair, head): maximum, sum, weights; the LSE
+    for (int u = warp; u < cnt * G; u += NW) {
+        const int i = first + u / G, g = u % G;
+        int off = 0;
+        for (int j = first; j < i; ++j)
+            off += bytes_of((pend[j][2] + pend[j][3] - 1) / W - pend[j][2] / W + 1);
+        const int n = (pend[i][2] + pend[i][3] - 1) / W - pend[i][2] / W + 1;
+        const float2* ml_s = reinterpret_cast<const float2*>(smem + off + n * rec_bytes);
+        float* w_s = reinterpret_cast<float*>(smem + off + n * rec_bytes + align16i(n * G * 8));
+        float2* st_s = reinterpret_cast<float2*>(smem + off + n * rec_bytes + align16i(n * G * 8) +
+                                                 align16i(n * G * 4));
+        float mx = -INFINITY;
+        for (int k = lane; k < n; k += 32) mx = fmaxf(mx, ml_s[k * G + g].x);
+        mx = warp_max(mx);
+        float sum = 0.0f;
+        for (int k = lane; k < n; k += 32) {
+            const float2 ml = ml_s[k * G + g];
+            const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - mx);
+            w_s[k * G + g] = w;
+            sum += w * ml.y;
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+            st_s[g] = make_float2(mx, sum);
+            if (p.lse)
+                p.lse[static_cast<int64_t>(pend[i][0]) * p.Hq + pend[i][1] * G + g] =
+                    sum > 0.0f ? (mx + log2f(sum)) * 0.6931471805599453f : -INFINITY;
+        }
+    }
+    __syncthreads();
+    // outputs: float4 columns of every pair of the batch
+    const float gvs = __ldg(p.gv);
+    const int C4 = G * D / 4;
+    for (int cc = tid; cc < cnt * C4; cc += NT) {
+        const int i = first + cc / C4, col = cc % C4, g = col * 4 / D;
+        int off = 0;
+        for (int j = first; j < i; ++j)
+            off += bytes_of((pend[j][2] + pend[j][3] - 1) / W - pend[j][2] / W + 1);
+        const int n = (pend[i][2] + pend[i][3] - 1) / W - pend[i][2] / W + 1;
+        const float4* o_s = reinterpret_cast<const float4*>(smem + off);
+        const float* w_s = reinterpret_cast<const float*>(smem + off + n * rec_bytes + align16i(n * G * 8));
+        const float2 st = reinterpret_cast<const float2*>(smem + off + n * rec_bytes +
+                                                          align16i(n * G * 8) + align16i(n * G * 4))[g];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < n; ++k) {
+            const float w = w_s[k * G + g];
+            const float4 v = o_s[k * C4 + col];
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        const float f = st.y > 0.0f ? gvs / st.y : 0.0f;
+        uint2 o;
+        o.x = pack_bf16x2(acc.x * f, acc.y * f);
+        o.y = pack_bf16x2(acc.z * f, acc.w * f);
+        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(pend[i][0]) * p.Hq + pend[i][1] * G) * D +
+                                  4 * col) = o;
+    }
+    __syncthreads();  // shared memory is reused by the next batch
+    return cnt;
+}
+
+template <int D>
+__global__ void __launch_bounds__(Geo<D>::THREADS, 1) decode_split_kernel(const DecodeParams p) {
     pdl_enter();
     using G_ = Geo<D>;
     constexpr int TOK = G_::TOK;
+    constexpr int NW = G_::WARPS;
+    constexpr int NT = G_::THREADS;
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ float red_m[kWarps][kMaxGroup];
-    __shared__ float red_l[kWarps][kMaxGroup];
-    __shared__ int page_ids[kPageBuf];
-    __shared__ int scan_warp[kWarps];
-    __shared__ int start_bp[2];  // pair walk start: sequence, its first stage
-    __shared__ int last_s;
-    __shared__ int pend_s[5];  // a pair whose count was bumped at the previous boundary: last?, b, h, start, stages
+    __shared__ int scan_warp[NW];
+    __shared__ int start_bp[NW][3];  // run start of each warp: sequence, its first stage, length
+    __shared__ int span_pair[2];     // first and last pair (b H + h) the CTA's runs touch
+    __shared__ int pend_n;           // pairs whose last piece finished in this CTA ...
+    __shared__ int pend[2 * NW][4];  // ... (b, h, first stage, stages): merged at the end
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -232,11 +504,18 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
 
     // ------------------------------------------------ stage prefix over the sequences
     // Thread t owns sequences [t C, t C + C); PS_b = H * sum_{b' < b} stages(b').
-    const int C = (p.B + kDecThreads - 1) / kDecThreads;
+    // The first two lengths stay in registers for the walk below (a second load of the same
+    // words would cost another round trip at the start).
+    const int C = (p.B + NT - 1) / NT;
     const int b_lo = min(p.B, tid * C), b_hi = min(p.B, b_lo + C);
+    const int kept0 = (b_lo < b_hi) ? __ldg(p.seq_lens + b_lo) : 0;
+    const int kept1 = (b_lo + 1 < b_hi) ? __ldg(p.seq_lens + b_lo + 1) : 0;
+    auto len_of = [&](int b) {
+        return b == b_lo ? kept0 : (b == b_lo + 1 ? kept1 : __ldg(p.seq_lens + b));
+    };
     int local = 0;
     for (int b = b_lo; b < b_hi; ++b) {
-        const int L = __ldg(p.seq_lens + b);
+        const int L = len_of(b);
         if (blockIdx.x == 0 && (L < 0 || L > max_tokens))
             flag_status(p.status, NVFP4KV_STATUS_BAD_SEQ_LEN);
         local += H * seq_stages(L, max_tokens, TOK);
@@ -248,16 +527,18 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
         if (lane >= o) incl += v;
     }
     if (lane == 31) scan_warp[warp] = incl;
+    if (tid < 2) span_pair[tid] = 0;
+    if (tid == 0) pend_n = 0;
     __syncthreads();
     int excl = incl - local, total = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
         if (w < warp) excl += scan_warp[w];
         total += scan_warp[w];
     }
-    // CTA c takes the run [c W, c W + W) of the stage list
-    const int n_ctas = gridDim.x;
-    const int W = max(p.min_w, max(1, (total + n_ctas - 1) / n_ctas));
+    // warp run gw takes [gw W, gw W + W) of the stage list
+    const int num_runs = p.num_runs;
+    const int W = max(1, (total + num_runs - 1) / num_runs);
     if (blockIdx.x == 0) {
         // sequences without stages (length 0 or invalid): output 0, LSE -inf
         for (int b = b_lo; b < b_hi; ++b) {
@@ -268,26 +549,58 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                 for (int i = 0; i < p.Hq; ++i) p.lse[static_cast<int64_t>(b) * p.Hq + i] = -INFINITY;
         }
     }
-    const int s_begin = blockIdx.x * W;
-    const int s_end = min(total, s_begin + W);
-    if (s_begin >= s_end) return;
-    if (s_begin >= excl && s_begin < excl + local) {
+    // One walk over this thread's sequences finds the sequence holding each of the CTA's run
+    // starts and its two span ends (32-bit arithmetic: the host bounds stages + runs below 2^31).
+    const int gw0 = blockIdx.x * NW;
+    const int n_runs_cta = max(0, min(num_runs - gw0, NW));
+    const int span_lo = (n_runs_cta > 0 && gw0 < (total + W - 1) / W) ? gw0 * W : total;
+    const int span_hi = min(total, (gw0 + n_runs_cta) * W);
+    if (local > 0 && span_lo < span_hi && span_lo < excl + local && span_hi > excl) {
         int acc = excl;
-        for (int b = b_lo; b < b_hi; ++b) {
-            const int n = H * seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
-            if (s_begin < acc + n) {
-                start_bp[0] = b;
-                start_bp[1] = acc;
-                break;
+        for (int b = b_lo; b < b_hi && acc < span_hi; ++b) {
+            const int L = len_of(b);
+            const int S = seq_stages(L, max_tokens, TOK);
+            const int n = H * S;
+            if (n > 0 && acc + n > span_lo) {
+                // runs of this CTA starting in [acc, acc + n): w in [w_a, w_b)
+                const int w_a = max(0, (acc - gw0 * W + W - 1) / W);
+                const int w_b = min(n_runs_cta, (acc + n - gw0 * W + W - 1) / W);
+                for (int w = w_a; w < w_b; ++w) {
+                    start_bp[w][0] = b;
+                    start_bp[w][1] = acc;
+                    start_bp[w][2] = L;
+                }
+                if (span_lo >= acc && span_lo < acc + n) span_pair[0] = b * H + (span_lo - acc) / S;
+                if (span_hi - 1 >= acc && span_hi - 1 < acc + n)
+                    span_pair[1] = b * H + (span_hi - 1 - acc) / S;
             }
             acc += n;
         }
     }
-    if (tid == 0) pend_s[0] = 0;
     __syncthreads();
 
+    // ------------------------------------------------ queries of the CTA's pairs
+    const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const uint32_t qcache = smem_base + G_::Q_OFF;
+    const int q_first = span_pair[0];
+    const int q_cached = (span_lo < span_hi)
+                             ? min(span_pair[1] - span_pair[0] + 1, G_::QCACHE / (G * D * 2))
+                             : 0;
+    {
+        const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q + static_cast<int64_t>(q_first) * G * D);
+        const int nq = q_cached * G * D * 2 / 16;
+        for (int ci = tid; ci < nq; ci += NT) cp_async16_plain(qcache + 16 * ci, qsrc + 16 * ci);
+        cp_async_commit();
+    }
+
+    const int gw = gw0 + warp;
+    const int64_t s_begin64 = static_cast<int64_t>(gw) * W;
+    const bool has_run = gw < num_runs && s_begin64 < total;
+    const int s_begin = has_run ? static_cast<int>(s_begin64) : 0;
+    const int n_st = has_run ? min(total - s_begin, W) : 0;
+
     // ------------------------------------------------ per-lane constants
-    const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(smem)) + warp * G_::RING;
+    const uint32_t ring = smem_base + warp * G_::RING;
     // V chunk j = lane + 32 i of a stage lands XOR-swizzled by its pair row
     uint32_t v_dst[G_::DCH];
 #pragma unroll
@@ -298,173 +611,222 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
     }
     const int rho = (r >> 1) | ((r & 1) << 2);  // V rows of this lane: chunk rho of a pair row
 
-    // ------------------------------------------------ walk the pieces of this CTA's run
-    int b = start_bp[0];
-    int S_b = seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
-    int h = (s_begin - start_bp[1]) / S_b;
-    int j = (s_begin - start_bp[1]) - h * S_b;
-    int pair_start = start_bp[1] + h * S_b;  // flat index of stage 0 of pair (b, h)
-    int s = s_begin;
-    bool first_piece = true;
-    while (s < s_end) {
-        const int j0 = j, j1 = min(S_b, j + (s_end - s));
-        const int L = __ldg(p.seq_lens + b);
-        const int tok_end = min(j1 * TOK, L);
-        const int first_page = (j0 * TOK) / T;
-        const int n_pages = (tok_end + T - 1) / T - first_page;
-        const int32_t* pt_row = p.page_table + static_cast<int64_t>(b) * p.max_pages;
-        if (first_piece) {
-            for (int i = tid; i < n_pages && i < kPageBuf; i += kDecThreads)
-                page_ids[i] = __ldg(pt_row + first_page + i);
-            __syncthreads();
+    // ------------------------------------------------ issue side: the walk over the run
+    int ib = has_run ? start_bp[warp][0] : 0;
+    int ilen = has_run ? start_bp[warp][2] : 0;
+    int iS = has_run ? seq_stages(ilen, max_tokens, TOK) : 1;
+    int ih = has_run ? (s_begin - start_bp[warp][1]) / iS : 0;
+    int ij = has_run ? (s_begin - start_bp[warp][1]) - ih * iS : 0;
+    int ips = has_run ? start_bp[warp][1] + ih * iS : 0;  // flat index of stage 0 of (ib, ih)
+    bool ifirst = true;                     // the next stage to issue starts a piece
+    int issued = 0;
+    int nlen = (has_run && ib + 1 < p.B) ? __ldg(p.seq_lens + ib + 1) : 0;  // next sequence
+    // page-id windows: lane l holds the id of page base + l of a sequence's page-table row; the
+    // window after the current one (in issue order) is loaded when the current one is taken
+    int wrow = -1, wbase = 0, win = 0;
+    int prow = -1, pbase = 0, pwin = 0;
+    auto load_window = [&](int b_, int base) -> int {
+        const int i = base + lane;
+        return (i < p.max_pages) ? __ldg(p.page_table + static_cast<int64_t>(b_) * p.max_pages + i)
+                                 : -1;
+    };
+    // make the window holding page pidx of sequence ib current (its loads are only issued) and
+    // start loading the one after it
+    auto set_window = [&](int pidx) {
+        const int nbase = pidx & ~31;
+        win = (ib == prow && nbase == pbase) ? pwin : load_window(ib, nbase);
+        wrow = ib;
+        wbase = nbase;
+        const int npg = (ilen + T - 1) / T;
+        if (nbase + 32 < npg) {
+            prow = ib;
+            pbase = nbase + 32;
+        } else {
+            prow = (ih + 1 < H) ? ib : ib + 1;  // a zero-length next sequence makes this a miss
+            pbase = 0;
         }
-        // (later pieces: their page ids were put in place before the previous piece's last barrier)
-        first_piece = false;
-        // the next piece of the run (the pair after (b, h), from its stage 0) and its page ids,
-        // loaded now so that they are in registers when this piece ends
-        const bool has_next = s + (j1 - j0) < s_end;
-        int nid[2] = {0, 0};
-        int nn_pages = 0;
-        if (has_next) {
-            int nb = b, nh = h + 1, nS = S_b;
-            if (nh == H) {
-                nh = 0;
-                do {
-                    ++nb;
-                    nS = seq_stages(__ldg(p.seq_lens + nb), max_tokens, TOK);
-                } while (nS == 0);
-            }
-            const int nj1 = min(nS, s_end - (pair_start + S_b));
-            nn_pages = (min(nj1 * TOK, __ldg(p.seq_lens + nb)) + T - 1) / T;
-            const int32_t* npt = p.page_table + static_cast<int64_t>(nb) * p.max_pages;
+        if (prow < p.B && !(prow == wrow && pbase == wbase))
+            pwin = load_window(prow, pbase);
+        else
+            prow = -1;
+    };
+    auto page_of = [&](int pidx) -> int {  // warp-uniform pidx of sequence ib; every lane calls
+        if (ib != wrow || pidx < wbase || pidx >= wbase + 32) set_window(pidx);
+        const int pg = __shfl_sync(0xFFFFFFFFu, win, pidx - wbase);
+        return (pg >= 0 && pg < p.pool_pages) ? pg : -1;
+    };
+
+    const int64_t page_rows = static_cast<int64_t>(H) * T;
+    const bool page_aligned = (T % TOK) == 0;
+    // issue the next stage of the walk into `slot`, then advance the walk
+    auto issue_next = [&](uint32_t slot) {
+        const uint64_t kv_pol = l2_policy_evict_first();
+        const int t0 = ij * TOK;
+        const int nval = min(TOK, ilen - t0);
+        const int64_t head_rows = static_cast<int64_t>(ih) * T;
+        int64_t row0[G_::SUB];  // token row of each sub-tile in its pool, -1: not real
+        if (page_aligned) {
+            const int pidx = static_cast<int>(__umul64hi(static_cast<uint64_t>(t0), p.t_magic));
+            const int pg = page_of(pidx);
+            const int64_t r0 = pg * page_rows + head_rows + (t0 - pidx * T);
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                const int i = tid + q2 * kDecThreads;
-                if (i < nn_pages && i < kPageBuf) nid[q2] = __ldg(npt + i);
+            for (int u = 0; u < G_::SUB; ++u)
+                row0[u] = (pg >= 0 && 16 * u < nval) ? r0 + 16 * u : -1;
+        } else {
+#pragma unroll
+            for (int u = 0; u < G_::SUB; ++u) {
+                const int t = t0 + 16 * u;
+                const int pidx = static_cast<int>(__umul64hi(static_cast<uint64_t>(t), p.t_magic));
+                const int pg = page_of(min(pidx, max(0, (ilen - 1) / T)));
+                row0[u] = (pg >= 0 && 16 * u < nval) ? pg * page_rows + head_rows + (t - pidx * T)
+                                                      : -1;
             }
         }
-        auto page_of = [&](int pidx) {
-            const int k = pidx - first_page;
-            const int pg = (k < kPageBuf) ? page_ids[k] : __ldg(pt_row + pidx);
-            return (pg >= 0 && pg < p.pool_pages) ? pg : -1;
-        };
-
-        // ---- issue of one stage (index js within the pair) into a ring slot
-        const int64_t head_rows = static_cast<int64_t>(h) * T;
-        const int64_t page_rows = static_cast<int64_t>(H) * T;
-        const bool page_aligned = (T % TOK) == 0;
-        auto issue_stage = [&](int js, uint32_t slot) {
-            const uint64_t kv_pol = l2_policy_evict_first();
-            const int t0 = js * TOK;
-            const int nval = min(TOK, L - t0);
-            int64_t row0[G_::SUB];  // token row of each sub-tile in its pool, -1: not real
-            if (page_aligned) {
-                const int pidx = static_cast<int>(__umul64hi(static_cast<uint64_t>(t0), p.t_magic));
-                const int pg = page_of(pidx);
-                const int64_t r0 = pg * page_rows + head_rows + (t0 - pidx * T);
+        uint32_t okbits = 0;
 #pragma unroll
-                for (int u = 0; u < G_::SUB; ++u)
-                    row0[u] = (pg >= 0 && 16 * u < nval) ? r0 + 16 * u : -1;
-            } else {
+        for (int u = 0; u < G_::SUB; ++u) okbits |= (row0[u] >= 0 ? 1u : 0u) << u;
+        const uint32_t want = (1u << ((nval + 15) / 16)) - 1u;
+        if (okbits != want && lane == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+        if (page_aligned && okbits == (1u << G_::SUB) - 1) {
+            // the whole stage is one run of each pool: offsets are compile-time constants
+            const int64_t doff = row0[0] * (D / 2) + 16 * lane;
+            const uint8_t* ksrc = p.kd + doff;
+            const uint8_t* vsrc = p.vd + doff;
+            static_for<G_::DCH>([&](auto I) {
+                constexpr int i = decltype(I)::value;
+                cp_async16<G_::K_OFF + 512 * i, 512 * i>(slot + 16 * lane, ksrc, kv_pol);
+                cp_async16<0, 512 * i>(slot + v_dst[i], vsrc, kv_pol);
+            });
+            const int64_t soff = row0[0] * G_::NB;
 #pragma unroll
-                for (int u = 0; u < G_::SUB; ++u) {
-                    row0[u] = -1;
-                    if (16 * u < nval) {
-                        const int t = t0 + 16 * u;
-                        const int pidx =
-                            static_cast<int>(__umul64hi(static_cast<uint64_t>(t), p.t_magic));
-                        const int pg = page_of(pidx);
-                        if (pg >= 0) row0[u] = pg * page_rows + head_rows + (t - pidx * T);
-                    }
-                }
+            for (int k = 0; k < G_::SC_PER_LANE; ++k) {
+                const int jc = lane + 32 * k;
+                const bool kpool = jc < G_::SCH;
+                const int jj = kpool ? jc : jc - G_::SCH;
+                cp_async16<0, 0>(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
+                                 (kpool ? p.ks : p.vs) + soff + 16 * jj, kv_pol);
             }
-            uint32_t okbits = 0;
+        } else {
 #pragma unroll
-            for (int u = 0; u < G_::SUB; ++u) okbits |= (row0[u] >= 0 ? 1u : 0u) << u;
-            const uint32_t want = (1u << ((nval + 15) / 16)) - 1u;
-            if (okbits != want && lane == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
-            if (page_aligned && okbits == (1u << G_::SUB) - 1) {
-                // the whole stage is one run of each pool: offsets are compile-time constants
-                const int64_t doff = row0[0] * (D / 2) + 16 * lane;
-                const uint8_t* ksrc = p.kd + doff;
-                const uint8_t* vsrc = p.vd + doff;
-                static_for<G_::DCH>([&](auto I) {
-                    constexpr int i = decltype(I)::value;
-                    cp_async16<G_::K_OFF + 512 * i, 512 * i>(slot + 16 * lane, ksrc, kv_pol);
-                    cp_async16<0, 512 * i>(slot + v_dst[i], vsrc, kv_pol);
-                });
-                const int64_t soff = row0[0] * G_::NB;
-#pragma unroll
-                for (int k = 0; k < G_::SC_PER_LANE; ++k) {
-                    const int jc = lane + 32 * k;
-                    const bool kpool = jc < G_::SCH;
-                    const int jj = kpool ? jc : jc - G_::SCH;
-                    cp_async16<0, 0>(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
-                                     (kpool ? p.ks : p.vs) + soff + 16 * jj, kv_pol);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < G_::DCH; ++i) {
-                    const int u = i / G_::SUB_DIV;
-                    const int jj = lane + 32 * i - u * (D / 2);  // chunk within the sub-tile
-                    const bool ok = row0[u] >= 0;
-                    const int64_t off = ok ? row0[u] * (D / 2) + 16 * jj : 0;
-                    cp_async16_zfill(slot + G_::K_OFF + 16 * (lane + 32 * i), p.kd + off,
-                                     ok ? 16u : 0u, kv_pol);
-                    cp_async16_zfill(slot + v_dst[i], p.vd + off, ok ? 16u : 0u, kv_pol);
-                }
-#pragma unroll
-                for (int k = 0; k < G_::SC_PER_LANE; ++k) {
-                    const int jc = lane + 32 * k;
-                    const bool kpool = jc < G_::SCH;
-                    const int jj = kpool ? jc : jc - G_::SCH;
-                    const int u = jj / (D / 16);
-                    int64_t ru = row0[0];  // row0[u] without a dynamically indexed array
-#pragma unroll
-                    for (int uu = 1; uu < G_::SUB; ++uu)
-                        if (u == uu) ru = row0[uu];
-                    const bool ok = ru >= 0;
-                    const int64_t off = ok ? ru * G_::NB + 16 * (jj - u * (D / 16)) : 0;
-                    cp_async16_zfill(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
-                                     (kpool ? p.ks : p.vs) + off, ok ? 16u : 0u, kv_pol);
-                }
+            for (int i = 0; i < G_::DCH; ++i) {
+                const int u = i / G_::SUB_DIV;
+                const int jj = lane + 32 * i - u * (D / 2);  // chunk within the sub-tile
+                const bool ok = row0[u] >= 0;
+                const int64_t off = ok ? row0[u] * (D / 2) + 16 * jj : 0;
+                cp_async16_zfill(slot + G_::K_OFF + 16 * (lane + 32 * i), p.kd + off,
+                                 ok ? 16u : 0u, kv_pol);
+                cp_async16_zfill(slot + v_dst[i], p.vd + off, ok ? 16u : 0u, kv_pol);
             }
-            if (lane == 0) sts_u32(slot + G_::HDR_OFF, okbits | (static_cast<uint32_t>(nval) << 8));
-        };
-
-        // this warp's stages of the piece: j0 + warp, j0 + warp + 4, ...
-        const int n_st = max(0, (j1 - j0 - warp + kWarps - 1) / kWarps);
 #pragma unroll
-        for (int k = 0; k < kSlots - 1; ++k) {
-            if (k < n_st) issue_stage(j0 + warp + kWarps * k, ring + k * G_::SLOT);
-            cp_async_commit();
+            for (int k = 0; k < G_::SC_PER_LANE; ++k) {
+                const int jc = lane + 32 * k;
+                const bool kpool = jc < G_::SCH;
+                const int jj = kpool ? jc : jc - G_::SCH;
+                const int u = jj / (D / 16);
+                int64_t ru = row0[0];  // row0[u] without a dynamically indexed array
+#pragma unroll
+                for (int uu = 1; uu < G_::SUB; ++uu)
+                    if (u == uu) ru = row0[uu];
+                const bool ok = ru >= 0;
+                const int64_t off = ok ? ru * G_::NB + 16 * (jj - u * (D / 16)) : 0;
+                cp_async16_zfill(slot + (kpool ? G_::KS_OFF : G_::VS_OFF) + 16 * jj,
+                                 (kpool ? p.ks : p.vs) + off, ok ? 16u : 0u, kv_pol);
+            }
         }
+        const bool last = (ij == iS - 1) || (issued == n_st - 1);
+        const uint32_t flags = (ifirst ? kFirst : 0u) | (last ? kLast : 0u);
+        if (lane == 0) {
+            sts_v4(slot + G_::HDR_OFF, okbits | (static_cast<uint32_t>(nval) << 8), flags,
+                   static_cast<uint32_t>(ib), static_cast<uint32_t>(ih));
+            sts_v4(slot + G_::HDR_OFF + 16, static_cast<uint32_t>(ips), static_cast<uint32_t>(iS),
+                   0u, 0u);
+        }
+        // advance the walk
+        ++issued;
+        ifirst = false;
+        if (last) {
+            ij = 0;
+            ips += iS;
+            ifirst = true;
+            if (issued < n_st && ++ih == H) {
+                ih = 0;
+                ++ib;
+                ilen = nlen;
+                iS = seq_stages(ilen, max_tokens, TOK);
+                while (iS == 0) {  // sequences without stages are not in the list
+                    ++ib;
+                    ilen = __ldg(p.seq_lens + ib);
+                    iS = seq_stages(ilen, max_tokens, TOK);
+                }
+                nlen = (ib + 1 < p.B) ? __ldg(p.seq_lens + ib + 1) : 0;
+            }
+        } else {
+            ++ij;
+        }
+    };
 
-        // ---- Q fragments of (b, h): lane (r, c) holds head r of the group; k-step kk covers
-        // head dims c*D/4 + 4kk + {0..3} (the same permutation is used for K), as FP16 q * 2^kq.
-        uint32_t qf[G_::KSTEPS][2];
-        float cs_row = 0.0f;
-        {
+    // ------------------------------------------------ start: stage 0, then the query cache
+    // The first page-id window is loaded while the query cache fills; the first copies go out
+    // as soon as the page ids are in, and the queries are waited for behind them.
+    if (n_st > 0) issue_next(ring);
+    cp_async_commit();
+    cp_async_wait<1>();  // this thread's query chunks have landed ...
+    __syncthreads();     // ... and every thread's: from here on warps run alone until the merge
+
+    // ------------------------------------------------ compute side
+    uint32_t qf[G_::KSTEPS][2];
+    float cs0 = 0.0f, cs1 = 0.0f;
+    float o[G_::KSTEPS][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    const float gvs = __ldg(p.gv);
+
+#pragma unroll 1
+    for (int i = 0; i < n_st; ++i) {
+        // the next stage goes into the slot computed at iteration i - 1
+        if (i + 1 < n_st) issue_next(ring + ((i + 1) % G_::SLOTS) * G_::SLOT);
+        cp_async_commit();
+        cp_async_wait<1>();  // this lane's copies of stage i are done ...
+        __syncwarp();        // ... and so are the other lanes'
+        const uint32_t st = ring + (i % G_::SLOTS) * G_::SLOT;
+        uint32_t hdr[4];
+        lds_words(hdr, st + G_::HDR_OFF);
+        const uint32_t okbits = hdr[0] & 0xFFu;
+        const int nval = static_cast<int>(hdr[0] >> 8);
+        const uint32_t flags = hdr[1];
+        if (flags & kFirst) {
+            // ---- Q fragments of the piece: lane (r, c) holds head r of the group; k-step kk
+            // covers head dims c*D/4 + 4kk + {0..3} (the same permutation is used for K), as
+            // FP16 q * 2^kq. From the query cache, or from global memory for a pair beyond it.
+            const int qpair = static_cast<int>(hdr[2]) * H + static_cast<int>(hdr[3]);
             float qv[D / 4];
             float qmax = 0.0f;
             if (r < G) {
-                const uint16_t* qp =
-                    p.q + (static_cast<int64_t>(b) * p.Hq + h * G + r) * D + c * (D / 4);
+                uint32_t qw[D / 8];
+                const int qi = qpair - q_first;
+                if (qi >= 0 && qi < q_cached) {
+                    lds_words(qw, qcache + ((qi * G + r) * D + c * (D / 4)) * 2);
+                } else {
+                    const uint4* qsrc = reinterpret_cast<const uint4*>(
+                        p.q + (static_cast<int64_t>(qpair) * G + r) * D + c * (D / 4));
 #pragma unroll
-                for (int i = 0; i < D / 4; i += 8) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(qp + i));
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        qv[i + 2 * k] = bf16_lo(wv[k]);
-                        qv[i + 2 * k + 1] = bf16_hi(wv[k]);
+                    for (int k = 0; k < D / 32; ++k) {
+                        const uint4 v = __ldg(qsrc + k);
+                        qw[4 * k] = v.x;
+                        qw[4 * k + 1] = v.y;
+                        qw[4 * k + 2] = v.z;
+                        qw[4 * k + 3] = v.w;
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < D / 4; ++i) qmax = fmaxf(qmax, fabsf(qv[i]));
+                for (int k = 0; k < D / 8; ++k) {
+                    qv[2 * k] = bf16_lo(qw[k]);
+                    qv[2 * k + 1] = bf16_hi(qw[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 4; ++k) qmax = fmaxf(qmax, fabsf(qv[k]));
             } else {
 #pragma unroll
-                for (int i = 0; i < D / 4; ++i) qv[i] = 0.0f;
+                for (int k = 0; k < D / 4; ++k) qv[k] = 0.0f;
             }
             qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, 1));
             qmax = fmaxf(qmax, __shfl_xor_sync(0xFFFFFFFFu, qmax, 2));
@@ -478,475 +840,270 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
                 qf[kk][0] = pack_f16x2(qv[4 * kk] * up, qv[4 * kk + 1] * up);
                 qf[kk][1] = pack_f16x2(qv[4 * kk + 2] * up, qv[4 * kk + 3] * up);
             }
-            if (r < G) cs_row = p.sm_scale * __ldg(p.gk) * kLog2e * ldexpf(1.0f, -kq);
+            const float cs_row = (r < G) ? p.sm_scale * __ldg(p.gk) * kLog2e * ldexpf(1.0f, -kq)
+                                         : 0.0f;
+            // score scale of this lane's two S^T columns (query heads 2c, 2c+1)
+            cs0 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c);
+            cs1 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c + 4);
+#pragma unroll
+            for (int m = 0; m < G_::KSTEPS; ++m)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) o[m][k] = 0.0f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.0f;
         }
-        // score scale of this lane's two S^T columns (query heads 2c, 2c+1)
-        const float cs0 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c);
-        const float cs1 = __shfl_sync(0xFFFFFFFFu, cs_row, 8 * c + 4);
 
-        float o[G_::KSTEPS][4];
+        if (okbits != 0u) {
+            const bool full = (okbits == (1u << G_::SUB) - 1) && nval >= TOK;
+            // valid-token bits of each sub-tile (only read when !full)
+            uint32_t tmask[G_::SUB];
 #pragma unroll
-        for (int m = 0; m < G_::KSTEPS; ++m)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[m][k] = 0.0f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+            for (int u = 0; u < G_::SUB; ++u) {
+                const int nv = min(16, max(0, nval - 16 * u));
+                tmask[u] = ((okbits >> u) & 1u) ? ((nv >= 16) ? 0xFFFFu : ((1u << nv) - 1u)) : 0u;
+            }
 
-        // ---- main loop over this warp's stages
-        for (int i = 0; i < n_st; ++i) {
-            if (i + kSlots - 1 < n_st)
-                issue_stage(j0 + warp + kWarps * (i + kSlots - 1),
-                            ring + ((i + kSlots - 1) % kSlots) * G_::SLOT);
-            cp_async_commit();
-            cp_async_wait<kSlots - 1>();  // this lane's copies of stage i are done ...
-            __syncwarp();                 // ... and so are the other lanes'
-            const uint32_t st = ring + (i % kSlots) * G_::SLOT;
-            const uint32_t hdr = lds_u32(st + G_::HDR_OFF);
-            const uint32_t okbits = hdr & 0xFFu;
-            const int nval = static_cast<int>(hdr >> 8);
-            if (okbits != 0u) {
-                const bool full = (okbits == (1u << G_::SUB) - 1) && nval >= TOK;
-                // valid-token bits of each sub-tile (only read when !full)
-                uint32_t tmask[G_::SUB];
+            // ---- S^T = K^ Q^T for the SUB sub-tiles
+            float x[G_::SUB][4];
+#pragma unroll
+            for (int u = 0; u < G_::SUB; ++u) {
+                const int row0 = 16 * u + r;
+                const int row1 = row0 + 8;
+                uint32_t kw0[G_::CW], kw1[G_::CW];
+                lds_words(kw0, st + G_::K_OFF + row0 * (D / 2) + c * G_::CHUNK);
+                lds_words(kw1, st + G_::K_OFF + row1 * (D / 2) + c * G_::CHUNK);
+                // FP16 (s, s) of the lane's D/64 blocks in rows row0 / row1: the scale byte
+                // is duplicated by an integer multiply, then converted as an E4M3 pair
+                uint32_t ks0[D / 64], ks1[D / 64];
+#pragma unroll
+                for (int q = 0; q < D / 64; ++q) {
+                    ks0[q] = e4m3x2_to_f16x2(
+                        lds_u8(st + G_::KS_OFF + row0 * G_::NB + c * (D / 64) + q) * 0x0101u);
+                    ks1[q] = e4m3x2_to_f16x2(
+                        lds_u8(st + G_::KS_OFF + row1 * G_::NB + c * (D / 64) + q) * 0x0101u);
+                }
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int q = 0; q < G_::CW; ++q) {
+                    uint32_t c0[4], c1[4];
+                    e2m1x8_to_f16x2x4(kw0[q], c0);
+                    e2m1x8_to_f16x2x4(kw1[q], c1);
+#pragma unroll
+                    for (int hk = 0; hk < 2; ++hk) {
+                        const int kk = 2 * q + hk;  // k-step: bytes 2kk, 2kk+1 of the chunk
+                        const int blk = kk / 4;     // block of the lane's chunk
+                        uint32_t a[4];
+                        a[0] = h2_mul(c0[2 * hk], ks0[blk]);
+                        a[1] = h2_mul(c1[2 * hk], ks1[blk]);
+                        a[2] = h2_mul(c0[2 * hk + 1], ks0[blk]);
+                        a[3] = h2_mul(c1[2 * hk + 1], ks1[blk]);
+                        mma_f16_16816(acc, a, qf[kk][0], qf[kk][1]);
+                    }
+                }
+                x[u][0] = acc[0] * cs0;
+                x[u][1] = acc[1] * cs1;
+                x[u][2] = acc[2] * cs0;
+                x[u][3] = acc[3] * cs1;
+            }
+
+            // ---- online softmax over the stage, columns = query heads 2c, 2c+1
+            if (!full) {
 #pragma unroll
                 for (int u = 0; u < G_::SUB; ++u) {
-                    const int nv = min(16, max(0, nval - 16 * u));
-                    tmask[u] = ((okbits >> u) & 1u) ? ((nv >= 16) ? 0xFFFFu : ((1u << nv) - 1u)) : 0u;
+                    if (!((tmask[u] >> r) & 1u)) x[u][0] = x[u][1] = -INFINITY;
+                    if (!((tmask[u] >> (r + 8)) & 1u)) x[u][2] = x[u][3] = -INFINITY;
                 }
-
-                // ---- S^T = K^ Q^T for the SUB sub-tiles
-                float x[G_::SUB][4];
+            }
+            float lm0 = fmaxf(x[0][0], x[0][2]), lm1 = fmaxf(x[0][1], x[0][3]);
 #pragma unroll
-                for (int u = 0; u < G_::SUB; ++u) {
-                    const int row0 = 16 * u + r;
-                    const int row1 = row0 + 8;
-                    uint32_t kw0[G_::CW], kw1[G_::CW];
-                    lds_words(kw0, st + G_::K_OFF + row0 * (D / 2) + c * G_::CHUNK);
-                    lds_words(kw1, st + G_::K_OFF + row1 * (D / 2) + c * G_::CHUNK);
-                    // FP16 (s, s) of the lane's D/64 blocks in rows row0 / row1: the scale byte
-                    // is duplicated by an integer multiply, then converted as an E4M3 pair
-                    uint32_t ks0[D / 64], ks1[D / 64];
+            for (int u = 1; u < G_::SUB; ++u) {
+                lm0 = fmaxf(lm0, fmaxf(x[u][0], x[u][2]));
+                lm1 = fmaxf(lm1, fmaxf(x[u][1], x[u][3]));
+            }
+            // column maxima over the stage, both columns in one FP16 pair (the running
+            // maximum only has to be close to the true one: p = 2^(x - m) stays below 2^8)
+            __half2 hm = __floats2half2_rn(lm0, lm1);
 #pragma unroll
-                    for (int q = 0; q < D / 64; ++q) {
-                        ks0[q] = e4m3x2_to_f16x2(
-                            lds_u8(st + G_::KS_OFF + row0 * G_::NB + c * (D / 64) + q) * 0x0101u);
-                        ks1[q] = e4m3x2_to_f16x2(
-                            lds_u8(st + G_::KS_OFF + row1 * G_::NB + c * (D / 64) + q) * 0x0101u);
-                    }
-                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int q = 0; q < G_::CW; ++q) {
-                        uint32_t c0[4], c1[4];
-                        e2m1x8_to_f16x2x4(kw0[q], c0);
-                        e2m1x8_to_f16x2x4(kw1[q], c1);
-#pragma unroll
-                        for (int hk = 0; hk < 2; ++hk) {
-                            const int kk = 2 * q + hk;  // k-step: bytes 2kk, 2kk+1 of the chunk
-                            const int blk = kk / 4;     // block of the lane's chunk
-                            uint32_t a[4];
-                            a[0] = h2_mul(c0[2 * hk], ks0[blk]);
-                            a[1] = h2_mul(c1[2 * hk], ks1[blk]);
-                            a[2] = h2_mul(c0[2 * hk + 1], ks0[blk]);
-                            a[3] = h2_mul(c1[2 * hk + 1], ks1[blk]);
-                            mma_f16_16816(acc, a, qf[kk][0], qf[kk][1]);
-                        }
-                    }
-                    x[u][0] = acc[0] * cs0;
-                    x[u][1] = acc[1] * cs1;
-                    x[u][2] = acc[2] * cs0;
-                    x[u][3] = acc[3] * cs1;
-                }
-
-                // ---- online softmax over the stage, columns = query heads 2c, 2c+1
-                if (!full) {
-#pragma unroll
-                    for (int u = 0; u < G_::SUB; ++u) {
-                        if (!((tmask[u] >> r) & 1u)) x[u][0] = x[u][1] = -INFINITY;
-                        if (!((tmask[u] >> (r + 8)) & 1u)) x[u][2] = x[u][3] = -INFINITY;
-                    }
-                }
-                float lm0 = fmaxf(x[0][0], x[0][2]), lm1 = fmaxf(x[0][1], x[0][3]);
-#pragma unroll
-                for (int u = 1; u < G_::SUB; ++u) {
-                    lm0 = fmaxf(lm0, fmaxf(x[u][0], x[u][2]));
-                    lm1 = fmaxf(lm1, fmaxf(x[u][1], x[u][3]));
-                }
-                // column maxima over the stage, both columns in one FP16 pair (the running
-                // maximum only has to be close to the true one: p = 2^(x - m) stays below 2^8)
-                __half2 hm = __floats2half2_rn(lm0, lm1);
+            for (int off = 4; off < 32; off <<= 1) {
+                const uint32_t uu =
+                    __shfl_xor_sync(0xFFFFFFFFu, *reinterpret_cast<const uint32_t*>(&hm), off);
+                hm = __hmax2(hm, *reinterpret_cast<const __half2*>(&uu));
+            }
+            float mx0 = __low2float(hm), mx1 = __high2float(hm);
+            if (__any_sync(0xFFFFFFFFu, fmaxf(mx0, mx1) > 65000.0f)) {
+                // scores beyond the FP16 range: reduce in fp32 instead
+                mx0 = lm0;
+                mx1 = lm1;
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
-                    const uint32_t uu =
-                        __shfl_xor_sync(0xFFFFFFFFu, *reinterpret_cast<const uint32_t*>(&hm), off);
-                    hm = __hmax2(hm, *reinterpret_cast<const __half2*>(&uu));
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
                 }
-                float mx0 = __low2float(hm), mx1 = __high2float(hm);
-                if (__any_sync(0xFFFFFFFFu, fmaxf(mx0, mx1) > 65000.0f)) {
-                    // scores beyond the FP16 range: reduce in fp32 instead
-                    mx0 = lm0;
-                    mx1 = lm1;
+            }
+            const bool grow = (mx0 > m0 + kRescaleThreshold) || (mx1 > m1 + kRescaleThreshold);
+            if (__any_sync(0xFFFFFFFFu, grow)) {
+                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                const float a0 = ex2_approx(m0 - n0), a1 = ex2_approx(m1 - n1);
+                m0 = n0;
+                m1 = n1;
+                l0 *= a0;
+                l1 *= a1;
 #pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
-                    }
+                for (int m = 0; m < G_::KSTEPS; ++m) {
+                    o[m][0] *= a0;
+                    o[m][1] *= a1;
+                    o[m][2] *= a0;
+                    o[m][3] *= a1;
                 }
-                const bool grow = (mx0 > m0 + kRescaleThreshold) || (mx1 > m1 + kRescaleThreshold);
-                if (__any_sync(0xFFFFFFFFu, grow)) {
-                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                    const float a0 = ex2_approx(m0 - n0), a1 = ex2_approx(m1 - n1);
-                    m0 = n0;
-                    m1 = n1;
-                    l0 *= a0;
-                    l1 *= a1;
+            }
+            uint32_t pb[G_::SUB][2];
 #pragma unroll
-                    for (int m = 0; m < G_::KSTEPS; ++m) {
-                        o[m][0] *= a0;
-                        o[m][1] *= a1;
-                        o[m][2] *= a0;
-                        o[m][3] *= a1;
-                    }
-                }
-                uint32_t pb[G_::SUB][2];
-#pragma unroll
-                for (int u = 0; u < G_::SUB; ++u) {
-                    const float p0 = ex2_approx(x[u][0] - m0), p1 = ex2_approx(x[u][1] - m1);
-                    const float p2 = ex2_approx(x[u][2] - m0), p3 = ex2_approx(x[u][3] - m1);
-                    l0 += p0 + p2;
-                    l1 += p1 + p3;
-                    // P^T (tokens x heads) -> B operand (k = tokens, n = heads)
-                    pb[u][0] = movmatrix_trans(pack_f16x2(p0, p1));
-                    pb[u][1] = movmatrix_trans(pack_f16x2(p2, p3));
-                }
+            for (int u = 0; u < G_::SUB; ++u) {
+                const float p0 = ex2_approx(x[u][0] - m0), p1 = ex2_approx(x[u][1] - m1);
+                const float p2 = ex2_approx(x[u][2] - m0), p3 = ex2_approx(x[u][3] - m1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // P^T (tokens x heads) -> B operand (k = tokens, n = heads)
+                pb[u][0] = movmatrix_trans(pack_f16x2(p0, p1));
+                pb[u][1] = movmatrix_trans(pack_f16x2(p2, p3));
+            }
 
-                // ---- O^T += V^^T P^T. Lane pairs: pr0 (tokens 2c, 2c+1), pr1 (tokens 2c+8, 2c+9)
+            // ---- O^T += V^^T P^T. Lane pairs: pr0 (tokens 2c, 2c+1), pr1 (tokens 2c+8, 2c+9)
 #pragma unroll
-                for (int u = 0; u < G_::SUB; ++u) {
-                    const int pr0 = 8 * u + c, pr1 = pr0 + 4;
-                    // the lane's chunk covers head dims rho*D/8 .. +D/8-1: blocks (rho*D/8)/16 ...
-                    constexpr int kBlkPerChunk = (D / 8 + 15) / 16;
-                    uint32_t vsc0[kBlkPerChunk], vsc1[kBlkPerChunk];
+            for (int u = 0; u < G_::SUB; ++u) {
+                const int pr0 = 8 * u + c, pr1 = pr0 + 4;
+                // the lane's chunk covers head dims rho*D/8 .. +D/8-1: blocks (rho*D/8)/16 ...
+                constexpr int kBlkPerChunk = (D / 8 + 15) / 16;
+                uint32_t vsc0[kBlkPerChunk], vsc1[kBlkPerChunk];
+#pragma unroll
+                for (int q = 0; q < kBlkPerChunk; ++q) {
+                    const int blk = (rho * (D / 8)) / 16 + q;
+                    vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk));
+                    vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk));
+                }
+                if (!full && tmask[u] != 0xFFFFu) {
+                    // tokens past the sequence end in a real page: their V scales may be
+                    // anything, so they are zeroed (P is 0 there already)
+                    const uint32_t tm = tmask[u];
+                    const uint32_t keep0 = (((tm >> (2 * c)) & 1u) ? 0x0000FFFFu : 0u) |
+                                           (((tm >> (2 * c + 1)) & 1u) ? 0xFFFF0000u : 0u);
+                    const uint32_t keep1 = (((tm >> (2 * c + 8)) & 1u) ? 0x0000FFFFu : 0u) |
+                                           (((tm >> (2 * c + 9)) & 1u) ? 0xFFFF0000u : 0u);
 #pragma unroll
                     for (int q = 0; q < kBlkPerChunk; ++q) {
-                        const int blk = (rho * (D / 8)) / 16 + q;
-                        vsc0[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr0 * 2 * G_::NB + 2 * blk));
-                        vsc1[q] = e4m3x2_to_f16x2(lds_u16(st + G_::VS_OFF + pr1 * 2 * G_::NB + 2 * blk));
+                        vsc0[q] &= keep0;
+                        vsc1[q] &= keep1;
                     }
-                    if (!full && tmask[u] != 0xFFFFu) {
-                        // tokens past the sequence end in a real page: their V scales may be
-                        // anything, so they are zeroed (P is 0 there already)
-                        const uint32_t tm = tmask[u];
-                        const uint32_t keep0 = (((tm >> (2 * c)) & 1u) ? 0x0000FFFFu : 0u) |
-                                               (((tm >> (2 * c + 1)) & 1u) ? 0xFFFF0000u : 0u);
-                        const uint32_t keep1 = (((tm >> (2 * c + 8)) & 1u) ? 0x0000FFFFu : 0u) |
-                                               (((tm >> (2 * c + 9)) & 1u) ? 0xFFFF0000u : 0u);
+                }
+                uint32_t vw0[G_::CW], vw1[G_::CW];
 #pragma unroll
-                        for (int q = 0; q < kBlkPerChunk; ++q) {
-                            vsc0[q] &= keep0;
-                            vsc1[q] &= keep1;
-                        }
+                for (int q = 0; q < G_::CW; q += (G_::CW >= 4 ? 4 : G_::CW)) {
+                    const int xb = rho * G_::CHUNK + 4 * q;  // logical byte of the chunk piece
+                    uint32_t t0w[G_::CW >= 4 ? 4 : G_::CW], t1w[G_::CW >= 4 ? 4 : G_::CW];
+                    lds_words(t0w, st + G_::V_OFF + v_swz<D>(pr0, xb));
+                    lds_words(t1w, st + G_::V_OFF + v_swz<D>(pr1, xb));
+#pragma unroll
+                    for (int e = 0; e < (G_::CW >= 4 ? 4 : G_::CW); ++e) {
+                        vw0[q + e] = t0w[e];
+                        vw1[q + e] = t1w[e];
                     }
-                    uint32_t vw0[G_::CW], vw1[G_::CW];
+                }
 #pragma unroll
-                    for (int q = 0; q < G_::CW; q += (G_::CW >= 4 ? 4 : G_::CW)) {
-                        const int xb = rho * G_::CHUNK + 4 * q;  // logical byte of the chunk piece
-                        uint32_t t0w[G_::CW >= 4 ? 4 : G_::CW], t1w[G_::CW >= 4 ? 4 : G_::CW];
-                        lds_words(t0w, st + G_::V_OFF + v_swz<D>(pr0, xb));
-                        lds_words(t1w, st + G_::V_OFF + v_swz<D>(pr1, xb));
+                for (int q = 0; q < G_::CW; ++q) {
+                    uint32_t c0[4], c1[4];
+                    e2m1x8_to_f16x2x4(vw0[q], c0);
+                    e2m1x8_to_f16x2x4(vw1[q], c1);
 #pragma unroll
-                        for (int e = 0; e < (G_::CW >= 4 ? 4 : G_::CW); ++e) {
-                            vw0[q + e] = t0w[e];
-                            vw1[q + e] = t1w[e];
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < G_::CW; ++q) {
-                        uint32_t c0[4], c1[4];
-                        e2m1x8_to_f16x2x4(vw0[q], c0);
-                        e2m1x8_to_f16x2x4(vw1[q], c1);
-#pragma unroll
-                        for (int hm2 = 0; hm2 < 2; ++hm2) {
-                            const int m = 2 * q + hm2;   // M-tile: bytes 2m, 2m+1 of the chunk
-                            const int sq = (2 * m) / 16; // block of that byte within the chunk
-                            uint32_t a[4];
-                            a[0] = h2_mul(c0[2 * hm2], vsc0[sq]);
-                            a[1] = h2_mul(c0[2 * hm2 + 1], vsc0[sq]);
-                            a[2] = h2_mul(c1[2 * hm2], vsc1[sq]);
-                            a[3] = h2_mul(c1[2 * hm2 + 1], vsc1[sq]);
-                            mma_f16_16816(o[m], a, pb[u][0], pb[u][1]);
-                        }
+                    for (int hm2 = 0; hm2 < 2; ++hm2) {
+                        const int m = 2 * q + hm2;   // M-tile: bytes 2m, 2m+1 of the chunk
+                        const int sq = (2 * m) / 16; // block of that byte within the chunk
+                        uint32_t a[4];
+                        a[0] = h2_mul(c0[2 * hm2], vsc0[sq]);
+                        a[1] = h2_mul(c0[2 * hm2 + 1], vsc0[sq]);
+                        a[2] = h2_mul(c1[2 * hm2], vsc1[sq]);
+                        a[3] = h2_mul(c1[2 * hm2 + 1], vsc1[sq]);
+                        mma_f16_16816(o[m], a, pb[u][0], pb[u][1]);
                     }
                 }
             }
-            __syncwarp();  // every lane is done reading the slot before it refills
         }
-        cp_async_wait<0>();
 
-        // ---- merge the 4 warps and write the piece's record
+        if (flags & kLast) {
+            // ---- end of a piece: the whole pair (outputs) or a record
+            uint32_t h2[4];
+            lds_words(h2, st + G_::HDR_OFF + 16);
+            const int pb_ = static_cast<int>(hdr[2]), ph = static_cast<int>(hdr[3]);
+            const int pps = static_cast<int>(h2[0]), pS = static_cast<int>(h2[1]);
+            float ls0 = l0, ls1 = l1;
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
-            l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
-        }
-        if (r == 0) {
-            red_m[warp][2 * c] = m0;
-            red_m[warp][2 * c + 1] = m1;
-            red_l[warp][2 * c] = l0;
-            red_l[warp][2 * c + 1] = l1;
-        }
-        __syncthreads();  // every warp is done with its ring: the rings hold the merge buffer
-        // the outcome of the count bumped at the previous boundary (written before this barrier)
-        const int pend_last = pend_s[0];
-        const int pend_b = pend_s[1], pend_h = pend_s[2], pend_ps = pend_s[3], pend_S = pend_s[4];
-        float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            M0 = fmaxf(M0, red_m[w][2 * c]);
-            M1 = fmaxf(M1, red_m[w][2 * c + 1]);
-        }
-        const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M0);
-        const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M1);
-        // over the drained rings: the warps' partial outputs [kWarps][kMaxGroup][D], then the
-        // merge weights of a pair's records [kMaxRecW][kMaxGroup], merged (max, sum) per head, and the
-        // records' sums [kMaxRecW][kMaxGroup]
-        float* so = reinterpret_cast<float*>(smem);
-        float (*mw_s)[kMaxGroup] = reinterpret_cast<float (*)[kMaxGroup]>(so + kWarps * kMaxGroup * D);
-        float (*ml_s)[2] = reinterpret_cast<float (*)[2]>(so + kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup);
-        float (*lw_s)[kMaxGroup] = reinterpret_cast<float (*)[kMaxGroup]>(
-            so + kWarps * kMaxGroup * D + kMaxRecW * kMaxGroup + 2 * kMaxGroup);
-#pragma unroll
-        for (int m = 0; m < G_::KSTEPS; ++m) {
-            const int d0 = rho * (D / 8) + 2 * m;
-            float* base = so + (warp * kMaxGroup + 2 * c) * D;
-            base[d0] = o[m][0] * f0;
-            base[D + d0] = o[m][1] * f1;
-            base[d0 + 1] = o[m][2] * f0;
-            base[D + d0 + 1] = o[m][3] * f1;
-        }
-        __syncthreads();
-        // CTAs c_first .. c_last cover the pair, each leaving record c + (b H + h); the last of
-        // them to finish merges the records
-        const int c_first = pair_start / W, c_last = (pair_start + S_b - 1) / W;
-        const int n_rec = c_last - c_first + 1;
-        const int64_t bh64 = static_cast<int64_t>(b) * H + h;
-        auto rec_index = [&](int k) -> int64_t { return c_first + k + bh64; };
-        const float gvs = __ldg(p.gv);
-        // merge the records of pair (mb, mh) once all of them are written (by the CTA whose
-        // count completed them), writing its output and LSE
-        auto merge_records = [&](int mb, int mh, int mps, int mS) {
-            const int c_first_m = mps / W, c_last_m = (mps + mS - 1) / W;
-            const int n_rec_m = c_last_m - c_first_m + 1;
-            const int64_t bh_m = static_cast<int64_t>(mb) * H + mh;
-            auto rec_index_m = [&](int k) -> int64_t { return c_first_m + k + bh_m; };
-            // every record of the pair is written: merge them (L2 reads, not L1). The (max,
-            // sum) pairs of up to kMaxRecW records are staged in shared memory by one round
-            // of loads while the first records' outputs are already in flight.
-            __threadfence();
-            // every CTA of the pair has counted, so the count can go back to 0: a replay of the
-            // same launch (a captured CUDA graph, same tag) starts from a clean word
-            if (tid == 0) atomicExch(p.done + bh_m, 0ull);
-            constexpr int NQ = kMaxGroup * D / kDecThreads;
-            constexpr int kRecUnroll = NQ >= 16 ? 2 : 8;  // record values in flight: 32 or 64
-            const int n_fast = min(n_rec_m, kMaxRecW);
-            for (int idx = tid; idx < n_fast * G; idx += kDecThreads) {
-                const int k = idx / G, col = idx - (idx / G) * G;
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-                    p.rec_ml + (rec_index_m(k) * G + col) * 2));
-                mw_s[k][col] = ml.x;
-                lw_s[k][col] = ml.y;
+            for (int off = 4; off < 32; off <<= 1) {
+                ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, off);
+                ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, off);
             }
-            float v[kRecUnroll][NQ];
-            auto load_recs = [&](int k0) {
+            const int g0 = 2 * c, g1 = 2 * c + 1;
+            const int gf = pps / W, gl = (pps + pS - 1) / W;
+            const int64_t bh = static_cast<int64_t>(pb_) * H + ph;
+            if (gf == gl) {
+                // the whole pair is this piece: normalise and write the output directly
+                uint16_t* ob = p.out + (static_cast<int64_t>(pb_) * p.Hq + ph * G) * D;
+                const float f0 = ls0 > 0.0f ? gvs / ls0 : 0.0f;
+                const float f1 = ls1 > 0.0f ? gvs / ls1 : 0.0f;
 #pragma unroll
-                for (int u = 0; u < kRecUnroll; ++u) {
-                    const int k = min(k0 + u, n_rec_m - 1);
-                    const float* rk = p.rec_o + rec_index_m(k) * G * D;
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q) {
-                        const int i = tid + kDecThreads * q;
-                        v[u][q] = (i < G * D) ? __ldcg(rk + i) : 0.0f;
-                    }
+                for (int m = 0; m < G_::KSTEPS; ++m) {
+                    const int d0 = rho * (D / 8) + 2 * m;
+                    if (g0 < G)
+                        *reinterpret_cast<uint32_t*>(ob + g0 * D + d0) =
+                            pack_bf16x2(o[m][0] * f0, o[m][2] * f0);
+                    if (g1 < G)
+                        *reinterpret_cast<uint32_t*>(ob + g1 * D + d0) =
+                            pack_bf16x2(o[m][1] * f1, o[m][3] * f1);
                 }
-            };
-            load_recs(0);
-            __syncthreads();
-            if (warp < G) {  // warp w: query heads w, w + 4
-                for (int col = warp; col < G; col += kWarps) {
-                    auto m_of = [&](int k) {
-                        return k < n_fast ? mw_s[k][col]
-                                          : __ldcg(p.rec_ml + (rec_index_m(k) * G + col) * 2);
-                    };
-                    float M = -INFINITY;
-                    for (int k = lane; k < n_rec_m; k += 32) M = fmaxf(M, m_of(k));
-#pragma unroll
-                    for (int o2 = 16; o2 > 0; o2 >>= 1)
-                        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o2));
-                    float lsum = 0.0f;
-                    for (int k = lane; k < n_rec_m; k += 32) {
-                        const float mk = m_of(k);
-                        const float lk = k < n_fast
-                                             ? lw_s[k][col]
-                                             : __ldcg(p.rec_ml + (rec_index_m(k) * G + col) * 2 + 1);
-                        const float wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - M);
-                        if (k < n_fast) mw_s[k][col] = wk;  // this lane alone reads entry k
-                        lsum += wk * lk;
-                    }
-#pragma unroll
-                    for (int o2 = 16; o2 > 0; o2 >>= 1)
-                        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o2);
-                    if (lane == 0) {
-                        ml_s[col][0] = M;
-                        ml_s[col][1] = lsum;
-                        if (p.lse)
-                            p.lse[static_cast<int64_t>(mb) * p.Hq + mh * G + col] =
-                                (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f
-                                              : -INFINITY;
-                    }
-                }
-            }
-            __syncthreads();
-            // thread tid owns outputs i = tid + kDecThreads q; kRecUnroll records at a time
-            float acc[NQ];
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) acc[q] = 0.0f;
-            for (int k0 = 0; k0 < n_rec_m; k0 += kRecUnroll) {
-                if (k0 > 0) load_recs(k0);
-#pragma unroll
-                for (int u = 0; u < kRecUnroll; ++u) {
-                    const int k = k0 + u;
-                    if (k >= n_rec_m) break;
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q) {
-                        const int i = tid + kDecThreads * q;
-                        if (i >= G * D) continue;
-                        const int col = i / D;
-                        float wk;
-                        if (k < n_fast) {
-                            wk = mw_s[k][col];
-                        } else {
-                            const float mk = __ldcg(p.rec_ml + (rec_index_m(k) * G + col) * 2);
-                            wk = (mk == -INFINITY) ? 0.0f : exp2f(mk - ml_s[col][0]);
-                        }
-                        acc[q] += wk * v[u][q];
-                    }
-                }
-            }
-            uint16_t* ob = p.out + (static_cast<int64_t>(mb) * p.Hq + mh * G) * D;
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const int i = tid + kDecThreads * q;
-                if (i >= G * D) continue;
-                const float ls = ml_s[i / D][1];
-                const __nv_bfloat16 yb = __float2bfloat16_rn(ls > 0.0f ? acc[q] * (gvs / ls) : 0.0f);
-                ob[i] = *reinterpret_cast<const uint16_t*>(&yb);
-            }
-        };
-        if (n_rec == 1) {
-            // the whole pair is this piece: normalise and write the output directly
-            if (tid < G) {
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
-                float lsum = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float mw = red_m[w][tid];
-                    if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
-                }
-                ml_s[tid][0] = M;
-                ml_s[tid][1] = lsum;
-                if (p.lse)
-                    p.lse[static_cast<int64_t>(b) * p.Hq + h * G + tid] =
-                        (lsum > 0.0f) ? (M + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
-            }
-            __syncthreads();
-            uint16_t* ob = p.out + (static_cast<int64_t>(b) * p.Hq + h * G) * D;
-            for (int i = tid; i < G * D; i += kDecThreads) {
-                const int col = i / D, d = i - (i / D) * D;
-                float acc = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
-                const float ls = ml_s[col][1];
-                const __nv_bfloat16 yb = __float2bfloat16_rn(ls > 0.0f ? acc * (gvs / ls) : 0.0f);
-                ob[i] = *reinterpret_cast<const uint16_t*>(&yb);
-            }
-        } else {
-            const int64_t rec = blockIdx.x + bh64;
-            float* ro = p.rec_o + rec * G * D;
-            for (int i = tid; i < G * D; i += kDecThreads) {
-                const int col = i / D, d = i - (i / D) * D;
-                float acc = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) acc += so[(w * kMaxGroup + col) * D + d];
-                ro[i] = acc;
-            }
-            if (tid < G) {
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
-                float lsum = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float mw = red_m[w][tid];
-                    if (mw != -INFINITY) lsum += red_l[w][tid] * ex2_approx(mw - M);
-                }
-                p.rec_ml[(rec * G + tid) * 2] = M;
-                p.rec_ml[(rec * G + tid) * 2 + 1] = lsum;
-            }
-        }
-        if (has_next) {
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                const int i = tid + q2 * kDecThreads;
-                if (i < nn_pages && i < kPageBuf) page_ids[i] = nid[q2];
-            }
-        }
-        __syncthreads();  // outputs / record written, merge buffer read, next page ids in place
-        if (pend_last) {
-            merge_records(pend_b, pend_h, pend_ps, pend_S);
-            __syncthreads();  // the merge is done with the rings
-        }
-        if (n_rec > 1) {
-            if (has_next) {
-                // publish the record without holding up the next piece: one lane of the last
-                // warp makes it visible and bumps the count; the outcome is read at the next
-                // piece's end, where a completed pair is merged
-                if (warp == kWarps - 1 && lane == 0) {
-                    __threadfence();
-                    unsigned long long* cnt = p.done + bh64;
-                    const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
-                    pend_s[0] = (k == static_cast<uint32_t>(n_rec - 1)) ? 1 : 0;
-                    pend_s[1] = b;
-                    pend_s[2] = h;
-                    pend_s[3] = pair_start;
-                    pend_s[4] = S_b;
+                if (r == 0 && p.lse) {
+                    float* lb = p.lse + static_cast<int64_t>(pb_) * p.Hq + ph * G;
+                    if (g0 < G) lb[g0] = ls0 > 0.0f ? (m0 + log2f(ls0)) * 0.6931471805599453f : -INFINITY;
+                    if (g1 < G) lb[g1] = ls1 > 0.0f ? (m1 + log2f(ls1)) * 0.6931471805599453f : -INFINITY;
                 }
             } else {
-                if (tid == 0) {
-                    __threadfence();  // the record is visible before the count says so
-                    unsigned long long* cnt = p.done + bh64;
-                    const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
-                    last_s = (k == static_cast<uint32_t>(n_rec - 1)) ? 1 : 0;
+                const int64_t rec = gw + bh;
+                float* ro = p.rec_o + rec * G * D;
+#pragma unroll
+                for (int m = 0; m < G_::KSTEPS; ++m) {
+                    const int d0 = rho * (D / 8) + 2 * m;
+                    if (g0 < G) *reinterpret_cast<float2*>(ro + g0 * D + d0) = make_float2(o[m][0], o[m][2]);
+                    if (g1 < G) *reinterpret_cast<float2*>(ro + g1 * D + d0) = make_float2(o[m][1], o[m][3]);
                 }
-                __syncthreads();
-                if (last_s) merge_records(b, h, pair_start, S_b);
+                if (r == 0) {
+                    if (g0 < G) *reinterpret_cast<float2*>(p.rec_ml + (rec * G + g0) * 2) = make_float2(m0, ls0);
+                    if (g1 < G) *reinterpret_cast<float2*>(p.rec_ml + (rec * G + g1) * 2) = make_float2(m1, ls1);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();  // the record is visible before the count says so
+                    unsigned long long* cnt = p.done + bh;
+                    const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
+                    if (k == kTagGiveUp) flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
+                    if (k == static_cast<uint32_t>(gl - gf)) {  // every piece is in: merge here
+                        const int slot = atomicAdd(&pend_n, 1);
+                        pend[slot][0] = pb_;
+                        pend[slot][1] = ph;
+                        pend[slot][2] = pps;
+                        pend[slot][3] = pS;
+                    }
+                }
             }
-        } else if (has_next && warp == kWarps - 1 && lane == 0) {
-            pend_s[0] = 0;
         }
-
-        // ---- next piece: the next pair with at least one stage
-        s += j1 - j0;
-        j = 0;
-        pair_start += S_b;
-        if (s < s_end) {
-            if (++h == H) {
-                h = 0;
-                do {
-                    ++b;
-                    S_b = seq_stages(__ldg(p.seq_lens + b), max_tokens, TOK);
-                } while (S_b == 0);
-            }
+        __syncwarp();  // every lane is done reading the slot before it refills
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every warp's run is done: the rings are free for the merge
+    const int n_pend = pend_n;
+    for (int k = 0; k < n_pend;) {
+        const int m = merge_batch<D>(p, pend, k, n_pend, W, smem);
+        if (m == 0) {  // a pair whose records do not fit at once: by chunks
+            merge_pair<D>(p, pend[k][0], pend[k][1], pend[k][2], pend[k][3], W, smem);
+            ++k;
         }
+        k += m;
     }
 }
 
@@ -956,22 +1113,23 @@ __global__ void __launch_bounds__(kDecThreads, Geo<D>::BLOCKS_PER_SM)
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int stage_tokens(int D) { return D == 256 ? 32 : 64; }
-int blocks_per_sm(int D) { return D == 64 ? 4 : (D == 256 ? 2 : 3); }
+int warps_per_cta(int D) { return D == 64 ? 16 : (D == 128 ? 12 : 8); }
 
-// CTAs of the split kernel: one wave (automatic), or n runs per (sequence, KV head) pair.
-int64_t decode_ctas(int batch, int H, int D, int max_num_splits) {
+// Warp runs of the split kernel: one per warp of one CTA per SM (automatic), or n runs per
+// (sequence, KV head) pair.
+int64_t decode_runs(int batch, int H, int D, int max_num_splits) {
     if (max_num_splits > 0) return static_cast<int64_t>(max_num_splits) * batch * H;
-    return static_cast<int64_t>(num_sms()) * blocks_per_sm(D);
+    return static_cast<int64_t>(num_sms()) * warps_per_cta(D);
 }
 
 struct WsLayout {
     size_t done, ml, o, total;
 };
 
-// Records: one per (CTA, pair) it covers; bounded by CTAs + pairs because runs are consecutive
-WsLayout ws_layout(int batch, int H, int Hq, int D, int64_t ctas) {
+// Records: one per (warp run, pair) piece; bounded by runs + pairs because runs are consecutive.
+WsLayout ws_layout(int batch, int H, int Hq, int D, int64_t runs) {
     const size_t pairs = static_cast<size_t>(batch) * H;
-    const size_t records = static_cast<size_t>(ctas) + pairs;
+    const size_t records = static_cast<size_t>(runs) + pairs;
     const size_t G = static_cast<size_t>(Hq / H);
     WsLayout w;
     w.done = 0;
@@ -992,23 +1150,24 @@ bool decode_shape_ok(const nvfp4kv_layout* l, int Hq) {
 }
 
 // The flat stage list, the token positions and the records index with 32-bit integers.
-bool decode_size_ok(int batch, int H, int D, int max_pages, int T, int64_t ctas) {
+bool decode_size_ok(int batch, int H, int D, int max_pages, int T, int64_t runs) {
     const int64_t max_tokens = static_cast<int64_t>(max_pages) * T;
     const int64_t tok = stage_tokens(D);
     const int64_t stages = (max_tokens + tok - 1) / tok * batch * H;
     const int64_t lim = (int64_t{1} << 31) - 1;
-    return max_tokens < lim - tok && stages + ctas * kWarps < lim &&
-           ctas + static_cast<int64_t>(batch) * H < lim;
+    return max_tokens < lim - tok && stages + runs < lim &&
+           runs + static_cast<int64_t>(batch) * H < lim;
 }
 
 template <int D>
-cudaError_t launch_decode(const DecodeParams& p, int64_t ctas, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams& p, int64_t runs, cudaStream_t s) {
+    using G_ = Geo<D>;
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Geo<D>::SMEM);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, G_::SMEM);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(decode_split_kernel<D>, static_cast<unsigned>(ctas), kDecThreads,
-                   static_cast<size_t>(Geo<D>::SMEM), s, p);
+    const int64_t ctas = (runs + G_::WARPS - 1) / G_::WARPS;
+    e = launch_pdl(decode_split_kernel<D>, static_cast<unsigned>(ctas), G_::THREADS,
+                   static_cast<size_t>(G_::SMEM), s, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1027,8 +1186,8 @@ extern "C" size_t nvfp4_paged_decode_workspace_size(const nvfp4kv_layout* layout
         return 0;
     if (num_q_heads % layout->num_kv_heads != 0) return 0;
     const int H = layout->num_kv_heads;
-    const int64_t ctas = decode_ctas(batch, H, layout->head_dim, max_num_splits);
-    return ws_layout(batch, H, num_q_heads, layout->head_dim, ctas).total;
+    const int64_t runs = decode_runs(batch, H, layout->head_dim, max_num_splits);
+    return ws_layout(batch, H, num_q_heads, layout->head_dim, runs).total;
 }
 
 extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
@@ -1053,9 +1212,9 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
     const int D = layout->head_dim;
     const int H = layout->num_kv_heads;
     const int T = layout->page_size;
-    const int64_t ctas = decode_ctas(batch, H, D, max_num_splits);
-    if (!decode_size_ok(batch, H, D, max_pages_per_seq, T, ctas)) return NVFP4KV_ERR_UNSUPPORTED;
-    const WsLayout wl = ws_layout(batch, H, num_q_heads, D, ctas);
+    const int64_t runs = decode_runs(batch, H, D, max_num_splits);
+    if (!decode_size_ok(batch, H, D, max_pages_per_seq, T, runs)) return NVFP4KV_ERR_UNSUPPORTED;
+    const WsLayout wl = ws_layout(batch, H, num_q_heads, D, runs);
     if (!workspace || workspace_bytes < wl.total || !aligned16(workspace))
         return NVFP4KV_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1085,15 +1244,15 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention(
     p.T = T;
     p.pool_pages = pool_pages;
     p.max_pages = max_pages_per_seq;
-    p.min_w = (max_num_splits > 0) ? 1 : kWarps;
+    p.num_runs = static_cast<int32_t>(runs);
     p.sm_scale = sm_scale;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (D) {
-    case 64: e = launch_decode<64>(p, ctas, s); break;
-    case 128: e = launch_decode<128>(p, ctas, s); break;
-    default: e = launch_decode<256>(p, ctas, s); break;
+    case 64: e = launch_decode<64>(p, runs, s); break;
+    case 128: e = launch_decode<128>(p, runs, s); break;
+    default: e = launch_decode<256>(p, runs, s); break;
     }
     if (e != cudaSuccess) return NVFP4KV_ERR_CUDA;
 

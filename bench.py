@@ -491,9 +491,178 @@ def kernel_table(path, peak):
         res[name] = {"ms": round(ms, 4), "bytes": int(nbytes), "GB_s": round(gbs, 1),
                      "frac_of_peak": round(gbs / peak, 4), "launches": nrot}
     del chunks, wss
+    extend_step_table(path, flush, peak, res)
+    decode_extra_table(path, flush, peak, res)
     res.update(cold_table(path, flush, time_kernel))
     del flush
+    # codec throughput in tokens: a launch encodes or decodes P pages of T tokens of one tensor
+    tok = path.rt.P * path.rt.T
+    for name, r in res.items():
+        if name.startswith(("quantize_", "dequantize_", "amax_")):
+            r["tokens_per_s"] = round(tok / (r["ms"] * 1e-3), 1)
     return res
+
+
+def per_config(result, peak):
+    """Fractions of the measured copy peak for each workload the targets name, from the kernel
+    table (each call timed alone after an L2 flush) and, where a serving loop issues the call
+    back to back, from that timing too."""
+    k = result["kernels"]
+    pick = lambda name: {key: k[name][key] for key in  # noqa: E731
+                         ("ms", "GB_s", "frac_of_peak", "bytes") if key in k[name]}
+    out = {
+        "page_roundtrip_quantize": {n: pick(n) for n in k if n.startswith("quantize_")},
+        "page_roundtrip_dequantize": {n: pick(n) for n in k if n.startswith("dequantize_")},
+        "decode_batch": dict(pick("decode (decode batch 32x8192, GQA 4)"),
+                             back_to_back=pick("decode (decode batch 32x8192, GQA 4), back to back")),
+        "long_context": dict(pick("decode (long context)"),
+                             in_step={"ms": result["roofline"]["launch_ms"],
+                                      "frac_of_peak": result["roofline"]["frac"]}),
+        "extend_step": pick("extend step: K+V prefix gather -> FP8 + K+V chunk write "
+                            "(4 launches back to back)"),
+        "decode_head_dim_64": pick("decode (32x8192, GQA 4, head_dim 64)"),
+        "decode_head_dim_256": pick("decode (32x8192, GQA 4, head_dim 256)"),
+    }
+    out["peak_GB_s"] = peak
+    return out
+
+
+def decode_cache(kv, dev, wl, seed_shift=0):
+    """NVFP4 K (dim pairs) and V (token pairs) pools of a decode workload, encoded on the GPU,
+    with its queries, page table and lengths; the BF16 sources are dropped."""
+    import torch
+    q, k, v, pt, sl = wl.make(device=dev)
+    lay = kv.Layout(wl.H, wl.D, wl.T)
+    u8 = torch.uint8
+    P = wl.pool_pages
+    c = dict(lay=lay, q=q, pt=pt, sl=sl)
+    c["kd"] = torch.empty((P, wl.H, wl.T, wl.D // 2), dtype=u8, device=dev)
+    c["ks"] = torch.empty((P, wl.H, wl.T, wl.D // 16), dtype=u8, device=dev)
+    c["vd"], c["vs"] = torch.empty_like(c["kd"]), torch.empty_like(c["ks"])
+    c["gk"] = torch.empty(1, dtype=torch.float32, device=dev)
+    c["gv"] = torch.empty(1, dtype=torch.float32, device=dev)
+    kv.nvfp4_kv_compute_global_scale(lay, k, c["gk"])
+    kv.nvfp4_kv_compute_global_scale(lay, v, c["gv"])
+    kv.nvfp4_kv_quantize_pages(lay, k, c["gk"], c["kd"], c["ks"])
+    kv.nvfp4_kv_quantize_pages(lay.with_packing(kv.PACK_TOKEN_PAIRS), v, c["gv"], c["vd"], c["vs"])
+    c["out"] = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.bfloat16, device=dev)
+    c["ws"] = torch.empty(kv.nvfp4_paged_decode_workspace_size(lay, wl.B, wl.Hq, pt.shape[1], 0),
+                          dtype=u8, device=dev)
+    del k, v
+    return c
+
+
+def decode_call(kv, wl, c):
+    return lambda: kv.nvfp4_paged_decode_attention(
+        c["lay"], c["q"], c["kd"], c["ks"], c["gk"], c["vd"], c["vs"], c["gv"], c["pt"], c["sl"],
+        wl.sm_scale, c["out"], workspace=c["ws"])
+
+
+def decode_bytes(wl, pt):
+    return (wl.kv_tokens * wl.H * (wl.D + wl.D // 8) + wl.B * wl.Hq * wl.D * 4 +
+            pt.numel() * 4 + wl.B * 4)
+
+
+def decode_extra_table(path, flush, peak, res):
+    """The decode batch issued back to back as a serving loop issues decode steps (two NVFP4
+    caches of 302 MB used in turn, so no call finds its inputs in the 129 MB L2; launches overlap
+    through programmatic dependent launch), and the decode batch at head_dim 64 and 256."""
+    import torch
+    import synthetic
+    kv, dev = path.kv, path.dev
+    wl = synthetic.decode_batch(seed=1)
+    caches = [decode_cache(kv, dev, wl), decode_cache(kv, dev, synthetic.decode_batch(seed=11))]
+    calls = [decode_call(kv, wl, c) for c in caches]
+    nbytes = decode_bytes(wl, caches[0]["pt"])
+    n = 20
+    for cl in calls * 2:
+        cl()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(5):
+        flush.fill_(1)
+        flush[: flush.numel() // 2].max()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n):
+            calls[i % 2]()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / n)
+    ms = statistics.median(ts)
+    gbs = nbytes / (ms * 1e-3) / GB
+    res["decode (decode batch 32x8192, GQA 4), back to back"] = {
+        "ms": round(ms, 4), "bytes": int(nbytes), "GB_s": round(gbs, 1),
+        "frac_of_peak": round(gbs / peak, 4), "launches": n,
+        "decode_tokens_per_s": round(wl.B / (ms * 1e-3), 1),
+        "kv_tokens_per_s": round(wl.kv_tokens / (ms * 1e-3), 1),
+        "method": "20 calls back to back over two caches used in turn (each 302 MB, above L2)"}
+    del caches, calls
+    for D in (64, 256):
+        wl = synthetic.DecodeWorkload(f"decode batch head_dim {D}", B=32, Hq=32, H=8, D=D, T=64,
+                                      seq_lens=[8192] * 32, pool_pages=4096, seed=1)
+        c = decode_cache(kv, dev, wl)
+        nbytes = decode_bytes(wl, c["pt"])
+        ms = time_kernel(decode_call(kv, wl, c), flush)
+        gbs = nbytes / (ms * 1e-3) / GB
+        res[f"decode (32x8192, GQA 4, head_dim {D})"] = {
+            "ms": round(ms, 4), "bytes": int(nbytes), "GB_s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "launches": 1,
+            "kv_tokens_per_s": round(wl.kv_tokens / (ms * 1e-3), 1)}
+        del c
+
+
+def extend_step_table(path, flush, peak, res):
+    """The extend workload as one step: for K and for V, the 4096-token NVFP4 prefix of each of
+    16 sequences gathered and dequantized into the FP8 workspace, and the 512-token BF16 chunk
+    written as NVFP4 pages and as its FP8 workspace copy: four launches back to back (K gather,
+    V gather, K chunk write, V chunk write), timed as one after an L2 flush."""
+    import torch
+    import synthetic
+    kv, dev = path.kv, path.dev
+    ex = synthetic.ExtendWorkload(seed=2)
+    H, T, D = ex.H, ex.T, ex.D
+    lay = kv.Layout(H, D, T)
+    u8 = torch.uint8
+    per_seq = ex.prefix // T + ex.chunk // T          # workspace slots of one sequence
+    slots = torch.arange(ex.B * per_seq, dtype=torch.int32, device=dev).view(ex.B, per_seq)
+    ws_prefix = slots[:, :ex.prefix // T].reshape(-1).contiguous()
+    ws_chunk = slots[:, ex.prefix // T:].reshape(-1).contiguous()
+    tens = []
+    for t, (packing, seed) in enumerate(((kv.PACK_DIM_PAIRS, 2), (kv.PACK_TOKEN_PAIRS, 3))):
+        exs = synthetic.ExtendWorkload(seed=seed)
+        prefix, ept, chunk, chunk_dst = exs.make(device=dev)
+        ly = lay.with_packing(packing)
+        pool = prefix.shape[0]
+        d = dict(lay=ly, ids=ept.reshape(-1).contiguous(), chunk=chunk, chunk_dst=chunk_dst)
+        d["pd"] = torch.empty((pool, H, T, D // 2), dtype=u8, device=dev)
+        d["ps"] = torch.empty((pool, H, T, D // 16), dtype=u8, device=dev)
+        d["g"] = torch.empty(1, dtype=torch.float32, device=dev)
+        kv.nvfp4_kv_compute_global_scale(ly, prefix, d["g"])
+        kv.nvfp4_kv_quantize_pages(ly, prefix, d["g"], d["pd"], d["ps"])
+        d["ws"] = torch.empty((ex.B * per_seq, H, T, D), dtype=u8, device=dev)
+        del prefix
+        tens.append(d)
+
+    def step():
+        for d in tens:
+            kv.nvfp4_kv_dequantize_pages(d["lay"], d["pd"], d["ps"], d["g"], d["ws"],
+                                         dst_dtype=kv.FP8_E4M3, src_page_ids=d["ids"],
+                                         dst_page_ids=ws_prefix)
+        for d in tens:
+            kv.nvfp4_kv_extend_write(d["lay"], d["chunk"], d["g"], d["pd"], d["ps"], d["ws"],
+                                     dst_page_ids=d["chunk_dst"], ws_page_ids=ws_chunk)
+    vals = H * T * D
+    gather = 2 * ex.prefix_pages * vals * 1.5625 + 2 * ex.prefix_pages * 4
+    write = 2 * ex.chunk_pages * vals * (2 + 0.5625 + 1) + 2 * ex.chunk_pages * 4
+    ms = time_kernel(step, flush)
+    gbs = (gather + write) / (ms * 1e-3) / GB
+    res["extend step: K+V prefix gather -> FP8 + K+V chunk write (4 launches back to back)"] = {
+        "ms": round(ms, 4), "bytes": int(gather + write), "GB_s": round(gbs, 1),
+        "frac_of_peak": round(gbs / peak, 4), "launches": 4,
+        "bytes_gather": int(gather), "bytes_chunk_write": int(write),
+        "tokens_per_s": round(ex.B * (ex.prefix + ex.chunk) / (ms * 1e-3), 1)}
+    del tens
 
 
 def cold_table(path, flush, timer, pages=2048):
@@ -666,7 +835,9 @@ def oracle_sample(seed=0, pages=1024, decode_seqs=1, max_tokens=None):
     t_dec = time.perf_counter() - t0
     dec_bytes = sum(lens) * wl.H * (wl.D + wl.D // 8)
     desc = (f"oracle on {rt.P} page round-trip pages of K (amax, encode, decode BF16 + FP8) and "
-            f"{decode_seqs} long-context sequence(s) ({sum(lens)} tokens, {wl.Hq} query heads)")
+            f"{decode_seqs} long-context sequence(s) ({sum(lens)} tokens, {wl.Hq} query heads) "
+            f"over random NVFP4 K/V bytes of the cache's shape (the oracle's time does not "
+            f"depend on the values)")
     return codec_bytes + dec_bytes, t_codec + t_dec, oracle.max_threads(), desc
 
 
@@ -756,7 +927,10 @@ def main():
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "dtype_detail": ("NVFP4 storage (E2M1 codes, E4M3 block scales, FP32 tensor scale); "
+                         "encode arithmetic in FP32; decode attention on FP16 tensor-core "
+                         "operands (exact dequantized K/V) with FP32 accumulation"),
         "data": "synthetic",
         "config": {"workload": WORKLOAD,
                    "l2": "inputs larger than L2 (129 MB); kernel table: L2 flushed before "
@@ -783,6 +957,7 @@ def main():
         result["roofline"]["achieved_isolated"] = iso["GB_s"]
         result["roofline"]["frac_isolated"] = iso["frac_of_peak"]
         result["roofline"]["launch_ms_isolated"] = iso["ms"]
+        result["roofline"]["per_config"] = per_config(result, peak)
     if not args.no_e2e:
         result["e2e"] = e2e(path, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

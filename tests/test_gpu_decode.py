@@ -66,14 +66,14 @@ class Cache:
                 assert np.array_equal(got.reshape(want.shape), want)
 
 
-def run_decode(kv, dev, cache, q, pt, sl, sm_scale, splits=0, status=None):
+def run_decode(kv, dev, cache, q, pt, sl, sm_scale, splits=0, status=None, workspace=None):
     B, Hq, D = q.shape
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
     lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=dev)
     kv.nvfp4_paged_decode_attention(cache.lay, q.to(dev), cache.kd, cache.ks, cache.gk,
                                     cache.vd, cache.vs, cache.gv, pt.to(dev), sl.to(dev),
                                     sm_scale, out, lse=lse, max_num_splits=splits,
-                                    status=status)
+                                    status=status, workspace=workspace)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
@@ -243,3 +243,40 @@ def test_bad_page_ids_and_lengths_are_flagged(kv, cuda):
     check(out[:1], lse[:1], ref, ref_lse)
     assert np.all(np.isfinite(out[1]))                    # the bad page is skipped
     assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+
+
+@pytest.mark.parametrize("fill", ["0xff", "random"])
+def test_workspace_needs_no_clearing(kv, cuda, fill):
+    """The decode workspace holds per-pair counters tagged with the call and the split records;
+    a workspace full of 0xFF bytes (every counter's tag above any call's) or of random bytes gives
+    the oracle's result, bit-identical to a call on a zeroed workspace, for the automatic split
+    and for 1, 5 and 64 forced splits. Only host-side writes to the buffer; nothing faults."""
+    H, G, D, T, B = 2, 4, 128, 64, 3
+    lens = [4096, 2500, 777]
+    maxp = max(-(-L // T) for L in lens)
+    g = synthetic.gen(31)
+    q = synthetic.randn_bf16((B, H * G, D), g)
+    pool = B * maxp
+    k = synthetic.kv_pages_bf16(pool, H, T, D, g, k_outliers=True)
+    v = synthetic.kv_pages_bf16(pool, H, T, D, g)
+    pt = torch.randperm(pool, generator=g).view(B, maxp).to(torch.int32)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    cache = Cache(kv, cuda, k, v, H, D, T)
+    sm = 1 / math.sqrt(D)
+    ref, ref_lse = oracle_decode(cache, q, pt, sl, sm)
+    for splits in (0, 1, 5, 64):
+        need = kv.nvfp4_paged_decode_workspace_size(cache.lay, B, H * G, maxp, splits)
+        ws = torch.empty(need, dtype=torch.uint8, device=cuda)
+        if fill == "0xff":
+            ws.fill_(0xFF)
+        else:
+            ws.copy_(torch.randint(0, 256, (need,), dtype=torch.uint8,
+                                   generator=synthetic.gen(1000 + splits)))
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        out, lse = run_decode(kv, cuda, cache, q, pt, sl, sm, splits=splits, status=status,
+                              workspace=ws)
+        check(out, lse, ref, ref_lse, tag=f"{fill} splits={splits}")
+        assert status.item() == 0
+        ws.zero_()
+        out0, lse0 = run_decode(kv, cuda, cache, q, pt, sl, sm, splits=splits, workspace=ws)
+        assert np.array_equal(out, out0) and np.array_equal(lse, lse0), (fill, splits)

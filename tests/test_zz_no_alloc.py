@@ -15,8 +15,6 @@ import synthetic
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 1e-3
-
 
 @pytest.fixture(scope="module")
 def kv(cuda):
@@ -64,18 +62,17 @@ def _run(kv, w, noalloc):
 
 def test_noalloc_decode_matches_workspace_entry_point(kv, cuda):
     """Two calls in a row (different sequences, so the second finds the first's partials in the
-    shared scratch) against the workspace entry point on the same inputs."""
+    shared scratch) against the workspace entry point on the same inputs. Both run the same
+    kernel with the same split plan and merge order, so the outputs and LSEs must be identical
+    bit for bit; a stale partial of the first call leaking into the second would show."""
     first = _workload(kv, cuda, seed=21, lens=[5000, 64, 1, 3000])
     second = _workload(kv, cuda, seed=22, lens=[200, 7777, 0])
     for w in (first, second):
         want, want_lse = _run(kv, w, noalloc=False)
         got, got_lse = _run(kv, w, noalloc=True)
-        err = np.abs(got - want)
         assert np.all(np.isfinite(got))
-        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS
-        fin = np.isfinite(want_lse)
-        assert np.array_equal(np.isfinite(got_lse), fin)
-        assert np.abs(got_lse[fin] - want_lse[fin]).max() <= LSE_ABS
+        assert np.array_equal(got, want)
+        assert np.array_equal(got_lse, want_lse)
 
 
 def test_noalloc_rejects_work_beyond_its_scratch(kv, cuda):

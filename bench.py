@@ -518,8 +518,10 @@ def per_config(result, peak):
         "long_context": dict(pick("decode (long context)"),
                              in_step={"ms": result["roofline"]["launch_ms"],
                                       "frac_of_peak": result["roofline"]["frac"]}),
-        "extend_step": pick("extend step: K+V prefix gather -> FP8 + K+V chunk write "
-                            "(4 launches back to back)"),
+        "extend_step": dict(pick("extend step: K+V prefix gather -> FP8 + K+V chunk write "
+                                 "(one launch)"),
+                            four_launches=pick("extend step: K+V prefix gather -> FP8 + K+V "
+                                               "chunk write (4 launches back to back)")),
         "decode_head_dim_64": pick("decode (32x8192, GQA 4, head_dim 64)"),
         "decode_head_dim_256": pick("decode (32x8192, GQA 4, head_dim 256)"),
     }
@@ -652,17 +654,28 @@ def extend_step_table(path, flush, peak, res):
         for d in tens:
             kv.nvfp4_kv_extend_write(d["lay"], d["chunk"], d["g"], d["pd"], d["ps"], d["ws"],
                                      dst_page_ids=d["chunk_dst"], ws_page_ids=ws_chunk)
+    parts = [dict(layout=d["lay"], global_scale=d["g"], data=d["pd"], scales=d["ps"],
+                  prefix_page_ids=d["ids"], ws=d["ws"], ws_prefix_ids=ws_prefix,
+                  ws_chunk_ids=ws_chunk, chunk=d["chunk"], chunk_dst_ids=d["chunk_dst"])
+             for d in tens]
+
+    def fused():
+        kv.nvfp4_kv_extend_step(parts)
     vals = H * T * D
     gather = 2 * ex.prefix_pages * vals * 1.5625 + 2 * ex.prefix_pages * 4
     write = 2 * ex.chunk_pages * vals * (2 + 0.5625 + 1) + 2 * ex.chunk_pages * 4
-    ms = time_kernel(step, flush)
-    gbs = (gather + write) / (ms * 1e-3) / GB
-    res["extend step: K+V prefix gather -> FP8 + K+V chunk write (4 launches back to back)"] = {
-        "ms": round(ms, 4), "bytes": int(gather + write), "GB_s": round(gbs, 1),
-        "frac_of_peak": round(gbs / peak, 4), "launches": 4,
-        "bytes_gather": int(gather), "bytes_chunk_write": int(write),
-        "tokens_per_s": round(ex.B * (ex.prefix + ex.chunk) / (ms * 1e-3), 1)}
-    del tens
+    for name, fn, launches in (
+            ("extend step: K+V prefix gather -> FP8 + K+V chunk write (4 launches back to back)",
+             step, 4),
+            ("extend step: K+V prefix gather -> FP8 + K+V chunk write (one launch)", fused, 1)):
+        ms = time_kernel(fn, flush)
+        gbs = (gather + write) / (ms * 1e-3) / GB
+        res[name] = {
+            "ms": round(ms, 4), "bytes": int(gather + write), "GB_s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "launches": launches,
+            "bytes_gather": int(gather), "bytes_chunk_write": int(write),
+            "tokens_per_s": round(ex.B * (ex.prefix + ex.chunk) / (ms * 1e-3), 1)}
+    del tens, parts
 
 
 def cold_table(path, flush, timer, pages=2048):

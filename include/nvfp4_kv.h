@@ -213,6 +213,46 @@ nvfp4kv_status nvfp4_kv_extend_write(const nvfp4kv_layout* layout, nvfp4kv_dtype
                                      int32_t num_pages, int32_t* status, nvfp4kv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * The extend step in one launch (LMSYS page, "Path 2: Chunked prefill / Extend": the cached
+ * prefix of the sequences is dequantized into the FP8 workspace that the extend attention reads,
+ * and the current chunk's K/V go into the NVFP4 cache and into that workspace). For each of
+ * num_tensors (1 or 2: K and V) tensors this does exactly what these two calls do, byte for byte:
+ *   nvfp4_kv_dequantize_pages(prefix pages -> FP8 workspace slots, dst_scale = ws_scale)
+ *   nvfp4_kv_extend_write(chunk pages -> NVFP4 pool pages + FP8 workspace slots, ws_scale)
+ * but the work items of every tensor's gather and chunk write form one grid: one launch, one
+ * ramp and one tail instead of four. Validation and errors are those of the two calls (a pool,
+ * id list or pointer the calls would reject gives the same status; nothing is launched); every
+ * tensor's chunk has the same dtype (else NVFP4KV_ERR_UNSUPPORTED). The chunk's NVFP4 destination
+ * pages must not be among the prefix pages the same call reads, and the workspace slots of the
+ * prefix and of the chunk must be distinct (the work items run in no fixed order).
+ * ------------------------------------------------------------------------------------------ */
+typedef struct nvfp4kv_extend_tensor {
+    nvfp4kv_layout layout;           /* geometry and packing of this tensor's NVFP4 pool */
+    const float* global_scale;       /* device scalar g of the tensor */
+    uint8_t* data;                   /* NVFP4 pool codes  [pool_pages][H][T][D/2] (packing) */
+    uint8_t* scales;                 /* NVFP4 pool scales [pool_pages][H][T][D/16] */
+    int32_t pool_pages;
+    const int32_t* prefix_page_ids;  /* [prefix_pages] pool pages of the cached prefix
+                                        (NULL = 0 .. prefix_pages-1) */
+    int32_t prefix_pages;
+    uint8_t* ws;                     /* FP8 E4M3 workspace [ws_pages][H][T][D], 16-byte aligned */
+    int32_t ws_pages;
+    const int32_t* ws_prefix_ids;    /* [prefix_pages] workspace slot of each prefix page */
+    const int32_t* ws_chunk_ids;     /* [chunk_pages] workspace slot of each chunk page */
+    const float* ws_scale;           /* device scalar: FP8 value = x / ws_scale (NULL = 1) */
+    int32_t chunk_dtype;             /* nvfp4kv_dtype of the chunk: BF16, FP16 or FP8 E4M3 */
+    const void* chunk;               /* chunk pages [chunk_pool_pages][H][T][D] */
+    int32_t chunk_pool_pages;
+    const int32_t* chunk_page_ids;   /* [chunk_pages] chunk pages to write (NULL = 0 .. n-1) */
+    const float* chunk_src_scale;    /* FP8 chunk: x = fp32(e4m3 * chunk_src_scale) (NULL = 1) */
+    const int32_t* chunk_dst_ids;    /* [chunk_pages] pool page of each chunk page */
+    int32_t chunk_pages;
+} nvfp4kv_extend_tensor;
+
+nvfp4kv_status nvfp4_kv_extend_step(const nvfp4kv_extend_tensor* tensors, int32_t num_tensors,
+                                    int32_t* status, nvfp4kv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Paged GQA decode attention reading NVFP4 K/V directly from the cache (LMSYS page, "Path 3:
  * Decode" and "NVFP4 KV Decode Attention Kernel Implementation", Figure 3: BF16 queries, packed
  * K/V tiles and their E4M3 block scales staged in shared memory, e2m1x2 conversion in

@@ -25,6 +25,7 @@ __all__ = [
     "STATUS_TIMEOUT", "NVFP4KVError", "load", "lib_path", "version",
     "nvfp4_kv_global_scale_workspace_size", "nvfp4_kv_compute_global_scale",
     "nvfp4_kv_quantize_pages", "nvfp4_kv_dequantize_pages", "nvfp4_kv_extend_write",
+    "ExtendTensor", "nvfp4_kv_extend_step",
     "nvfp4_paged_decode_workspace_size", "nvfp4_paged_decode_attention", "nvfp4_kv_round_f32",
     "nvfp4_paged_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES",
     "ColdBlockLayout", "ColdRope", "ROPE_QUANTIZE", "ROPE_SKIP", "ROPE_2FP4",
@@ -79,6 +80,19 @@ class ColdBlockLayout(ctypes.Structure):
                                               self._fields_) + ")"
 
 
+class ExtendTensor(ctypes.Structure):
+    """One tensor (K or V) of an extend step (``nvfp4kv_extend_tensor``)."""
+    _fields_ = [("layout", Layout), ("global_scale", ctypes.c_void_p), ("data", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p), ("pool_pages", ctypes.c_int32),
+                ("prefix_page_ids", ctypes.c_void_p), ("prefix_pages", ctypes.c_int32),
+                ("ws", ctypes.c_void_p), ("ws_pages", ctypes.c_int32),
+                ("ws_prefix_ids", ctypes.c_void_p), ("ws_chunk_ids", ctypes.c_void_p),
+                ("ws_scale", ctypes.c_void_p), ("chunk_dtype", ctypes.c_int32),
+                ("chunk", ctypes.c_void_p), ("chunk_pool_pages", ctypes.c_int32),
+                ("chunk_page_ids", ctypes.c_void_p), ("chunk_src_scale", ctypes.c_void_p),
+                ("chunk_dst_ids", ctypes.c_void_p), ("chunk_pages", ctypes.c_int32)]
+
+
 class NVFP4KVError(RuntimeError):
     def __init__(self, fn: str, code: int, msg: str):
         super().__init__(f"{fn}: {msg} (status {code})")
@@ -117,6 +131,7 @@ def load():
                                             P, I32, P, P]),
             "nvfp4_kv_dequantize_pages": (I32, [LP, P, P, I32, P, P, I32, P, I32, P, P, I32, P,
                                                 P]),
+            "nvfp4_kv_extend_step": (I32, [ctypes.POINTER(ExtendTensor), I32, P, P]),
             "nvfp4_paged_decode_workspace_size": (SZ, [LP, I32, I32, I32, I32]),
             "nvfp4_paged_decode_attention": (I32, [LP, I32, I32, P, P, P, P, P, P, P, I32, P,
                                                    I32, P, F, I32, P, SZ, P, P, P, P]),
@@ -266,6 +281,46 @@ def nvfp4_kv_extend_write(layout: Layout, src: torch.Tensor, global_scale: torch
             _ptr(dst_scales), dst_data.shape[0], _ids(dst_page_ids), _ptr(ws_fp8), ws_fp8.shape[0],
             _ids(ws_page_ids), _ptr(ws_scale), int(num_pages), _ptr(status), s)
     _check("nvfp4_kv_extend_write", code)
+
+
+def nvfp4_kv_extend_step(parts, *, status=None, stream=None):
+    """The extend step of one or two tensors (K, V) in one launch. Each part is a dict with
+    layout, global_scale, data, scales (the NVFP4 pool), prefix_page_ids, ws (FP8 workspace
+    [pages, H, T, D] uint8), ws_prefix_ids, ws_chunk_ids, chunk (chunk pages), chunk_dst_ids,
+    and optionally ws_scale, chunk_page_ids, chunk_src_scale, chunk_dtype. Equals
+    nvfp4_kv_dequantize_pages (prefix -> FP8 workspace) plus nvfp4_kv_extend_write (chunk) for
+    every part, byte for byte."""
+    lib = load()
+    arr = (ExtendTensor * len(parts))()
+    tensors = []
+    for x, d in zip(arr, parts):
+        chunk = d["chunk"]
+        x.layout = d["layout"]
+        x.global_scale = _ptr(d["global_scale"])
+        x.data, x.scales = _ptr(d["data"]), _ptr(d["scales"])
+        x.pool_pages = d["data"].shape[0]
+        x.prefix_page_ids = _ids(d.get("prefix_page_ids"))
+        x.prefix_pages = (d["prefix_page_ids"].numel() if d.get("prefix_page_ids") is not None
+                          else int(d.get("prefix_pages", 0)))
+        x.ws, x.ws_pages = _ptr(d["ws"]), d["ws"].shape[0]
+        x.ws_prefix_ids = _ids(d.get("ws_prefix_ids"))
+        x.ws_chunk_ids = _ids(d.get("ws_chunk_ids"))
+        x.ws_scale = _ptr(d.get("ws_scale"))
+        x.chunk_dtype = _dtype_code(chunk, d.get("chunk_dtype"))
+        x.chunk, x.chunk_pool_pages = _ptr(chunk), chunk.shape[0]
+        x.chunk_page_ids = _ids(d.get("chunk_page_ids"))
+        x.chunk_src_scale = _ptr(d.get("chunk_src_scale"))
+        x.chunk_dst_ids = _ids(d.get("chunk_dst_ids"))
+        x.chunk_pages = (d["chunk_dst_ids"].numel() if d.get("chunk_dst_ids") is not None
+                         else chunk.shape[0])
+        tensors += [d[k] for k in ("global_scale", "data", "scales", "ws", "chunk")
+                    if d.get(k) is not None]
+        tensors += [d[k] for k in ("prefix_page_ids", "ws_prefix_ids", "ws_chunk_ids",
+                                   "ws_scale", "chunk_page_ids", "chunk_src_scale",
+                                   "chunk_dst_ids") if d.get(k) is not None]
+    with _on_device(tensors + [status], stream) as s:
+        code = lib.nvfp4_kv_extend_step(arr, len(parts), _ptr(status), s)
+    _check("nvfp4_kv_extend_step", code)
 
 
 def nvfp4_kv_dequantize_pages(layout: Layout, src_data: torch.Tensor, src_scales: torch.Tensor,

@@ -75,107 +75,114 @@ constexpr int quantize_min_ctas() {
     return WS ? 0 : ((SRC == NVFP4KV_FP16 && PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? 3 : 4);
 }
 
+// One work item of the encode: item = (page i, chunk k of its units). g, d = fp32(6 g), the FP8
+// source scale and the workspace multiplier are the call's scalars.
+template <int SRC, bool A32, int PACK, bool WS>
+__device__ __forceinline__ void quant_item(const QuantParams& p, int64_t item, float g, float d,
+                                           float sscale, float wm) {
+    constexpr int kUnitsPerThread = (PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? kBlocksPerThread / 2
+                                                                        : kBlocksPerThread;
+    constexpr int kItemUnits = kThreads * kUnitsPerThread;
+    const int32_t i = static_cast<int32_t>(item / p.items_per_page);
+    const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
+    const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
+    const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
+    int32_t wp = 0;
+    if constexpr (WS) wp = p.ws_ids ? __ldg(p.ws_ids + i) : i;
+    if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool ||
+        (WS && (wp < 0 || wp >= p.ws_pool))) {
+        if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+        return;
+    }
+    const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
+    const int64_t dst_blk0 = static_cast<int64_t>(dp) * p.bpp;
+    uint8_t* const ws_page = WS ? p.ws + static_cast<int64_t>(wp) * p.bpp * 16 : nullptr;
+    const int32_t u_begin = k * kItemUnits + threadIdx.x;
+    if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+        U8x32 raw[kUnitsPerThread];
+#pragma unroll
+        for (int u = 0; u < kUnitsPerThread; ++u) {
+            const int32_t blk = u_begin + u * kThreads;
+            if (blk < p.units) raw[u] = load_raw<SRC, A32>(p.src, src_blk0 + blk);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnitsPerThread; ++u) {
+            const int32_t blk = u_begin + u * kThreads;
+            if (blk >= p.units) continue;
+            float x[16];
+            widen<SRC>(raw[u], sscale, x);
+            uint32_t sb;
+            float r;
+            pick_scale(x, g, d, sb, r);
+            uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w0 |= f32x2_to_e2m1x2(__fmul_rn(x[2 * j], r), __fmul_rn(x[2 * j + 1], r))
+                      << (8 * j);
+                w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r))
+                      << (8 * j);
+            }
+            st_cs(p.dst_data + (dst_blk0 + blk) * 8, make_uint2(w0, w1));
+            st_cs_u8(p.dst_scales + dst_blk0 + blk, sb);
+            if constexpr (WS)
+                st_cs(ws_page + static_cast<int64_t>(blk) * 16, fp8_block(x, wm));
+        }
+    } else {
+        U8x32 raw0[kUnitsPerThread], raw1[kUnitsPerThread];
+#pragma unroll
+        for (int u = 0; u < kUnitsPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit < p.units) {
+                const uint32_t row_pair = fast_div(unit, p.nb_magic);
+                const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
+                const int64_t blk = src_blk0 + static_cast<int64_t>(2 * row_pair) * p.nb + b;
+                raw0[u] = load_raw<SRC, A32>(p.src, blk);
+                raw1[u] = load_raw<SRC, A32>(p.src, blk + p.nb);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnitsPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit >= p.units) continue;
+            float x0[16], x1[16];
+            widen<SRC>(raw0[u], sscale, x0);
+            widen<SRC>(raw1[u], sscale, x1);
+            uint32_t s0, s1;
+            float r0, r1;
+            pick_scale(x0, g, d, s0, r0);
+            pick_scale(x1, g, d, s1, r1);
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[e >> 2] |= f32x2_to_e2m1x2(__fmul_rn(x0[e], r0), __fmul_rn(x1[e], r1))
+                             << (8 * (e & 3));
+            // unit index = (row pair, block): data at unit * 16, scales at unit * 2
+            const int64_t o = dst_blk0 / 2 + unit;
+            st_cs(p.dst_data + o * 16, make_uint4(w[0], w[1], w[2], w[3]));
+            st_cs_u16(p.dst_scales + o * 2, s0 | (s1 << 8));
+            if constexpr (WS) {
+                // the same block of tokens 2p and 2p+1 in the plain [token][dim] workspace
+                const uint32_t row_pair = fast_div(unit, p.nb_magic);
+                const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
+                const int64_t wb = static_cast<int64_t>(2 * row_pair) * p.nb + b;
+                st_cs(ws_page + wb * 16, fp8_block(x0, wm));
+                st_cs(ws_page + (wb + p.nb) * 16, fp8_block(x1, wm));
+            }
+        }
+    }
+}
+
 template <int SRC, bool A32, int PACK, bool WS = false>
 __global__ void __launch_bounds__(kThreads, quantize_min_ctas<SRC, PACK, WS>())
     quantize_pages_kernel(const QuantParams p) {
     pdl_enter();
-    constexpr int kUnitsPerThread = (PACK == NVFP4KV_PACK_TOKEN_PAIRS) ? kBlocksPerThread / 2
-                                                                        : kBlocksPerThread;
-    constexpr int kItemUnits = kThreads * kUnitsPerThread;
     const float g = __ldg(p.g);
     const float d = __fmul_rn(6.0f, g);
     const float sscale = (SRC == NVFP4KV_FP8_E4M3 && p.src_scale) ? __ldg(p.src_scale) : 1.0f;
     const float wm = (WS && p.ws_scale) ? __frcp_rn(__ldg(p.ws_scale)) : 1.0f;
     const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
-    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int32_t i = static_cast<int32_t>(item / p.items_per_page);
-        const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
-        const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
-        const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
-        int32_t wp = 0;
-        if constexpr (WS) wp = p.ws_ids ? __ldg(p.ws_ids + i) : i;
-        if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool ||
-            (WS && (wp < 0 || wp >= p.ws_pool))) {
-            if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
-            continue;
-        }
-        const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
-        const int64_t dst_blk0 = static_cast<int64_t>(dp) * p.bpp;
-        uint8_t* const ws_page = WS ? p.ws + static_cast<int64_t>(wp) * p.bpp * 16 : nullptr;
-        const int32_t u_begin = k * kItemUnits + threadIdx.x;
-        if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
-            U8x32 raw[kUnitsPerThread];
-#pragma unroll
-            for (int u = 0; u < kUnitsPerThread; ++u) {
-                const int32_t blk = u_begin + u * kThreads;
-                if (blk < p.units) raw[u] = load_raw<SRC, A32>(p.src, src_blk0 + blk);
-            }
-#pragma unroll
-            for (int u = 0; u < kUnitsPerThread; ++u) {
-                const int32_t blk = u_begin + u * kThreads;
-                if (blk >= p.units) continue;
-                float x[16];
-                widen<SRC>(raw[u], sscale, x);
-                uint32_t sb;
-                float r;
-                pick_scale(x, g, d, sb, r);
-                uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    w0 |= f32x2_to_e2m1x2(__fmul_rn(x[2 * j], r), __fmul_rn(x[2 * j + 1], r))
-                          << (8 * j);
-                    w1 |= f32x2_to_e2m1x2(__fmul_rn(x[8 + 2 * j], r), __fmul_rn(x[9 + 2 * j], r))
-                          << (8 * j);
-                }
-                st_cs(p.dst_data + (dst_blk0 + blk) * 8, make_uint2(w0, w1));
-                st_cs_u8(p.dst_scales + dst_blk0 + blk, sb);
-                if constexpr (WS)
-                    st_cs(ws_page + static_cast<int64_t>(blk) * 16, fp8_block(x, wm));
-            }
-        } else {
-            U8x32 raw0[kUnitsPerThread], raw1[kUnitsPerThread];
-#pragma unroll
-            for (int u = 0; u < kUnitsPerThread; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit < p.units) {
-                    const uint32_t row_pair = fast_div(unit, p.nb_magic);
-                    const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
-                    const int64_t blk = src_blk0 + static_cast<int64_t>(2 * row_pair) * p.nb + b;
-                    raw0[u] = load_raw<SRC, A32>(p.src, blk);
-                    raw1[u] = load_raw<SRC, A32>(p.src, blk + p.nb);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kUnitsPerThread; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit >= p.units) continue;
-                float x0[16], x1[16];
-                widen<SRC>(raw0[u], sscale, x0);
-                widen<SRC>(raw1[u], sscale, x1);
-                uint32_t s0, s1;
-                float r0, r1;
-                pick_scale(x0, g, d, s0, r0);
-                pick_scale(x1, g, d, s1, r1);
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e >> 2] |= f32x2_to_e2m1x2(__fmul_rn(x0[e], r0), __fmul_rn(x1[e], r1))
-                                 << (8 * (e & 3));
-                // unit index = (row pair, block): data at unit * 16, scales at unit * 2
-                const int64_t o = dst_blk0 / 2 + unit;
-                st_cs(p.dst_data + o * 16, make_uint4(w[0], w[1], w[2], w[3]));
-                st_cs_u16(p.dst_scales + o * 2, s0 | (s1 << 8));
-                if constexpr (WS) {
-                    // the same block of tokens 2p and 2p+1 in the plain [token][dim] workspace
-                    const uint32_t row_pair = fast_div(unit, p.nb_magic);
-                    const int32_t b = unit - static_cast<int32_t>(row_pair) * p.nb;
-                    const int64_t wb = static_cast<int64_t>(2 * row_pair) * p.nb + b;
-                    st_cs(ws_page + wb * 16, fp8_block(x0, wm));
-                    st_cs(ws_page + (wb + p.nb) * 16, fp8_block(x1, wm));
-                }
-            }
-        }
-    }
+    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x)
+        quant_item<SRC, A32, PACK, WS>(p, item, g, d, sscale, wm);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -228,162 +235,168 @@ __device__ __forceinline__ void store8(void* dst, int64_t elem, const float (&y)
     }
 }
 
+// One work item of the decode: item = (page i, chunk k of its units); mult is g, or
+// fp32(g / dst_scale) for FP8 output.
+template <int DST, int PACK>
+__device__ __forceinline__ void dequant_item(const DequantParams& p, int64_t item, float mult) {
+    constexpr int kU = kBlocksPerThread;  // units per thread per item
+    const int32_t i = static_cast<int32_t>(item / p.items_per_page);
+    const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
+    const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
+    const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
+    if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool) {
+        if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
+        return;
+    }
+    const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
+    const int64_t dst_elem0 = static_cast<int64_t>(dp) * p.bpp * 16;
+    const int32_t u_begin = k * kThreads * kU + threadIdx.x;
+    if constexpr (DST == NVFP4KV_FP8_E4M3) {
+        // one 16-byte load of codes (dim pairs: 8 bytes) per unit, 16-byte FP8 stores
+        uint4 code[kU];
+        uint32_t sc[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit < p.units) {
+                if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+                    const uint2 c2 = ld_stream_8B(p.src_data + (src_blk0 + unit) * 8);
+                    code[u] = make_uint4(c2.x, c2.y, 0u, 0u);
+                    sc[u] = ld_stream_1B(p.src_scales + src_blk0 + unit) * 0x0101u;
+                } else {
+                    code[u] = ld_stream_16B(p.src_data + src_blk0 * 8 + static_cast<int64_t>(unit) * 16);
+                    sc[u] = *reinterpret_cast<const uint16_t*>(p.src_scales + src_blk0 +
+                                                               static_cast<int64_t>(unit) * 2);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit >= p.units) continue;
+            if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+                // 16 values of one token: (s, s) times each code pair
+                const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
+                uint32_t v[8];
+                e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
+                e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t a = hmul2_u32(v[2 * j], s2), b = hmul2_u32(v[2 * j + 1], s2);
+                    o[j] = f32x2_to_e4m3x2(__fmul_rn(f16_lo(a), mult), __fmul_rn(f16_hi(a), mult)) |
+                           (f32x2_to_e4m3x2(__fmul_rn(f16_lo(b), mult), __fmul_rn(f16_hi(b), mult))
+                            << 16);
+                }
+                st_cs(static_cast<uint8_t*>(p.dst) + dst_elem0 + static_cast<int64_t>(unit) * 16,
+                      make_uint4(o[0], o[1], o[2], o[3]));
+            } else {
+                const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
+                // 16 head dims of tokens 2rp (low nibbles) and 2rp+1 (high nibbles)
+                const uint32_t rp = fast_div(unit, p.nb_magic);
+                const int32_t blk = unit - static_cast<int32_t>(rp) * p.nb;
+                const uint32_t words[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
+                uint32_t o0[4], o1[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[4];
+                    e2m1x8_to_f16x2x4(words[q], v);  // v[j]: dim 4q + j of (token 2rp, 2rp+1)
+                    const uint32_t a0 = hmul2_u32(v[0], s2), a1 = hmul2_u32(v[1], s2);
+                    const uint32_t a2 = hmul2_u32(v[2], s2), a3 = hmul2_u32(v[3], s2);
+                    o0[q] = f32x2_to_e4m3x2(__fmul_rn(f16_lo(a0), mult), __fmul_rn(f16_lo(a1), mult)) |
+                            (f32x2_to_e4m3x2(__fmul_rn(f16_lo(a2), mult), __fmul_rn(f16_lo(a3), mult))
+                             << 16);
+                    o1[q] = f32x2_to_e4m3x2(__fmul_rn(f16_hi(a0), mult), __fmul_rn(f16_hi(a1), mult)) |
+                            (f32x2_to_e4m3x2(__fmul_rn(f16_hi(a2), mult), __fmul_rn(f16_hi(a3), mult))
+                             << 16);
+                }
+                const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * rp) * p.nb * 16 + blk * 16;
+                uint8_t* d8 = static_cast<uint8_t*>(p.dst);
+                st_cs(d8 + e0, make_uint4(o0[0], o0[1], o0[2], o0[3]));
+                st_cs(d8 + e0 + p.nb * 16, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+            }
+        }
+    } else if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
+        // a unit is one block: 8 code bytes and its scale in, 16 outputs (32 bytes) out
+        uint2 code[kBlocksPerThread];
+        uint32_t sbyte[kBlocksPerThread];
+#pragma unroll
+        for (int u = 0; u < kBlocksPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit < p.units) {
+                code[u] = ld_stream_8B(p.src_data + (src_blk0 + unit) * 8);
+                sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + unit);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBlocksPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit >= p.units) continue;
+            const uint32_t s2 = e4m3x2_to_f16x2(sbyte[u] * 0x0101u);  // (s, s)
+            uint32_t v[8];
+            e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
+            e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t v2 = hmul2_u32(v[j], s2);
+                const float lo = __fmul_rn(f16_lo(v2), mult), hi = __fmul_rn(f16_hi(v2), mult);
+                o[j] = (DST == NVFP4KV_BF16) ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+            }
+            st_global_32B(static_cast<uint8_t*>(p.dst) + (dst_elem0 + static_cast<int64_t>(unit) * 16) * 2, o);
+        }
+    } else {
+        uint2 code[kBlocksPerThread];
+        uint32_t spair[kBlocksPerThread];
+#pragma unroll
+        for (int u = 0; u < kBlocksPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit < p.units) {
+                code[u] = *reinterpret_cast<const uint2*>(p.src_data + src_blk0 * 8 +
+                                                          static_cast<int64_t>(unit) * 8);
+                // the unit's block: (row pair, block) = unit / 2; its two scales side by side
+                spair[u] = *reinterpret_cast<const uint16_t*>(p.src_scales + src_blk0 +
+                                                              (unit >> 1) * 2);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBlocksPerThread; ++u) {
+            const int32_t unit = u_begin + u * kThreads;
+            if (unit >= p.units) continue;
+            const uint32_t s2 = e4m3x2_to_f16x2(spair[u]);  // (s token 2p, s token 2p+1)
+            const uint32_t row_pair = fast_div(unit, p.nb2_magic);
+            const int32_t rem = unit - static_cast<int32_t>(row_pair) * 2 * p.nb;  // 8-dim slot
+            float y0[8], y1[8];
+            const uint32_t words[2] = {code[u].x, code[u].y};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t v[4];
+                e2m1x8_to_f16x2x4(words[q], v);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t v2 = hmul2_u32(v[j], s2);  // (token 2p, token 2p+1)
+                    y0[4 * q + j] = __fmul_rn(f16_lo(v2), mult);
+                    y1[4 * q + j] = __fmul_rn(f16_hi(v2), mult);
+                }
+            }
+            const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * row_pair) * p.nb * 16 +
+                               rem * 8;
+            store8<DST>(p.dst, e0, y0);
+            store8<DST>(p.dst, e0 + p.nb * 16, y1);
+        }
+    }
+}
+
 template <int DST, int PACK>
 __global__ void __launch_bounds__(kThreads) dequantize_pages_kernel(const DequantParams p) {
     pdl_enter();
-    constexpr int kU = kBlocksPerThread;  // units per thread per item
     const float g = __ldg(p.g);
     const float mult = (DST == NVFP4KV_FP8_E4M3)
                            ? (p.dst_scale ? __fdiv_rn(g, __ldg(p.dst_scale)) : g)
                            : g;
     const int64_t total_items = static_cast<int64_t>(p.num_pages) * p.items_per_page;
-    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const int32_t i = static_cast<int32_t>(item / p.items_per_page);
-        const int32_t k = static_cast<int32_t>(item - static_cast<int64_t>(i) * p.items_per_page);
-        const int32_t sp = p.src_ids ? __ldg(p.src_ids + i) : i;
-        const int32_t dp = p.dst_ids ? __ldg(p.dst_ids + i) : i;
-        if (sp < 0 || sp >= p.src_pool || dp < 0 || dp >= p.dst_pool) {
-            if (threadIdx.x == 0) flag_status(p.status, NVFP4KV_STATUS_PAGE_OOB);
-            continue;
-        }
-        const int64_t src_blk0 = static_cast<int64_t>(sp) * p.bpp;
-        const int64_t dst_elem0 = static_cast<int64_t>(dp) * p.bpp * 16;
-        const int32_t u_begin = k * kThreads * kU + threadIdx.x;
-        if constexpr (DST == NVFP4KV_FP8_E4M3) {
-            // one 16-byte load of codes (dim pairs: 8 bytes) per unit, 16-byte FP8 stores
-            uint4 code[kU];
-            uint32_t sc[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit < p.units) {
-                    if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
-                        const uint2 c2 = ld_stream_8B(p.src_data + (src_blk0 + unit) * 8);
-                        code[u] = make_uint4(c2.x, c2.y, 0u, 0u);
-                        sc[u] = ld_stream_1B(p.src_scales + src_blk0 + unit) * 0x0101u;
-                    } else {
-                        code[u] = ld_stream_16B(p.src_data + src_blk0 * 8 + static_cast<int64_t>(unit) * 16);
-                        sc[u] = *reinterpret_cast<const uint16_t*>(p.src_scales + src_blk0 +
-                                                                   static_cast<int64_t>(unit) * 2);
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit >= p.units) continue;
-                if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
-                    // 16 values of one token: (s, s) times each code pair
-                    const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
-                    uint32_t v[8];
-                    e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
-                    e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
-                    uint32_t o[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t a = hmul2_u32(v[2 * j], s2), b = hmul2_u32(v[2 * j + 1], s2);
-                        o[j] = f32x2_to_e4m3x2(__fmul_rn(f16_lo(a), mult), __fmul_rn(f16_hi(a), mult)) |
-                               (f32x2_to_e4m3x2(__fmul_rn(f16_lo(b), mult), __fmul_rn(f16_hi(b), mult))
-                                << 16);
-                    }
-                    st_cs(static_cast<uint8_t*>(p.dst) + dst_elem0 + static_cast<int64_t>(unit) * 16,
-                          make_uint4(o[0], o[1], o[2], o[3]));
-                } else {
-                    const uint32_t s2 = e4m3x2_to_f16x2(sc[u]);
-                    // 16 head dims of tokens 2rp (low nibbles) and 2rp+1 (high nibbles)
-                    const uint32_t rp = fast_div(unit, p.nb_magic);
-                    const int32_t blk = unit - static_cast<int32_t>(rp) * p.nb;
-                    const uint32_t words[4] = {code[u].x, code[u].y, code[u].z, code[u].w};
-                    uint32_t o0[4], o1[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t v[4];
-                        e2m1x8_to_f16x2x4(words[q], v);  // v[j]: dim 4q + j of (token 2rp, 2rp+1)
-                        const uint32_t a0 = hmul2_u32(v[0], s2), a1 = hmul2_u32(v[1], s2);
-                        const uint32_t a2 = hmul2_u32(v[2], s2), a3 = hmul2_u32(v[3], s2);
-                        o0[q] = f32x2_to_e4m3x2(__fmul_rn(f16_lo(a0), mult), __fmul_rn(f16_lo(a1), mult)) |
-                                (f32x2_to_e4m3x2(__fmul_rn(f16_lo(a2), mult), __fmul_rn(f16_lo(a3), mult))
-                                 << 16);
-                        o1[q] = f32x2_to_e4m3x2(__fmul_rn(f16_hi(a0), mult), __fmul_rn(f16_hi(a1), mult)) |
-                                (f32x2_to_e4m3x2(__fmul_rn(f16_hi(a2), mult), __fmul_rn(f16_hi(a3), mult))
-                                 << 16);
-                    }
-                    const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * rp) * p.nb * 16 + blk * 16;
-                    uint8_t* d8 = static_cast<uint8_t*>(p.dst);
-                    st_cs(d8 + e0, make_uint4(o0[0], o0[1], o0[2], o0[3]));
-                    st_cs(d8 + e0 + p.nb * 16, make_uint4(o1[0], o1[1], o1[2], o1[3]));
-                }
-            }
-        } else if constexpr (PACK == NVFP4KV_PACK_DIM_PAIRS) {
-            // a unit is one block: 8 code bytes and its scale in, 16 outputs (32 bytes) out
-            uint2 code[kBlocksPerThread];
-            uint32_t sbyte[kBlocksPerThread];
-#pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit < p.units) {
-                    code[u] = ld_stream_8B(p.src_data + (src_blk0 + unit) * 8);
-                    sbyte[u] = ld_stream_1B(p.src_scales + src_blk0 + unit);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit >= p.units) continue;
-                const uint32_t s2 = e4m3x2_to_f16x2(sbyte[u] * 0x0101u);  // (s, s)
-                uint32_t v[8];
-                e2m1x8_to_f16x2x4(code[u].x, *reinterpret_cast<uint32_t(*)[4]>(v));
-                e2m1x8_to_f16x2x4(code[u].y, *reinterpret_cast<uint32_t(*)[4]>(v + 4));
-                uint32_t o[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t v2 = hmul2_u32(v[j], s2);
-                    const float lo = __fmul_rn(f16_lo(v2), mult), hi = __fmul_rn(f16_hi(v2), mult);
-                    o[j] = (DST == NVFP4KV_BF16) ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
-                }
-                st_global_32B(static_cast<uint8_t*>(p.dst) + (dst_elem0 + static_cast<int64_t>(unit) * 16) * 2, o);
-            }
-        } else {
-            uint2 code[kBlocksPerThread];
-            uint32_t spair[kBlocksPerThread];
-#pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit < p.units) {
-                    code[u] = *reinterpret_cast<const uint2*>(p.src_data + src_blk0 * 8 +
-                                                              static_cast<int64_t>(unit) * 8);
-                    // the unit's block: (row pair, block) = unit / 2; its two scales side by side
-                    spair[u] = *reinterpret_cast<const uint16_t*>(p.src_scales + src_blk0 +
-                                                                  (unit >> 1) * 2);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kBlocksPerThread; ++u) {
-                const int32_t unit = u_begin + u * kThreads;
-                if (unit >= p.units) continue;
-                const uint32_t s2 = e4m3x2_to_f16x2(spair[u]);  // (s token 2p, s token 2p+1)
-                const uint32_t row_pair = fast_div(unit, p.nb2_magic);
-                const int32_t rem = unit - static_cast<int32_t>(row_pair) * 2 * p.nb;  // 8-dim slot
-                float y0[8], y1[8];
-                const uint32_t words[2] = {code[u].x, code[u].y};
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t v[4];
-                    e2m1x8_to_f16x2x4(words[q], v);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t v2 = hmul2_u32(v[j], s2);  // (token 2p, token 2p+1)
-                        y0[4 * q + j] = __fmul_rn(f16_lo(v2), mult);
-                        y1[4 * q + j] = __fmul_rn(f16_hi(v2), mult);
-                    }
-                }
-                const int64_t e0 = dst_elem0 + static_cast<int64_t>(2 * row_pair) * p.nb * 16 +
-                                   rem * 8;
-                store8<DST>(p.dst, e0, y0);
-                store8<DST>(p.dst, e0 + p.nb * 16, y1);
-            }
-        }
-    }
+    for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x)
+        dequant_item<DST, PACK>(p, item, mult);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -537,9 +550,194 @@ __global__ void round_f32_kernel(const float* x, size_t n, int32_t target, uint8
     }
 }
 
+// ------------------------------------------------------------------------------------------
+// Extend step: the cached prefix of K and V gathered into the FP8 workspace and the current chunk
+// of K and V written as NVFP4 pages and as its FP8 workspace copy, all in one grid. The grid is
+// cut into four consecutive CTA ranges, one per job (gather K, gather V, write K, write V), sized
+// in proportion to the job's work items; a CTA takes the items of its own job with the job's
+// CTA count as stride, as in the separate calls. One launch, one ramp and one tail instead of
+// four; a CTA holds only its own job's parameters.
+// ------------------------------------------------------------------------------------------
+struct ExtendStepParams {
+    DequantParams gather[2];   // per tensor: NVFP4 prefix pages -> FP8 workspace slots
+    QuantParams write[2];      // per tensor: chunk pages -> NVFP4 pages + FP8 workspace slots
+    int32_t packing[2];        // per tensor: NVFP4 pool packing
+    int32_t cta_end[4];        // cumulative CTA counts of the jobs
+};
+
+template <int SRC, bool A32, int PACK>
+__device__ __forceinline__ void extend_write_job(const QuantParams& q, int c0, int nc) {
+    const float g = __ldg(q.g);
+    const float d = __fmul_rn(6.0f, g);
+    const float sscale = (SRC == NVFP4KV_FP8_E4M3 && q.src_scale) ? __ldg(q.src_scale) : 1.0f;
+    const float wm = q.ws_scale ? __frcp_rn(__ldg(q.ws_scale)) : 1.0f;
+    const int64_t total = static_cast<int64_t>(q.num_pages) * q.items_per_page;
+    for (int64_t item = blockIdx.x - c0; item < total; item += nc)
+        quant_item<SRC, A32, PACK, true>(q, item, g, d, sscale, wm);
+}
+
+template <int PACK>
+__device__ __forceinline__ void gather_job(const DequantParams& q, int c0, int nc) {
+    const float g = __ldg(q.g);
+    const float mult = q.dst_scale ? __fdiv_rn(g, __ldg(q.dst_scale)) : g;
+    const int64_t total = static_cast<int64_t>(q.num_pages) * q.items_per_page;
+    for (int64_t item = blockIdx.x - c0; item < total; item += nc)
+        dequant_item<NVFP4KV_FP8_E4M3, PACK>(q, item, mult);
+}
+
+// Register budget of 4 CTAs per SM (64 registers): the gather items stream best with many warps,
+// and the encode items spill only a few bytes at that budget. Measured on the extend workload
+// (16 x 4096-token prefix + 16 x 512-token chunk, K and V, 269 MB): 2 CTAs per SM (the
+// compiler's 108 registers) 62.5 us, 3 per SM 50.4 us, 4 per SM 45.1 us; 5 and 6 spill
+// 650-1250 bytes per thread.
+template <int SRC, bool A32>
+__global__ void __launch_bounds__(kThreads, 4) extend_step_kernel(const ExtendStepParams p) {
+    pdl_enter();
+    const int c = blockIdx.x;
+    if (c < p.cta_end[0]) {
+        if (p.packing[0] == NVFP4KV_PACK_TOKEN_PAIRS)
+            gather_job<NVFP4KV_PACK_TOKEN_PAIRS>(p.gather[0], 0, p.cta_end[0]);
+        else
+            gather_job<NVFP4KV_PACK_DIM_PAIRS>(p.gather[0], 0, p.cta_end[0]);
+    } else if (c < p.cta_end[1]) {
+        const int c0 = p.cta_end[0], nc = p.cta_end[1] - c0;
+        if (p.packing[1] == NVFP4KV_PACK_TOKEN_PAIRS)
+            gather_job<NVFP4KV_PACK_TOKEN_PAIRS>(p.gather[1], c0, nc);
+        else
+            gather_job<NVFP4KV_PACK_DIM_PAIRS>(p.gather[1], c0, nc);
+    } else if (c < p.cta_end[2]) {
+        const int c0 = p.cta_end[1], nc = p.cta_end[2] - c0;
+        if (p.packing[0] == NVFP4KV_PACK_TOKEN_PAIRS)
+            extend_write_job<SRC, A32, NVFP4KV_PACK_TOKEN_PAIRS>(p.write[0], c0, nc);
+        else
+            extend_write_job<SRC, A32, NVFP4KV_PACK_DIM_PAIRS>(p.write[0], c0, nc);
+    } else {
+        const int c0 = p.cta_end[2], nc = p.cta_end[3] - c0;
+        if (p.packing[1] == NVFP4KV_PACK_TOKEN_PAIRS)
+            extend_write_job<SRC, A32, NVFP4KV_PACK_TOKEN_PAIRS>(p.write[1], c0, nc);
+        else
+            extend_write_job<SRC, A32, NVFP4KV_PACK_DIM_PAIRS>(p.write[1], c0, nc);
+    }
+}
+
 int grid_for(int64_t items, int ctas_per_sm) {
     const int64_t cap = static_cast<int64_t>(num_sms()) * ctas_per_sm;
     return static_cast<int>(items < cap ? (items < 1 ? 1 : items) : cap);
+}
+
+// Launch the extend step: one wave of resident CTAs, split over the jobs in proportion to the
+// bytes each moves (an encode item moves 2 + 9/16 + 1 bytes per value, a decode item 9/16 + 1),
+// at least one CTA for a job with items and no more CTAs than items.
+template <int SRC, bool A32>
+cudaError_t launch_extend_step(ExtendStepParams& p, const int64_t (&items)[4],
+                               const double (&bytes)[4], cudaStream_t s) {
+    const int64_t budget = static_cast<int64_t>(num_sms()) *
+                           resident_ctas<extend_step_kernel<SRC, A32>>(kThreads, 0);
+    double total = 0.0;
+    for (int j = 0; j < 4; ++j) total += bytes[j];
+    int acc = 0;
+    for (int j = 0; j < 4; ++j) {
+        int64_t cj = 0;
+        if (items[j] > 0) {
+            cj = static_cast<int64_t>(bytes[j] / total * static_cast<double>(budget) + 0.5);
+            cj = cj < 1 ? 1 : (cj > items[j] ? items[j] : cj);
+        }
+        acc += static_cast<int>(cj);
+        p.cta_end[j] = acc;
+    }
+    const cudaError_t e = launch_pdl(extend_step_kernel<SRC, A32>, acc, kThreads, 0, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Host-side validation and parameters of an encode job (quantize, or the NVFP4 half of an
+// extend write). Returns NVFP4KV_OK with p filled, or the error the entry point reports;
+// num_pages == 0 is OK with nothing to launch. The source dtype is checked by the caller.
+nvfp4kv_status encode_job(const nvfp4kv_layout* layout, const void* src, int32_t src_pool_pages,
+                          const int32_t* src_page_ids, const float* src_scale,
+                          const float* global_scale, uint8_t* dst_data, uint8_t* dst_scales,
+                          int32_t dst_pool_pages, const int32_t* dst_page_ids, int32_t num_pages,
+                          int32_t* status, QuantParams& p) {
+    p = QuantParams{};
+    if (num_pages == 0) return NVFP4KV_OK;
+    if (!src || !global_scale || !dst_data || !dst_scales || !aligned16(src) ||
+        !aligned16(dst_data) || !aligned16(dst_scales))
+        return NVFP4KV_ERR_INVALID_ARG;
+    // without id lists the pages are 0..num_pages-1 and the pools must hold them
+    if ((!src_page_ids && src_pool_pages < num_pages) ||
+        (!dst_page_ids && dst_pool_pages < num_pages))
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int pack = layout->packing;
+    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
+    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
+                          (layout->head_dim / 16);
+    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
+    p.src = src;
+    p.src_ids = src_page_ids;
+    p.src_scale = src_scale;
+    p.g = global_scale;
+    p.dst_data = dst_data;
+    p.dst_scales = dst_scales;
+    p.dst_ids = dst_page_ids;
+    p.src_pool = src_pool_pages;
+    p.dst_pool = dst_pool_pages;
+    p.num_pages = num_pages;
+    p.bpp = static_cast<int32_t>(bpp64);
+    p.nb = layout->head_dim / 16;
+    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
+    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
+    const int item_units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? kItemBlocks / 2 : kItemBlocks;
+    p.items_per_page = (p.units + item_units - 1) / item_units;
+    p.status = status;
+    return NVFP4KV_OK;
+}
+
+// Host-side validation and parameters of a decode job (to BF16 / FP16, or to FP8 E4M3).
+nvfp4kv_status decode_job(const nvfp4kv_layout* layout, const uint8_t* src_data,
+                          const uint8_t* src_scales, int32_t src_pool_pages,
+                          const int32_t* src_page_ids, const float* global_scale,
+                          nvfp4kv_dtype dst_dtype, void* dst, int32_t dst_pool_pages,
+                          const int32_t* dst_page_ids, const float* dst_scale, int32_t num_pages,
+                          int32_t* status, DequantParams& p) {
+    p = DequantParams{};
+    if (num_pages == 0) return NVFP4KV_OK;
+    if (!src_data || !src_scales || !global_scale || !dst || !aligned16(src_data) ||
+        !aligned16(src_scales) || !aligned16(dst))
+        return NVFP4KV_ERR_INVALID_ARG;
+    if ((!src_page_ids && src_pool_pages < num_pages) ||
+        (!dst_page_ids && dst_pool_pages < num_pages))
+        return NVFP4KV_ERR_INVALID_ARG;
+    const int pack = layout->packing;
+    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
+        return NVFP4KV_ERR_INVALID_ARG;
+    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
+    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
+                          (layout->head_dim / 16);
+    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
+    p.src_data = src_data;
+    p.src_scales = src_scales;
+    p.src_ids = src_page_ids;
+    p.g = global_scale;
+    p.dst_scale = dst_scale;
+    p.dst = dst;
+    p.dst_ids = dst_page_ids;
+    p.src_pool = src_pool_pages;
+    p.dst_pool = dst_pool_pages;
+    p.num_pages = num_pages;
+    p.bpp = static_cast<int32_t>(bpp64);
+    p.nb = layout->head_dim / 16;
+    p.nb2_magic = div_magic(static_cast<uint32_t>(2 * p.nb));
+    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
+    // BF16 / FP16 out: a block per dim-pair unit, 16 codes per token-pair unit (2 per block
+    // pair); FP8 out: a block per dim-pair unit, 32 codes per token-pair unit
+    if (dst_dtype == NVFP4KV_FP8_E4M3)
+        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
+    else
+        p.units = p.bpp;
+    p.items_per_page = (p.units + kItemBlocks - 1) / kItemBlocks;
+    p.status = status;
+    return NVFP4KV_OK;
 }
 
 }  // namespace
@@ -606,39 +804,12 @@ extern "C" nvfp4kv_status nvfp4_kv_quantize_pages(
     if (!layout_ok(layout) || !dtype_ok(src_dtype) || num_pages < 0 || src_pool_pages < 0 ||
         dst_pool_pages < 0)
         return NVFP4KV_ERR_INVALID_ARG;
-    if (num_pages == 0) return NVFP4KV_OK;
-    if (!src || !global_scale || !dst_data || !dst_scales || !aligned16(src) ||
-        !aligned16(dst_data) || !aligned16(dst_scales))
-        return NVFP4KV_ERR_INVALID_ARG;
-    // without id lists the pages are 0..num_pages-1 and the pools must hold them
-    if ((!src_page_ids && src_pool_pages < num_pages) ||
-        (!dst_page_ids && dst_pool_pages < num_pages))
-        return NVFP4KV_ERR_INVALID_ARG;
+    QuantParams p;
+    const nvfp4kv_status st = encode_job(layout, src, src_pool_pages, src_page_ids, src_scale,
+                                         global_scale, dst_data, dst_scales, dst_pool_pages,
+                                         dst_page_ids, num_pages, status, p);
+    if (st != NVFP4KV_OK || num_pages == 0) return st;
     const int pack = layout->packing;
-    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
-    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
-                          (layout->head_dim / 16);
-    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
-    QuantParams p{};
-    p.src = src;
-    p.src_ids = src_page_ids;
-    p.src_scale = src_scale;
-    p.g = global_scale;
-    p.dst_data = dst_data;
-    p.dst_scales = dst_scales;
-    p.dst_ids = dst_page_ids;
-    p.src_pool = src_pool_pages;
-    p.dst_pool = dst_pool_pages;
-    p.num_pages = num_pages;
-    p.bpp = static_cast<int32_t>(bpp64);
-    p.nb = layout->head_dim / 16;
-    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
-    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
-    const int item_units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? kItemBlocks / 2 : kItemBlocks;
-    p.items_per_page = (p.units + item_units - 1) / item_units;
-    p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(static_cast<int64_t>(num_pages) * p.items_per_page, 8);
     const bool a32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
@@ -679,38 +850,14 @@ extern "C" nvfp4kv_status nvfp4_kv_extend_write(
     if (src_dtype != NVFP4KV_BF16 && src_dtype != NVFP4KV_FP16 && src_dtype != NVFP4KV_FP8_E4M3)
         return NVFP4KV_ERR_UNSUPPORTED;
     if (num_pages == 0) return NVFP4KV_OK;
-    if (!src || !global_scale || !dst_data || !dst_scales || !ws_fp8 || !aligned16(src) ||
-        !aligned16(dst_data) || !aligned16(dst_scales) || !aligned16(ws_fp8))
+    if (!ws_fp8 || !aligned16(ws_fp8) || (!ws_page_ids && ws_pool_pages < num_pages))
         return NVFP4KV_ERR_INVALID_ARG;
-    if ((!src_page_ids && src_pool_pages < num_pages) ||
-        (!dst_page_ids && dst_pool_pages < num_pages) ||
-        (!ws_page_ids && ws_pool_pages < num_pages))
-        return NVFP4KV_ERR_INVALID_ARG;
+    QuantParams p;
+    const nvfp4kv_status st = encode_job(layout, src, src_pool_pages, src_page_ids, src_scale,
+                                         global_scale, dst_data, dst_scales, dst_pool_pages,
+                                         dst_page_ids, num_pages, status, p);
+    if (st != NVFP4KV_OK) return st;
     const int pack = layout->packing;
-    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
-    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
-                          (layout->head_dim / 16);
-    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
-    QuantParams p{};
-    p.src = src;
-    p.src_ids = src_page_ids;
-    p.src_scale = src_scale;
-    p.g = global_scale;
-    p.dst_data = dst_data;
-    p.dst_scales = dst_scales;
-    p.dst_ids = dst_page_ids;
-    p.src_pool = src_pool_pages;
-    p.dst_pool = dst_pool_pages;
-    p.num_pages = num_pages;
-    p.bpp = static_cast<int32_t>(bpp64);
-    p.nb = layout->head_dim / 16;
-    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
-    p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
-    const int item_units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? kItemBlocks / 2 : kItemBlocks;
-    p.items_per_page = (p.units + item_units - 1) / item_units;
-    p.status = status;
     p.ws = ws_fp8;
     p.ws_ids = ws_page_ids;
     p.ws_scale = ws_scale;
@@ -746,43 +893,13 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     if (!layout_ok(layout) || !dtype_ok(dst_dtype) || num_pages < 0 || src_pool_pages < 0 ||
         dst_pool_pages < 0)
         return NVFP4KV_ERR_INVALID_ARG;
-    if (num_pages == 0) return NVFP4KV_OK;
-    if (!src_data || !src_scales || !global_scale || !dst || !aligned16(src_data) ||
-        !aligned16(src_scales) || !aligned16(dst))
-        return NVFP4KV_ERR_INVALID_ARG;
-    if ((!src_page_ids && src_pool_pages < num_pages) ||
-        (!dst_page_ids && dst_pool_pages < num_pages))
-        return NVFP4KV_ERR_INVALID_ARG;
+    DequantParams p;
+    const nvfp4kv_status st = decode_job(layout, src_data, src_scales, src_pool_pages,
+                                         src_page_ids, global_scale, dst_dtype, dst,
+                                         dst_pool_pages, dst_page_ids, dst_scale, num_pages,
+                                         status, p);
+    if (st != NVFP4KV_OK || num_pages == 0) return st;
     const int pack = layout->packing;
-    if (pack != NVFP4KV_PACK_DIM_PAIRS && pack != NVFP4KV_PACK_TOKEN_PAIRS)
-        return NVFP4KV_ERR_INVALID_ARG;
-    if (pack == NVFP4KV_PACK_TOKEN_PAIRS && (layout->page_size & 1)) return NVFP4KV_ERR_INVALID_ARG;
-    const int64_t bpp64 = static_cast<int64_t>(layout->num_kv_heads) * layout->page_size *
-                          (layout->head_dim / 16);
-    if (bpp64 > (int64_t{1} << 29) || layout->head_dim > 16 * 1024) return NVFP4KV_ERR_UNSUPPORTED;
-    DequantParams p{};
-    p.src_data = src_data;
-    p.src_scales = src_scales;
-    p.src_ids = src_page_ids;
-    p.g = global_scale;
-    p.dst_scale = dst_scale;
-    p.dst = dst;
-    p.dst_ids = dst_page_ids;
-    p.src_pool = src_pool_pages;
-    p.dst_pool = dst_pool_pages;
-    p.num_pages = num_pages;
-    p.bpp = static_cast<int32_t>(bpp64);
-    p.nb = layout->head_dim / 16;
-    p.nb2_magic = div_magic(static_cast<uint32_t>(2 * p.nb));
-    p.nb_magic = div_magic(static_cast<uint32_t>(p.nb));
-    // BF16 / FP16 out: a block per dim-pair unit, 16 codes per token-pair unit (2 per block
-    // pair); FP8 out: a block per dim-pair unit, 32 codes per token-pair unit
-    if (dst_dtype == NVFP4KV_FP8_E4M3)
-        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp / 2 : p.bpp;
-    else
-        p.units = (pack == NVFP4KV_PACK_TOKEN_PAIRS) ? p.bpp : p.bpp;
-    p.items_per_page = (p.units + kItemBlocks - 1) / kItemBlocks;
-    p.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // up to 32 CTAs per SM, several waves of short-lived CTAs (one or two 32 KB items each): the
     // block scheduler then hands the remaining items to whichever SM frees a slot first, which
@@ -802,6 +919,74 @@ extern "C" nvfp4kv_status nvfp4_kv_dequantize_pages(
     default: NVFP4KV_DQLAUNCH(NVFP4KV_FP8_E4M3); break;
     }
 #undef NVFP4KV_DQLAUNCH
+    return launch_status();
+}
+
+extern "C" nvfp4kv_status nvfp4_kv_extend_step(const nvfp4kv_extend_tensor* tensors,
+                                               int32_t num_tensors, int32_t* status,
+                                               nvfp4kv_stream_t stream) {
+    if (!tensors || num_tensors < 1 || num_tensors > 2) return NVFP4KV_ERR_INVALID_ARG;
+    ExtendStepParams p{};
+    int src_dtype = -1;
+    bool a32 = true;
+    for (int t = 0; t < num_tensors; ++t) {
+        const nvfp4kv_extend_tensor& x = tensors[t];
+        const nvfp4kv_layout* layout = &x.layout;
+        if (!layout_ok(layout) || x.pool_pages < 0 || x.prefix_pages < 0 || x.ws_pages < 0 ||
+            x.chunk_pool_pages < 0 || x.chunk_pages < 0)
+            return NVFP4KV_ERR_INVALID_ARG;
+        if (x.chunk_pages > 0) {
+            if (x.chunk_dtype != NVFP4KV_BF16 && x.chunk_dtype != NVFP4KV_FP16 &&
+                x.chunk_dtype != NVFP4KV_FP8_E4M3)
+                return NVFP4KV_ERR_UNSUPPORTED;
+            if (src_dtype >= 0 && src_dtype != x.chunk_dtype) return NVFP4KV_ERR_UNSUPPORTED;
+            src_dtype = x.chunk_dtype;
+            a32 = a32 && (reinterpret_cast<uintptr_t>(x.chunk) & 31u) == 0;
+        }
+        // the prefix: FP8 decode into the workspace slots, with the workspace scale
+        nvfp4kv_status st = decode_job(layout, x.data, x.scales, x.pool_pages, x.prefix_page_ids,
+                                       x.global_scale, NVFP4KV_FP8_E4M3, x.ws, x.ws_pages,
+                                       x.ws_prefix_ids, x.ws_scale, x.prefix_pages, status,
+                                       p.gather[t]);
+        if (st != NVFP4KV_OK) return st;
+        // the chunk: NVFP4 pages of the pool plus the FP8 copy in the workspace slots
+        if (x.chunk_pages > 0 && (!x.ws || !aligned16(x.ws) ||
+                                  (!x.ws_chunk_ids && x.ws_pages < x.chunk_pages)))
+            return NVFP4KV_ERR_INVALID_ARG;
+        st = encode_job(layout, x.chunk, x.chunk_pool_pages, x.chunk_page_ids,
+                        x.chunk_src_scale, x.global_scale, x.data, x.scales, x.pool_pages,
+                        x.chunk_dst_ids, x.chunk_pages, status, p.write[t]);
+        if (st != NVFP4KV_OK) return st;
+        p.write[t].ws = x.ws;
+        p.write[t].ws_ids = x.ws_chunk_ids;
+        p.write[t].ws_scale = x.ws_scale;
+        p.write[t].ws_pool = x.ws_pages;
+        p.packing[t] = layout->packing;
+    }
+    // the jobs: gather 0, gather 1, write 0, write 1 (absent jobs have no items)
+    const int64_t items[4] = {
+        static_cast<int64_t>(p.gather[0].num_pages) * p.gather[0].items_per_page,
+        static_cast<int64_t>(p.gather[1].num_pages) * p.gather[1].items_per_page,
+        static_cast<int64_t>(p.write[0].num_pages) * p.write[0].items_per_page,
+        static_cast<int64_t>(p.write[1].num_pages) * p.write[1].items_per_page};
+    const double bytes[4] = {
+        static_cast<double>(p.gather[0].num_pages) * p.gather[0].bpp * 25.0,
+        static_cast<double>(p.gather[1].num_pages) * p.gather[1].bpp * 25.0,
+        static_cast<double>(p.write[0].num_pages) * p.write[0].bpp * 57.0,
+        static_cast<double>(p.write[1].num_pages) * p.write[1].bpp * 57.0};
+    if (items[0] + items[1] + items[2] + items[3] == 0) return NVFP4KV_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (src_dtype == NVFP4KV_FP16) {
+        e = a32 ? launch_extend_step<NVFP4KV_FP16, true>(p, items, bytes, s)
+                : launch_extend_step<NVFP4KV_FP16, false>(p, items, bytes, s);
+    } else if (src_dtype == NVFP4KV_FP8_E4M3) {
+        e = launch_extend_step<NVFP4KV_FP8_E4M3, false>(p, items, bytes, s);
+    } else {  // BF16 chunks, or no chunk at all
+        e = a32 ? launch_extend_step<NVFP4KV_BF16, true>(p, items, bytes, s)
+                : launch_extend_step<NVFP4KV_BF16, false>(p, items, bytes, s);
+    }
+    if (e != cudaSuccess) return NVFP4KV_ERR_CUDA;
     return launch_status();
 }
 

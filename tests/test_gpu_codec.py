@@ -440,3 +440,80 @@ def test_round_trips_back_to_back_do_not_accumulate_error(kv, cuda, pack):
     for k in (2, 3):
         assert np.array_equal(backs[k], backs[1]), f"values moved on trip {k + 1}"
         assert torch.equal(trips[k][0], trips[1][0]) and torch.equal(trips[k][1], trips[1][1])
+
+
+@pytest.mark.parametrize("kind", ["bf16", "fp16", "fp8"])
+def test_extend_step_equals_the_separate_calls(kv, cuda, kind):
+    """The extend step of K (dim pairs) and V (token pairs) in one launch: scattered prefix
+    pages gathered to FP8 workspace slots and a ragged chunk written as NVFP4 pages and FP8
+    slots, with a workspace scale. Bit-identical to the two separate calls per tensor, and the
+    gathered prefix and the chunk's pages equal the oracle's."""
+    H, T, D = 2, 32, 128
+    P_pool, n_prefix, n_chunk, n_ws = 60, 23, 9, 40
+    ws_scale = float(np.float32(1.5))
+    src_scale = float(np.float32(0.375)) if kind == "fp8" else 1.0
+    rng = np.random.default_rng(11)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(cuda)  # noqa: E731
+    perm = rng.permutation(P_pool).astype(np.int32)
+    prefix_ids, chunk_dst = perm[:n_prefix], perm[n_prefix:n_prefix + n_chunk]
+    wperm = rng.permutation(n_ws).astype(np.int32)
+    ws_prefix, ws_chunk = wperm[:n_prefix], wperm[n_prefix:n_prefix + n_chunk]
+    parts, sep, want = [], [], []
+    for ti, pack in enumerate((oracle.DIM_PAIRS, oracle.TOKEN_PAIRS)):
+        lay = kv.Layout(H, D, T).with_packing(pack)
+        pool_src = _make_src("bf16", P_pool, H, T, D, seed=60 + ti).to(cuda)
+        pbits = _src_bits(pool_src)
+        g = oracle.global_scale(pbits, oracle.BF16, H, D, T)
+        gs = _scalar(g, cuda)
+        ds, ss = oracle.pool_shapes(P_pool, H, T, D, pack)
+        data = torch.zeros(ds, dtype=torch.uint8, device=cuda)
+        scales = torch.zeros(ss, dtype=torch.uint8, device=cuda)
+        kv.nvfp4_kv_quantize_pages(lay, pool_src, gs, data, scales)
+        chunk = _make_src(kind, 12, H, T, D, seed=70 + ti).to(cuda)
+        chunk_ids = rng.permutation(12)[:n_chunk].astype(np.int32)
+        sst = _scalar(src_scale, cuda) if kind == "fp8" else None
+        sdt = kv.FP8_E4M3 if kind == "fp8" else None
+        ws = torch.zeros((n_ws, H, T, D), dtype=torch.uint8, device=cuda)
+        part = dict(layout=lay, global_scale=gs, data=data.clone(), scales=scales.clone(),
+                    prefix_page_ids=t(prefix_ids), ws=ws.clone(), ws_prefix_ids=t(ws_prefix),
+                    ws_chunk_ids=t(ws_chunk), ws_scale=_scalar(ws_scale, cuda), chunk=chunk,
+                    chunk_page_ids=t(chunk_ids), chunk_src_scale=sst, chunk_dst_ids=t(chunk_dst),
+                    chunk_dtype=sdt)
+        parts.append(part)
+        # the separate calls on their own copies
+        d2, s2, w2 = data.clone(), scales.clone(), ws.clone()
+        kv.nvfp4_kv_dequantize_pages(lay, d2, s2, gs, w2, dst_dtype=kv.FP8_E4M3,
+                                     src_page_ids=t(prefix_ids), dst_page_ids=t(ws_prefix),
+                                     dst_scale=_scalar(ws_scale, cuda))
+        kv.nvfp4_kv_extend_write(lay, chunk, gs, d2, s2, w2, src_page_ids=t(chunk_ids),
+                                 dst_page_ids=t(chunk_dst), ws_page_ids=t(ws_chunk),
+                                 ws_scale=_scalar(ws_scale, cuda), src_scale=sst, src_dtype=sdt)
+        sep.append((d2, s2, w2))
+        # the oracle: the prefix pages' FP8 values and the chunk's NVFP4 pages
+        hd, hs = data.cpu().numpy(), scales.cpu().numpy()
+        want_prefix = oracle.dequantize_pages(hd, hs, H, D, T, g, oracle.FP8_E4M3,
+                                              out_scale=ws_scale, src_page_ids=prefix_ids,
+                                              packing=pack)
+        cbits = _src_bits(chunk)
+        want_d, want_s = oracle.quantize_pages(cbits, _odt(chunk), H, D, T, g,
+                                               num_dst_pages=P_pool, src_page_ids=chunk_ids,
+                                               dst_page_ids=chunk_dst, src_scale=src_scale,
+                                               packing=pack)
+        want.append((want_prefix, want_d, want_s))
+    kv.nvfp4_kv_extend_step(parts)
+    torch.cuda.synchronize()
+    for part, (d2, s2, w2), (want_prefix, want_d, want_s) in zip(parts, sep, want):
+        assert torch.equal(part["data"], d2) and torch.equal(part["scales"], s2)
+        assert torch.equal(part["ws"], w2)
+        got_ws = part["ws"].cpu().numpy()
+        assert np.array_equal(got_ws[ws_prefix], want_prefix.reshape(got_ws[ws_prefix].shape))
+        gd, gsc = part["data"].cpu().numpy(), part["scales"].cpu().numpy()
+        assert np.array_equal(gd[chunk_dst], want_d[chunk_dst])
+        assert np.array_equal(gsc[chunk_dst], want_s[chunk_dst])
+    # one tensor alone, and an empty call
+    solo = dict(parts[1])
+    solo["data"], solo["scales"], solo["ws"] = (torch.zeros_like(solo["data"]),
+                                                torch.zeros_like(solo["scales"]),
+                                                torch.zeros_like(solo["ws"]))
+    kv.nvfp4_kv_extend_step([solo])
+    assert torch.equal(solo["ws"][t(ws_chunk).long()], sep[1][2][t(ws_chunk).long()])

@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
                  "nvfp4_kv_host_device_pointer",
                  "nvfp4_paged_decode_attention", "nvfp4_paged_decode_workspace_size",
                  "nvfp4_kv_compute_global_scale", "nvfp4_kv_global_scale_workspace_size",
-                 "nvfp4_kv_round_f32", "nvfp4kv_status_string", "nvfp4kv_version"):
+                 "nvfp4_kv_round_f32", "nvfp4kv_status_string", "nvfp4kv_version",
+                 "nvfp4_kv_extend_step", "nvfp4_paged_decode_attention_noalloc"):
         assert want in names
 
 
@@ -173,3 +174,36 @@ def test_cold_block_layout_matches_its_definition(lib):
     bad = kv.ColdRope(kv.ROPE_SKIP, 120, 16)
     assert lib.nvfp4_kv_cold_block_layout(ctypes.byref(kv.Layout(8, 128, 32)),
                                           ctypes.byref(bad), 0, ctypes.byref(out)) == 1
+
+
+def test_extend_step_host_validation(lib):
+    """The one-launch extend step checks every tensor as the separate calls do, on the host,
+    before any launch: no tensor list, a tensor count other than 1 or 2, a missing pool or
+    workspace, chunks of different dtypes. The pointers below are never dereferenced."""
+    import nvfp4_paged_kv_gb300 as kv
+    fake = ctypes.c_void_p(1 << 20)   # 16-byte aligned address, never touched
+    def tensor(**kw):
+        x = kv.ExtendTensor()
+        x.layout = kv.Layout(8, 128, 64)
+        x.global_scale = fake
+        x.data = x.scales = x.ws = x.chunk = fake
+        x.pool_pages = x.ws_pages = x.chunk_pool_pages = 4
+        x.prefix_pages = 2
+        x.chunk_pages = 1
+        x.chunk_dtype = kv.BF16
+        for k, v in kw.items():
+            setattr(x, k, v)
+        return x
+    call = lib.nvfp4_kv_extend_step
+    arr = (kv.ExtendTensor * 2)(tensor(), tensor())
+    assert call(None, 1, None, None) == 1
+    assert call(arr, 0, None, None) == 1
+    assert call(arr, 3, None, None) == 1
+    assert call((kv.ExtendTensor * 1)(tensor(data=None)), 1, None, None) == 1
+    assert call((kv.ExtendTensor * 1)(tensor(ws=None)), 1, None, None) == 1
+    assert call((kv.ExtendTensor * 1)(tensor(layout=kv.Layout(8, 120, 64))), 1, None, None) == 1
+    assert call((kv.ExtendTensor * 1)(tensor(chunk_dtype=7)), 1, None, None) == 2
+    mixed = (kv.ExtendTensor * 2)(tensor(), tensor(chunk_dtype=kv.FP16))
+    assert call(mixed, 2, None, None) == 2
+    empty = (kv.ExtendTensor * 1)(tensor(prefix_pages=0, chunk_pages=0))
+    assert call(empty, 1, None, None) == 0

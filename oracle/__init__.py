@@ -18,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "nvfp4_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_SAN_LIB_PATH = os.path.join(_OUT_DIR, "liboracle_asan_ubsan.so")
 
 BF16, FP16, FP8_E4M3 = 0, 1, 2
 DIM_PAIRS, TOKEN_PAIRS = 0, 1   # byte packing of an NVFP4 pool (see nvfp4_oracle.c, R2)
@@ -26,23 +27,31 @@ _lock = threading.Lock()
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (no fused multiply-add, OpenMP over pages / heads)."""
+def build(force: bool = False, sanitize: bool = False) -> str:
+    """Compile the oracle with gcc (no fused multiply-add, OpenMP over pages / heads).
+
+    sanitize=True builds a second copy instrumented with AddressSanitizer and
+    UndefinedBehaviorSanitizer (any finding aborts the process); a process loads it instead of
+    the plain build when NVFP4_ORACLE_LIB names it, and must then preload gcc's libasan."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    compile_to(_SRC, tmp)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    path = _SAN_LIB_PATH if sanitize else _LIB_PATH
+    if (not force and os.path.exists(path)
+            and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
+    compile_to(_SRC, tmp, sanitize=sanitize)
+    os.replace(tmp, path)
+    return path
 
 
-def compile_to(src: str, out: str) -> str:
+def compile_to(src: str, out: str, sanitize: bool = False) -> str:
     """Compile an oracle C source (this one, or a copy with a deliberate mistake planted by the
     tests that check the pins catch it) to the shared library `out`, with the oracle's flags."""
     cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
            "-Wall", "-shared", "-fPIC", src, "-o", out, "-lm"]
+    if sanitize:
+        cmd[1:1] = ["-fsanitize=address,undefined", "-fno-sanitize-recover=all",
+                    "-fno-omit-frame-pointer", "-g"]
     subprocess.run(cmd, check=True)
     return out
 
@@ -91,7 +100,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            _lib = bind(build())
+            _lib = bind(os.environ.get("NVFP4_ORACLE_LIB") or build())
     return _lib
 
 

@@ -515,11 +515,11 @@ __global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const AmaxParams p) 
         // the CTA's maximum into the call's tagged maximum, then the count; the CTA that
         // completes the count writes g
         if (!tagged_max(p.word, p.nonce, r)) flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
-        __threadfence();
+        fence_acq_rel_gpu();  // release: the maximum is in before the count says so
         const uint32_t k = tagged_finish(p.word + 1, atomicAdd(p.word + 1, 1ull), p.nonce, 1);
         if (k == kTagGiveUp) flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
         if (k == gridDim.x - 1) {
-            __threadfence();
+            fence_acq_rel_gpu();  // acquire: every CTA's maximum is read after the count
             const unsigned long long w = atomicAdd(p.word, 0ull);
             const uint32_t best = (static_cast<uint32_t>(w >> 32) == p.nonce)
                                       ? static_cast<uint32_t>(w)

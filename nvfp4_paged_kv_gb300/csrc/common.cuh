@@ -49,6 +49,14 @@ __device__ __forceinline__ uint32_t tagged_finish(unsigned long long* w, unsigne
     return kTagGiveUp;  // could not install the tag: the caller reports NVFP4KV_STATUS_TIMEOUT
 }
 
+// Acquire-release fence at GPU scope: with a relaxed atomic after it, the writes before it are
+// visible to whoever reads the atomic's result (release); after a relaxed atomic whose result
+// was read, the reads after it see what was released (acquire). Lighter than __threadfence(),
+// which is a sequentially consistent fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Programmatic dependent launch: wait until the previous grid on the stream has completed and
 // its memory is visible (a no-op when the launch did not allow overlap), then let the next grid
 // be scheduled.

@@ -1,4 +1,4 @@
-// Split-KV paged GQA decode attention over NVFP4 K/V for sm_103a, and its combine pass.
+// Split-KV paged GQA decode attention over NVFP4 K/V for sm_103a, with its split merge.
 //
 // What it computes ("Accelerating Long-Context and Agentic Inference with NVFP4 KV Cache",
 // LMSYS: "Path 3: Decode", "NVFP4 KV Decode Attention Kernel Implementation", Figure 3): for
@@ -39,11 +39,13 @@
 //  * O^T += V^^T P^T with head dims as M: V is stored token-pair packed, so every converted byte
 //    is one A-register (one head dim of two adjacent tokens) times the pair's two block scales.
 //  * at the end of a piece the warp writes the BF16 output and the natural-log LSE directly
-//    when the piece is the whole pair, otherwise its record (from registers); the warp holding
-//    a split pair's first stage also writes the pair's descriptors (record range, tagged with
-//    the call). A second, small kernel (launched behind the first with programmatic dependent
-//    launch) merges the records of every split pair by log-sum-exp, one CTA per (pair, query
-//    head), and clears the descriptors it used.
+//    when the piece is the whole pair, otherwise its record (from registers), then bumps the
+//    pair's finished-piece count (a word tagged with the call, release/acquire fences around
+//    the atomic). The warp whose count completes the pair queues it in its CTA; after every
+//    run of the CTA is done, the CTA merges its queued pairs by log-sum-exp: the records of as
+//    many pairs as fit are staged in shared memory in one round trip, and every thread then
+//    takes float4 output columns and forms its head's weights from the staged maxima itself.
+//    A pair with more records than fit at once is merged by chunks.
 // Bytes per (token, KV head) at head_dim 128: 64 + 8 (K) + 64 + 8 (V) = 144.
 #include <cstdint>
 #include <utility>
@@ -228,17 +230,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 // split over the threads: thread t takes one float4 column of the G x D outputs and every R-th
 // record of the chunk, R = threads / columns.
 template <int D>
-__device__ __forceinline__ void merge_pair(const DecodeParams& p, int b, int h, int ps, int S,
-                                           int W, uint8_t* smem) {
+__device__ __forceinline__ void merge_pair(const DecodeParams& p, int b, int h, int64_t rec0,
+                                           int n, uint8_t* smem) {
     using G_ = Geo<D>;
     constexpr int NT = G_::THREADS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.G;
-    const int gf = ps / W, gl = (ps + S - 1) / W;
-    const int n = gl - gf + 1;
     const int64_t bh = static_cast<int64_t>(b) * p.H + h;
-    const int64_t rec0 = gf + bh;
-    __threadfence();  // the count said every record is written: read them after it
+    // no fence here: the thread that saw the count complete fenced after it, and the CTA
+    // barrier between that and this merge orders every thread's reads after the fence
     if (tid == 0) atomicExch(p.done + bh, 0ull);  // a replay with the same tag starts from 0
     const int rec_bytes = G * D * 4;
     // shared memory: records' outputs [KC][G][D], (max, sum) [KC][G], weights [KC][G],
@@ -367,43 +367,40 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
 
 __device__ __forceinline__ int align16i(int x) { return (x + 15) & ~15; }
 
-// Merge pending pairs pend[first], pend[first + 1], ... together, as many as fit in shared memory
-// at once (whole CTA, after its runs): the records' outputs and (max, sum) pairs of all of them
-// are staged by asynchronous copies in one round trip; then one warp per (pair, query head)
-// reduces the maxima and sums and turns the records' maxima into weights, and every thread takes
-// float4 columns of the outputs. Returns how many pairs were merged (0 when the first pair alone
-// does not fit: the caller merges it by chunks).
+// Merge pending pairs pend[first], pend[first + 1], ... (b, h, first record, records) together,
+// as many as fit in shared memory at once (whole CTA, after its runs). The records' outputs and
+// (max, sum) pairs of all of them are staged by asynchronous copies in one round trip; then every
+// thread takes float4 columns of the outputs and forms the weights of its column's query head
+// from the staged maxima itself, so no reduction across threads and no second barrier is needed.
+// Returns how many pairs were merged (0 when the first pair alone does not fit: the caller merges
+// it by chunks).
 template <int D>
 __device__ __forceinline__ int merge_batch(const DecodeParams& p, const int (*pend)[4], int first,
-                                           int n_pend, int W, uint8_t* smem) {
+                                           int n_pend, uint8_t* smem) {
     using G_ = Geo<D>;
-    constexpr int NT = G_::THREADS, NW = G_::WARPS;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NT = G_::THREADS;
+    const int tid = threadIdx.x;
     const int G = p.G;
     const int rec_bytes = G * D * 4;
-    // per pair: outputs n x rec_bytes, (max, sum) n x G x 8, weights n x G x 4, (M, L) G x 8
-    auto bytes_of = [&](int n) {
-        return n * rec_bytes + align16i(n * G * 8) + align16i(n * G * 4) + align16i(G * 8);
-    };
+    // per pair: outputs n x rec_bytes, then (max, sum) n x G x 8
+    auto bytes_of = [&](int n) { return n * rec_bytes + align16i(n * G * 8); };
     int cnt = 0, used = 0;
     for (int i = first; i < n_pend; ++i) {
-        const int n = (pend[i][2] + pend[i][3] - 1) / W - pend[i][2] / W + 1;
-        const int need = bytes_of(n);
+        const int need = bytes_of(pend[i][3]);
         if (used + need > G_::SMEM) break;
         used += need;
         ++cnt;
     }
     if (cnt == 0) return 0;
-    __threadfence();  // the counts said every record is written: read them after it
+    // no fence here: the threads that saw the counts complete fenced after them, and the CTA
+    // barrier since then orders every thread's reads after those fences
     const uint32_t s_base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    // stage every record of the batch
     {
         int off = 0;
         for (int i = first; i < first + cnt; ++i) {
-            const int ps = pend[i][2], S = pend[i][3];
-            const int gf = ps / W, n = (ps + S - 1) / W - gf + 1;
+            const int n = pend[i][3];
+            const int64_t rec0 = pend[i][2];
             const int64_t bh = static_cast<int64_t>(pend[i][0]) * p.H + pend[i][1];
-            const int64_t rec0 = gf + bh;
             if (tid == 0) atomicExch(p.done + bh, 0ull);  // a replay with the same tag starts from 0
             const uint8_t* src = reinterpret_cast<const uint8_t*>(p.rec_o + rec0 * G * D);
             const int nc = n * rec_bytes / 16;
@@ -411,70 +408,46 @@ __device__ __forceinline__ int merge_batch(const DecodeParams& p, const int (*pe
             off += n * rec_bytes;
             const float* msrc = p.rec_ml + rec0 * G * 2;
             for (int c = tid; c < n * G; c += NT) cp_async8(s_base + off + 8 * c, msrc + 2 * c);
-            off += align16i(n * G * 8) + align16i(n * G * 4) + align16i(G * 8);
+            off += align16i(n * G * 8);
         }
         cp_async_commit();
         cp_async_wait<0>();
     }
     __syncthreads();
-    // one warp per (pair, head): maximum, sum, weights; the LSE
-    for (int u = warp; u < cnt * G; u += NW) {
-        const int i = first + u / G, g = u % G;
-        int off = 0;
-        for (int j = first; j < i; ++j)
-            off += bytes_of((pend[j][2] + pend[j][3] - 1) / W - pend[j][2] / W + 1);
-        const int n = (pend[i][2] + pend[i][3] - 1) / W - pend[i][2] / W + 1;
-        const float2* ml_s = reinterpret_cast<const float2*>(smem + off + n * rec_bytes);
-        float* w_s = reinterpret_cast<float*>(smem + off + n * rec_bytes + align16i(n * G * 8));
-        float2* st_s = reinterpret_cast<float2*>(smem + off + n * rec_bytes + align16i(n * G * 8) +
-                                                 align16i(n * G * 4));
-        float mx = -INFINITY;
-        for (int k = lane; k < n; k += 32) mx = fmaxf(mx, ml_s[k * G + g].x);
-        mx = warp_max(mx);
-        float sum = 0.0f;
-        for (int k = lane; k < n; k += 32) {
-            const float2 ml = ml_s[k * G + g];
-            const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - mx);
-            w_s[k * G + g] = w;
-            sum += w * ml.y;
-        }
-        sum = warp_sum(sum);
-        if (lane == 0) {
-            st_s[g] = make_float2(mx, sum);
-            if (p.lse)
-                p.lse[static_cast<int64_t>(pend[i][0]) * p.Hq + pend[i][1] * G + g] =
-                    sum > 0.0f ? (mx + log2f(sum)) * 0.6931471805599453f : -INFINITY;
-        }
-    }
-    __syncthreads();
-    // outputs: float4 columns of every pair of the batch
     const float gvs = __ldg(p.gv);
     const int C4 = G * D / 4;
+    int i = first, off = 0, base = 0;  // columns [base, base + C4) belong to pair i, staged at off
     for (int cc = tid; cc < cnt * C4; cc += NT) {
-        const int i = first + cc / C4, col = cc % C4, g = col * 4 / D;
-        int off = 0;
-        for (int j = first; j < i; ++j)
-            off += bytes_of((pend[j][2] + pend[j][3] - 1) / W - pend[j][2] / W + 1);
-        const int n = (pend[i][2] + pend[i][3] - 1) / W - pend[i][2] / W + 1;
+        while (cc >= base + C4) {
+            off += bytes_of(pend[i][3]);
+            base += C4;
+            ++i;
+        }
+        const int n = pend[i][3], col = cc - base, g = col * 4 / D;
         const float4* o_s = reinterpret_cast<const float4*>(smem + off);
-        const float* w_s = reinterpret_cast<const float*>(smem + off + n * rec_bytes + align16i(n * G * 8));
-        const float2 st = reinterpret_cast<const float2*>(smem + off + n * rec_bytes +
-                                                          align16i(n * G * 8) + align16i(n * G * 4))[g];
+        const float2* ml_s = reinterpret_cast<const float2*>(smem + off + n * rec_bytes);
+        float M = -INFINITY;
+        for (int k = 0; k < n; ++k) M = fmaxf(M, ml_s[k * G + g].x);
+        float L = 0.0f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < n; ++k) {
-            const float w = w_s[k * G + g];
+            const float2 ml = ml_s[k * G + g];
+            const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
+            L += w * ml.y;
             const float4 v = o_s[k * C4 + col];
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
             acc.w += w * v.w;
         }
-        const float f = st.y > 0.0f ? gvs / st.y : 0.0f;
+        const float f = L > 0.0f ? gvs / L : 0.0f;
         uint2 o;
         o.x = pack_bf16x2(acc.x * f, acc.y * f);
         o.y = pack_bf16x2(acc.z * f, acc.w * f);
-        *reinterpret_cast<uint2*>(p.out + (static_cast<int64_t>(pend[i][0]) * p.Hq + pend[i][1] * G) * D +
-                                  4 * col) = o;
+        const int64_t row = static_cast<int64_t>(pend[i][0]) * p.Hq + pend[i][1] * G;
+        *reinterpret_cast<uint2*>(p.out + row * D + 4 * col) = o;
+        if (p.lse && col * 4 == g * D)  // the head's first column also writes its LSE
+            p.lse[row + g] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();  // shared memory is reused by the next batch
     return cnt;
@@ -492,7 +465,7 @@ __global__ void __launch_bounds__(Geo<D>::THREADS, 1) decode_split_kernel(const 
     __shared__ int start_bp[NW][3];  // run start of each warp: sequence, its first stage, length
     __shared__ int span_pair[2];     // first and last pair (b H + h) the CTA's runs touch
     __shared__ int pend_n;           // pairs whose last piece finished in this CTA ...
-    __shared__ int pend[2 * NW][4];  // ... (b, h, first stage, stages): merged at the end
+    __shared__ int pend[2 * NW][4];  // ... (b, h, first record, records): merged at the end
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -1078,16 +1051,19 @@ __global__ void __launch_bounds__(Geo<D>::THREADS, 1) decode_split_kernel(const 
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    __threadfence();  // the record is visible before the count says so
+                    fence_acq_rel_gpu();  // release: the record is visible before the count says so
                     unsigned long long* cnt = p.done + bh;
                     const uint32_t k = tagged_finish(cnt, atomicAdd(cnt, 1ull), p.nonce, 1);
                     if (k == kTagGiveUp) flag_status(p.status, NVFP4KV_STATUS_TIMEOUT);
                     if (k == static_cast<uint32_t>(gl - gf)) {  // every piece is in: merge here
+                        // acquire: the other pieces' records are read after their counts (the
+                        // CTA barrier before the merge carries this to every thread)
+                        fence_acq_rel_gpu();
                         const int slot = atomicAdd(&pend_n, 1);
                         pend[slot][0] = pb_;
                         pend[slot][1] = ph;
-                        pend[slot][2] = pps;
-                        pend[slot][3] = pS;
+                        pend[slot][2] = static_cast<int>(gf + bh);
+                        pend[slot][3] = gl - gf + 1;
                     }
                 }
             }
@@ -1098,9 +1074,9 @@ __global__ void __launch_bounds__(Geo<D>::THREADS, 1) decode_split_kernel(const 
     __syncthreads();  // every warp's run is done: the rings are free for the merge
     const int n_pend = pend_n;
     for (int k = 0; k < n_pend;) {
-        const int m = merge_batch<D>(p, pend, k, n_pend, W, smem);
+        const int m = merge_batch<D>(p, pend, k, n_pend, smem);
         if (m == 0) {  // a pair whose records do not fit at once: by chunks
-            merge_pair<D>(p, pend[k][0], pend[k][1], pend[k][2], pend[k][3], W, smem);
+            merge_pair<D>(p, pend[k][0], pend[k][1], pend[k][2], pend[k][3], smem);
             ++k;
         }
         k += m;

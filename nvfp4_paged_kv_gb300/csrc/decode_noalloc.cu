@@ -65,8 +65,9 @@ extern "C" nvfp4kv_status nvfp4_paged_decode_attention_noalloc(
     }
     void* scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return NVFP4KV_ERR_CUDA;
-    // Same kernels and split plan as the workspace entry point; every partial the combine pass
-    // reads is written by the same call first, so the scratch needs no clearing between calls.
+    // Same kernel and split plan as the workspace entry point; every record the split merge
+    // reads is written by the same call first, and the finished-piece counts are tagged with
+    // the call, so the scratch needs no clearing between calls.
     return nvfp4_paged_decode_attention(layout, batch, num_q_heads, q, k_data, k_scales,
                                         k_global_scale, v_data, v_scales, v_global_scale,
                                         pool_pages, page_table, max_pages_per_seq, seq_lens,

@@ -67,7 +67,8 @@ def parse():
                     help="reference arm: cap on the sampled sequence length (0 = none)")
     ap.add_argument("--profile-case", default="",
                     help="run only one kernel family a few times (for ncu): decode_batch | "
-                         "long_context | quantize | dequantize | dequantize_fp8 | amax | codec")
+                         "long_context | decode_head_dim_64 | decode_head_dim_256 | "
+                         "extend_step | quantize | dequantize | dequantize_fp8 | amax | codec")
     return ap.parse_args()
 
 
@@ -619,9 +620,34 @@ def extend_step_table(path, flush, peak, res):
     16 sequences gathered and dequantized into the FP8 workspace, and the 512-token BF16 chunk
     written as NVFP4 pages and as its FP8 workspace copy: four launches back to back (K gather,
     V gather, K chunk write, V chunk write), timed as one after an L2 flush."""
+    kv, dev = path.kv, path.dev
+    ex, tens, step, parts = extend_setup(kv, dev)
+
+    def fused():
+        kv.nvfp4_kv_extend_step(parts)
+    H, T, D = ex.H, ex.T, ex.D
+    vals = H * T * D
+    gather = 2 * ex.prefix_pages * vals * 1.5625 + 2 * ex.prefix_pages * 4
+    write = 2 * ex.chunk_pages * vals * (2 + 0.5625 + 1) + 2 * ex.chunk_pages * 4
+    for name, fn, launches in (
+            ("extend step: K+V prefix gather -> FP8 + K+V chunk write (4 launches back to back)",
+             step, 4),
+            ("extend step: K+V prefix gather -> FP8 + K+V chunk write (one launch)", fused, 1)):
+        ms = time_kernel(fn, flush)
+        gbs = (gather + write) / (ms * 1e-3) / GB
+        res[name] = {
+            "ms": round(ms, 4), "bytes": int(gather + write), "GB_s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "launches": launches,
+            "bytes_gather": int(gather), "bytes_chunk_write": int(write),
+            "tokens_per_s": round(ex.B * (ex.prefix + ex.chunk) / (ms * 1e-3), 1)}
+    del tens, parts
+
+
+def extend_setup(kv, dev):
+    """The extend workload's K and V tensors (NVFP4 prefix pools encoded on the GPU, BF16
+    chunks, FP8 workspaces), the four-launch step and the fused call's parts."""
     import torch
     import synthetic
-    kv, dev = path.kv, path.dev
     ex = synthetic.ExtendWorkload(seed=2)
     H, T, D = ex.H, ex.T, ex.D
     lay = kv.Layout(H, D, T)
@@ -658,24 +684,7 @@ def extend_step_table(path, flush, peak, res):
                   prefix_page_ids=d["ids"], ws=d["ws"], ws_prefix_ids=ws_prefix,
                   ws_chunk_ids=ws_chunk, chunk=d["chunk"], chunk_dst_ids=d["chunk_dst"])
              for d in tens]
-
-    def fused():
-        kv.nvfp4_kv_extend_step(parts)
-    vals = H * T * D
-    gather = 2 * ex.prefix_pages * vals * 1.5625 + 2 * ex.prefix_pages * 4
-    write = 2 * ex.chunk_pages * vals * (2 + 0.5625 + 1) + 2 * ex.chunk_pages * 4
-    for name, fn, launches in (
-            ("extend step: K+V prefix gather -> FP8 + K+V chunk write (4 launches back to back)",
-             step, 4),
-            ("extend step: K+V prefix gather -> FP8 + K+V chunk write (one launch)", fused, 1)):
-        ms = time_kernel(fn, flush)
-        gbs = (gather + write) / (ms * 1e-3) / GB
-        res[name] = {
-            "ms": round(ms, 4), "bytes": int(gather + write), "GB_s": round(gbs, 1),
-            "frac_of_peak": round(gbs / peak, 4), "launches": launches,
-            "bytes_gather": int(gather), "bytes_chunk_write": int(write),
-            "tokens_per_s": round(ex.B * (ex.prefix + ex.chunk) / (ms * 1e-3), 1)}
-    del tens, parts
+    return ex, tens, step, parts
 
 
 def cold_table(path, flush, timer, pages=2048):
@@ -1100,8 +1109,19 @@ def profile_case(kv, dev, case):
     import torch
     import synthetic
     u8 = torch.uint8
-    if case in ("decode_batch", "long_context"):
-        wl = synthetic.decode_batch() if case == "decode_batch" else synthetic.long_context()
+    if case == "extend_step":
+        _, _, _, parts = extend_setup(kv, dev)
+        for _ in range(4):
+            kv.nvfp4_kv_extend_step(parts)
+    elif case in ("decode_batch", "long_context", "decode_head_dim_64", "decode_head_dim_256"):
+        if case == "decode_batch":
+            wl = synthetic.decode_batch()
+        elif case == "long_context":
+            wl = synthetic.long_context()
+        else:
+            D = int(case.rsplit("_", 1)[1])
+            wl = synthetic.DecodeWorkload(f"decode batch head_dim {D}", B=32, Hq=32, H=8, D=D,
+                                          T=64, seq_lens=[8192] * 32, pool_pages=4096, seed=1)
         q, k, v, pt, sl = wl.make(device=dev)
         lay = kv.Layout(wl.H, wl.D, wl.T)
         P = wl.pool_pages

@@ -863,6 +863,15 @@ def oracle_sample(seed=0, pages=1024, decode_seqs=1, max_tokens=None):
     return codec_bytes + dec_bytes, t_codec + t_dec, oracle.max_threads(), desc
 
 
+def workload_config(seed):
+    """The `config` object of both arms' lines: what the step runs on, nothing measured."""
+    import synthetic
+    return {"workload": WORKLOAD,
+            "l2": "inputs larger than L2 (129 MB); kernel table: L2 flushed before each launch "
+                  "(512 MB written, then 256 MB of it read)",
+            "long_context_seq_lens": synthetic.long_context_lengths(seed)}
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step is a bounded sample of the workload."""
     world, rank, local = dist_setup()
@@ -885,7 +894,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": desc},
+        "config": workload_config(args.seed),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": thr,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -954,13 +963,9 @@ def main():
                          "encode arithmetic in FP32; decode attention on FP16 tensor-core "
                          "operands (exact dequantized K/V) with FP32 accumulation"),
         "data": "synthetic",
-        "config": {"workload": WORKLOAD,
-                   "l2": "inputs larger than L2 (129 MB); kernel table: L2 flushed before "
-                         "each launch (512 MB written, then 256 MB of it read)",
-                   "bytes_per_step_per_gpu": int(step_bytes),
-                   "frac_of_peak": round(value / world / peak, 4),
-                   "peak_GB_s": peak, "peak_kind": peak_kind,
-                   "long_context_seq_lens": path.wl.seq_lens},
+        "config": workload_config(args.seed),
+        "bytes_per_step_per_gpu": int(step_bytes),
+        "peak": {"GB_s": peak, "kind": peak_kind, "frac": round(value / world / peak, 4)},
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel (nvfp4_paged_decode_attention, one launch)",
                      "achieved": round(path.bytes_decode / (dec_ms * 1e-3) / GB, 1),
                      "peak": peak, "unit": "GB/s",

@@ -280,3 +280,32 @@ def test_workspace_needs_no_clearing(kv, cuda, fill):
         ws.zero_()
         out0, lse0 = run_decode(kv, cuda, cache, q, pt, sl, sm, splits=splits, workspace=ws)
         assert np.array_equal(out, out0) and np.array_equal(lse, lse0), (fill, splits)
+
+
+@pytest.mark.parametrize("H,G", [(8, 4), (4, 1), (2, 3), (3, 4), (1, 2), (2, 8)])
+def test_head_dim_64_heads_and_groups(kv, cuda, H, G):
+    """Head_dim 64 over even and odd KV-head counts and query groups 1 to 8, against the oracle
+    on ragged lengths and a shuffled pool, with the automatic split and with 1 and 7 forced
+    splits, and once more with a workspace full of 0xFF bytes."""
+    D, T, B = 64, 64, 4
+    lens = [3000, 1, 640, 2049]
+    maxp = max(-(-L // T) for L in lens)
+    pool = B * maxp + 2
+    g = synthetic.gen(640 + 10 * H + G)
+    q = synthetic.randn_bf16((B, H * G, D), g)
+    k = synthetic.kv_pages_bf16(pool, H, T, D, g, k_outliers=True)
+    v = synthetic.kv_pages_bf16(pool, H, T, D, g)
+    pt = torch.randperm(pool, generator=g)[:B * maxp].view(B, maxp).to(torch.int32)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    cache = Cache(kv, cuda, k, v, H, D, T)
+    sm = 1 / math.sqrt(D)
+    ref, ref_lse = oracle_decode(cache, q, pt, sl, sm)
+    for splits in (0, 1, 7):
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        out, lse = run_decode(kv, cuda, cache, q, pt, sl, sm, splits=splits, status=status)
+        check(out, lse, ref, ref_lse, tag=f"H={H} G={G} splits={splits}")
+        assert status.item() == 0
+    need = kv.nvfp4_paged_decode_workspace_size(cache.lay, B, H * G, maxp, 0)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=cuda)
+    out, lse = run_decode(kv, cuda, cache, q, pt, sl, sm, workspace=ws)
+    check(out, lse, ref, ref_lse, tag=f"H={H} G={G} 0xff workspace")

@@ -129,7 +129,7 @@ def test_tiny_decode_workload(kv, cuda):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("T,G", [(16, 1), (32, 4), (64, 8), (48, 2), (128, 4)])
+@pytest.mark.parametrize("T,G", [(16, 1), (32, 4), (64, 8), (48, 2), (128, 4), (256, 3)])
 def test_decode_shapes(kv, cuda, D, T, G):
     """Ragged lengths (partial pages, partial 64-token stages, 1 token, 0 tokens), a shuffled
     pool, several splits."""

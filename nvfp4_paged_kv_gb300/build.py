@@ -40,23 +40,34 @@ def _deps():
         glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "nvfp4_kv.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# A second copy of the library whose host code (argument checks, workspace carving, launch
+# set-up) is instrumented with AddressSanitizer and UndefinedBehaviorSanitizer, for the host-only
+# checks of the C ABI; the device code is the same.
+SAN_OUT = os.path.join(OUT, "sanitized")
+SAN_LIB = os.path.join(SAN_OUT, "libnvfp4kv.so")
+SAN_FLAGS = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
+             "-Xcompiler", "-fno-sanitize-recover=all", "-Xcompiler", "-fno-omit-frame-pointer"]
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, sanitize: bool = False) -> str:
+    out, lib = (SAN_OUT, SAN_LIB) if sanitize else (OUT, LIB)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out, exist_ok=True)
     nvcc = _nvcc()
     objs = []
+    extra = SAN_FLAGS if sanitize else []
 
     def compile_one(src):
-        obj = os.path.join(OUT, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(out, os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -68,17 +79,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(sources())) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     # shared CUDA runtime: in a process that already loaded libcudart.so.13 (e.g. through
     # torch) the same instance is reused, so the library and its caller agree on the current
     # device; the rpath lets a plain C caller find the toolkit's copy.
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", *extra, "-o", tmp, *objs,
            "-Xlinker", "-rpath," + _cuda_lib_dir()]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -117,6 +117,84 @@ int main(void) {
           "extend step without tensors");
     check(nvfp4_kv_extend_step(parts, 3, NULL, NULL) == NVFP4KV_ERR_INVALID_ARG,
           "extend step with three tensors");
+    parts[0].layout = bad;
+    check(nvfp4_kv_extend_step(parts, 1, NULL, NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "extend step with head_dim 120");
+    parts[0].layout = lay;
+    parts[0].chunk_pages = 1;
+    parts[0].chunk_dtype = 7;
+    check(nvfp4_kv_extend_step(parts, 1, NULL, NULL) == NVFP4KV_ERR_UNSUPPORTED,
+          "extend step with an unknown chunk dtype");
+    /* a first tensor that passes every check, then a second whose chunk dtype differs */
+    parts[0].chunk_dtype = NVFP4KV_BF16;
+    parts[0].global_scale = (const float*)fake;
+    parts[0].data = (uint8_t*)fake;
+    parts[0].scales = (uint8_t*)fake;
+    parts[0].pool_pages = 1;
+    parts[0].prefix_pages = 1;
+    parts[0].ws = (uint8_t*)fake;
+    parts[0].ws_pages = 2;
+    parts[0].chunk = fake;
+    parts[0].chunk_pool_pages = 1;
+    parts[1] = parts[0];
+    parts[1].chunk_dtype = NVFP4KV_FP16;
+    check(nvfp4_kv_extend_step(parts, 2, NULL, NULL) == NVFP4KV_ERR_UNSUPPORTED,
+          "extend step with two chunk dtypes");
+    parts[1].chunk_dtype = NVFP4KV_BF16;
+    parts[1].ws = NULL;
+    check(nvfp4_kv_extend_step(parts, 2, NULL, NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "extend step whose second tensor has no workspace");
+
+    check(nvfp4_kv_dequantize_pages(&lay, (const uint8_t*)fake, (const uint8_t*)fake, 1, NULL,
+                                    (const float*)fake, (nvfp4kv_dtype)9, fake, 1, NULL, NULL, 1,
+                                    NULL, NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "dequantize to an unknown dtype");
+    check(nvfp4_kv_dequantize_pages(&lay, (const uint8_t*)fake, (const uint8_t*)fake, 1, NULL,
+                                    (const float*)fake, NVFP4KV_BF16,
+                                    (void*)((uintptr_t)4096 + 4), 1, NULL, NULL, 1, NULL,
+                                    NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "dequantize to a misaligned destination");
+    check(nvfp4_kv_compute_global_scale(&lay, NVFP4KV_BF16, fake, 1, NULL, 1, NULL, NULL, fake,
+                                        16, NULL, NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "global scale without an output");
+    check(nvfp4_kv_extend_write(&lay, NVFP4KV_BF16, fake, 1, NULL, NULL, (const float*)fake,
+                                (uint8_t*)fake, (uint8_t*)fake, 1, NULL, NULL, 1, NULL, NULL, 1,
+                                NULL, NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "extend write without a workspace");
+    {
+        /* forced splits: the workspace need is known on the host, no device query */
+        size_t need = nvfp4_paged_decode_workspace_size(&lay, 2, 32, 4, 2);
+        check(need > 0, "decode workspace with forced splits");
+        check(nvfp4_paged_decode_attention(&lay, 2, 32, fake, (const uint8_t*)fake,
+                                           (const uint8_t*)fake, (const float*)fake,
+                                           (const uint8_t*)fake, (const uint8_t*)fake,
+                                           (const float*)fake, 8, (const int32_t*)fake, 4,
+                                           (const int32_t*)fake, 0.1f, 2, fake, need - 1, fake,
+                                           NULL, NULL, NULL) == NVFP4KV_ERR_WORKSPACE,
+              "decode with a workspace one byte short");
+        check(nvfp4_paged_decode_attention(&lay, 2, 72, fake, (const uint8_t*)fake,
+                                           (const uint8_t*)fake, (const float*)fake,
+                                           (const uint8_t*)fake, (const uint8_t*)fake,
+                                           (const float*)fake, 8, (const int32_t*)fake, 4,
+                                           (const int32_t*)fake, 0.1f, 2, fake, need, fake, NULL,
+                                           NULL, NULL) == NVFP4KV_ERR_UNSUPPORTED,
+              "decode with a query group of 9");
+        check(nvfp4_paged_decode_attention(&lay, 2, 32, (const void*)((uintptr_t)4096 + 2),
+                                           (const uint8_t*)fake, (const uint8_t*)fake,
+                                           (const float*)fake, (const uint8_t*)fake,
+                                           (const uint8_t*)fake, (const float*)fake, 8,
+                                           (const int32_t*)fake, 4, (const int32_t*)fake, 0.1f,
+                                           2, fake, need, fake, NULL, NULL,
+                                           NULL) == NVFP4KV_ERR_INVALID_ARG,
+              "decode with misaligned queries");
+    }
+    rope.mode = NVFP4KV_ROPE_2FP4;
+    rope.first_dim = 120;
+    rope.dims = 16;
+    check(nvfp4_kv_offload_pages(&lay, NVFP4KV_BF16, fake, fake, 8 * 64 * 128, 1, NULL, NULL,
+                                 NULL, &rope, NULL, 0, 0, (uint8_t*)fake, 1, NULL, 1, NULL,
+                                 NULL) == NVFP4KV_ERR_INVALID_ARG,
+          "offload with a RoPE part past head_dim");
 
     if (failures == 0) printf("all checks passed\n");
     return failures == 0 ? 0 : 1;

@@ -47,3 +47,28 @@ def test_header_alone_is_a_complete_c_translation_unit(tmp_path):
                             str(tmp_path / f"only_header_{std}.o")], capture_output=True,
                            text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_host_calls_under_asan_and_ubsan(tmp_path):
+    """The same C program linked against a copy of the library whose host code is instrumented
+    with AddressSanitizer and UndefinedBehaviorSanitizer (the device code is unchanged): every
+    host-only call and argument check runs with bounds, lifetime, overflow and shift checks, and
+    any finding aborts the program."""
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    from nvfp4_paged_kv_gb300 import build
+    lib = build.build(sanitize=True)
+    exe = str(tmp_path / "abi_c99_sanitized")
+    libdir = os.path.dirname(lib)
+    cmd = ["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+           "-fsanitize=address", "-fsanitize=undefined", "-fno-sanitize-recover=all",
+           "-I", os.path.join(ROOT, "include"), SRC, "-o", exe,
+           "-L", libdir, "-lnvfp4kv", "-Wl,-rpath," + libdir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    env = {k: v for k, v in os.environ.items() if k != "LD_PRELOAD"}
+    env["ASAN_OPTIONS"] = "detect_leaks=0:protect_shadow_gap=0:abort_on_error=1"
+    env["UBSAN_OPTIONS"] = "print_stacktrace=1:halt_on_error=1"
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("all checks passed"), r.stdout
